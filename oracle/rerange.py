@@ -1,0 +1,48 @@
+"""Oracle: all-gathered KV buffer -> logical token order (the rerange).
+
+Test infrastructure only (see the package docstring).
+
+Source: "[DeepSeek v3.2] 上下文并行详解", section 2.C (cp_all_gather_rerange_output) and
+section 4 part 3 step B: after the all-gather, rows sit rank by rank ("T0,T4, T1,T5, ..."), and
+the rerange puts them back in the logical order T0, T1, T2, ... because the top-k selection needs
+the KV logically contiguous.
+
+Reading taken where the page is silent: the page gives the rank-major order but not whether
+each rank's block is padded. Both layouts are modelled: padded (every rank's block starts at
+rank * stride, stride >= ceil(N/sp), the equal-size all-gather) and packed (blocks back to back,
+stride = 0).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .split import shard_tokens
+
+
+def rank_offsets(n_tokens: int, sp: int, stride: int = 0) -> np.ndarray:
+    """Row where each rank's block starts in the gathered buffer."""
+    if stride > 0:
+        return np.arange(sp, dtype=np.int64) * stride
+    sizes = [len(shard_tokens(n_tokens, sp, q)) for q in range(sp)]
+    return np.concatenate([[0], np.cumsum(sizes)[:-1]]).astype(np.int64)
+
+
+def all_gather(shards, stride: int = 0) -> np.ndarray:
+    """Concatenate the ranks' local rows rank by rank; with stride > 0 pad each block with zeros."""
+    if stride <= 0:
+        return np.concatenate(shards, axis=0)
+    blocks = []
+    for s in shards:
+        pad = np.zeros((stride - s.shape[0],) + s.shape[1:], dtype=s.dtype)
+        blocks.append(np.concatenate([s, pad], axis=0))
+    return np.concatenate(blocks, axis=0)
+
+
+def rerange(gathered: np.ndarray, n_tokens: int, sp: int, stride: int = 0) -> np.ndarray:
+    """Undo the rank-major layout: rank q's j-th local row is token q + j*sp."""
+    off = rank_offsets(n_tokens, sp, stride)
+    out = np.empty((n_tokens,) + gathered.shape[1:], dtype=gathered.dtype)
+    for q in range(sp):
+        tokens = shard_tokens(n_tokens, sp, q)
+        out[tokens] = gathered[off[q]:off[q] + len(tokens)]
+    return out
