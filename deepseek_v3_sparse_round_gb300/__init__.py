@@ -1,0 +1,170 @@
+"""Round-robin sequence-shard DSA prefill attention for GB300 (sm_103a).
+
+Python binding of the C ABI in include/dsa_rr.h. Every function here only marshals arguments
+(torch tensors -> device pointers, the current CUDA stream) and calls the native library of the
+same name; all computation runs in the library's CUDA kernels. If libdsa_rr.so is missing the
+calls raise: there is no CPU or PyTorch fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from . import _native
+
+__all__ = [
+    "DsaError", "dsa_version", "dsa_rr_shard_len", "dsa_rr_split_metadata", "dsa_rr_rerange",
+    "dsa_indexer_topk_workspace_size", "dsa_score_row_stride", "dsa_indexer_scores",
+    "dsa_topk_select", "dsa_indexer_topk", "dsa_sparse_mla", "dsa_read_device_errors",
+    "DEVERR_TIMEOUT", "DEVERR_BAD_INDEX", "DEVERR_BAD_LENGTH",
+]
+
+DEVERR_TIMEOUT = 0x80000000
+DEVERR_BAD_INDEX = 0x40000000
+DEVERR_BAD_LENGTH = 0x20000000
+
+
+class DsaError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"dsa error {code}: {msg}")
+        self.code = code
+
+
+def _lib():
+    return _native.load()
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise DsaError(rc, _lib().dsa_last_error_string().decode(errors="replace"))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if t.numel() > 0 and not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t, dtype=None, name="tensor"):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _row_bytes(t):
+    return math.prod(t.shape[1:]) * t.element_size()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def dsa_version() -> int:
+    return _lib().dsa_version()
+
+
+def dsa_rr_shard_len(n_tokens: int, sp: int, rank: int) -> int:
+    return int(_lib().dsa_rr_shard_len(n_tokens, sp, rank))
+
+
+def dsa_score_row_stride(max_ctx: int) -> int:
+    return int(_lib().dsa_score_row_stride(max_ctx))
+
+
+def dsa_indexer_topk_workspace_size(n_q: int, max_ctx: int, k: int) -> int:
+    return int(_lib().dsa_indexer_topk_workspace_size(n_q, max_ctx, k))
+
+
+def dsa_read_device_errors() -> int:
+    flags = ctypes.c_uint32(0)
+    _check(_lib().dsa_read_device_errors(ctypes.byref(flags)))
+    return int(flags.value)
+
+
+def dsa_rr_split_metadata(cu, n_tokens, sp, rank, cu_shard, pos, bid, gidx=None,
+                          src_rows=None, dst_rows=None, stream=None):
+    """cu int32 [B+1] -> cu_shard [B+1], pos/bid/gidx [n_r]; optional dst_rows = src_rows[g_t]."""
+    for name, t in (("cu", cu), ("cu_shard", cu_shard), ("pos", pos), ("bid", bid), ("gidx", gidx)):
+        _dev(t, torch.int32, name)
+    row_bytes = 0
+    if src_rows is not None:
+        _dev(src_rows, None, "src_rows")
+        _dev(dst_rows, src_rows.dtype, "dst_rows")
+        row_bytes = _row_bytes(src_rows)
+    _check(_lib().dsa_rr_split_metadata(_ptr(cu), cu.numel() - 1, n_tokens, sp, rank,
+                                        _ptr(cu_shard), _ptr(pos), _ptr(bid), _ptr(gidx),
+                                        _ptr(src_rows), _ptr(dst_rows), row_bytes,
+                                        _stream(stream)))
+
+
+def dsa_rr_rerange(gathered, out, n_tokens, sp, rank_stride_rows=0, stream=None):
+    """out[g] = gathered[off[g % sp] + g // sp] (padded blocks if rank_stride_rows > 0)."""
+    _dev(gathered, None, "gathered")
+    _dev(out, gathered.dtype, "out")
+    row_bytes = _row_bytes(out)
+    _check(_lib().dsa_rr_rerange(_ptr(gathered), _ptr(out), n_tokens, sp, rank_stride_rows,
+                                 row_bytes, _stream(stream)))
+
+
+def dsa_indexer_scores(q_idx, w, k_idx, cu, n_req, pos, bid, max_ctx, scores, workspace,
+                       block_table=None, page_size=64, stream=None):
+    """scores[t, s] = sum_h w[t,h] relu(q_idx[t,h] . k_idx[row(b_t, s)]) for s <= pos_t."""
+    _dev(q_idx, torch.bfloat16, "q_idx"); _dev(k_idx, torch.bfloat16, "k_idx")
+    _dev(w, torch.float32, "w"); _dev(scores, torch.float32, "scores")
+    _dev(pos, torch.int32, "pos"); _dev(bid, torch.int32, "bid"); _dev(cu, torch.int32, "cu")
+    _dev(block_table, torch.int32, "block_table")
+    n_q, Hi, Di = q_idx.shape
+    max_pages = block_table.shape[1] if block_table is not None else 0
+    _check(_lib().dsa_indexer_scores(
+        _ptr(q_idx), _ptr(w), _ptr(k_idx), k_idx.shape[0], _ptr(cu), n_req, _ptr(pos), _ptr(bid),
+        n_q, Hi, Di, max_ctx, _ptr(block_table), max_pages, page_size, _ptr(scores),
+        scores.shape[1], _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def dsa_topk_select(scores, pos, k, max_ctx, topk, stream=None):
+    _dev(scores, torch.float32, "scores"); _dev(pos, torch.int32, "pos")
+    _dev(topk, torch.int32, "topk")
+    _check(_lib().dsa_topk_select(_ptr(scores), scores.shape[1], _ptr(pos), pos.numel(), k,
+                                  max_ctx, _ptr(topk), _stream(stream)))
+
+
+def dsa_indexer_topk(q_idx, w, k_idx, cu, n_req, pos, bid, k, max_ctx, topk, workspace,
+                     block_table=None, page_size=64, stream=None):
+    """Indexer scores + top-k; the score rows live in `workspace` (uint8, 256-byte aligned)."""
+    _dev(q_idx, torch.bfloat16, "q_idx"); _dev(k_idx, torch.bfloat16, "k_idx")
+    _dev(w, torch.float32, "w"); _dev(topk, torch.int32, "topk")
+    _dev(pos, torch.int32, "pos"); _dev(bid, torch.int32, "bid"); _dev(cu, torch.int32, "cu")
+    _dev(block_table, torch.int32, "block_table")
+    n_q, Hi, Di = q_idx.shape
+    max_pages = block_table.shape[1] if block_table is not None else 0
+    _check(_lib().dsa_indexer_topk(
+        _ptr(q_idx), _ptr(w), _ptr(k_idx), k_idx.shape[0], _ptr(cu), n_req, _ptr(pos), _ptr(bid),
+        n_q, Hi, Di, k, max_ctx, _ptr(block_table), max_pages, page_size, _ptr(topk),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def dsa_sparse_mla(q, c, cu, n_req, bid, topk, scale, o, lse=None, block_table=None,
+                   page_size=64, stream=None):
+    """o[t,h] = softmax(scale q[t,h] . c[rows]) c[rows, :dv] over the valid top-k rows."""
+    _dev(q, torch.bfloat16, "q"); _dev(c, torch.bfloat16, "c"); _dev(o, torch.bfloat16, "o")
+    _dev(bid, torch.int32, "bid"); _dev(topk, torch.int32, "topk"); _dev(cu, torch.int32, "cu")
+    _dev(lse, torch.float32, "lse"); _dev(block_table, torch.int32, "block_table")
+    n_q, H, dqk = q.shape
+    dv = o.shape[2]
+    max_pages = block_table.shape[1] if block_table is not None else 0
+    _check(_lib().dsa_sparse_mla(
+        _ptr(q), _ptr(c), c.shape[0], _ptr(cu), n_req, _ptr(bid), _ptr(topk), n_q, H, dqk, dv,
+        topk.shape[1], float(scale), _ptr(block_table), max_pages, page_size, _ptr(o), _ptr(lse),
+        _stream(stream)))

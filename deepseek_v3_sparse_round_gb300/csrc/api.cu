@@ -1,0 +1,176 @@
+// extern "C" entry points declared in include/dsa_rr.h: argument checks, error text, workspace
+// sizing, and dispatch to the kernels of split.cu, topk.cu, indexer.cu and mla.cu.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <cuda_runtime.h>
+
+#include "status.cuh"
+
+namespace dsa {
+
+// ---- defined in the kernel translation units ----
+int64_t shard_len(int64_t n_tokens, int sp, int rank);
+int split_metadata(const int32_t* cu, int n_req, int64_t n_tokens, int sp, int rank,
+                   int32_t* cu_shard, int32_t* pos, int32_t* bid, int32_t* gidx,
+                   const void* src_rows, void* dst_rows, int64_t row_bytes, cudaStream_t stream);
+int rerange(const void* gathered, void* out, int64_t n_tokens, int sp, int64_t rank_stride_rows,
+            int64_t row_bytes, cudaStream_t stream);
+size_t indexer_plan_bytes(int64_t n_q);
+int indexer_scores(const void* q_idx, const float* w, const void* k_idx, int64_t n_kv_rows,
+                   const int32_t* cu, const int32_t* pos, const int32_t* bid, int64_t n_q, int n_req,
+                   int Hi, int Di, int max_ctx, const int32_t* block_table, int max_pages,
+                   int page_size, float* scores, int64_t stride, void* ws, size_t ws_bytes,
+                   cudaStream_t stream);
+int topk_select(const float* scores, int64_t score_stride, const int32_t* pos, int64_t n_q, int k,
+                int max_ctx, int32_t* topk, cudaStream_t stream);
+int sparse_mla(const void* q, const void* c, int64_t n_kv_rows, const int32_t* cu, int n_req,
+               const int32_t* bid, const int32_t* topk, int64_t n_q, int H, int dqk, int dv, int k,
+               float scale, const int32_t* block_table, int max_pages, int page_size, void* o,
+               float* lse, cudaStream_t stream);
+cudaError_t split_read_errors(uint32_t* flags);
+cudaError_t topk_read_errors(uint32_t* flags);
+cudaError_t indexer_read_errors(uint32_t* flags);
+cudaError_t mla_read_errors(uint32_t* flags);
+
+namespace {
+thread_local char g_msg[512] = "no error";
+}
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+}
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  snprintf(g_msg, sizeof(g_msg), "CUDA error %d (%s) in %s", static_cast<int>(e),
+           cudaGetErrorString(e), what);
+  return DSA_ERR_CUDA;
+}
+
+int num_sms_cached() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return 148;
+  return sms;
+}
+
+static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace dsa
+
+#define DSA_EXPORT __attribute__((visibility("default")))
+
+extern "C" {
+
+DSA_EXPORT const char* dsa_last_error_string(void) { return dsa::g_msg; }
+
+DSA_EXPORT int dsa_version(void) { return 1; }
+
+DSA_EXPORT int dsa_read_device_errors(uint32_t* flags) {
+  if (!flags) return dsa::fail(DSA_ERR_INVALID, "flags is NULL");
+  *flags = 0;
+  DSA_CHECK_CUDA(cudaDeviceSynchronize());
+  DSA_CHECK_CUDA(dsa::split_read_errors(flags));
+  DSA_CHECK_CUDA(dsa::topk_read_errors(flags));
+  DSA_CHECK_CUDA(dsa::indexer_read_errors(flags));
+  DSA_CHECK_CUDA(dsa::mla_read_errors(flags));
+  return DSA_OK;
+}
+
+DSA_EXPORT int64_t dsa_rr_shard_len(int64_t n_tokens, int sp, int rank) {
+  return dsa::shard_len(n_tokens, sp, rank);
+}
+
+DSA_EXPORT int dsa_rr_split_metadata(const int32_t* cu, int n_req, int64_t n_tokens, int sp, int rank,
+                          int32_t* cu_shard, int32_t* pos, int32_t* bid, int32_t* gidx,
+                          const void* src_rows, void* dst_rows, int64_t row_bytes,
+                          dsa_stream_t stream) {
+  return dsa::split_metadata(cu, n_req, n_tokens, sp, rank, cu_shard, pos, bid, gidx, src_rows,
+                             dst_rows, row_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+DSA_EXPORT int dsa_rr_rerange(const void* gathered, void* out, int64_t n_tokens, int sp,
+                   int64_t rank_stride_rows, int64_t row_bytes, dsa_stream_t stream) {
+  return dsa::rerange(gathered, out, n_tokens, sp, rank_stride_rows, row_bytes,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+DSA_EXPORT int64_t dsa_score_row_stride(int max_ctx) {
+  if (max_ctx < 1) return 0;
+  return static_cast<int64_t>((max_ctx + 3) / 4) * 4;
+}
+
+DSA_EXPORT size_t dsa_indexer_topk_workspace_size(int64_t n_q, int max_ctx, int k) {
+  (void)k;
+  if (n_q < 0 || max_ctx < 1) return 0;
+  const size_t plan = dsa::indexer_plan_bytes(n_q);
+  const size_t scores = static_cast<size_t>(n_q) * static_cast<size_t>(dsa_score_row_stride(max_ctx)) *
+                        sizeof(float);
+  return dsa::round_up(plan, 256) + dsa::round_up(scores, 256);
+}
+
+DSA_EXPORT int dsa_indexer_scores(const void* q_idx, const float* w, const void* k_idx, int64_t n_kv_rows,
+                       const int32_t* cu, int n_req, const int32_t* pos, const int32_t* bid,
+                       int64_t n_q, int Hi, int Di, int max_ctx, const int32_t* block_table,
+                       int max_pages, int page_size, float* scores, int64_t score_stride,
+                       void* workspace, size_t workspace_bytes, dsa_stream_t stream) {
+  if (n_req < 1) return dsa::fail(DSA_ERR_INVALID, "indexer: n_req must be >= 1");
+  if (score_stride % 4 != 0 || reinterpret_cast<uintptr_t>(scores) % 16 != 0)
+    return dsa::fail(DSA_ERR_INVALID, "indexer: score rows must be 16-byte aligned");
+  return dsa::indexer_scores(q_idx, w, k_idx, n_kv_rows, cu, pos, bid, n_q, n_req, Hi, Di,
+                             max_ctx, block_table, max_pages, page_size, scores, score_stride,
+                             workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+DSA_EXPORT int dsa_topk_select(const float* scores, int64_t score_stride, const int32_t* pos, int64_t n_q,
+                    int k, int max_ctx, int32_t* topk, dsa_stream_t stream) {
+  return dsa::topk_select(scores, score_stride, pos, n_q, k, max_ctx, topk,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+DSA_EXPORT int dsa_indexer_topk(const void* q_idx, const float* w, const void* k_idx, int64_t n_kv_rows,
+                     const int32_t* cu, int n_req, const int32_t* pos, const int32_t* bid,
+                     int64_t n_q, int Hi, int Di, int k, int max_ctx, const int32_t* block_table,
+                     int max_pages, int page_size, int32_t* topk, void* workspace,
+                     size_t workspace_bytes, dsa_stream_t stream) {
+  if (n_q < 0 || max_ctx < 1 || k < 1)
+    return dsa::fail(DSA_ERR_INVALID, "indexer_topk: need n_q >= 0, max_ctx >= 1, k >= 1");
+  if (n_q == 0) return DSA_OK;
+  const size_t need = dsa_indexer_topk_workspace_size(n_q, max_ctx, k);
+  if (!workspace || workspace_bytes < need)
+    return dsa::fail(DSA_ERR_WORKSPACE, "indexer_topk: workspace of %zu bytes < %zu",
+                     workspace_bytes, need);
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return dsa::fail(DSA_ERR_INVALID, "indexer_topk: workspace must be 256-byte aligned");
+  const size_t plan = dsa::round_up(dsa::indexer_plan_bytes(n_q), 256);
+  float* scores = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan);
+  const int64_t stride = dsa_score_row_stride(max_ctx);
+  int rc = dsa_indexer_scores(q_idx, w, k_idx, n_kv_rows, cu, n_req, pos, bid, n_q, Hi, Di,
+                              max_ctx, block_table, max_pages, page_size, scores, stride,
+                              workspace, plan, stream);
+  if (rc) return rc;
+  return dsa_topk_select(scores, stride, pos, n_q, k, max_ctx, topk, stream);
+}
+
+DSA_EXPORT int dsa_sparse_mla(const void* q, const void* c, int64_t n_kv_rows, const int32_t* cu, int n_req,
+                   const int32_t* bid, const int32_t* topk, int64_t n_q, int H, int dqk, int dv,
+                   int k, float scale, const int32_t* block_table, int max_pages, int page_size,
+                   void* o, float* lse, dsa_stream_t stream) {
+  return dsa::sparse_mla(q, c, n_kv_rows, cu, n_req, bid, topk, n_q, H, dqk, dv, k, scale,
+                         block_table, max_pages, page_size, o, lse,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

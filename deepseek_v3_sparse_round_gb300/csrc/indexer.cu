@@ -1,0 +1,491 @@
+// Lightning-indexer scores on tcgen05 tensor cores.
+//
+//   I[t, s] = sum_h w[t, h] * ReLU( q_idx[t, h, :] . k_idx[row(b_t, s), :] ),  0 <= s <= pos_t
+//
+// "[RFC]: Parallel strategy for Deepseek v3.2 like models" (comments) names this history scan
+// the model's bottleneck; sequence sharding divides it by sp. Design for sm_103a:
+//
+//  * The contraction is D[s, (t,h)] = K[s, :] . Q[(t,h), :] with the KEYS on the UMMA M side
+//    (128 keys per tile, one TMEM lane each) and (query, head) pairs on N. Every epilogue
+//    thread then owns one key and reduces its row over heads entirely in registers:
+//    sum_h w[t,h] * max(D, 0). Per-head logits never leave TMEM; only the head-reduced fp32
+//    score reaches global memory.
+//  * One CTA works on a "group" of up to 2 x 256/Hi consecutive queries of one request
+//    (8 queries for Hi = 64). Their Q rows (512 x Di bf16) stay in shared memory while the key
+//    tiles stream through a 3-stage TMA ring. Each key tile feeds two MMAs (queries 0-3 and
+//    4-7) into two TMEM accumulators of 256 fp32 columns, so one key tile is reused by 8
+//    queries and the second accumulator's MMA hides the first one's epilogue.
+//  * Warp roles: warps 0-3 and 4-7 are the epilogues of accumulators 0 and 1 (TMEM lane
+//    quadrant = warp % 4), warp 8 issues TMA, warp 9 issues tcgen05.mma.
+//  * Persistent grid (one CTA per SM). A one-CTA planning kernel cuts the queries into groups
+//    (never across a request, at most 8 queries) and each group's causal key range into
+//    chunks of whole 128-key tiles; CTA i takes chunks i, i + grid, ... Only tiles that hold
+//    some causal key are computed; keys past a query's position are masked in the epilogue.
+//  * Key rows: contiguous (cu[b] + s, the logical order after the rerange) or paged
+//    (block_table, 64-token pages, one TMA box per page).
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+#include "status.cuh"
+#include "tmap.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kPlanThreads = 1024;
+constexpr int kKeysPerTile = 128;
+constexpr int kPageRows = 64;          // TMA box height for keys (also the page size)
+
+struct Plan {
+  int total_units;
+  int chunk_tiles;
+  int n_groups;
+  int error;
+};
+
+// Workspace carving for the schedule (scores, when owned by the workspace, follow it).
+struct PlanLayout {
+  size_t plan_off, groups_off, unit_off, t0_off, bytes;
+  explicit PlanLayout(int64_t n_q) {
+    auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    const size_t nq = static_cast<size_t>(n_q > 0 ? n_q : 1);
+    plan_off = 0;
+    groups_off = up(sizeof(Plan));
+    unit_off = up(groups_off + nq * sizeof(int4));
+    t0_off = up(unit_off + (nq + 1) * sizeof(int32_t));
+    bytes = up(t0_off + nq * sizeof(int32_t));
+  }
+};
+
+template <int HI, int DI>
+struct Shape {
+  static constexpr int kQPA = 256 / HI;                  // queries per accumulator
+  static constexpr int kGQ = 2 * kQPA;                   // queries per group
+  static constexpr int kBRows = kGQ * HI;                // 512 rows of Q per group
+  static constexpr int kAtomElems = DI >= 64 ? 64 : DI;  // elements per swizzled row
+  static constexpr int kAtomBytes = kAtomElems * 2;      // 128 (SW128) or 64 (SW64)
+  static constexpr int kAtoms = DI / kAtomElems;
+  static constexpr uint32_t kSwz = DI >= 64 ? kSwizzle128B : kSwizzle64B;
+  static constexpr CUtensorMapSwizzle kTmaSwz =
+      DI >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  static constexpr int kSBO = 8 * kAtomBytes;            // 8-row core-matrix group stride
+  static constexpr int kAStage = kKeysPerTile * DI * 2;
+  static constexpr int kAAtom = kKeysPerTile * kAtomBytes;
+  static constexpr int kBAtom = kBRows * kAtomBytes;
+  static constexpr int kStages = DI >= 64 ? 3 : 4;
+  static constexpr int kBBytes = kBRows * DI * 2;
+  static constexpr int kKSteps = DI / 16;
+  static constexpr int kStepsPerAtom = kAtomElems / 16;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kStages * kAStage;
+  static constexpr int kOffW = kOffB + kBBytes;          // fp32 [kGQ][HI]
+  static constexpr int kOffPos = kOffW + kGQ * HI * 4;   // int32 [kGQ]
+  static constexpr int kOffBar = (kOffPos + kGQ * 4 + 7) & ~7;
+  static constexpr int kNumBars = 2 * kStages + 10;
+  static constexpr int kOffTmem = kOffBar + kNumBars * 8;
+  static constexpr int kOffAbort = kOffTmem + 4;
+  static constexpr int kSmem = kOffAbort + 4;
+  static constexpr int kThreads = 320;                   // 8 epilogue warps + TMA + MMA
+  static_assert(kSmem <= 232448, "shared memory budget");
+  static_assert(kOffB % 1024 == 0 && kAStage % 1024 == 0 && kBAtom % 1024 == 0, "alignment");
+};
+
+// ------------------------------------------------------------------------------------------
+// Planning: groups of <= GQ consecutive queries of one request, chunks of whole key tiles.
+__device__ __forceinline__ uint32_t plan_scan(uint32_t v, uint32_t* wt, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int kW = kPlanThreads / 32;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wt[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = lane < kW ? wt[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    wt[lane] = w;
+  }
+  __syncthreads();
+  const uint32_t before = (warp > 0 ? wt[warp - 1] : 0u) + x - v;
+  *total = wt[kW - 1];
+  __syncthreads();
+  return before;
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+indexer_plan_kernel(const int32_t* __restrict__ pos, const int32_t* __restrict__ bid, int n_q,
+                    int n_req, int max_ctx, int gq, int n_ctas, Plan* plan, int4* groups,
+                    int32_t* unit_start, int32_t* t0_list) {
+  __shared__ uint32_t wt[32];
+  const int per = (n_q + kPlanThreads - 1) / kPlanThreads;
+  const int lo = min(static_cast<int>(threadIdx.x) * per, n_q), hi = min(lo + per, n_q);
+  auto starts = [&](int t) {
+    return t == 0 || (t % gq) == 0 || __ldg(bid + t) != __ldg(bid + t - 1);
+  };
+  uint32_t cnt = 0;
+  for (int t = lo; t < hi; ++t) cnt += starts(t);
+  uint32_t n_groups;
+  uint32_t g = plan_scan(cnt, wt, &n_groups);
+  for (int t = lo; t < hi; ++t)
+    if (starts(t)) t0_list[g++] = t;
+  __syncthreads();
+
+  const int G = static_cast<int>(n_groups);
+  const int pg = (G + kPlanThreads - 1) / kPlanThreads;
+  const int glo = min(static_cast<int>(threadIdx.x) * pg, G), ghi = min(glo + pg, G);
+  uint32_t tiles_sum = 0;
+  bool bad = false;
+  for (int gi = glo; gi < ghi; ++gi) {
+    const int t0 = t0_list[gi], t1 = gi + 1 < G ? t0_list[gi + 1] : n_q;
+    int b = __ldg(bid + t0);
+    if (b < 0 || b >= n_req) { bad = true; b = b < 0 ? 0 : n_req - 1; }
+    int pmax = -1;
+    for (int t = t0; t < t1; ++t) pmax = max(pmax, __ldg(pos + t));
+    if (pmax >= max_ctx) { bad = true; pmax = max_ctx - 1; }
+    const int tiles = pmax >= 0 ? pmax / kKeysPerTile + 1 : 0;
+    groups[gi] = make_int4(t0, t1 - t0, b, pmax);
+    tiles_sum += tiles;
+  }
+  if (bad) report_device_error(kErrBadIndex);
+  uint32_t total_tiles;
+  plan_scan(tiles_sum, wt, &total_tiles);
+  // Chunk size: about six chunks per CTA, between 1 and 64 tiles.
+  int chunk = static_cast<int>((total_tiles + static_cast<uint32_t>(n_ctas) * 6 - 1) /
+                               (static_cast<uint32_t>(n_ctas) * 6));
+  chunk = max(1, min(chunk, 64));
+  uint32_t units = 0;
+  for (int gi = glo; gi < ghi; ++gi) {
+    const int pmax = groups[gi].w;
+    const int tiles = pmax >= 0 ? pmax / kKeysPerTile + 1 : 0;
+    units += (tiles + chunk - 1) / chunk;
+  }
+  uint32_t total_units;
+  uint32_t u = plan_scan(units, wt, &total_units);
+  for (int gi = glo; gi < ghi; ++gi) {
+    unit_start[gi] = static_cast<int32_t>(u);
+    const int pmax = groups[gi].w;
+    const int tiles = pmax >= 0 ? pmax / kKeysPerTile + 1 : 0;
+    u += (tiles + chunk - 1) / chunk;
+  }
+  if (threadIdx.x == 0) {
+    unit_start[G] = static_cast<int32_t>(total_units);
+    plan->total_units = static_cast<int>(total_units);
+    plan->chunk_tiles = chunk;
+    plan->n_groups = G;
+    plan->error = 0;
+  }
+}
+
+// The unit's group: largest g with unit_start[g] <= u (unit_start non-decreasing, size G+1).
+__device__ __forceinline__ int find_group(const int32_t* __restrict__ unit_start, int G, int u) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(unit_start + mid) <= u) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+struct Unit {
+  int t0, count, b, pmax, tile_begin, tile_end;
+};
+
+__device__ __forceinline__ Unit load_unit(const Plan* plan, const int4* groups,
+                                          const int32_t* unit_start, int u) {
+  const int G = plan->n_groups, chunk = plan->chunk_tiles;
+  const int g = find_group(unit_start, G, u);
+  const int4 rec = __ldg(groups + g);
+  const int c = u - __ldg(unit_start + g);
+  const int tiles = rec.w / kKeysPerTile + 1;
+  Unit x;
+  x.t0 = rec.x; x.count = rec.y; x.b = rec.z; x.pmax = rec.w;
+  x.tile_begin = c * chunk;
+  x.tile_end = min(tiles, x.tile_begin + chunk);
+  return x;
+}
+
+struct KeyRows {
+  const int32_t* cu;
+  const int32_t* block_table;   // nullptr: contiguous
+  int max_pages;
+  int n_pages;                  // pages in the pool (paged mode)
+  int64_t n_rows;
+};
+
+// Row of the first key of the 64-key sub-tile that starts at position s (s % 64 == 0 when
+// paged). Out-of-range pages map to a row past the tensor, which TMA fills with zeros.
+__device__ __forceinline__ int32_t subtile_row(const KeyRows& kr, int b, int s) {
+  if (kr.block_table == nullptr) return __ldg(kr.cu + b) + s;
+  const int pi = s / kPageRows;
+  const int page = pi < kr.max_pages ? __ldg(kr.block_table + static_cast<int64_t>(b) * kr.max_pages + pi) : -1;
+  if (page < 0 || page >= kr.n_pages) return static_cast<int32_t>(kr.n_rows);
+  return page * kPageRows;
+}
+
+template <int HI, int DI>
+__global__ void __launch_bounds__(Shape<HI, DI>::kThreads, 1)
+indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+               const float* __restrict__ w, const int32_t* __restrict__ pos, KeyRows kr,
+               const Plan* __restrict__ plan, const int4* __restrict__ groups,
+               const int32_t* __restrict__ unit_start, float* __restrict__ scores,
+               int64_t stride, int max_ctx, int n_q) {
+  using S = Shape<HI, DI>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t warp = warp_id(), lane = lane_id();
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + S::kOffAbort);
+  auto bar = [&](int i) { return sbase + S::kOffBar + 8u * static_cast<uint32_t>(i); };
+  // barrier indices
+  const int kAFull = 0, kAEmpty = S::kStages, kBFull = 2 * S::kStages, kBEmpty = kBFull + 1,
+            kAccFull = kBFull + 2, kAccEmpty = kBFull + 4, kWFull = kBFull + 6,
+            kWEmpty = kBFull + 8;
+
+  if ((sbase & 1023u) != 0) {                          // swizzle atoms need 1 KB alignment
+    if (threadIdx.x == 0) report_device_error(kErrBadIndex | 0xA1u);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S::kStages; ++i) { mbar_init(bar(kAFull + i), 1); mbar_init(bar(kAEmpty + i), 1); }
+    mbar_init(bar(kBFull), 1);
+    mbar_init(bar(kBEmpty), 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bar(kAccFull + h), 1);
+      mbar_init(bar(kAccEmpty + h), 4);
+      mbar_init(bar(kWFull + h), 128);
+      mbar_init(bar(kWEmpty + h), 128);
+    }
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc<512>(sbase + S::kOffTmem);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + S::kOffTmem);
+  const int total_units = plan->total_units;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_q);
+      int stage = 0;
+      uint32_t phase = 0, b_uses = 0;
+      for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+        const Unit un = load_unit(plan, groups, unit_start, u);
+        if (!mbar_wait(bar(kBEmpty), (b_uses & 1u) ^ 1u, 0x01, abort_flag)) break;
+        ++b_uses;
+        mbar_expect_tx(bar(kBFull), S::kBBytes);
+        for (int a = 0; a < S::kAtoms; ++a)
+          for (int hh = 0; hh < S::kBRows / 256; ++hh)
+            tma_load_2d(sbase + S::kOffB + a * S::kBAtom + hh * 256 * S::kAtomBytes, &tm_q,
+                        a * S::kAtomElems, un.t0 * HI + hh * 256, bar(kBFull));
+        bool ok = true;
+        for (int tile = un.tile_begin; tile < un.tile_end; ++tile) {
+          if (!mbar_wait(bar(kAEmpty + stage), phase ^ 1u, 0x02, abort_flag)) { ok = false; break; }
+          mbar_expect_tx(bar(kAFull + stage), S::kAStage);
+          const uint32_t dst = sbase + S::kOffA + stage * S::kAStage;
+          for (int sub = 0; sub < kKeysPerTile / kPageRows; ++sub) {
+            const int32_t row = subtile_row(kr, un.b, tile * kKeysPerTile + sub * kPageRows);
+            for (int a = 0; a < S::kAtoms; ++a)
+              tma_load_2d(dst + a * S::kAAtom + sub * kPageRows * S::kAtomBytes, &tm_k,
+                          a * S::kAtomElems, row, bar(kAFull + stage));
+          }
+          if (++stage == S::kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, b_uses = 0, acc_uses[2] = {0u, 0u};
+      for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
+        const Unit un = load_unit(plan, groups, unit_start, u);
+        if (!mbar_wait(bar(kBFull), b_uses & 1u, 0x03, abort_flag)) break;
+        ++b_uses;
+        tc_fence_after();
+        int nq[2];
+        uint32_t idesc[2];
+        for (int h = 0; h < 2; ++h) {
+          nq[h] = max(0, min(un.count - h * S::kQPA, S::kQPA));
+          uint32_t n_cols = static_cast<uint32_t>(nq[h] * HI);
+          n_cols = (n_cols + 15u) & ~15u;
+          idesc[h] = idesc_bf16(128, n_cols < 16u ? 16u : n_cols, 0, 0);
+        }
+        bool ok = true;
+        for (int tile = un.tile_begin; tile < un.tile_end && ok; ++tile) {
+          if (!mbar_wait(bar(kAFull + stage), phase, 0x04, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_base = sbase + S::kOffA + stage * S::kAStage;
+          for (int h = 0; h < 2; ++h) {
+            if (nq[h] == 0) continue;
+            if (!mbar_wait(bar(kAccEmpty + h), (acc_uses[h] & 1u) ^ 1u, 0x05, abort_flag)) { ok = false; break; }
+            ++acc_uses[h];
+            tc_fence_after();
+            const uint32_t b_base = sbase + S::kOffB + h * S::kQPA * HI * S::kAtomBytes;
+#pragma unroll
+            for (int kk = 0; kk < S::kKSteps; ++kk) {
+              const int a = kk / S::kStepsPerAtom, off = (kk % S::kStepsPerAtom) * 32;
+              const uint64_t da = smem_desc(a_base + a * S::kAAtom + off, 16, S::kSBO, S::kSwz);
+              const uint64_t db = smem_desc(b_base + a * S::kBAtom + off, 16, S::kSBO, S::kSwz);
+              umma_ss(tmem + static_cast<uint32_t>(h * 256), da, db, idesc[h], kk > 0 ? 1u : 0u);
+            }
+            umma_commit(bar(kAccFull + h));
+          }
+          umma_commit(bar(kAEmpty + stage));          // key tile free once both MMAs finish
+          if (++stage == S::kStages) { stage = 0; phase ^= 1u; }
+        }
+        umma_commit(bar(kBEmpty));                    // Q tile free once the unit's MMAs finish
+        if (!ok) break;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogues (warps 0-7)
+    const int h = static_cast<int>(warp >> 2);        // accumulator / query half
+    const uint32_t quad = warp & 3u;                  // TMEM lane quadrant
+    const int row = static_cast<int>(quad * 32u + lane);  // key inside the tile
+    const uint32_t t_acc = tmem + ((quad * 32u) << 16) + static_cast<uint32_t>(h * 256);
+    float* sw = reinterpret_cast<float*>(smem + S::kOffW) + h * S::kQPA * HI;
+    int* spos = reinterpret_cast<int*>(smem + S::kOffPos) + h * S::kQPA;
+    uint32_t acc_uses = 0, w_uses = 0;
+    for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
+      const Unit un = load_unit(plan, groups, unit_start, u);
+      const int nq = max(0, min(un.count - h * S::kQPA, S::kQPA));
+      if (nq == 0) continue;
+      const int tq0 = un.t0 + h * S::kQPA;
+      // The half's four warps share w / pos in smem: wait until all 128 threads finished with
+      // the previous unit's copy, write this unit's, wait until every thread has written.
+      if (!warp_wait(bar(kWEmpty + h), (w_uses & 1u) ^ 1u, 0x07, abort_flag)) break;
+      for (int i = static_cast<int>(quad * 32u + lane); i < S::kQPA * HI; i += 128) {
+        const int q = i / HI;
+        sw[i] = q < nq ? __ldg(w + static_cast<int64_t>(tq0 + q) * HI + (i % HI)) : 0.f;
+      }
+      for (int q = static_cast<int>(quad * 32u + lane); q < S::kQPA; q += 128)
+        spos[q] = q < nq ? __ldg(pos + tq0 + q) : -1;
+      mbar_arrive(bar(kWFull + h));
+      if (!warp_wait(bar(kWFull + h), w_uses & 1u, 0x08, abort_flag)) break;
+      ++w_uses;
+      bool ok = true;
+      for (int tile = un.tile_begin; tile < un.tile_end; ++tile) {
+        if (!warp_wait(bar(kAccFull + h), acc_uses & 1u, 0x06, abort_flag)) { ok = false; break; }
+        ++acc_uses;
+        tc_fence_after();
+        float acc[S::kQPA];
+#pragma unroll
+        for (int q = 0; q < S::kQPA; ++q) acc[q] = 0.f;
+#pragma unroll
+        for (int c0 = 0; c0 < S::kQPA * HI; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(t_acc + static_cast<uint32_t>(c0), v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int col = c0 + j, q = col / HI;
+            acc[q] = fmaf(sw[col], fmaxf(__uint_as_float(v[j]), 0.f), acc[q]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kAccEmpty + h));
+        const int s = tile * kKeysPerTile + row;
+#pragma unroll
+        for (int q = 0; q < S::kQPA; ++q) {
+          if (q < nq && s <= spos[q] && s < max_ctx)
+            scores[static_cast<int64_t>(tq0 + q) * stride + s] = acc[q];
+        }
+      }
+      mbar_arrive(bar(kWEmpty + h));                  // done reading this unit's w / pos
+      if (!ok) break;
+    }
+  }
+
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc<512>(tmem);
+  }
+}
+
+template <int HI, int DI>
+int launch_indexer(const void* q_idx, const float* w, const void* k_idx, int64_t n_kv_rows,
+                   const int32_t* pos, const int32_t* bid, int64_t n_q, int n_req, int max_ctx,
+                   const KeyRows& kr, float* scores, int64_t stride, Plan* plan, int4* groups,
+                   int32_t* unit_start, int32_t* t0_list, int n_ctas, cudaStream_t stream) {
+  using S = Shape<HI, DI>;
+  const int n_req_eff = kr.block_table ? n_req : n_req;
+  indexer_plan_kernel<<<1, kPlanThreads, 0, stream>>>(pos, bid, static_cast<int>(n_q), n_req_eff,
+                                                      max_ctx, S::kGQ, n_ctas, plan, groups,
+                                                      unit_start, t0_list);
+  DSA_CHECK_CUDA(cudaGetLastError());
+  CUtensorMap tk, tq;
+  int rc = make_tmap_bf16_2d(&tk, k_idx, static_cast<uint64_t>(n_kv_rows), DI, DI * 2,
+                             S::kAtomElems, kPageRows, S::kTmaSwz);
+  if (rc) return rc;
+  rc = make_tmap_bf16_2d(&tq, q_idx, static_cast<uint64_t>(n_q * HI), DI, DI * 2, S::kAtomElems,
+                         256, S::kTmaSwz);
+  if (rc) return rc;
+  DSA_CHECK_CUDA(cudaFuncSetAttribute(indexer_kernel<HI, DI>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmem));
+  indexer_kernel<HI, DI><<<n_ctas, S::kThreads, S::kSmem, stream>>>(
+      tk, tq, w, pos, kr, plan, groups, unit_start, scores, stride, max_ctx,
+      static_cast<int>(n_q));
+  DSA_CHECK_CUDA(cudaGetLastError());
+  return DSA_OK;
+}
+
+}  // namespace
+
+size_t indexer_plan_bytes(int64_t n_q) { return PlanLayout(n_q).bytes; }
+
+int indexer_scores(const void* q_idx, const float* w, const void* k_idx, int64_t n_kv_rows,
+                   const int32_t* cu, const int32_t* pos, const int32_t* bid, int64_t n_q, int n_req,
+                   int Hi, int Di, int max_ctx, const int32_t* block_table, int max_pages,
+                   int page_size, float* scores, int64_t stride, void* ws, size_t ws_bytes,
+                   cudaStream_t stream) {
+  if (n_q < 0 || max_ctx < 1 || n_kv_rows < 0)
+    return fail(DSA_ERR_INVALID, "indexer: need n_q >= 0, max_ctx >= 1, n_kv_rows >= 0");
+  if (n_q == 0) return DSA_OK;
+  if (!q_idx || !w || !k_idx || !pos || !bid || !scores)
+    return fail(DSA_ERR_INVALID, "indexer: null pointer");
+  if (!block_table && !cu) return fail(DSA_ERR_INVALID, "indexer: need cu or block_table");
+  if (block_table && (page_size != kPageRows || max_pages < 1))
+    return fail(DSA_ERR_UNSUPPORTED, "indexer: paged KV needs page_size 64 (got %d)", page_size);
+  if (n_q > (1 << 24) || n_kv_rows >= (1ll << 31) || n_q * Hi >= (1ll << 31))
+    return fail(DSA_ERR_UNSUPPORTED, "indexer: sizes beyond 32-bit TMA coordinates");
+  if (stride < max_ctx) return fail(DSA_ERR_INVALID, "indexer: score stride < max_ctx");
+  const PlanLayout L(n_q);
+  if (!ws || ws_bytes < L.bytes)
+    return fail(DSA_ERR_WORKSPACE, "indexer: workspace of %zu bytes < %zu", ws_bytes, L.bytes);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  Plan* plan = reinterpret_cast<Plan*>(base + L.plan_off);
+  int4* groups = reinterpret_cast<int4*>(base + L.groups_off);
+  int32_t* unit_start = reinterpret_cast<int32_t*>(base + L.unit_off);
+  int32_t* t0_list = reinterpret_cast<int32_t*>(base + L.t0_off);
+
+  const int n_ctas = num_sms_cached();
+  KeyRows kr{cu, block_table, max_pages, 0, n_kv_rows};
+  if (block_table) kr.n_pages = static_cast<int>(n_kv_rows / kPageRows);
+  if (Hi == 64 && Di == 128)
+    return launch_indexer<64, 128>(q_idx, w, k_idx, n_kv_rows, pos, bid, n_q, n_req, max_ctx, kr,
+                                   scores, stride, plan, groups, unit_start, t0_list, n_ctas,
+                                   stream);
+  if (Hi == 4 && Di == 32)
+    return launch_indexer<4, 32>(q_idx, w, k_idx, n_kv_rows, pos, bid, n_q, n_req, max_ctx, kr,
+                                 scores, stride, plan, groups, unit_start, t0_list, n_ctas, stream);
+  return fail(DSA_ERR_UNSUPPORTED, "indexer: (Hi, Di) = (%d, %d) not built; supported (64, 128), "
+                                   "(4, 32)", Hi, Di);
+}
+
+cudaError_t indexer_read_errors(uint32_t* flags) { return read_and_clear_device_error(flags); }
+
+}  // namespace dsa

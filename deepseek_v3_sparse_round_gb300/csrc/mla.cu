@@ -1,0 +1,460 @@
+// Sparse MLA on tcgen05 tensor cores: every shard query attends, with all heads at once, to the
+// latent rows its top-k selected ("[RFC]: Parallel strategy for Deepseek v3.2 like models":
+// "full head on mla part, high tflops").
+//
+//   S[h, j] = scale * q[t, h, :] . c[row_j, :]          (dqk = 576 = 512 latent + 64 rope)
+//   o[t, h, :] = sum_j softmax_j(S[h, :]) c[row_j, 0:dv]  (dv = 512), lse[t, h] = ln sum exp S
+//
+// GB300 mapping (H = 128, dqk = 576, dv = 512): the fp32 output block O = 128 x 512 alone fills
+// a whole SM's tensor memory (128 lanes x 512 columns), so each query runs on a cluster of two
+// CTAs. CTA c owns
+//   * half of the QK contraction: dims [288c, 288c + 288) -- its slice of Q lives in TMEM
+//     (144 columns, the MMA's A operand) and its slice of every gathered key row in smem,
+//   * half of the output: dims [256c, 256c + 256) of O (256 TMEM columns).
+// Each 64-key tile: TMA tile::gather4 brings the selected rows (5 swizzled 64-column atoms per
+// CTA, 40 KB) into a 4-stage ring; one MMA chain computes the CTA's partial S (128 x 64 fp32,
+// 64 TMEM columns); the softmax warps swap partial tiles with the peer CTA through distributed
+// shared memory, add them (both CTAs obtain bit-identical S), run the online softmax (exp2,
+// running maximum, rescaling O only when the maximum grows by more than 2^8), write P as bf16
+// into a swizzled smem tile and the MMA warp accumulates O += P . V, where V is the same
+// gathered tile read MN-major. QK(j+1) is issued before PV(j) so the tensor pipe works while
+// the softmax of tile j runs.
+//
+// Small heads (H <= 128 with dv <= 256, e.g. H = 8, dqk = 80, dv = 64) run the same code on a
+// single CTA that owns the whole contraction and output.
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+#include "status.cuh"
+#include "tmap.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kTileKeys = 64;
+constexpr int kMaxK = 4096;
+constexpr int kPageRows = 64;
+
+template <int H, int DQK, int DV>
+struct MlaShape {
+  static constexpr int kSplit = DV > 256 ? 2 : 1;           // CTAs per query
+  static constexpr int kAtomsTotal = (DQK + 63) / 64;        // 64-column swizzle atoms per row
+  static constexpr int kQKSteps = DQK / 16 / kSplit;         // k-steps (16 dims) per CTA
+  static constexpr int kQDims = kQKSteps * 16;               // dims of Q per CTA
+  static constexpr int kQCols = ((kQDims / 2) + 15) / 16 * 16;  // TMEM columns for Q
+  static constexpr int kDVc = DV / kSplit;                   // output dims per CTA
+  static constexpr int kVAtoms = (kDVc + 63) / 64;
+  // Atoms a CTA gathers: enough to cover its QK dims and its V dims.
+  // (CTA 1's slice starts kQDims % 64 columns into an atom; both CTAs need the same count.)
+  static constexpr int kGAtoms =
+      kSplit == 2 ? ((kQDims % 64) + kQDims + 63) / 64 : kAtomsTotal;
+  static constexpr int kAtomBytes = kTileKeys * 128;         // 64 rows x 128 B
+  static constexpr int kStageBytes = kGAtoms * kAtomBytes;
+  static constexpr int kStages = 4;
+  static constexpr int kPBytes = 128 * 128;                  // 128 rows x 64 keys bf16
+  static constexpr int kXBytes = kSplit == 2 ? 128 * kTileKeys * 4 : 0;
+  static constexpr int kOffKV = 0;
+  static constexpr int kOffP = kStages * kStageBytes;
+  static constexpr int kOffX = kOffP + 2 * kPBytes;
+  static constexpr int kOffMask = kOffX + kXBytes;
+  static constexpr int kOffBar = kOffMask + (kMaxK / kTileKeys) * 8;
+  static constexpr int kNumBars = 2 * kStages + 12;
+  static constexpr int kOffTmem = kOffBar + kNumBars * 8;
+  static constexpr int kOffAbort = kOffTmem + 4;
+  static constexpr int kOffNTiles = kOffAbort + 4;
+  static constexpr int kSmem = kOffNTiles + 8;
+  // TMEM columns: O | S | Q
+  static constexpr int kColO = 0;
+  static constexpr int kColS = kDVc < 64 ? 64 : kDVc;
+  static constexpr int kColQ = kColS + kTileKeys;
+  static constexpr int kTmemCols = (kColQ + kQCols) <= 256 ? 256 : 512;
+  static constexpr int kThreads = 192;                       // 4 softmax warps + TMA + MMA
+  static_assert(H <= 128, "heads per CTA");
+  static_assert(DQK % (16 * kSplit) == 0, "qk split");
+  static_assert(kColQ + kQCols <= 512, "TMEM budget");
+  static_assert(kSmem <= 232448, "smem budget");
+  static_assert(kDVc % 16 == 0 && kDVc <= 256, "PV N");
+  // For the split case, CTA 1's V atoms must start where its gathered atoms start.
+  static_assert(kSplit == 1 || (kDVc % 64 == 0 && kQDims / 64 == kDVc / 64), "layout");
+};
+
+struct KvMap {
+  const int32_t* cu;           // contiguous mode
+  const int32_t* block_table;  // paged mode (nullptr: contiguous)
+  int max_pages;
+  int n_req;
+  int64_t n_rows;
+};
+
+// KV row of position s in request b, or n_rows (read as zeros) when it is not addressable.
+__device__ __forceinline__ int32_t kv_row(const KvMap& m, int b, int s, bool* bad) {
+  if (s < 0) return static_cast<int32_t>(m.n_rows);
+  int64_t r;
+  if (m.block_table == nullptr) {
+    r = static_cast<int64_t>(__ldg(m.cu + b)) + s;
+  } else {
+    const int pi = s / kPageRows;
+    const int page = pi < m.max_pages ? __ldg(m.block_table + static_cast<int64_t>(b) * m.max_pages + pi) : -1;
+    r = page < 0 ? m.n_rows : static_cast<int64_t>(page) * kPageRows + s % kPageRows;
+  }
+  if (r < 0 || r >= m.n_rows) { *bad = true; return static_cast<int32_t>(m.n_rows); }
+  return static_cast<int32_t>(r);
+}
+
+template <int H, int DQK, int DV>
+__global__ void __launch_bounds__(MlaShape<H, DQK, DV>::kThreads, 1)
+sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16* __restrict__ q,
+                  const int32_t* __restrict__ bid, const int32_t* __restrict__ topk, int k,
+                  KvMap kv, float scale_log2, __nv_bfloat16* __restrict__ o,
+                  float* __restrict__ lse) {
+  using S = MlaShape<H, DQK, DV>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t warp = warp_id(), lane = lane_id();
+  const uint32_t crank = S::kSplit == 2 ? cluster_ctarank() : 0u;
+  const uint32_t peer = crank ^ 1u;
+  const int64_t t = blockIdx.x / S::kSplit;
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + S::kOffAbort);
+  uint64_t* masks = reinterpret_cast<uint64_t*>(smem + S::kOffMask);
+  auto bar = [&](int i) { return sbase + S::kOffBar + 8u * static_cast<uint32_t>(i); };
+  const int kKvFull = 0, kKvEmpty = S::kStages, kQReady = 2 * S::kStages, kSFull = kQReady + 1,
+            kSEmpty = kQReady + 2, kPFull = kQReady + 3, kPEmpty = kQReady + 5,
+            kOReady = kQReady + 7, kXFull = kQReady + 8, kXFree = kQReady + 9,
+            kOFinal = kQReady + 10;
+
+  const bool aligned = (sbase & 1023u) == 0;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S::kStages; ++i) { mbar_init(bar(kKvFull + i), 1); mbar_init(bar(kKvEmpty + i), 1); }
+    mbar_init(bar(kQReady), 128);
+    mbar_init(bar(kSFull), 1);
+    mbar_init(bar(kSEmpty), 4);
+    for (int i = 0; i < 2; ++i) { mbar_init(bar(kPFull + i), 128); mbar_init(bar(kPEmpty + i), 1); }
+    mbar_init(bar(kOReady), 1);
+    mbar_init(bar(kXFull), 128);
+    mbar_init(bar(kXFree), 128);
+    mbar_init(bar(kOFinal), 1);
+    *abort_flag = aligned ? 0u : 1u;
+    if (!aligned) report_device_error(kErrBadIndex | 0xB1u);
+    fence_mbar_init();
+  }
+  // Tile validity masks and the number of tiles up to the last valid entry.
+  const int32_t* trow = topk + t * k;
+  const int n_tiles_max = (k + kTileKeys - 1) / kTileKeys;
+  if (threadIdx.x == 0) *reinterpret_cast<volatile int*>(smem + S::kOffNTiles) = 0;
+  __syncthreads();
+  for (int tile = static_cast<int>(warp); tile < n_tiles_max; tile += S::kThreads / 32) {
+    const int j0 = tile * kTileKeys + static_cast<int>(lane), j1 = j0 + 32;
+    const bool v0 = j0 < k && __ldg(trow + j0) >= 0;
+    const bool v1 = j1 < k && __ldg(trow + j1) >= 0;
+    const uint32_t b0 = __ballot_sync(0xffffffffu, v0), b1 = __ballot_sync(0xffffffffu, v1);
+    if (lane == 0) {
+      masks[tile] = static_cast<uint64_t>(b0) | (static_cast<uint64_t>(b1) << 32);
+      if (b0 | b1) atomicMax(reinterpret_cast<int*>(smem + S::kOffNTiles), tile + 1);
+    }
+  }
+  if (warp == 0) tmem_alloc<S::kTmemCols>(sbase + S::kOffTmem);
+  __syncthreads();
+  if (S::kSplit == 2) cluster_sync();                  // the peer's barriers exist from here on
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + S::kOffTmem);
+  const int n_tiles = *reinterpret_cast<volatile int*>(smem + S::kOffNTiles);
+  const int b = __ldg(bid + t);
+  const bool b_ok = b >= 0 && b < kv.n_req;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------------ TMA gather producer
+    if (lane == 0) tma_prefetch_desc(&tm_c);
+    const int atom0 = S::kSplit == 2 ? static_cast<int>(crank) * (S::kQKSteps * 16 / 64) : 0;
+    bool bad = !b_ok;
+    int stage = 0, issued = 0;
+    uint32_t phase = 0;
+    for (int j = 0; j < n_tiles; ++j) {
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(bar(kKvEmpty + stage), phase ^ 1u, 0x11, abort_flag);
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      if (lane == 0) mbar_expect_tx(bar(kKvFull + stage), S::kStageBytes);
+      __syncwarp();
+      if (lane < kTileKeys / 4) {
+        int32_t rows[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int e = j * kTileKeys + static_cast<int>(lane) * 4 + i;
+          const int s = (e < k && b_ok) ? __ldg(trow + e) : -1;
+          rows[i] = kv_row(kv, b_ok ? b : 0, s, &bad);
+        }
+        const uint32_t dst = sbase + S::kOffKV + stage * S::kStageBytes + lane * 4 * 128;
+#pragma unroll
+        for (int a = 0; a < S::kGAtoms; ++a)
+          tma_gather4(dst + a * S::kAtomBytes, &tm_c, (atom0 + a) * 64, rows[0], rows[1], rows[2],
+                      rows[3], bar(kKvFull + stage));
+      }
+      ++issued;
+      if (++stage == S::kStages) { stage = 0; phase ^= 1u; }
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) report_device_error(kErrBadIndex);
+    if (*abort_flag && lane == 0) {                   // let issued copies land before exiting
+      for (int i = 0; i < S::kStages && i < issued; ++i) {
+        const int jl = issued - 1 - i;
+        const long long t0 = clock64();
+        while (!mbar_try_wait(bar(kKvFull + jl % S::kStages), (jl / S::kStages) & 1u) &&
+               clock64() - t0 < kWaitLimitCycles) {
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_qk = idesc_bf16(128, kTileKeys, 0, 0);
+      const uint32_t idesc_pv = idesc_bf16(128, S::kDVc, 0, 1);
+      const int kstep0 = S::kSplit == 2 ? static_cast<int>(crank) * S::kQKSteps : 0;
+      const int atom0 = S::kSplit == 2 ? static_cast<int>(crank) * (S::kQKSteps * 16 / 64) : 0;
+      auto pv = [&](int j) -> bool {
+        if (!mbar_wait(bar(kPFull + (j & 1)), (j >> 1) & 1, 0x12, abort_flag)) return false;
+        tc_fence_after();
+        const int st = j % S::kStages;
+        const uint32_t p_base = sbase + S::kOffP + (j & 1) * S::kPBytes;
+        const uint32_t v_base = sbase + S::kOffKV + st * S::kStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTileKeys / 16; ++kk) {
+          const uint64_t da = smem_desc(p_base + kk * 32, 16, 1024, kSwizzle128B);
+          const uint64_t dv = smem_desc(v_base + kk * 2048, S::kAtomBytes, 1024, kSwizzle128B);
+          umma_ss(tmem + S::kColO, da, dv, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(bar(kPEmpty + (j & 1)));
+        umma_commit(bar(kKvEmpty + st));
+        umma_commit(bar(kOReady));
+        return true;
+      };
+      bool ok = mbar_wait(bar(kQReady), 0, 0x13, abort_flag);
+      tc_fence_after();
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int st = j % S::kStages;
+        if (!mbar_wait(bar(kKvFull + st), (j / S::kStages) & 1, 0x14, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(bar(kSEmpty), (j & 1) ^ 1, 0x15, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t kv_base = sbase + S::kOffKV + st * S::kStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < S::kQKSteps; ++kk) {
+          const int g = kstep0 + kk;                   // global 16-dim step
+          const int a = g / 4 - atom0, off = (g % 4) * 32;
+          const uint64_t db = smem_desc(kv_base + a * S::kAtomBytes + off, 16, 1024, kSwizzle128B);
+          umma_ts(tmem + S::kColS, tmem + S::kColQ + kk * 8, db, idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(bar(kSFull));
+        if (j > 0 && !pv(j - 1)) { ok = false; break; }
+      }
+      if (ok && n_tiles > 0 && pv(n_tiles - 1)) umma_commit(bar(kOFinal));
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax + epilogue
+    const int h = static_cast<int>(threadIdx.x);     // head row == TMEM lane
+    const uint32_t lane_base = (warp * 32u) << 16;
+    // Q slice -> TMEM (A operand of QK).
+    {
+      const int d0 = S::kSplit == 2 ? static_cast<int>(crank) * S::kQDims : 0;
+      const uint4* src = reinterpret_cast<const uint4*>(q + (t * H + (h < H ? h : 0)) * DQK + d0);
+#pragma unroll
+      for (int c0 = 0; c0 < S::kQCols; c0 += 16) {
+        uint32_t r[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int e = (c0 + 4 * i) * 2;              // first element of this 16-byte chunk
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (h < H && e < S::kQDims) v = __ldg(src + e / 8);
+          r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
+        }
+        tmem_st16(tmem + lane_base + S::kColQ + c0, r);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(kQReady));
+    }
+    float m_run = -INFINITY, l_run = 0.f;
+    const uint32_t x_row = sbase + S::kOffX + static_cast<uint32_t>(h) * 16u;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      if (!warp_wait(bar(kSFull), j & 1, 0x16, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      float sv[kTileKeys];
+      {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_base + S::kColS, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sv[i] = __uint_as_float(r[i]);
+        tmem_ld32(tmem + lane_base + S::kColS + 32, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sv[32 + i] = __uint_as_float(r[i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kSEmpty));
+      if (S::kSplit == 2) {
+        // partial tile -> peer, then add the peer's partial tile (identical sum on both CTAs)
+        if (!warp_wait(bar(kXFree), (j & 1) ^ 1, 0x17, abort_flag)) { ok = false; break; }
+#pragma unroll
+        for (int c = 0; c < kTileKeys / 4; ++c)
+          st_cluster_v4(x_row + c * 128 * 16, peer, sv[4 * c], sv[4 * c + 1], sv[4 * c + 2],
+                        sv[4 * c + 3]);
+        mbar_arrive_cluster(bar(kXFull), peer);
+        if (!warp_wait_cluster(bar(kXFull), j & 1, 0x18, abort_flag)) { ok = false; break; }
+        const float4* xr = reinterpret_cast<const float4*>(smem + S::kOffX) + h;
+#pragma unroll
+        for (int c = 0; c < kTileKeys / 4; ++c) {
+          const float4 v = xr[c * 128];
+          sv[4 * c] += v.x; sv[4 * c + 1] += v.y; sv[4 * c + 2] += v.z; sv[4 * c + 3] += v.w;
+        }
+        mbar_arrive_cluster(bar(kXFree), peer);
+      }
+      // online softmax in the log2 domain
+      const uint64_t mk = masks[j];
+      float mt = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kTileKeys; ++i) {
+        sv[i] = ((mk >> i) & 1ull) ? sv[i] * scale_log2 : -INFINITY;
+        mt = fmaxf(mt, sv[i]);
+      }
+      float alpha = 1.f;
+      if (m_run == -INFINITY) {
+        m_run = mt;                                    // first tile with a valid key (or still -inf)
+      } else if (mt > m_run + 8.f) {
+        alpha = ex2_approx(m_run - mt);
+        m_run = mt;
+      }
+      // Rescale this row of O when its reference maximum moved (rare): after PV(j-1) finished.
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        if (!warp_wait(bar(kOReady), (j - 1) & 1, 0x19, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c0 = 0; c0 < S::kDVc; c0 += 16) {
+          uint32_t r[16];
+          tmem_ld16(tmem + lane_base + S::kColO + c0, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          tmem_st16(tmem + lane_base + S::kColO + c0, r);
+        }
+        tmem_wait_st();
+      }
+      l_run *= alpha;
+      float psum = 0.f;
+      uint32_t pk[kTileKeys / 2];
+#pragma unroll
+      for (int i = 0; i < kTileKeys; i += 2) {
+        const float p0 = m_run == -INFINITY ? 0.f : ex2_approx(sv[i] - m_run);
+        const float p1 = m_run == -INFINITY ? 0.f : ex2_approx(sv[i + 1] - m_run);
+        psum += p0 + p1;
+        pk[i / 2] = bf16x2_bits(p0, p1);
+      }
+      l_run += psum;
+      // P row -> swizzled K-major smem tile (A operand of PV)
+      if (!warp_wait(bar(kPEmpty + (j & 1)), ((j >> 1) & 1) ^ 1, 0x1A, abort_flag)) { ok = false; break; }
+      uint8_t* prow = smem + S::kOffP + (j & 1) * S::kPBytes + (h >> 3) * 1024 + (h & 7) * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(prow + ((c ^ (h & 7)) * 16)) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(kPFull + (j & 1)));
+    }
+    // epilogue: O / l -> bf16, lse
+    if (ok && n_tiles > 0) ok = warp_wait(bar(kOFinal), 0, 0x1B, abort_flag);
+    tc_fence_after();
+    const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+    const int dv0 = S::kSplit == 2 ? static_cast<int>(crank) * S::kDVc : 0;
+#pragma unroll 1
+    for (int c0 = 0; c0 < S::kDVc; c0 += 16) {
+      uint32_t r[16];
+      if (ok && n_tiles > 0) {
+        tmem_ld16(tmem + lane_base + S::kColO + c0, r);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) r[i] = 0u;
+      }
+      if (h < H) {
+        uint32_t pk[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          pk[i] = bf16x2_bits(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
+        uint4* dst = reinterpret_cast<uint4*>(o + (t * H + h) * DV + dv0 + c0);
+        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      }
+    }
+    if (lse != nullptr && h < H && crank == 0)
+      lse[t * H + h] = l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+  }
+
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc<S::kTmemCols>(tmem);
+  }
+  if (S::kSplit == 2) cluster_sync();                 // no CTA leaves while its peer may write
+}
+
+template <int H, int DQK, int DV>
+int launch_mla(const void* q, const void* c, int64_t n_kv_rows, const KvMap& kv,
+               const int32_t* bid, const int32_t* topk, int64_t n_q, int k, float scale,
+               void* o, float* lse, cudaStream_t stream) {
+  using S = MlaShape<H, DQK, DV>;
+  CUtensorMap tc;
+  int rc = make_tmap_bf16_2d(&tc, c, static_cast<uint64_t>(n_kv_rows), DQK, DQK * 2, 64, 1,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc) return rc;
+  auto kern = sparse_mla_kernel<H, DQK, DV>;
+  DSA_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmem));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(n_q * S::kSplit));
+  cfg.blockDim = dim3(S::kThreads);
+  cfg.dynamicSmemBytes = S::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = S::kSplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const float scale_log2 = scale * 1.4426950408889634f;
+  DSA_CHECK_CUDA(cudaLaunchKernelEx(&cfg, kern, tc, static_cast<const __nv_bfloat16*>(q), bid, topk,
+                                    k, kv, scale_log2, static_cast<__nv_bfloat16*>(o), lse));
+  return DSA_OK;
+}
+
+}  // namespace
+
+int sparse_mla(const void* q, const void* c, int64_t n_kv_rows, const int32_t* cu, int n_req,
+               const int32_t* bid, const int32_t* topk, int64_t n_q, int H, int dqk, int dv, int k,
+               float scale, const int32_t* block_table, int max_pages, int page_size, void* o,
+               float* lse, cudaStream_t stream) {
+  if (n_q < 0 || k < 1 || n_kv_rows < 0 || n_req < 1)
+    return fail(DSA_ERR_INVALID, "mla: need n_q >= 0, k >= 1, n_kv_rows >= 0, n_req >= 1");
+  if (n_q == 0) return DSA_OK;
+  if (!q || !c || !bid || !topk || !o) return fail(DSA_ERR_INVALID, "mla: null pointer");
+  if (!block_table && !cu) return fail(DSA_ERR_INVALID, "mla: need cu or block_table");
+  if (block_table && (page_size != kPageRows || max_pages < 1))
+    return fail(DSA_ERR_UNSUPPORTED, "mla: paged KV needs page_size 64 (got %d)", page_size);
+  if (k > kMaxK) return fail(DSA_ERR_UNSUPPORTED, "mla: k = %d > %d", k, kMaxK);
+  if (n_kv_rows >= (1ll << 31) || n_q > (1ll << 30))
+    return fail(DSA_ERR_UNSUPPORTED, "mla: sizes beyond 32-bit TMA coordinates");
+  if (reinterpret_cast<uintptr_t>(q) % 16 || reinterpret_cast<uintptr_t>(o) % 16)
+    return fail(DSA_ERR_INVALID, "mla: q and o must be 16-byte aligned");
+  KvMap kv{cu, block_table, max_pages, n_req, n_kv_rows};
+  if (H == 128 && dqk == 576 && dv == 512)
+    return launch_mla<128, 576, 512>(q, c, n_kv_rows, kv, bid, topk, n_q, k, scale, o, lse, stream);
+  if (H == 8 && dqk == 80 && dv == 64)
+    return launch_mla<8, 80, 64>(q, c, n_kv_rows, kv, bid, topk, n_q, k, scale, o, lse, stream);
+  return fail(DSA_ERR_UNSUPPORTED, "mla: (H, dqk, dv) = (%d, %d, %d) not built; supported "
+                                   "(128, 576, 512), (8, 80, 64)", H, dqk, dv);
+}
+
+cudaError_t mla_read_errors(uint32_t* flags) { return read_and_clear_device_error(flags); }
+
+}  // namespace dsa

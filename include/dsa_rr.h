@@ -1,0 +1,198 @@
+/*
+ * dsa_rr.h — C ABI of the GB300 (sm_103a) round-robin sequence-shard DSA attention library.
+ *
+ * One shard of DeepSeek-V3.2-style sparse-attention prefill when tokens are dealt round robin
+ * over `sp` sequence shards (flattened token g goes to shard g % sp):
+ *
+ *   dsa_rr_split_metadata  shard token list, batch ids, positions, shard cu_seqlens, row gather
+ *   dsa_rr_rerange         all-gathered (rank-major) KV rows -> logical token order
+ *   dsa_indexer_topk       lightning-indexer scores over the causal history + per-query top-k
+ *     (= dsa_indexer_scores followed by dsa_topk_select, also exported on their own)
+ *   dsa_sparse_mla         sparse MLA of every shard query over its top-k latent rows
+ *
+ * Conventions (every function):
+ *   - Tensor pointers are DEVICE pointers owned by the caller; the library allocates no device
+ *     memory. Scratch space comes from the caller (dsa_indexer_topk_workspace_size).
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream). Scalars are host values; no call reads device data back to the host, so the
+ *     calls can be captured in a CUDA graph.
+ *   - Return value: DSA_OK (0) or a negative DSA_ERR_* code; dsa_last_error_string() gives the
+ *     reason (per host thread). Validation happens before anything is enqueued.
+ *   - No exception, trap or device assert crosses this ABI. Kernels that meet an out-of-range
+ *     index skip it and set a bit in a device error word (dsa_read_device_errors); every wait
+ *     inside a kernel is bounded in time.
+ *   - bf16 tensors are passed as `const void*` (IEEE bfloat16, little endian).
+ *   - Row-major layouts; "[a, b]" lists dimensions outermost first. Rows of bf16 tensors handed
+ *     to the tensor-core calls must start on 16-byte boundaries (the base pointer 16-byte
+ *     aligned; row widths 2*Di and 2*dqk bytes are multiples of 16 for every supported shape).
+ */
+#ifndef DSA_RR_H
+#define DSA_RR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dsa_stream_t; /* identical to cudaStream_t */
+
+enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID = -1,     /* invalid argument (null pointer, negative size, rank >= sp ...) */
+  DSA_ERR_UNSUPPORTED = -2, /* a shape the kernels are not built for */
+  DSA_ERR_WORKSPACE = -3,   /* workspace missing or too small */
+  DSA_ERR_CUDA = -4         /* a CUDA runtime / driver call failed (launch, tensor map ...) */
+};
+
+/* Bits of the device error word. */
+#define DSA_DEVERR_TIMEOUT 0x80000000u    /* a bounded in-kernel wait gave up (low byte: site) */
+#define DSA_DEVERR_BAD_INDEX 0x40000000u  /* an index input was out of range; it was skipped */
+#define DSA_DEVERR_BAD_LENGTH 0x20000000u /* a query row exceeded max_ctx; the row was skipped */
+
+/* Human-readable reason for the last non-zero return on this host thread. */
+const char* dsa_last_error_string(void);
+
+/* Library ABI version (increments on any signature change). */
+int dsa_version(void);
+
+/* Synchronise the device, OR every kernel's device error word into *flags and clear them. */
+int dsa_read_device_errors(uint32_t* flags);
+
+/*
+ * Host helper: number of tokens shard `rank` of `sp` holds, ceil((n_tokens - rank) / sp), or
+ * 0 when rank >= n_tokens. Source: "[DeepSeek v3.2] 上下文并行详解", section 2.B
+ * (arange(cp_rank, tokens, cp_size)). Returns -1 for sp < 1, rank < 0, rank >= sp or
+ * n_tokens < 0.
+ */
+int64_t dsa_rr_shard_len(int64_t n_tokens, int sp, int rank);
+
+/*
+ * Round-robin split metadata for shard `rank` of `sp`, plus an optional row gather.
+ * Source: "[DeepSeek v3.2] 上下文并行详解", section 2.B (nsa_cp_round_robin_split_data and the
+ * metadata kernel that recomputes cu_seqlens and batch indices after the scatter) and section 4
+ * part 1 (the "rank X token <-> batch Y position Z" mapping).
+ *
+ * Shard token t (0 <= t < n_r, n_r = dsa_rr_shard_len(n_tokens, sp, rank)) is the flattened
+ * token g_t = rank + t*sp. Outputs (device, int32):
+ *   cu_shard [n_req+1]  cu_shard[b] = number of shard tokens with g < cu[b]
+ *   pos      [n_r]      g_t - cu[bid_t]           (position inside its request)
+ *   bid      [n_r]      the largest b with cu[b] <= g_t (empty requests are skipped)
+ *   gidx     [n_r]      g_t; may be NULL
+ * Inputs: cu [n_req+1] int32 request offsets, cu[0] = 0, non-decreasing, cu[n_req] = n_tokens
+ * (the caller guarantees this; it is not read back). n_req >= 1.
+ * Row gather (optional): if src_rows != NULL, dst_rows[t, :] = src_rows[g_t, :] for rows of
+ * row_bytes bytes (src [n_tokens, row_bytes], dst [n_r, row_bytes]); 16-byte vectors when both
+ * pointers and row_bytes are multiples of 16, else byte copies.
+ * Errors: DSA_ERR_INVALID for sp < 1, rank outside [0, sp), n_req < 1, n_tokens < 0 or a null
+ * required pointer. n_tokens == 0 is valid (only cu_shard is written, all zeros).
+ */
+int dsa_rr_split_metadata(const int32_t* cu, int n_req, int64_t n_tokens, int sp, int rank,
+                          int32_t* cu_shard, int32_t* pos, int32_t* bid, int32_t* gidx,
+                          const void* src_rows, void* dst_rows, int64_t row_bytes,
+                          dsa_stream_t stream);
+
+/*
+ * Rerange an all-gathered buffer to logical token order.
+ * Source: "[DeepSeek v3.2] 上下文并行详解", section 2.C (cp_all_gather_rerange_output) and
+ * section 4 part 3 step B (the gathered rows come rank by rank, T0,T4,T1,T5,...; the rerange
+ * restores T0,T1,T2,... so that the top-k sees logically contiguous KV).
+ *
+ * out[g, :] = gathered[off[g % sp] + g / sp, :] for 0 <= g < n_tokens, rows of row_bytes bytes.
+ * off[q] = q * rank_stride_rows when rank_stride_rows > 0 (equal-size all-gather with padding,
+ * rank_stride_rows >= ceil(n_tokens / sp)); rank_stride_rows == 0 means packed blocks,
+ * off[q] = sum of the shard lengths of ranks < q.
+ * gathered: [sp * rank_stride_rows or n_tokens, row_bytes]; out: [n_tokens, row_bytes]; the two
+ * must not overlap. Errors: DSA_ERR_INVALID for sp < 1, a stride smaller than ceil(N/sp),
+ * n_tokens < 0, row_bytes <= 0 or null pointers (n_tokens == 0 is a no-op).
+ */
+int dsa_rr_rerange(const void* gathered, void* out, int64_t n_tokens, int sp,
+                   int64_t rank_stride_rows, int64_t row_bytes, dsa_stream_t stream);
+
+/*
+ * Bytes of scratch dsa_indexer_topk needs: the fp32 score rows [n_q, stride(max_ctx)] plus a
+ * small scheduling area. max_ctx = an upper bound of pos_t + 1 over the queries.
+ */
+size_t dsa_indexer_topk_workspace_size(int64_t n_q, int max_ctx, int k);
+
+/* Row stride (in floats) of the score rows for a given max_ctx (a multiple of 4). */
+int64_t dsa_score_row_stride(int max_ctx);
+
+/*
+ * Lightning-indexer scores over each query's causal history (tcgen05 tensor cores).
+ * The pages name this scan the bottleneck ("[RFC]: Parallel strategy for Deepseek v3.2 like
+ * models", the comments on the indexer) but print no formula; the DeepSeek-V3.2 lightning
+ * indexer defines, for shard query t of request b_t at position pos_t,
+ *
+ *     I[t, s] = sum_h w[t, h] * ReLU( sum_d q_idx[t, h, d] * k_idx[row(b_t, s), d] ),
+ *     0 <= s <= pos_t,
+ *
+ * with row(b, s) = cu[b] + s (contiguous, logical order after the rerange) or
+ * block_table[b * max_pages + s / page_size] * page_size + s % page_size (paged).
+ *
+ *   q_idx  bf16 [n_q, Hi, Di]     w fp32 [n_q, Hi]     k_idx bf16 [n_kv_rows, Di]
+ *   cu     int32 [n_req+1] (contiguous mode; ignored when block_table != NULL)
+ *   n_req  number of requests (rows of block_table when paged); bid must lie in [0, n_req)
+ *   pos, bid int32 [n_q]          queries of one request must be consecutive in this order
+ *   scores fp32 [n_q, score_stride]: row t receives I[t, 0..pos_t]; the rest is not written.
+ * Supported: (Hi, Di) in {(64, 128), (4, 32)}; page_size 64 when paged. max_ctx >= pos_t + 1
+ * for every t (rows that violate it are skipped and flagged DSA_DEVERR_BAD_LENGTH).
+ * `workspace`/`workspace_bytes`: at least dsa_indexer_topk_workspace_size(n_q, max_ctx, 1)
+ * bytes (only the scheduling area is used when scores are supplied separately).
+ */
+int dsa_indexer_scores(const void* q_idx, const float* w, const void* k_idx, int64_t n_kv_rows,
+                       const int32_t* cu, int n_req, const int32_t* pos, const int32_t* bid,
+                       int64_t n_q, int Hi, int Di, int max_ctx, const int32_t* block_table,
+                       int max_pages, int page_size, float* scores, int64_t score_stride,
+                       void* workspace, size_t workspace_bytes, dsa_stream_t stream);
+
+/*
+ * Per-query top-k of fp32 score rows ("history top-K", [RFC] page, comments): for row t of
+ * length L_t = pos_t + 1 (scores[t * score_stride + s], 0 <= s < L_t), the k indices with the
+ * largest score; equal scores go to the lower index; -0.0 equals +0.0; if L_t <= k all indices
+ * are taken. topk [n_q, k] int32 lists the chosen indices in ascending order, padded with -1.
+ * Scores must not be NaN. Radix select on CUDA cores.
+ */
+int dsa_topk_select(const float* scores, int64_t score_stride, const int32_t* pos, int64_t n_q,
+                    int k, int max_ctx, int32_t* topk, dsa_stream_t stream);
+
+/*
+ * dsa_indexer_scores followed by dsa_topk_select, the score rows living in `workspace`.
+ * topk: int32 [n_q, k], entries are positions s inside the query's request (0..pos_t) or -1.
+ */
+int dsa_indexer_topk(const void* q_idx, const float* w, const void* k_idx, int64_t n_kv_rows,
+                     const int32_t* cu, int n_req, const int32_t* pos, const int32_t* bid,
+                     int64_t n_q, int Hi, int Di, int k, int max_ctx, const int32_t* block_table,
+                     int max_pages, int page_size, int32_t* topk, void* workspace,
+                     size_t workspace_bytes, dsa_stream_t stream);
+
+/*
+ * Sparse MLA (tcgen05 tensor cores, TMA row gather). "[RFC]: Parallel strategy for Deepseek
+ * v3.2 like models": each query attends only its top-k keys, with all heads at once. For query
+ * t and head h, over the valid entries idx_j >= 0 of topk[t, :]:
+ *
+ *     S[h, j]   = scale * sum_{d < dqk} q[t, h, d] * c[row(b_t, idx_j), d]
+ *     o[t, h,:] = sum_j softmax_j(S[h, :]) * c[row(b_t, idx_j), 0:dv]
+ *     lse[t, h] = ln sum_j exp(S[h, j])
+ *
+ * (absorbed MLA: V is the first dv columns of the same latent row). A query without valid
+ * entries gets o = 0 and lse = -inf.
+ *   q  bf16 [n_q, H, dqk]     c bf16 [n_kv_rows, dqk]     topk int32 [n_q, k]
+ *   cu int32 [n_req+1] (contiguous mode) / block_table int32 [n_req, max_pages] (paged)
+ *   n_req >= 1; bid entries outside [0, n_req) read zero rows and set DSA_DEVERR_BAD_INDEX
+ *   bid int32 [n_q]           o bf16 [n_q, H, dv]         lse fp32 [n_q, H] or NULL
+ * Supported: (H, dqk, dv) in {(128, 576, 512), (8, 80, 64)}, page_size 64 when paged.
+ * Softmax in fp32 (exp2 with a running maximum), P rounded to bf16 for the P.V product.
+ * Index entries that land outside the KV buffer read zero rows and set DSA_DEVERR_BAD_INDEX.
+ */
+int dsa_sparse_mla(const void* q, const void* c, int64_t n_kv_rows, const int32_t* cu, int n_req,
+                   const int32_t* bid, const int32_t* topk, int64_t n_q, int H, int dqk, int dv,
+                   int k, float scale, const int32_t* block_table, int max_pages, int page_size,
+                   void* o, float* lse, dsa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_RR_H */

@@ -28,3 +28,12 @@ def read_golden(name):
             else:
                 out.append((line, []))
     return out
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _native_library(request):
+    """Build libdsa_rr.so once per session when GPU tests are collected (a no-op when fresh)."""
+    if any(item.get_closest_marker("gpu") for item in request.session.items):
+        from deepseek_v3_sparse_round_gb300 import build as b
+        b.build()
+    yield

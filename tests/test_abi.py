@@ -1,0 +1,72 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every function include/dsa_rr.h
+declares; host-side helpers and argument validation work without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from deepseek_v3_sparse_round_gb300 import build as b
+    from deepseek_v3_sparse_round_gb300 import _native
+    b.build()
+    return _native.load()
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "dsa_rr.h"), encoding="utf-8") as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+    from deepseek_v3_sparse_round_gb300._native import SIGNATURES
+    assert sorted(SIGNATURES) == names
+
+
+def test_library_is_sm103a_build():
+    from deepseek_v3_sparse_round_gb300 import build as b
+    assert "arch=compute_103a,code=sm_103a" in " ".join(b.ARCH)
+
+
+def test_host_helpers(lib):
+    import deepseek_v3_sparse_round_gb300 as dsa
+    assert dsa.dsa_version() == 1
+    assert dsa.dsa_rr_shard_len(11805, 8, 3) == 1476
+    assert dsa.dsa_rr_shard_len(3, 8, 5) == 0
+    assert dsa.dsa_rr_shard_len(0, 4, 0) == 0
+    assert dsa.dsa_rr_shard_len(10, 0, 0) == -1 and dsa.dsa_rr_shard_len(10, 4, 4) == -1
+    assert sum(dsa.dsa_rr_shard_len(71014, 4, r) for r in range(4)) == 71014
+    assert dsa.dsa_score_row_stride(8001) == 8004
+    ws = dsa.dsa_indexer_topk_workspace_size(1476, 8000, 2048)
+    assert ws >= 1476 * 8000 * 4 and ws % 256 == 0
+
+
+def test_invalid_arguments_rejected_before_any_launch(lib):
+    null = ctypes.c_void_p(0)
+    # sp = 0, rank >= sp, n_req = 0
+    assert lib.dsa_rr_split_metadata(null, 1, 10, 0, 0, null, null, null, null, null, null, 0, null) == -1
+    assert lib.dsa_rr_split_metadata(null, 1, 10, 4, 4, null, null, null, null, null, null, 0, null) == -1
+    assert b"sp" in lib.dsa_last_error_string()
+    assert lib.dsa_rr_rerange(null, null, 10, 4, 1, 16, null) == -1          # stride < ceil(N/sp)
+    assert lib.dsa_rr_rerange(null, null, 0, 4, 0, 16, null) == 0            # empty is a no-op
+    # unsupported shapes and missing workspace
+    fake = ctypes.c_void_p(4096)
+    assert lib.dsa_sparse_mla(fake, fake, 10, fake, 1, fake, fake, 4, 64, 576, 512, 2048, 0.1,
+                              null, 0, 0, fake, null, null) == -2
+    assert lib.dsa_sparse_mla(fake, fake, 10, fake, 1, fake, fake, 4, 128, 576, 512, 8192, 0.1,
+                              null, 0, 0, fake, null, null) == -2
+    assert lib.dsa_indexer_topk(fake, fake, fake, 10, fake, 1, fake, fake, 4, 64, 128, 2048, 10,
+                                null, 0, 0, fake, null, 0, null) == -3
+    assert lib.dsa_topk_select(fake, 3, fake, 4, 8, 10, fake, null) == -1    # stride < max_ctx
+    assert lib.dsa_indexer_scores(fake, fake, fake, 10, fake, 1, fake, fake, 4, 32, 128, 10, null,
+                                  0, 0, fake, 12, fake, 1 << 20, null) == -2

@@ -1,0 +1,60 @@
+"""GPU parity: radix-select top-k on fp32 score rows vs the oracle's full sort (bit-exact)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle.topk import topk_indices
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(rows, k):
+    import deepseek_v3_sparse_round_gb300 as dsa
+    max_ctx = max(len(r) for r in rows)
+    stride = dsa.dsa_score_row_stride(max_ctx)
+    s = np.full((len(rows), stride), np.nan, dtype=np.float32)
+    for i, r in enumerate(rows):
+        s[i, :len(r)] = r
+    pos = torch.tensor([len(r) - 1 for r in rows], dtype=torch.int32, device="cuda")
+    out = torch.full((len(rows), k), -9, dtype=torch.int32, device="cuda")
+    dsa.dsa_topk_select(torch.as_tensor(s).cuda(), pos, k, max_ctx, out)
+    return out.cpu().numpy()
+
+
+@pytest.mark.parametrize("k", [1, 7, 32, 2048])
+def test_integer_rows_with_ties(k):
+    rng = np.random.default_rng(k)
+    lengths = [1, 2, k, k + 1, 3 * k + 5, 4096, 4097, 9000]
+    rows = [rng.integers(-5, 6, L).astype(np.float32) for L in lengths]
+    got = _run(rows, k)
+    for i, r in enumerate(rows):
+        assert np.array_equal(got[i], topk_indices(r, k)), (k, len(r))
+
+
+@pytest.mark.parametrize("L", [40960, 40961, 65536])
+def test_long_rows_shared_and_global_paths(L):
+    rng = np.random.default_rng(L)
+    rows = [rng.integers(-1000, 1000, L).astype(np.float32),
+            np.round(rng.normal(size=L), 2).astype(np.float32)]
+    got = _run(rows, 2048)
+    for i, r in enumerate(rows):
+        assert np.array_equal(got[i], topk_indices(r, 2048))
+
+
+def test_signed_zero_and_constant_rows():
+    z = np.array([-0.0, 0.0] * 50, dtype=np.float32)
+    neg = -np.abs(np.random.default_rng(1).normal(size=300)).astype(np.float32)
+    neg[::7] = -0.0
+    rows = [z, np.full(5000, 3.5, np.float32), neg, np.zeros(3000, np.float32)]
+    for k in (1, 10, 64):
+        got = _run(rows, k)
+        for i, r in enumerate(rows):
+            assert np.array_equal(got[i], topk_indices(r, k)), (i, k)
+
+
+def test_real_valued_rows_match_exactly():
+    rng = np.random.default_rng(9)
+    rows = [rng.normal(size=L).astype(np.float32) for L in (100, 2049, 8000, 32768)]
+    got = _run(rows, 2048)
+    for i, r in enumerate(rows):
+        assert np.array_equal(got[i], topk_indices(r, 2048))
