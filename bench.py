@@ -1,0 +1,394 @@
+"""Benchmark: one shard of round-robin sequence-sharded DSA prefill attention on GB300.
+
+Workload (default): the varlen batch {8000, 800, 5, 3000} tokens, sp = 8, shard rank 3
+(1,476 queries); indexer 64 heads x 128, top-k 2048; MLA 128 heads, qk 576 / v 512, bf16.
+A step is one pass of the whole shard path through the C ABI:
+  split metadata + the shard's row gather -> rerange of the all-gathered k_idx and latent rows
+  -> indexer scores + top-k -> sparse MLA.
+The other shards' rows are inputs (one GPU, no collective). With --gpus N (torchrun), GPU i
+takes shard (3 + i) % 8 of the same batch: independent problems, weak scaling.
+
+value = shard queries processed / device time of the timed steps (CUDA events on the launch
+stream, L2 flushed between steps); e2e = the same through host buffers (pinned H2D of the
+step's inputs + D2H of o inside the timed region). --impl reference times the fp64 CPU oracle
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "shard prefill query tokens/s (indexer+top-k+sparse MLA); % of BF16 TC roofline"
+WORKLOAD_ID = 1
+BASE_RANK = 3
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"bf16": float(d["bf16_tflops"]), "bf16_sustained": float(d["bf16_tflops_sustained"]),
+                "hbm": float(d["hbm_gbs"]), "source": "measured"}
+    return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+class ShardStep:
+    """Device buffers and the launches of one step for shard `rank` of the varlen workload."""
+
+    def __init__(self, torch, dsa, W, rank, device):
+        self.torch, self.dsa = torch, dsa
+        wl = W.WORKLOADS[WORKLOAD_ID]
+        self.wl, self.rank, self.dev = wl, rank, device
+        cu_np = W.cu_seqlens(wl.lengths)
+        self.N = int(cu_np[-1])
+        self.n_req = len(wl.lengths)
+        self.n_r = dsa.dsa_rr_shard_len(self.N, wl.sp, rank)
+        self.max_ctx = int(max(wl.lengths))
+        idx = W.indexer_inputs(wl, self.n_r, self.N, rank)
+        mi = W.mla_inputs(wl, self.n_r, self.N, rank)
+        # host inputs (pinned): the shard's queries, and the all-gathered (rank-major) KV rows
+        # that the other shards contribute; built by plain indexing of the logical rows.
+        perm = np.concatenate([np.arange(q, self.N, wl.sp) for q in range(wl.sp)])
+        self.h = {
+            "cu": torch.as_tensor(cu_np).pin_memory(),
+            "q_idx": idx.q_idx.pin_memory(), "w": idx.w.pin_memory(), "q": mi.q.pin_memory(),
+            "k_gath": idx.k_idx[torch.as_tensor(perm)].contiguous().pin_memory(),
+            "c_gath": mi.c[torch.as_tensor(perm)].contiguous().pin_memory(),
+            "c_log": mi.c.pin_memory(),
+        }
+        self.d = {k: v.to(device) for k, v in self.h.items()}
+        e = lambda *s, dt=torch.int32: torch.empty(*s, dtype=dt, device=device)
+        self.cu_shard, self.pos, self.bid, self.gidx = e(self.n_req + 1), e(self.n_r), e(self.n_r), e(self.n_r)
+        self.c_local = e(self.n_r, wl.dqk, dt=torch.bfloat16)
+        self.k_idx = e(self.N, wl.Di, dt=torch.bfloat16)
+        self.c = e(self.N, wl.dqk, dt=torch.bfloat16)
+        self.ws = e(dsa.dsa_indexer_topk_workspace_size(self.n_r, self.max_ctx, wl.topk), dt=torch.uint8)
+        self.topk = e(self.n_r, wl.topk)
+        self.o = e(self.n_r, wl.H, wl.dv, dt=torch.bfloat16)
+        self.lse = e(self.n_r, wl.H, dt=torch.float32)
+        self.launches_per_step = 8   # split meta + gather, 2 reranges, plan + indexer + top-k, MLA
+        self.h_o = torch.empty(self.o.shape, dtype=torch.bfloat16).pin_memory()
+
+    def run(self, ev=None):
+        dsa, wl, d = self.dsa, self.wl, self.d
+        dsa.dsa_rr_split_metadata(d["cu"], self.N, wl.sp, self.rank, self.cu_shard, self.pos,
+                                  self.bid, self.gidx, src_rows=d["c_log"], dst_rows=self.c_local)
+        dsa.dsa_rr_rerange(d["k_gath"], self.k_idx, self.N, wl.sp, 0)
+        dsa.dsa_rr_rerange(d["c_gath"], self.c, self.N, wl.sp, 0)
+        dsa.dsa_indexer_topk(d["q_idx"], d["w"], self.k_idx, d["cu"], self.n_req, self.pos,
+                             self.bid, wl.topk, self.max_ctx, self.topk, self.ws)
+        if ev is not None:
+            ev[0].record()
+        dsa.dsa_sparse_mla(d["q"], self.c, d["cu"], self.n_req, self.bid, self.topk, wl.scale,
+                           self.o, self.lse)
+        if ev is not None:
+            ev[1].record()
+
+    def upload(self):
+        for k in ("cu", "q_idx", "w", "q", "k_gath", "c_gath", "c_log"):
+            self.d[k].copy_(self.h[k], non_blocking=True)
+
+    def h2d_bytes(self):
+        return sum(self.h[k].numel() * self.h[k].element_size()
+                   for k in ("cu", "q_idx", "w", "q", "k_gath", "c_gath", "c_log"))
+
+    def work(self):
+        pos = self.pos.cpu().numpy().astype(np.int64)
+        wl = self.wl
+        sel = np.minimum(pos + 1, wl.topk)
+        idx_flops = 2.0 * wl.Hi * wl.Di * float(np.sum(pos + 1))
+        mla_flops = 2.0 * wl.H * (wl.dqk + wl.dv) * float(np.sum(sel))
+        return idx_flops, mla_flops
+
+
+def gpu_arm(args):
+    import torch
+    ws, rank, local = dist_env()
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    import __graft_entry__ as ge
+    ge.build()
+    import deepseek_v3_sparse_round_gb300 as dsa
+    import workloads as W
+
+    shard = (BASE_RANK + rank) % W.WORKLOADS[WORKLOAD_ID].sp
+    st = ShardStep(torch, dsa, W, shard, device)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)   # > L2
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        st.run()
+    torch.cuda.synchronize()
+    idx_flops, mla_flops = st.work()
+
+    # ---- device-timed steps (inputs resident in HBM), L2 flushed between steps ----
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            evs[i][0].record(stream)
+            st.run(ev=(evs[i][2], evs[i][3]))
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    step_ms = [a.elapsed_time(b) for a, b, _, _ in evs]
+    mla_ms = [c.elapsed_time(d) for _, _, c, d in evs]
+    dev_s = sum(step_ms) / 1e3
+    if dist:
+        t = torch.tensor([dev_s], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dev_s = float(t.item())
+        dist.barrier()
+    torch.cuda.synchronize()
+
+    # ---- end to end through host buffers: H2D inputs, step, D2H of o ----
+    e2e_steps = max(1, min(args.steps, 10))
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        st.upload()
+        st.run()
+        st.h_o.copy_(st.o, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = e0.elapsed_time(e1) / 1e3
+    if dist:
+        t = torch.tensor([e2e_s], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    errors = dsa.dsa_read_device_errors()
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    pk = peaks()
+    queries = st.n_r * ws
+    value = queries * args.steps / dev_s
+    mla_avg_s = float(np.mean(mla_ms)) / 1e3
+    achieved = mla_flops / mla_avg_s / 1e12
+    cpu = cpu_baseline(sample_queries=args.cpu_baseline_queries) if not args.no_cpu_baseline else None
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dev_s * 1e3 / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded bf16 N(0,1) queries/keys/latents; no weights needed)",
+        "config": {"workload": "varlen {8000,800,5,3000} tokens, sp=8, shard rank 3 (+i per GPU): "
+                               "1476 queries, indexer 64x128 top-2048, MLA 128 heads 576/512",
+                   "queries_per_gpu": st.n_r, "kv_tokens": st.N, "topk": st.wl.topk,
+                   "l2": "flushed between timed steps (256 MB write)",
+                   "step": "split+gather, 2x rerange, indexer scores, top-k, sparse MLA"},
+        "roofline": {"bound": "tensor", "kernel": "sparse_mla_kernel<128,576,512>",
+                     "achieved": round(achieved, 1), "peak": pk["bf16"], "unit": "TFLOP/s",
+                     "frac": round(achieved / pk["bf16"], 4), "traffic": None,
+                     "peak_source": f"{pk['source']} bf16 burst (MEASURED_PEAKS.json)",
+                     "algorithmic_flop_per_launch": mla_flops},
+        "indexer_topk": {"algorithmic_flop_per_step": idx_flops},
+        "e2e": {"value": round(queries * e2e_steps / e2e_s, 2), "unit": "tokens/s",
+                "h2d_bytes_per_step": st.h2d_bytes(),
+                "d2h_bytes_per_step": st.o.numel() * st.o.element_size()},
+        "gpu_launches": st.launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "device_errors": errors,
+        "wall_s_timed_region": round(wall, 4),
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+def _oracle_step(W, wl, sh, sel):
+    from oracle import indexer as oidx, mla as omla, topk as otopk
+    from oracle.kv import ContiguousKV
+    kv = ContiguousKV(sh["cu"])
+    rows = oidx.indexer_scores(sh["q_idx"][sel], sh["w"][sel], sh["k_idx"], kv, sh["pos"][sel],
+                               sh["bid"][sel])
+    topk = otopk.topk_rows(rows, wl.topk)
+    return omla.sparse_mla(sh["q"][sel], sh["c"], kv, sh["bid"][sel], topk, wl.scale, wl.dv)
+
+
+def _oracle_inputs(n_sample):
+    import workloads as W
+    from oracle import split as osplit
+    wl = W.WORKLOADS[WORKLOAD_ID]
+    cu = W.cu_seqlens(wl.lengths)
+    meta = osplit.round_robin_split(cu, wl.sp, BASE_RANK)
+    n_r = len(meta["pos"])
+    idx = W.indexer_inputs(wl, n_r, int(cu[-1]), BASE_RANK)
+    mi = W.mla_inputs(wl, n_r, int(cu[-1]), BASE_RANK)
+    # a bounded sample spread over the shard (every request, short and long histories)
+    sel = np.unique(np.linspace(0, n_r - 1, n_sample).round().astype(np.int64))
+    sh = {"cu": cu, "pos": meta["pos"], "bid": meta["bid"],
+          "q_idx": idx.q_idx.float().numpy().astype(np.float64)[sel],
+          "w": idx.w.numpy().astype(np.float64)[sel],
+          "k_idx": idx.k_idx.float().numpy().astype(np.float64),
+          "q": mi.q[sel].float().numpy().astype(np.float64),
+          "c": mi.c.float().numpy().astype(np.float64)}
+    sh["pos"], sh["bid"] = sh["pos"][sel], sh["bid"][sel]
+    return W, wl, sh, n_r
+
+
+def cpu_baseline(sample_queries=12, steps=1):
+    W, wl, sh, n_r = _oracle_inputs(sample_queries)
+    sel = np.arange(len(sh["pos"]))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        _oracle_step(W, wl, sh, sel)
+    dt = time.perf_counter() - t0
+    cores = _blas_threads()
+    return {"value": round(len(sel) * steps / dt, 4), "unit": "tokens/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{len(sel)} of the {n_r} rank-3 queries (evenly spaced, all requests), "
+                      f"fp64 NumPy indexer + full-sort top-k + sparse MLA, {steps} pass(es), "
+                      f"{dt:.1f} s"}
+
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+
+def reference_arm(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    W, wl, sh, n_r = _oracle_inputs(args.cpu_sample)
+    sel = np.arange(len(sh["pos"]))
+    for _ in range(args.warmup):
+        _oracle_step(W, wl, sh, sel[:1])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(W, wl, sh, sel)
+    dt = time.perf_counter() - t0
+    value = len(sel) * args.steps / dt
+    cores = _blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3 / args.steps, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "varlen {8000,800,5,3000} tokens, sp=8, shard rank 3: a bounded "
+                               f"sample of {len(sel)} of its {n_r} queries per step"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"{len(sel)} evenly spaced queries of the rank-3 shard per step"},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-sample", type=int, default=96, help="queries per reference-arm step")
+    ap.add_argument("--cpu-baseline-queries", type=int, default=1476)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "native":
+        args.warmup = 3
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

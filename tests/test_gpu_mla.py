@@ -79,14 +79,23 @@ def test_padding_holes_and_empty_rows():
 
 
 def test_large_logits_trigger_rescale():
-    """Keys whose logits rise steeply along the selection order force the running maximum to
-    move by more than 2^8 several times (the O-rescaling path)."""
+    """Logits scaled up 6x move the running maximum by more than 2^8 several times (the
+    O-rescaling path). Outputs then reach |o| ~ 4-8, where one bf16 ulp of o is 2^-5, so the
+    fixed 2e-2 absolute bound of the N(0,1) workloads does not apply. Bound used, elementwise:
+    bf16 rounding of o (2^-8 |o|) plus bf16 rounding of P (2^-8 max |v| over the selected rows),
+    plus 1e-3; rel-RMS stays <= 5e-3."""
     sh = Shard(W.WORKLOADS[1], 3)
     sel = np.flatnonzero(sh.pos > 3000)[:4]
-    q = sh.mla.q[torch.as_tensor(sel, device=sh.mla.q.device)].clone()
-    q.mul_(6.0)                                         # logits std ~6 in natural units
-    topk = np.tile(np.arange(2048), (len(sel), 1))
+    idx = torch.as_tensor(sel, device=sh.mla.q.device)
     sh.mla.q = sh.mla.q.clone()
-    sh.mla.q[torch.as_tensor(sel, device=sh.mla.q.device)] = q
+    sh.mla.q[idx] = (sh.mla.q[idx].float() * 6.0).to(torch.bfloat16)
+    topk = np.tile(np.arange(2048), (len(sel), 1))
     view = sh.oracle_view(sel)
-    _check(sh, sel, topk, view)
+    o, lse = sh.run_mla(i32(topk), q=sh.mla.q[idx].cuda(), bid=i32(sh.bid[sel]))
+    ref_o, ref_lse = sh.oracle_mla(sel, topk, view)
+    og = f64(o)
+    vmax = np.max(np.abs(view["c"][:, :sh.wl.dv]))
+    bound = 2.0 ** -8 * np.abs(ref_o) + 2.0 ** -8 * vmax + 1e-3
+    assert np.all(np.abs(og - ref_o) <= bound), float(np.max(np.abs(og - ref_o) / bound))
+    assert np.linalg.norm(og - ref_o) / np.linalg.norm(ref_o) <= 5e-3
+    assert np.allclose(lse.cpu().numpy(), ref_lse, atol=1e-3, rtol=1e-4)
