@@ -17,7 +17,7 @@ from . import _native
 __all__ = [
     "DsaError", "dsa_version", "dsa_rr_shard_len", "dsa_rr_split_metadata", "dsa_rr_rerange",
     "dsa_indexer_topk_workspace_size", "dsa_score_row_stride", "dsa_indexer_scores",
-    "dsa_topk_select", "dsa_indexer_topk", "dsa_sparse_mla", "dsa_read_device_errors",
+    "dsa_topk_select", "dsa_indexer_topk", "dsa_indexer_topk_noalloc", "dsa_sparse_mla", "dsa_read_device_errors",
     "DEVERR_TIMEOUT", "DEVERR_BAD_INDEX", "DEVERR_BAD_LENGTH",
 ]
 
@@ -153,6 +153,22 @@ def dsa_indexer_topk(q_idx, w, k_idx, cu, n_req, pos, bid, k, max_ctx, topk, wor
         _ptr(q_idx), _ptr(w), _ptr(k_idx), k_idx.shape[0], _ptr(cu), n_req, _ptr(pos), _ptr(bid),
         n_q, Hi, Di, k, max_ctx, _ptr(block_table), max_pages, page_size, _ptr(topk),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def dsa_indexer_topk_noalloc(q_idx, w, k_idx, cu, n_req, pos, bid, k, max_ctx, topk,
+                             block_table=None, page_size=64, stream=None):
+    """dsa_indexer_topk without a workspace argument: for callers that cannot allocate device
+    memory; the library's static scratch array is used instead (calls must not overlap)."""
+    _dev(q_idx, torch.bfloat16, "q_idx"); _dev(k_idx, torch.bfloat16, "k_idx")
+    _dev(w, torch.float32, "w"); _dev(topk, torch.int32, "topk")
+    _dev(pos, torch.int32, "pos"); _dev(bid, torch.int32, "bid"); _dev(cu, torch.int32, "cu")
+    _dev(block_table, torch.int32, "block_table")
+    n_q, Hi, Di = q_idx.shape
+    max_pages = block_table.shape[1] if block_table is not None else 0
+    _check(_lib().dsa_indexer_topk_noalloc(
+        _ptr(q_idx), _ptr(w), _ptr(k_idx), k_idx.shape[0], _ptr(cu), n_req, _ptr(pos), _ptr(bid),
+        n_q, Hi, Di, k, max_ctx, _ptr(block_table), max_pages, page_size, _ptr(topk),
+        _stream(stream)))
 
 
 def dsa_sparse_mla(q, c, cu, n_req, bid, topk, scale, o, lse=None, block_table=None,

@@ -28,6 +28,9 @@ SIGNATURES = {
     "dsa_topk_select": (c_int, [c_vp, c_i64, c_vp, c_i64, c_int, c_int, c_vp, c_vp]),
     "dsa_indexer_topk": (c_int, [c_vp, c_vp, c_vp, c_i64, c_vp, c_int, c_vp, c_vp, c_i64, c_int,
                                  c_int, c_int, c_int, c_vp, c_int, c_int, c_vp, c_vp, c_sz, c_vp]),
+    "dsa_indexer_topk_noalloc": (c_int, [c_vp, c_vp, c_vp, c_i64, c_vp, c_int, c_vp, c_vp, c_i64,
+                                         c_int, c_int, c_int, c_int, c_vp, c_int, c_int, c_vp,
+                                         c_vp]),
     "dsa_sparse_mla": (c_int, [c_vp, c_vp, c_i64, c_vp, c_int, c_vp, c_vp, c_i64, c_int, c_int,
                                c_int, c_int, c_f, c_vp, c_int, c_int, c_vp, c_vp, c_vp]),
 }

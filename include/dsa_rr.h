@@ -191,6 +191,28 @@ int dsa_sparse_mla(const void* q, const void* c, int64_t n_kv_rows, const int32_
                    int k, float scale, const int32_t* block_table, int max_pages, int page_size,
                    void* o, float* lse, dsa_stream_t stream);
 
+/*
+ * Allocation-free variant of dsa_indexer_topk. (The pages have no counterpart: this is a
+ * convenience of the library, not a step of the method.)
+ *
+ * For callers that cannot allocate device memory -- a framework that reserved all device memory
+ * in its own pool and forbids further cudaMalloc, a runtime without a CUDA allocator binding, or
+ * a serving loop that must not call cudaMalloc / cudaFree because they can synchronise the
+ * device. The scratch space lives in one file-scope __device__ array of
+ * DSA_NOALLOC_SCRATCH_BYTES bytes that every GPU loading the library keeps until exit.
+ * Arguments and results are those of dsa_indexer_topk without workspace / workspace_bytes.
+ * The first call on a device (that device current) looks up the array's address; make it before
+ * any stream capture. All calls share the array: calls that may overlap on the GPU race and must
+ * not be issued. Requests needing more scratch than the array (dsa_indexer_topk_workspace_size)
+ * return DSA_ERR_WORKSPACE. No device memory is allocated or freed.
+ */
+#define DSA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int dsa_indexer_topk_noalloc(const void* q_idx, const float* w, const void* k_idx,
+                             int64_t n_kv_rows, const int32_t* cu, int n_req, const int32_t* pos,
+                             const int32_t* bid, int64_t n_q, int Hi, int Di, int k, int max_ctx,
+                             const int32_t* block_table, int max_pages, int page_size,
+                             int32_t* topk, dsa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
