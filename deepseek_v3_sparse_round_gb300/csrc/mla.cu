@@ -399,6 +399,380 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16*
   if (S::kSplit == 2) cluster_sync();                 // no CTA leaves while its peer may write
 }
 
+// =============================================================================================
+// H = 128, dqk = 576, dv = 512: a cluster of two CTAs per query with split roles.
+//   CTA 0 ("S side"): Q (128 x 576 bf16) in TMEM as the A operand (288 columns) and two S tiles
+//     of 128 x 64 fp32 (128 columns), so QK(j+1) runs while the softmax of tile j runs. Its
+//     softmax warps write P (bf16) straight into CTA 1's shared memory, with the per-row
+//     rescale factors, then arrive on CTA 1's barrier.
+//   CTA 1 ("O side"): O (128 x 512 fp32) fills its TMEM; it accumulates O += P . V with two
+//     N = 256 MMAs per 16 keys and writes o = O / l at the end.
+// Each CTA gathers the selected rows it needs into its own 3-stage ring (CTA 0: all 576 columns,
+// CTA 1: the 512 latent columns), so the two rings advance independently. The running maximum
+// is lazy: O is rescaled only when a row's maximum grows by more than 2^16 (rare; then CTA 1's
+// four row warps rescale O between two PV steps).
+namespace pair {
+constexpr int kH = 128, kDQK = 576, kDV = 512;
+constexpr int kKeys = 64;                       // keys per tile
+constexpr int kStages = 3;
+constexpr int kAtomBytes = kKeys * 128;         // one 64-column swizzle atom of a tile: 8 KB
+constexpr int kAtomsS = 9;                      // CTA 0: dims 0..575
+constexpr int kAtomsO = 8;                      // CTA 1: dims 0..511
+constexpr int kStageS = kAtomsS * kAtomBytes;   // 72 KB
+constexpr int kStageO = kAtomsO * kAtomBytes;   // 64 KB
+constexpr int kPBytes = 128 * 128;              // 128 rows x 64 keys bf16, SW128 K-major
+constexpr int kOffP = kStages * kStageO;        // CTA 1
+constexpr int kRegion = (kStages * kStageS > kOffP + 2 * kPBytes) ? kStages * kStageS
+                                                                   : kOffP + 2 * kPBytes;
+constexpr int kOffAlpha = kRegion;              // fp32 [2][128]   (CTA 1)
+constexpr int kOffFlags = kOffAlpha + 2 * 128 * 4;  // u32 [2][4]  (CTA 1)
+constexpr int kOffL = kOffFlags + 32;           // fp32 [128]      (CTA 1)
+constexpr int kOffMask = kOffL + 128 * 4;       // u64 [kMaxK / 64] (CTA 0)
+constexpr int kOffBar = kOffMask + (kMaxK / kKeys) * 8;
+constexpr int kNumBars = 20;
+constexpr int kOffTmem = kOffBar + kNumBars * 8;
+constexpr int kOffAbort = kOffTmem + 4;
+constexpr int kOffNTiles = kOffAbort + 4;
+constexpr int kOffCorrJ = kOffNTiles + 4;
+constexpr int kSmem = kOffCorrJ + 4;
+constexpr int kColQ = 0, kQCols = kDQK / 2;     // CTA 0 TMEM
+constexpr int kColS = kQCols;                   // two 64-column S tiles
+constexpr int kThreads = 256;                   // 4 row warps, MMA warp, 3 gather warps
+constexpr int kMmaWarp = 4, kGatherWarp0 = 5;   // gather warp 5 + s owns ring stage s
+constexpr float kLazyLog2 = 16.f;               // rescale O only when the max grows by > 2^16
+// barrier indices
+constexpr int kKvFull = 0, kKvEmpty = 3, kQReady = 6, kSFull = 7, kSEmpty = 9, kPFull = 11,
+              kPEmpty = 13, kCorrGo = 15, kCorrReady = 16, kCorrDone = 17, kOFinal = 18,
+              kLReady = 19;
+static_assert(kSmem <= 232448, "smem budget");
+static_assert(kColS + 2 * kKeys <= 512, "TMEM budget");
+}  // namespace pair
+
+__global__ void __launch_bounds__(pair::kThreads, 1)
+sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16* __restrict__ q,
+                       const int32_t* __restrict__ bid, const int32_t* __restrict__ topk, int k,
+                       KvMap kv, float scale_log2, __nv_bfloat16* __restrict__ o,
+                       float* __restrict__ lse) {
+  using namespace pair;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t warp = warp_id(), lane = lane_id();
+  const uint32_t crank = cluster_ctarank();
+  const int64_t t = blockIdx.x >> 1;
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffAbort);
+  uint64_t* masks = reinterpret_cast<uint64_t*>(smem + kOffMask);
+  auto bar = [&](int i) { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
+
+  const bool aligned = (sbase & 1023u) == 0;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) { mbar_init(bar(kKvFull + i), 32); mbar_init(bar(kKvEmpty + i), 1); }
+    mbar_init(bar(kQReady), 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kSFull + i), 1);
+      mbar_init(bar(kSEmpty + i), 4);
+      mbar_init(bar(kPFull + i), 128);
+      mbar_init(bar(kPEmpty + i), 1);
+    }
+    mbar_init(bar(kCorrGo), 1);
+    mbar_init(bar(kCorrReady), 1);
+    mbar_init(bar(kCorrDone), 128);
+    mbar_init(bar(kOFinal), 1);
+    mbar_init(bar(kLReady), 128);
+    *abort_flag = aligned ? 0u : 1u;
+    if (!aligned) report_device_error(kErrBadIndex | 0xB2u);
+    *reinterpret_cast<volatile int*>(smem + kOffNTiles) = 0;
+    fence_mbar_init();
+  }
+  const int32_t* trow = topk + t * k;
+  const int n_tiles_max = (k + kKeys - 1) / kKeys;
+  __syncthreads();
+  for (int tile = static_cast<int>(warp); tile < n_tiles_max; tile += kThreads / 32) {
+    const int j0 = tile * kKeys + static_cast<int>(lane), j1 = j0 + 32;
+    const bool v0 = j0 < k && __ldg(trow + j0) >= 0;
+    const bool v1 = j1 < k && __ldg(trow + j1) >= 0;
+    const uint32_t b0 = __ballot_sync(0xffffffffu, v0), b1 = __ballot_sync(0xffffffffu, v1);
+    if (lane == 0) {
+      masks[tile] = static_cast<uint64_t>(b0) | (static_cast<uint64_t>(b1) << 32);
+      if (b0 | b1) atomicMax(reinterpret_cast<int*>(smem + kOffNTiles), tile + 1);
+    }
+  }
+  if (warp == 0) tmem_alloc<512>(sbase + kOffTmem);
+  __syncthreads();
+  cluster_sync();                                    // the peer's barriers exist from here on
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmem);
+  const int n_tiles = *reinterpret_cast<volatile int*>(smem + kOffNTiles);
+  const int b = __ldg(bid + t);
+  const bool b_ok = b >= 0 && b < kv.n_req;
+  const uint32_t peer = crank ^ 1u;
+
+  if (warp >= kGatherWarp0) {
+    // ---------------------------------------------------------------- row gather (both CTAs)
+    // Warp 5 + s fills ring stage s with tiles s, s + 3, ...: 16-byte cp.async copies into the
+    // 128B-swizzled K-major layout (row r of atom a at a * 8 KB + r * 128, 16-byte chunk c at
+    // (c ^ (r % 8)) * 16), then waits for its own copies, fences them for the tensor core
+    // (async proxy) and arrives. Each of the three warps keeps one tile in flight.
+    const int s = static_cast<int>(warp) - kGatherWarp0;
+    const int n_atoms = crank == 0 ? kAtomsS : kAtomsO;
+    const uint32_t stage = sbase + s * (crank == 0 ? kStageS : kStageO);
+    const int chunk = static_cast<int>(lane & 7);
+    bool bad = !b_ok;
+    for (int j = s; j < n_tiles; j += kStages) {
+      if (!warp_wait(bar(kKvEmpty + s), ((j / kStages) & 1) ^ 1, 0x21, abort_flag)) break;
+      const int e0 = j * kKeys + static_cast<int>(lane);
+      const int s0 = (e0 < k && b_ok) ? __ldg(trow + e0) : -1;
+      const int s1 = (e0 + 32 < k && b_ok) ? __ldg(trow + e0 + 32) : -1;
+      const int32_t r0 = kv_row(kv, b_ok ? b : 0, s0, &bad);
+      const int32_t r1 = kv_row(kv, b_ok ? b : 0, s1, &bad);
+#pragma unroll 4
+      for (int i = 0; i < kKeys / 4; ++i) {
+        const int r = static_cast<int>(lane >> 3) + 4 * i;          // tile row of this lane
+        const int32_t ra = __shfl_sync(0xffffffffu, r0, r & 31);
+        const int32_t rb = __shfl_sync(0xffffffffu, r1, r & 31);
+        const int32_t row = r < 32 ? ra : rb;
+        const bool valid = row < kv.n_rows;
+        const __nv_bfloat16* src = c + (valid ? static_cast<int64_t>(row) * kDQK : 0) + chunk * 8;
+        const uint32_t dst = stage + r * 128 + ((chunk ^ (r & 7)) * 16);
+        for (int a = 0; a < n_atoms; ++a)
+          cp_async16(dst + a * kAtomBytes, src + a * 64, valid ? 16u : 0u);
+      }
+      cp_async_commit();
+      cp_async_wait_all();
+      fence_proxy_async_smem();
+      mbar_arrive(bar(kKvFull + s));
+    }
+    cp_async_wait_all();
+    if (__any_sync(0xffffffffu, bad) && lane == 0) report_device_error(kErrBadIndex);
+  } else if (warp == kMmaWarp) {
+    if (lane == 0 && crank == 0) {
+      // -------------------------------------------------------------- CTA 0: QK issuer
+      const uint32_t idesc = idesc_bf16(128, kKeys, 0, 0);
+      bool ok = mbar_wait(bar(kQReady), 0, 0x22, abort_flag);
+      tc_fence_after();
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int s = j % kStages, sb = j & 1;
+        if (!mbar_wait(bar(kKvFull + s), (j / kStages) & 1, 0x23, abort_flag)) break;
+        if (!mbar_wait(bar(kSEmpty + sb), ((j >> 1) & 1) ^ 1, 0x24, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t kv_base = sbase + s * kStageS;
+#pragma unroll
+        for (int g = 0; g < kDQK / 16; ++g) {
+          const uint64_t db = smem_desc(kv_base + (g >> 2) * kAtomBytes + (g & 3) * 32, 16, 1024,
+                                        kSwizzle128B);
+          umma_ts(tmem + kColS + sb * kKeys, tmem + kColQ + g * 8, db, idesc, g > 0 ? 1u : 0u);
+        }
+        umma_commit(bar(kSFull + sb));
+        umma_commit(bar(kKvEmpty + s));
+      }
+    } else if (lane == 0) {
+      // -------------------------------------------------------------- CTA 1: PV issuer
+      const uint32_t idesc = idesc_bf16(128, 256, 0, 1);
+      volatile int* corr_j = reinterpret_cast<volatile int*>(smem + kOffCorrJ);
+      const volatile uint32_t* flags = reinterpret_cast<const volatile uint32_t*>(smem + kOffFlags);
+      uint32_t n_ev = 0;
+      bool ok = true;
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int s = j % kStages, pb = j & 1;
+        if (!mbar_wait(bar(kKvFull + s), (j / kStages) & 1, 0x25, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_cluster(bar(kPFull + pb), (j >> 1) & 1, 0x26, abort_flag)) { ok = false; break; }
+        if (flags[pb * 4] | flags[pb * 4 + 1] | flags[pb * 4 + 2] | flags[pb * 4 + 3]) {
+          // some row's reference maximum moved: the row warps rescale O after PV(j-1)
+          *corr_j = j;
+          umma_commit(bar(kCorrReady));
+          mbar_arrive(bar(kCorrGo));
+          if (!mbar_wait(bar(kCorrDone), n_ev & 1u, 0x27, abort_flag)) { ok = false; break; }
+          ++n_ev;
+        }
+        tc_fence_after();
+        const uint32_t p_base = sbase + kOffP + pb * kPBytes;
+        const uint32_t v_base = sbase + s * kStageO;
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          const uint64_t da = smem_desc(p_base + kk * 32, 16, 1024, kSwizzle128B);
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const uint64_t dv = smem_desc(v_base + hf * 4 * kAtomBytes + kk * 2048, kAtomBytes, 1024,
+                                          kSwizzle128B);
+            umma_ss(tmem + hf * 256, da, dv, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        umma_commit_multicast(bar(kPEmpty + pb), static_cast<uint16_t>(1u << peer));
+        umma_commit(bar(kKvEmpty + s));
+      }
+      umma_commit(bar(kOFinal));
+      *corr_j = -1;
+      mbar_arrive(bar(kCorrGo));
+    }
+  } else if (crank == 0) {
+    // ---------------------------------------------------------------- CTA 0: softmax warps
+    const int h = static_cast<int>(threadIdx.x);
+    const uint32_t lane_base = (warp * 32u) << 16;
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(q + (t * kH + h) * kDQK);
+#pragma unroll 1
+      for (int c0 = 0; c0 < kQCols; c0 += 16) {
+        uint32_t r[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 v = __ldg(src + (c0 * 2) / 8 + i);
+          r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
+        }
+        tmem_st16(tmem + lane_base + kColQ + c0, r);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(kQReady));
+    }
+    float m_ref = -INFINITY, l_run = 0.f;
+    const uint32_t p_row = sbase + kOffP + (h >> 3) * 1024 + (h & 7) * 128;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int sb = j & 1;
+      if (!warp_wait(bar(kSFull + sb), (j >> 1) & 1, 0x28, abort_flag)) break;
+      tc_fence_after();
+      float sv[kKeys];
+      {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_base + kColS + sb * kKeys, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sv[i] = __uint_as_float(r[i]);
+        tmem_ld32(tmem + lane_base + kColS + sb * kKeys + 32, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sv[32 + i] = __uint_as_float(r[i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kSEmpty + sb));
+      const uint64_t mk = masks[j];
+      float mt = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kKeys; ++i) {
+        sv[i] = ((mk >> i) & 1ull) ? sv[i] * scale_log2 : -INFINITY;
+        mt = fmaxf(mt, sv[i]);
+      }
+      float alpha = 1.f;
+      if (m_ref == -INFINITY) {
+        m_ref = mt;
+      } else if (mt > m_ref + kLazyLog2) {
+        alpha = ex2_approx(m_ref - mt);
+        m_ref = mt;
+      }
+      l_run *= alpha;
+      float psum = 0.f;
+      uint32_t pk[kKeys / 2];
+#pragma unroll
+      for (int i = 0; i < kKeys; i += 2) {
+        const float p0 = m_ref == -INFINITY ? 0.f : ex2_approx(sv[i] - m_ref);
+        const float p1 = m_ref == -INFINITY ? 0.f : ex2_approx(sv[i + 1] - m_ref);
+        psum += p0 + p1;
+        pk[i / 2] = bf16x2_bits(p0, p1);
+      }
+      l_run += psum;
+      const uint32_t any = __any_sync(0xffffffffu, alpha != 1.f) ? 1u : 0u;
+      if (!warp_wait(bar(kPEmpty + sb), ((j >> 1) & 1) ^ 1, 0x29, abort_flag)) break;
+      const uint32_t prow = p_row + sb * kPBytes;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        st_cluster_v4u(prow + ((c ^ (h & 7)) * 16), peer,
+                       make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
+      st_cluster_u32(sbase + kOffAlpha + (sb * 128 + h) * 4, peer, __float_as_uint(alpha));
+      if (lane == 0) st_cluster_u32(sbase + kOffFlags + (sb * 4 + warp) * 4, peer, any);
+      fence_proxy_async_cluster();
+      mbar_arrive_cluster(bar(kPFull + sb), peer);
+    }
+    st_cluster_u32(sbase + kOffL + h * 4, peer, __float_as_uint(l_run));
+    mbar_arrive_cluster(bar(kLReady), peer);
+    if (lse != nullptr)
+      lse[t * kH + h] = l_run > 0.f ? (m_ref + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+  } else {
+    // ---------------------------------------------------------------- CTA 1: O rows
+    const int h = static_cast<int>(threadIdx.x);
+    const uint32_t lane_base = (warp * 32u) << 16;
+    const volatile int* corr_j = reinterpret_cast<const volatile int*>(smem + kOffCorrJ);
+    const float* alpha_buf = reinterpret_cast<const float*>(smem + kOffAlpha);
+    bool ok = true;
+    for (uint32_t n_ev = 0;; ++n_ev) {                // rescale requests, then the end marker
+      if (!warp_wait(bar(kCorrGo), n_ev & 1u, 0x2A, abort_flag)) { ok = false; break; }
+      const int j = *corr_j;
+      if (j < 0) break;
+      if (!warp_wait(bar(kCorrReady), n_ev & 1u, 0x2B, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      const float a = alpha_buf[(j & 1) * 128 + h];
+      if (__any_sync(0xffffffffu, a != 1.f)) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < kDV; c0 += 16) {
+          uint32_t r[16];
+          tmem_ld16(tmem + lane_base + c0, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a);
+          tmem_st16(tmem + lane_base + c0, r);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      mbar_arrive(bar(kCorrDone));
+    }
+    if (ok) ok = warp_wait_cluster(bar(kLReady), 0, 0x2C, abort_flag);
+    if (ok) ok = warp_wait(bar(kOFinal), 0, 0x2D, abort_flag);
+    tc_fence_after();
+    const float l = reinterpret_cast<const volatile float*>(smem + kOffL)[h];
+    const float inv_l = (ok && l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll 1
+    for (int c0 = 0; c0 < kDV; c0 += 16) {
+      uint32_t r[16];
+      if (ok && n_tiles > 0) {
+        tmem_ld16(tmem + lane_base + c0, r);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) r[i] = 0u;
+      }
+      uint32_t pk[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        pk[i] = bf16x2_bits(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
+      uint4* dst = reinterpret_cast<uint4*>(o + (t * kH + h) * kDV + c0);
+      dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc<512>(tmem);
+  }
+  cluster_sync();                                    // no CTA leaves while its peer may write
+}
+
+int launch_mla_pair(const void* q, const void* c, int64_t n_kv_rows, const KvMap& kv,
+                    const int32_t* bid, const int32_t* topk, int64_t n_q, int k, float scale,
+                    void* o, float* lse, cudaStream_t stream) {
+  (void)n_kv_rows;
+  DSA_CHECK_CUDA(cudaFuncSetAttribute(sparse_mla_pair_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, pair::kSmem));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(n_q * 2));
+  cfg.blockDim = dim3(pair::kThreads);
+  cfg.dynamicSmemBytes = pair::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const float scale_log2 = scale * 1.4426950408889634f;
+  DSA_CHECK_CUDA(cudaLaunchKernelEx(&cfg, sparse_mla_pair_kernel,
+                                    static_cast<const __nv_bfloat16*>(c),
+                                    static_cast<const __nv_bfloat16*>(q), bid, topk, k, kv,
+                                    scale_log2, static_cast<__nv_bfloat16*>(o), lse));
+  return DSA_OK;
+}
+
 template <int H, int DQK, int DV>
 int launch_mla(const void* q, const void* c, int64_t n_kv_rows, const KvMap& kv,
                const int32_t* bid, const int32_t* topk, int64_t n_q, int k, float scale,
@@ -448,7 +822,7 @@ int sparse_mla(const void* q, const void* c, int64_t n_kv_rows, const int32_t* c
     return fail(DSA_ERR_INVALID, "mla: q and o must be 16-byte aligned");
   KvMap kv{cu, block_table, max_pages, n_req, n_kv_rows};
   if (H == 128 && dqk == 576 && dv == 512)
-    return launch_mla<128, 576, 512>(q, c, n_kv_rows, kv, bid, topk, n_q, k, scale, o, lse, stream);
+    return launch_mla_pair(q, c, n_kv_rows, kv, bid, topk, n_q, k, scale, o, lse, stream);
   if (H == 8 && dqk == 80 && dv == 64)
     return launch_mla<8, 80, 64>(q, c, n_kv_rows, kv, bid, topk, n_q, k, scale, o, lse, stream);
   return fail(DSA_ERR_UNSUPPORTED, "mla: (H, dqk, dv) = (%d, %d, %d) not built; supported "
