@@ -421,31 +421,38 @@ constexpr int kAtomsO = 8;                      // CTA 1: dims 0..511
 constexpr int kStageS = kAtomsS * kAtomBytes;   // 72 KB
 constexpr int kStageO = kAtomsO * kAtomBytes;   // 64 KB
 constexpr int kPBytes = 128 * 128;              // 128 rows x 64 keys bf16, SW128 K-major
-constexpr int kOffP = kStages * kStageO;        // CTA 1
+constexpr int kAFBytes = 128 * 4 + 16;          // alpha[128] fp32 + flags[4] u32 (528 bytes)
+constexpr int kAFStride = 544;
+constexpr int kOffP = kStages * kStageO;        // CTA 1: two P buffers
 constexpr int kRegion = (kStages * kStageS > kOffP + 2 * kPBytes) ? kStages * kStageS
                                                                    : kOffP + 2 * kPBytes;
-constexpr int kOffAlpha = kRegion;              // fp32 [2][128]   (CTA 1)
-constexpr int kOffFlags = kOffAlpha + 2 * 128 * 4;  // u32 [2][4]  (CTA 1)
-constexpr int kOffL = kOffFlags + 32;           // fp32 [128]      (CTA 1)
-constexpr int kOffMask = kOffL + 128 * 4;       // u64 [kMaxK / 64] (CTA 0)
+constexpr int kOffAlpha = kRegion;              // CTA 1: [2][kAFStride] alpha + flags
+constexpr int kOffL = kOffAlpha + 2 * kAFStride;  // CTA 1: fp32 [128]
+constexpr int kOffMask = kOffL + 128 * 4;       // CTA 0: u64 [kMaxK / 64]
 constexpr int kOffBar = kOffMask + (kMaxK / kKeys) * 8;
-constexpr int kNumBars = 20;
+constexpr int kNumBars = 23;
 constexpr int kOffTmem = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmem + 4;
 constexpr int kOffNTiles = kOffAbort + 4;
 constexpr int kOffCorrJ = kOffNTiles + 4;
 constexpr int kSmem = kOffCorrJ + 4;
-constexpr int kColQ = 0, kQCols = kDQK / 2;     // CTA 0 TMEM
-constexpr int kColS = kQCols;                   // two 64-column S tiles
-constexpr int kThreads = 256;                   // 4 row warps, MMA warp, 3 gather warps
-constexpr int kMmaWarp = 4, kGatherWarp0 = 5;   // gather warp 5 + s owns ring stage s
+constexpr int kColQ = 0, kQCols = kDQK / 2;     // CTA 0 TMEM: Q, then two 64-column S tiles
+constexpr int kColS = kQCols;
+constexpr int kThreads = 320;
+// warp roles: 0-3 row warps (TMEM lane quadrants); 4 MMA issuer (CTA 0: QK of even tiles,
+// CTA 1: PV); 5-7 row gather (warp 5 + s owns ring slot s); 8 P courier (CTA 0); 9 QK issuer
+// of odd tiles (CTA 0). One thread issues a 64-column MMA in ~54 cycles against 32 cycles of
+// tensor work, so QK needs two issuers to keep the tensor pipe busy.
+constexpr int kMmaWarp = 4, kGatherWarp0 = 5, kCourierWarp = 8, kMmaWarp2 = 9;
 constexpr float kLazyLog2 = 16.f;               // rescale O only when the max grows by > 2^16
+constexpr int kQBatch = 24;                     // 16-byte Q loads in flight per thread
 // barrier indices
 constexpr int kKvFull = 0, kKvEmpty = 3, kQReady = 6, kSFull = 7, kSEmpty = 9, kPFull = 11,
               kPEmpty = 13, kCorrGo = 15, kCorrReady = 16, kCorrDone = 17, kOFinal = 18,
-              kLReady = 19;
+              kLReady = 19, kPStaged = 20;     // kPStaged + ring slot (3 barriers)
 static_assert(kSmem <= 232448, "smem budget");
 static_assert(kColS + 2 * kKeys <= 512, "TMEM budget");
+static_assert(kAFBytes % 16 == 0 && kPBytes + kAFBytes <= 3 * kAtomBytes, "P staging");
 }  // namespace pair
 
 __global__ void __launch_bounds__(pair::kThreads, 1)
@@ -458,19 +465,31 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
   const uint32_t sbase = smem_u32(smem);
   const uint32_t warp = warp_id(), lane = lane_id();
   const uint32_t crank = cluster_ctarank();
+  const uint32_t peer = crank ^ 1u;
   const int64_t t = blockIdx.x >> 1;
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffAbort);
   uint64_t* masks = reinterpret_cast<uint64_t*>(smem + kOffMask);
   auto bar = [&](int i) { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
 
+  // CTA 0's row warps start fetching their Q rows at once; the loads land during the set-up.
+  uint4 qreg[kQBatch];
+  const uint4* qsrc = reinterpret_cast<const uint4*>(q + (t * kH + (threadIdx.x & 127)) * kDQK);
+  if (crank == 0 && warp < 4) {
+#pragma unroll
+    for (int i = 0; i < kQBatch; ++i) qreg[i] = __ldg(qsrc + i);
+  }
   const bool aligned = (sbase & 1023u) == 0;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) { mbar_init(bar(kKvFull + i), 32); mbar_init(bar(kKvEmpty + i), 1); }
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(bar(kKvFull + i), 32);
+      mbar_init(bar(kKvEmpty + i), 1);
+      mbar_init(bar(kPStaged + i), 128);
+    }
     mbar_init(bar(kQReady), 128);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kSFull + i), 1);
       mbar_init(bar(kSEmpty + i), 4);
-      mbar_init(bar(kPFull + i), 128);
+      mbar_init(bar(kPFull + i), 1);
       mbar_init(bar(kPEmpty + i), 1);
     }
     mbar_init(bar(kCorrGo), 1);
@@ -486,14 +505,30 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
   const int32_t* trow = topk + t * k;
   const int n_tiles_max = (k + kKeys - 1) / kKeys;
   __syncthreads();
-  for (int tile = static_cast<int>(warp); tile < n_tiles_max; tile += kThreads / 32) {
-    const int j0 = tile * kKeys + static_cast<int>(lane), j1 = j0 + 32;
-    const bool v0 = j0 < k && __ldg(trow + j0) >= 0;
-    const bool v1 = j1 < k && __ldg(trow + j1) >= 0;
-    const uint32_t b0 = __ballot_sync(0xffffffffu, v0), b1 = __ballot_sync(0xffffffffu, v1);
-    if (lane == 0) {
-      masks[tile] = static_cast<uint64_t>(b0) | (static_cast<uint64_t>(b1) << 32);
-      if (b0 | b1) atomicMax(reinterpret_cast<int*>(smem + kOffNTiles), tile + 1);
+  // Tile validity masks: every thread tests 8 consecutive entries; the loop trip count is the
+  // same for all threads, so the shuffles below always see full warps.
+  {
+    uint32_t* mwords = reinterpret_cast<uint32_t*>(masks);
+    for (int base = 0; base < n_tiles_max * kKeys; base += kThreads * 8) {
+      const int e0 = base + static_cast<int>(threadIdx.x) * 8;
+      uint32_t bits = 0;
+      if (e0 + 8 <= k && (k & 3) == 0) {
+        const int4 a = __ldg(reinterpret_cast<const int4*>(trow + e0));
+        const int4 bq = __ldg(reinterpret_cast<const int4*>(trow + e0 + 4));
+        const int v[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) bits |= (v[i] >= 0 ? 1u : 0u) << i;
+      } else {
+        for (int i = 0; i < 8; ++i)
+          bits |= ((e0 + i < k && __ldg(trow + e0 + i) >= 0) ? 1u : 0u) << i;
+      }
+      const uint32_t w = bits << ((threadIdx.x & 3) * 8);       // 4 threads -> one 32-bit word
+      const uint32_t w2 = w | __shfl_xor_sync(0xffffffffu, w, 1);
+      const uint32_t word = w2 | __shfl_xor_sync(0xffffffffu, w2, 2);
+      if ((threadIdx.x & 3) == 0 && e0 < n_tiles_max * kKeys) {
+        mwords[e0 / 32] = word;
+        if (word) atomicMax(reinterpret_cast<int*>(smem + kOffNTiles), e0 / kKeys + 1);
+      }
     }
   }
   if (warp == 0) tmem_alloc<512>(sbase + kOffTmem);
@@ -504,26 +539,32 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
   const int n_tiles = *reinterpret_cast<volatile int*>(smem + kOffNTiles);
   const int b = __ldg(bid + t);
   const bool b_ok = b >= 0 && b < kv.n_req;
-  const uint32_t peer = crank ^ 1u;
 
-  if (warp >= kGatherWarp0) {
+  if (warp >= kGatherWarp0 && warp < kGatherWarp0 + kStages) {
     // ---------------------------------------------------------------- row gather (both CTAs)
-    // Warp 5 + s fills ring stage s with tiles s, s + 3, ...: 16-byte cp.async copies into the
+    // Warp 5 + s fills ring slot s with tiles s, s + 3, ...: 16-byte cp.async copies into the
     // 128B-swizzled K-major layout (row r of atom a at a * 8 KB + r * 128, 16-byte chunk c at
     // (c ^ (r % 8)) * 16), then waits for its own copies, fences them for the tensor core
-    // (async proxy) and arrives. Each of the three warps keeps one tile in flight.
+    // (async proxy) and arrives. The indices of the warp's next tile are fetched before the
+    // current tile's copies are issued.
     const int s = static_cast<int>(warp) - kGatherWarp0;
     const int n_atoms = crank == 0 ? kAtomsS : kAtomsO;
     const uint32_t stage = sbase + s * (crank == 0 ? kStageS : kStageO);
     const int chunk = static_cast<int>(lane & 7);
+    const int bb = b_ok ? b : 0;
     bool bad = !b_ok;
+    auto fetch = [&](int j, int& s0, int& s1) {
+      const int e0 = j * kKeys + static_cast<int>(lane);
+      s0 = (j < n_tiles && e0 < k && b_ok) ? __ldg(trow + e0) : -1;
+      s1 = (j < n_tiles && e0 + 32 < k && b_ok) ? __ldg(trow + e0 + 32) : -1;
+    };
+    int s0, s1;
+    fetch(s, s0, s1);
     for (int j = s; j < n_tiles; j += kStages) {
       if (!warp_wait(bar(kKvEmpty + s), ((j / kStages) & 1) ^ 1, 0x21, abort_flag)) break;
-      const int e0 = j * kKeys + static_cast<int>(lane);
-      const int s0 = (e0 < k && b_ok) ? __ldg(trow + e0) : -1;
-      const int s1 = (e0 + 32 < k && b_ok) ? __ldg(trow + e0 + 32) : -1;
-      const int32_t r0 = kv_row(kv, b_ok ? b : 0, s0, &bad);
-      const int32_t r1 = kv_row(kv, b_ok ? b : 0, s1, &bad);
+      const int32_t r0 = kv_row(kv, bb, s0, &bad);
+      const int32_t r1 = kv_row(kv, bb, s1, &bad);
+      fetch(j + kStages, s0, s1);
 #pragma unroll 4
       for (int i = 0; i < kKeys / 4; ++i) {
         const int r = static_cast<int>(lane >> 3) + 4 * i;          // tile row of this lane
@@ -543,39 +584,50 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
     }
     cp_async_wait_all();
     if (__any_sync(0xffffffffu, bad) && lane == 0) report_device_error(kErrBadIndex);
-  } else if (warp == kMmaWarp) {
-    if (lane == 0 && crank == 0) {
-      // -------------------------------------------------------------- CTA 0: QK issuer
+  } else if ((warp == kMmaWarp || warp == kMmaWarp2) && crank == 0) {
+    if (lane == 0) {
+      // -------------------------------------------------------------- CTA 0: QK issuers
+      // Even tiles -> S buffer 0 (warp 4), odd tiles -> S buffer 1 (warp 9). Descriptors are
+      // precomputed; each k-step only adds a constant to the encoded start address.
+      const int sb = warp == kMmaWarp ? 0 : 1;
       const uint32_t idesc = idesc_bf16(128, kKeys, 0, 0);
+      const uint64_t desc0 = smem_desc(sbase, 16, 1024, kSwizzle128B);
+      const uint32_t d_s = tmem + kColS + sb * kKeys;
       bool ok = mbar_wait(bar(kQReady), 0, 0x22, abort_flag);
       tc_fence_after();
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int s = j % kStages, sb = j & 1;
+      for (int j = sb; j < n_tiles && ok; j += 2) {
+        const int s = j % kStages;
         if (!mbar_wait(bar(kKvFull + s), (j / kStages) & 1, 0x23, abort_flag)) break;
         if (!mbar_wait(bar(kSEmpty + sb), ((j >> 1) & 1) ^ 1, 0x24, abort_flag)) break;
         tc_fence_after();
-        const uint32_t kv_base = sbase + s * kStageS;
+        const uint64_t db0 = desc0 + static_cast<uint64_t>((s * kStageS) >> 4);
 #pragma unroll
-        for (int g = 0; g < kDQK / 16; ++g) {
-          const uint64_t db = smem_desc(kv_base + (g >> 2) * kAtomBytes + (g & 3) * 32, 16, 1024,
-                                        kSwizzle128B);
-          umma_ts(tmem + kColS + sb * kKeys, tmem + kColQ + g * 8, db, idesc, g > 0 ? 1u : 0u);
-        }
+        for (int g = 0; g < kDQK / 16; ++g)
+          umma_ts(d_s, tmem + kColQ + g * 8,
+                  db0 + static_cast<uint64_t>(((g >> 2) * kAtomBytes + (g & 3) * 32) >> 4), idesc,
+                  g > 0 ? 1u : 0u);
         umma_commit(bar(kSFull + sb));
-        umma_commit(bar(kKvEmpty + s));
       }
-    } else if (lane == 0) {
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
       // -------------------------------------------------------------- CTA 1: PV issuer
       const uint32_t idesc = idesc_bf16(128, 256, 0, 1);
       volatile int* corr_j = reinterpret_cast<volatile int*>(smem + kOffCorrJ);
-      const volatile uint32_t* flags = reinterpret_cast<const volatile uint32_t*>(smem + kOffFlags);
+      const uint64_t p_desc0 = smem_desc(sbase + kOffP, 16, 1024, kSwizzle128B);
+      const uint64_t v_desc0 = smem_desc(sbase, kAtomBytes, 1024, kSwizzle128B);
       uint32_t n_ev = 0;
       bool ok = true;
+      for (int i = 0; i < 2 && i < n_tiles; ++i)     // each P buffer expects one bulk delivery
+        mbar_expect_tx(bar(kPFull + i), kPBytes + kAFBytes);
       for (int j = 0; j < n_tiles && ok; ++j) {
         const int s = j % kStages, pb = j & 1;
         if (!mbar_wait(bar(kKvFull + s), (j / kStages) & 1, 0x25, abort_flag)) { ok = false; break; }
-        if (!mbar_wait_cluster(bar(kPFull + pb), (j >> 1) & 1, 0x26, abort_flag)) { ok = false; break; }
-        if (flags[pb * 4] | flags[pb * 4 + 1] | flags[pb * 4 + 2] | flags[pb * 4 + 3]) {
+        if (!mbar_wait(bar(kPFull + pb), (j >> 1) & 1, 0x26, abort_flag)) { ok = false; break; }
+        if (j + 2 < n_tiles) mbar_expect_tx(bar(kPFull + pb), kPBytes + kAFBytes);
+        const volatile uint32_t* flags =
+            reinterpret_cast<const volatile uint32_t*>(smem + kOffAlpha + pb * kAFStride + 512);
+        if (flags[0] | flags[1] | flags[2] | flags[3]) {
           // some row's reference maximum moved: the row warps rescale O after PV(j-1)
           *corr_j = j;
           umma_commit(bar(kCorrReady));
@@ -584,17 +636,15 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
           ++n_ev;
         }
         tc_fence_after();
-        const uint32_t p_base = sbase + kOffP + pb * kPBytes;
-        const uint32_t v_base = sbase + s * kStageO;
+        const uint64_t da0 = p_desc0 + static_cast<uint64_t>((pb * kPBytes) >> 4);
+        const uint64_t dv0 = v_desc0 + static_cast<uint64_t>((s * kStageO) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {
-          const uint64_t da = smem_desc(p_base + kk * 32, 16, 1024, kSwizzle128B);
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            const uint64_t dv = smem_desc(v_base + hf * 4 * kAtomBytes + kk * 2048, kAtomBytes, 1024,
-                                          kSwizzle128B);
-            umma_ss(tmem + hf * 256, da, dv, idesc, (j > 0 || kk > 0) ? 1u : 0u);
-          }
+          for (int hf = 0; hf < 2; ++hf)
+            umma_ss(tmem + hf * 256, da0 + static_cast<uint64_t>((kk * 32) >> 4),
+                    dv0 + static_cast<uint64_t>((hf * 4 * kAtomBytes + kk * 2048) >> 4), idesc,
+                    (j > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit_multicast(bar(kPEmpty + pb), static_cast<uint16_t>(1u << peer));
         umma_commit(bar(kKvEmpty + s));
@@ -603,28 +653,54 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
       *corr_j = -1;
       mbar_arrive(bar(kCorrGo));
     }
-  } else if (crank == 0) {
+  } else if (warp == kCourierWarp) {
+    if (lane == 0 && crank == 0) {
+      // -------------------------------------------------------------- CTA 0: P courier
+      // Ships each staged P tile (+ alpha, flags) to CTA 1 with two bulk copies that complete
+      // on CTA 1's p_full barrier, then hands the ring slot back to its gather warp.
+      for (int j = 0; j < n_tiles; ++j) {
+        const int s = j % kStages, pb = j & 1;
+        if (!mbar_wait(bar(kPStaged + s), (j / kStages) & 1, 0x2E, abort_flag)) break;
+        if (!mbar_wait(bar(kPEmpty + pb), ((j >> 1) & 1) ^ 1, 0x2F, abort_flag)) break;
+        const uint32_t src = sbase + s * kStageS;
+        bulk_copy_to_peer(sbase + kOffP + pb * kPBytes, src, kPBytes, bar(kPFull + pb), peer);
+        bulk_copy_to_peer(sbase + kOffAlpha + pb * kAFStride, src + kPBytes, kAFBytes,
+                          bar(kPFull + pb), peer);
+        bulk_commit();
+        bulk_wait_read_all();
+        mbar_arrive(bar(kKvEmpty + s));
+      }
+      bulk_wait_read_all();
+    }
+  } else if (crank == 0 && warp < 4) {
     // ---------------------------------------------------------------- CTA 0: softmax warps
     const int h = static_cast<int>(threadIdx.x);
     const uint32_t lane_base = (warp * 32u) << 16;
     {
-      const uint4* src = reinterpret_cast<const uint4*>(q + (t * kH + h) * kDQK);
+      // Q row -> TMEM (A operand of QK): 72 loads of 16 bytes, in batches of kQBatch.
+      constexpr int kQLoads = kDQK * 2 / 16;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kQCols; c0 += 16) {
-        uint32_t r[16];
+      for (int base = 0; base < kQLoads; base += kQBatch) {
+        if (base > 0) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint4 v = __ldg(src + (c0 * 2) / 8 + i);
-          r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
+          for (int i = 0; i < kQBatch; ++i) qreg[i] = __ldg(qsrc + base + i);
         }
-        tmem_st16(tmem + lane_base + kColQ + c0, r);
+#pragma unroll
+        for (int i = 0; i < kQBatch; i += 4) {
+          uint32_t r[16];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            r[4 * u] = qreg[i + u].x; r[4 * u + 1] = qreg[i + u].y;
+            r[4 * u + 2] = qreg[i + u].z; r[4 * u + 3] = qreg[i + u].w;
+          }
+          tmem_st16(tmem + lane_base + kColQ + (base + i) * 4, r);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(kQReady));
     }
     float m_ref = -INFINITY, l_run = 0.f;
-    const uint32_t p_row = sbase + kOffP + (h >> 3) * 1024 + (h & 7) * 128;
     for (int j = 0; j < n_tiles; ++j) {
       const int sb = j & 1;
       if (!warp_wait(bar(kSFull + sb), (j >> 1) & 1, 0x28, abort_flag)) break;
@@ -670,27 +746,28 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
       }
       l_run += psum;
       const uint32_t any = __any_sync(0xffffffffu, alpha != 1.f) ? 1u : 0u;
-      if (!warp_wait(bar(kPEmpty + sb), ((j >> 1) & 1) ^ 1, 0x29, abort_flag)) break;
-      const uint32_t prow = p_row + sb * kPBytes;
+      // Stage P (swizzled K-major rows), alpha and the warp flags in ring slot j % 3, which
+      // QK(j) no longer needs; the courier ships them and then frees the slot.
+      uint8_t* slot = smem + (j % kStages) * kStageS;
+      uint8_t* prow = slot + (h >> 3) * 1024 + (h & 7) * 128;
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        st_cluster_v4u(prow + ((c ^ (h & 7)) * 16), peer,
-                       make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
-      st_cluster_u32(sbase + kOffAlpha + (sb * 128 + h) * 4, peer, __float_as_uint(alpha));
-      if (lane == 0) st_cluster_u32(sbase + kOffFlags + (sb * 4 + warp) * 4, peer, any);
-      fence_proxy_async_cluster();
-      mbar_arrive_cluster(bar(kPFull + sb), peer);
+      for (int cc = 0; cc < 8; ++cc)
+        *reinterpret_cast<uint4*>(prow + ((cc ^ (h & 7)) * 16)) =
+            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+      reinterpret_cast<float*>(slot + kPBytes)[h] = alpha;
+      if (lane == 0) reinterpret_cast<uint32_t*>(slot + kPBytes + 512)[warp] = any;
+      fence_proxy_async_smem();
+      mbar_arrive(bar(kPStaged + j % kStages));
     }
     st_cluster_u32(sbase + kOffL + h * 4, peer, __float_as_uint(l_run));
     mbar_arrive_cluster(bar(kLReady), peer);
     if (lse != nullptr)
       lse[t * kH + h] = l_run > 0.f ? (m_ref + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
-  } else {
+  } else if (crank == 1 && warp < 4) {
     // ---------------------------------------------------------------- CTA 1: O rows
     const int h = static_cast<int>(threadIdx.x);
     const uint32_t lane_base = (warp * 32u) << 16;
     const volatile int* corr_j = reinterpret_cast<const volatile int*>(smem + kOffCorrJ);
-    const float* alpha_buf = reinterpret_cast<const float*>(smem + kOffAlpha);
     bool ok = true;
     for (uint32_t n_ev = 0;; ++n_ev) {                // rescale requests, then the end marker
       if (!warp_wait(bar(kCorrGo), n_ev & 1u, 0x2A, abort_flag)) { ok = false; break; }
@@ -698,7 +775,7 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
       if (j < 0) break;
       if (!warp_wait(bar(kCorrReady), n_ev & 1u, 0x2B, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      const float a = alpha_buf[(j & 1) * 128 + h];
+      const float a = reinterpret_cast<const float*>(smem + kOffAlpha + (j & 1) * kAFStride)[h];
       if (__any_sync(0xffffffffu, a != 1.f)) {
 #pragma unroll 1
         for (int c0 = 0; c0 < kDV; c0 += 16) {
@@ -720,22 +797,28 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
     const float l = reinterpret_cast<const volatile float*>(smem + kOffL)[h];
     const float inv_l = (ok && l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll 1
-    for (int c0 = 0; c0 < kDV; c0 += 16) {
-      uint32_t r[16];
+    for (int c0 = 0; c0 < kDV; c0 += 64) {             // 64 columns per TMEM round trip
+      uint32_t r[64];
       if (ok && n_tiles > 0) {
-        tmem_ld16(tmem + lane_base + c0, r);
+        uint32_t (&ra)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
+        uint32_t (&rb)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[32]);
+        tmem_ld32(tmem + lane_base + c0, ra);
+        tmem_ld32(tmem + lane_base + c0 + 32, rb);
         tmem_wait_ld();
       } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) r[i] = 0u;
+        for (int i = 0; i < 64; ++i) r[i] = 0u;
       }
-      uint32_t pk[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        pk[i] = bf16x2_bits(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
       uint4* dst = reinterpret_cast<uint4*>(o + (t * kH + h) * kDV + c0);
-      dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          pk[i] = bf16x2_bits(__uint_as_float(r[8 * v + 2 * i]) * inv_l,
+                              __uint_as_float(r[8 * v + 2 * i + 1]) * inv_l);
+        dst[v] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
     }
   }
 

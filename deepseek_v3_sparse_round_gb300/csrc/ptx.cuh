@@ -159,6 +159,26 @@ __device__ __forceinline__ void fence_proxy_async_cluster() {
   asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to the buffer at the same
+// offset as `dst_local` in CTA `cta_rank`, completing `bytes` of transaction on that CTA's
+// barrier at the offset of `bar_local`.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_local, uint32_t src, uint32_t bytes,
+                                                  uint32_t bar_local, uint32_t cta_rank) {
+  asm volatile(
+      "{\n .reg .b32 rd, rb;\n mapa.shared::cluster.u32 rd, %0, %4;\n"
+      " mapa.shared::cluster.u32 rb, %3, %4;\n"
+      " cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [rd], [%1], %2, [rb];\n}\n"
+      ::"r"(dst_local), "r"(src), "r"(bytes), "r"(bar_local), "r"(cta_rank)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until every committed bulk copy of this thread has finished reading its source.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
