@@ -22,6 +22,7 @@
 //
 // Small heads (H <= 128 with dv <= 256, e.g. H = 8, dqk = 80, dv = 64) run the same code on a
 // single CTA that owns the whole contraction and output.
+#include <algorithm>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -415,6 +416,7 @@ namespace pair {
 constexpr int kH = 128, kDQK = 576, kDV = 512;
 constexpr int kKeys = 64;                       // keys per tile
 constexpr int kStages = 3;
+constexpr int kMaxTiles = kMaxK / kKeys;        // 64
 constexpr int kAtomBytes = kKeys * 128;         // one 64-column swizzle atom of a tile: 8 KB
 constexpr int kAtomsS = 9;                      // CTA 0: dims 0..575
 constexpr int kAtomsO = 8;                      // CTA 1: dims 0..511
@@ -426,39 +428,46 @@ constexpr int kAFStride = 544;
 constexpr int kOffP = kStages * kStageO;        // CTA 1: two P buffers
 constexpr int kRegion = (kStages * kStageS > kOffP + 2 * kPBytes) ? kStages * kStageS
                                                                    : kOffP + 2 * kPBytes;
+constexpr int kOffMask = kStages * kStageS;     // CTA 0: u64 [2][kMaxTiles] (spare 8 KB)
 constexpr int kOffAlpha = kRegion;              // CTA 1: [2][kAFStride] alpha + flags
-constexpr int kOffL = kOffAlpha + 2 * kAFStride;  // CTA 1: fp32 [128]
-constexpr int kOffMask = kOffL + 128 * 4;       // CTA 0: u64 [kMaxK / 64]
-constexpr int kOffBar = kOffMask + (kMaxK / kKeys) * 8;
-constexpr int kNumBars = 23;
+constexpr int kOffL = kOffAlpha + 2 * kAFStride;  // CTA 1: fp32 [2][128]
+constexpr int kOffNT = kOffL + 2 * 128 * 4;     // both: int [2] tiles of the query
+constexpr int kOffBar = kOffNT + 8;
+constexpr int kNumBars = 31;
 constexpr int kOffTmem = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmem + 4;
-constexpr int kOffNTiles = kOffAbort + 4;
-constexpr int kOffCorrJ = kOffNTiles + 4;
+constexpr int kOffCorrJ = kOffAbort + 4;
 constexpr int kSmem = kOffCorrJ + 4;
 constexpr int kColQ = 0, kQCols = kDQK / 2;     // CTA 0 TMEM: Q, then two 64-column S tiles
 constexpr int kColS = kQCols;
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 // warp roles: 0-3 row warps (TMEM lane quadrants); 4 MMA issuer (CTA 0: QK of even tiles,
 // CTA 1: PV); 5-7 row gather (warp 5 + s owns ring slot s); 8 P courier (CTA 0); 9 QK issuer
-// of odd tiles (CTA 0). One thread issues a 64-column MMA in ~54 cycles against 32 cycles of
-// tensor work, so QK needs two issuers to keep the tensor pipe busy.
-constexpr int kMmaWarp = 4, kGatherWarp0 = 5, kCourierWarp = 8, kMmaWarp2 = 9;
+// of odd tiles (CTA 0); 10 query metadata (both). One thread issues a 64-column MMA in ~54
+// cycles against 32 cycles of tensor work, so QK needs two issuers to keep the pipe busy.
+constexpr int kMmaWarp = 4, kGatherWarp0 = 5, kCourierWarp = 8, kMmaWarp2 = 9, kMetaWarp = 10;
 constexpr float kLazyLog2 = 16.f;               // rescale O only when the max grows by > 2^16
-constexpr int kQBatch = 24;                     // 16-byte Q loads in flight per thread
+constexpr int kQBatch = 36;                     // 16-byte Q loads in flight per thread
 // barrier indices
-constexpr int kKvFull = 0, kKvEmpty = 3, kQReady = 6, kSFull = 7, kSEmpty = 9, kPFull = 11,
-              kPEmpty = 13, kCorrGo = 15, kCorrReady = 16, kCorrDone = 17, kOFinal = 18,
-              kLReady = 19, kPStaged = 20;     // kPStaged + ring slot (3 barriers)
+constexpr int kKvFull = 0, kKvEmpty = 3, kPStaged = 6, kSFull = 9, kSEmpty = 11, kPFull = 13,
+              kPEmpty = 15, kMetaFull = 17, kMetaEmpty = 19, kLReady = 21, kLEmpty = 23,
+              kQReady = 25, kQAck = 26, kCorrGo = 27, kCorrReady = 28, kCorrDone = 29,
+              kOFinal = 30;
+constexpr int kODrained = kOFinal;              // see below: CTA 1 reuses index 30 pairs
 static_assert(kSmem <= 232448, "smem budget");
+static_assert(kOffMask + 2 * kMaxTiles * 8 <= kRegion, "masks fit in CTA 0's spare region");
 static_assert(kColS + 2 * kKeys <= 512, "TMEM budget");
 static_assert(kAFBytes % 16 == 0 && kPBytes + kAFBytes <= 3 * kAtomBytes, "P staging");
 }  // namespace pair
 
+// Persistent: cluster i of n processes queries i, i + n, i + 2n, ... Every role walks the same
+// query sequence and, inside it, the same global tile sequence (tiles of earlier queries
+// included), so ring slots, S/P buffers and their barrier phases continue across queries.
+// Every role waits for every per-query phase in order, also for queries where it has no tile.
 __global__ void __launch_bounds__(pair::kThreads, 1)
 sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16* __restrict__ q,
                        const int32_t* __restrict__ bid, const int32_t* __restrict__ topk, int k,
-                       KvMap kv, float scale_log2, __nv_bfloat16* __restrict__ o,
+                       int64_t n_q, KvMap kv, float scale_log2, __nv_bfloat16* __restrict__ o,
                        float* __restrict__ lse) {
   using namespace pair;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -466,18 +475,16 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
   const uint32_t warp = warp_id(), lane = lane_id();
   const uint32_t crank = cluster_ctarank();
   const uint32_t peer = crank ^ 1u;
-  const int64_t t = blockIdx.x >> 1;
+  const int64_t cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+  const int n_my = static_cast<int>((n_q - cluster + n_clusters - 1) / n_clusters);  // queries
+  auto query = [&](int n) { return cluster + static_cast<int64_t>(n) * n_clusters; };
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffAbort);
-  uint64_t* masks = reinterpret_cast<uint64_t*>(smem + kOffMask);
+  volatile int* nt_buf = reinterpret_cast<volatile int*>(smem + kOffNT);
   auto bar = [&](int i) { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
+  // CTA 1 has no S tiles, Q or courier: it reuses barrier slots 9..12 for its own per-query
+  // barriers (o_drained at 9, o_final at 30).
+  const int kOD = kSFull;
 
-  // CTA 0's row warps start fetching their Q rows at once; the loads land during the set-up.
-  uint4 qreg[kQBatch];
-  const uint4* qsrc = reinterpret_cast<const uint4*>(q + (t * kH + (threadIdx.x & 127)) * kDQK);
-  if (crank == 0 && warp < 4) {
-#pragma unroll
-    for (int i = 0; i < kQBatch; ++i) qreg[i] = __ldg(qsrc + i);
-  }
   const bool aligned = (sbase & 1023u) == 0;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -485,128 +492,179 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
       mbar_init(bar(kKvEmpty + i), 1);
       mbar_init(bar(kPStaged + i), 128);
     }
-    mbar_init(bar(kQReady), 128);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(kSFull + i), 1);
+      mbar_init(bar(kSFull + i), crank == 0 ? 1 : 4);      // CTA 1: [9] = o_drained (4 warps)
       mbar_init(bar(kSEmpty + i), 4);
       mbar_init(bar(kPFull + i), 1);
       mbar_init(bar(kPEmpty + i), 1);
+      mbar_init(bar(kMetaFull + i), 1);
+      mbar_init(bar(kMetaEmpty + i), crank == 0 ? 10 : 8);
+      mbar_init(bar(kLReady + i), 128);
+      mbar_init(bar(kLEmpty + i), 128);
     }
+    mbar_init(bar(kQReady), 128);
+    mbar_init(bar(kQAck), 2);
     mbar_init(bar(kCorrGo), 1);
     mbar_init(bar(kCorrReady), 1);
     mbar_init(bar(kCorrDone), 128);
     mbar_init(bar(kOFinal), 1);
-    mbar_init(bar(kLReady), 128);
     *abort_flag = aligned ? 0u : 1u;
     if (!aligned) report_device_error(kErrBadIndex | 0xB2u);
-    *reinterpret_cast<volatile int*>(smem + kOffNTiles) = 0;
     fence_mbar_init();
-  }
-  const int32_t* trow = topk + t * k;
-  const int n_tiles_max = (k + kKeys - 1) / kKeys;
-  __syncthreads();
-  // Tile validity masks: every thread tests 8 consecutive entries; the loop trip count is the
-  // same for all threads, so the shuffles below always see full warps.
-  {
-    uint32_t* mwords = reinterpret_cast<uint32_t*>(masks);
-    for (int base = 0; base < n_tiles_max * kKeys; base += kThreads * 8) {
-      const int e0 = base + static_cast<int>(threadIdx.x) * 8;
-      uint32_t bits = 0;
-      if (e0 + 8 <= k && (k & 3) == 0) {
-        const int4 a = __ldg(reinterpret_cast<const int4*>(trow + e0));
-        const int4 bq = __ldg(reinterpret_cast<const int4*>(trow + e0 + 4));
-        const int v[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) bits |= (v[i] >= 0 ? 1u : 0u) << i;
-      } else {
-        for (int i = 0; i < 8; ++i)
-          bits |= ((e0 + i < k && __ldg(trow + e0 + i) >= 0) ? 1u : 0u) << i;
-      }
-      const uint32_t w = bits << ((threadIdx.x & 3) * 8);       // 4 threads -> one 32-bit word
-      const uint32_t w2 = w | __shfl_xor_sync(0xffffffffu, w, 1);
-      const uint32_t word = w2 | __shfl_xor_sync(0xffffffffu, w2, 2);
-      if ((threadIdx.x & 3) == 0 && e0 < n_tiles_max * kKeys) {
-        mwords[e0 / 32] = word;
-        if (word) atomicMax(reinterpret_cast<int*>(smem + kOffNTiles), e0 / kKeys + 1);
-      }
-    }
   }
   if (warp == 0) tmem_alloc<512>(sbase + kOffTmem);
   __syncthreads();
   cluster_sync();                                    // the peer's barriers exist from here on
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmem);
-  const int n_tiles = *reinterpret_cast<volatile int*>(smem + kOffNTiles);
-  const int b = __ldg(bid + t);
-  const bool b_ok = b >= 0 && b < kv.n_req;
 
-  if (warp >= kGatherWarp0 && warp < kGatherWarp0 + kStages) {
+  // meta_empty arrivals per query: CTA 0: 3 gather + 2 QK + courier + 4 softmax warps (at the
+  // end of the query: they read the masks until then); CTA 1: 3 gather + PV + 4 row warps.
+  auto meta_wait = [&](int n, bool warp_uniform) -> int {
+    const uint32_t mb = bar(kMetaFull + (n & 1)), par = (n >> 1) & 1;
+    const bool ok = warp_uniform ? warp_wait(mb, par, 0x40, abort_flag)
+                                 : mbar_wait(mb, par, 0x40, abort_flag);
+    return ok ? nt_buf[n & 1] : -1;
+  };
+
+  if (warp == kMetaWarp) {
+    // ---------------------------------------------------------------- query metadata
+    // Tile count (tiles up to the last valid entry) and, in CTA 0, the per-tile validity masks
+    // of each query, two queries ahead; also pulls the query's Q rows into L2.
+    for (int n = 0; n < n_my; ++n) {
+      if (!warp_wait(bar(kMetaEmpty + (n & 1)), ((n >> 1) & 1) ^ 1, 0x41, abort_flag)) break;
+      const int64_t t = query(n);
+      const int32_t* trow = topk + t * k;
+      if (crank == 0) {
+        const char* qrow = reinterpret_cast<const char*>(q + t * kH * kDQK);
+        for (int off = static_cast<int>(lane) * 128; off < kH * kDQK * 2; off += 32 * 128)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow + off));
+      }
+      uint32_t* mwords = reinterpret_cast<uint32_t*>(smem + kOffMask) + (n & 1) * kMaxTiles * 2;
+      const int n_tiles_max = (k + kKeys - 1) / kKeys;
+      int last = 0;
+      for (int base = 0; base < n_tiles_max * kKeys; base += 32 * 8) {
+        const int e0 = base + static_cast<int>(lane) * 8;
+        uint32_t bits = 0;
+        if (e0 + 8 <= k && (k & 3) == 0) {
+          const int4 a = __ldg(reinterpret_cast<const int4*>(trow + e0));
+          const int4 bq = __ldg(reinterpret_cast<const int4*>(trow + e0 + 4));
+          const int v[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) bits |= (v[i] >= 0 ? 1u : 0u) << i;
+        } else {
+          for (int i = 0; i < 8; ++i)
+            bits |= ((e0 + i < k && __ldg(trow + e0 + i) >= 0) ? 1u : 0u) << i;
+        }
+        const uint32_t w = bits << ((lane & 3) * 8);           // 4 lanes -> one 32-bit word
+        const uint32_t w2 = w | __shfl_xor_sync(0xffffffffu, w, 1);
+        const uint32_t word = w2 | __shfl_xor_sync(0xffffffffu, w2, 2);
+        if ((lane & 3) == 0 && e0 < n_tiles_max * kKeys) {
+          if (crank == 0) mwords[e0 / 32] = word;
+          if (word) last = e0 / kKeys + 1;
+        }
+      }
+      last = __reduce_max_sync(0xffffffffu, last);
+      if (lane == 0) {
+        nt_buf[n & 1] = last;
+        mbar_arrive(bar(kMetaFull + (n & 1)));
+      }
+      __syncwarp();
+    }
+  } else if (warp >= kGatherWarp0 && warp < kGatherWarp0 + kStages) {
     // ---------------------------------------------------------------- row gather (both CTAs)
-    // Warp 5 + s fills ring slot s with tiles s, s + 3, ...: 16-byte cp.async copies into the
-    // 128B-swizzled K-major layout (row r of atom a at a * 8 KB + r * 128, 16-byte chunk c at
-    // (c ^ (r % 8)) * 16), then waits for its own copies, fences them for the tensor core
-    // (async proxy) and arrives. The indices of the warp's next tile are fetched before the
-    // current tile's copies are issued.
+    // Warp 5 + s fills ring slot s with the global tiles g = s (mod 3): 16-byte cp.async
+    // copies into the 128B-swizzled K-major layout (row r of atom a at a * 8 KB + r * 128,
+    // 16-byte chunk c at (c ^ (r % 8)) * 16), then waits for its own copies, fences them for
+    // the tensor core (async proxy) and arrives.
     const int s = static_cast<int>(warp) - kGatherWarp0;
     const int n_atoms = crank == 0 ? kAtomsS : kAtomsO;
     const uint32_t stage = sbase + s * (crank == 0 ? kStageS : kStageO);
     const int chunk = static_cast<int>(lane & 7);
-    const int bb = b_ok ? b : 0;
-    bool bad = !b_ok;
-    auto fetch = [&](int j, int& s0, int& s1) {
-      const int e0 = j * kKeys + static_cast<int>(lane);
-      s0 = (j < n_tiles && e0 < k && b_ok) ? __ldg(trow + e0) : -1;
-      s1 = (j < n_tiles && e0 + 32 < k && b_ok) ? __ldg(trow + e0 + 32) : -1;
-    };
-    int s0, s1;
-    fetch(s, s0, s1);
-    for (int j = s; j < n_tiles; j += kStages) {
-      if (!warp_wait(bar(kKvEmpty + s), ((j / kStages) & 1) ^ 1, 0x21, abort_flag)) break;
-      const int32_t r0 = kv_row(kv, bb, s0, &bad);
-      const int32_t r1 = kv_row(kv, bb, s1, &bad);
-      fetch(j + kStages, s0, s1);
+    bool bad = false;
+    int64_t g0 = 0;                                  // global index of the query's first tile
+    for (int n = 0; n < n_my && !*abort_flag; ++n) {
+      const int nt = meta_wait(n, true);
+      if (nt < 0) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kMetaEmpty + (n & 1)));
+      const int64_t t = query(n);
+      const int32_t* trow = topk + t * k;
+      const int b = __ldg(bid + t);
+      const bool b_ok = b >= 0 && b < kv.n_req;
+      bad |= !b_ok;
+      const int bb = b_ok ? b : 0;
+      const int j_first = static_cast<int>(((s - g0) % kStages + kStages) % kStages);
+      auto fetch = [&](int j, int& s0, int& s1) {
+        const int e0 = j * kKeys + static_cast<int>(lane);
+        s0 = (j < nt && e0 < k && b_ok) ? __ldg(trow + e0) : -1;
+        s1 = (j < nt && e0 + 32 < k && b_ok) ? __ldg(trow + e0 + 32) : -1;
+      };
+      int s0, s1;
+      fetch(j_first, s0, s1);
+      bool ok = true;
+      for (int j = j_first; j < nt; j += kStages) {
+        const int64_t g = g0 + j;
+        if (!warp_wait(bar(kKvEmpty + s), static_cast<uint32_t>(((g / kStages) & 1) ^ 1), 0x21,
+                       abort_flag)) { ok = false; break; }
+        const int32_t r0 = kv_row(kv, bb, s0, &bad);
+        const int32_t r1 = kv_row(kv, bb, s1, &bad);
+        fetch(j + kStages, s0, s1);
 #pragma unroll 4
-      for (int i = 0; i < kKeys / 4; ++i) {
-        const int r = static_cast<int>(lane >> 3) + 4 * i;          // tile row of this lane
-        const int32_t ra = __shfl_sync(0xffffffffu, r0, r & 31);
-        const int32_t rb = __shfl_sync(0xffffffffu, r1, r & 31);
-        const int32_t row = r < 32 ? ra : rb;
-        const bool valid = row < kv.n_rows;
-        const __nv_bfloat16* src = c + (valid ? static_cast<int64_t>(row) * kDQK : 0) + chunk * 8;
-        const uint32_t dst = stage + r * 128 + ((chunk ^ (r & 7)) * 16);
-        for (int a = 0; a < n_atoms; ++a)
-          cp_async16(dst + a * kAtomBytes, src + a * 64, valid ? 16u : 0u);
+        for (int i = 0; i < kKeys / 4; ++i) {
+          const int r = static_cast<int>(lane >> 3) + 4 * i;        // tile row of this lane
+          const int32_t ra = __shfl_sync(0xffffffffu, r0, r & 31);
+          const int32_t rb = __shfl_sync(0xffffffffu, r1, r & 31);
+          const int32_t row = r < 32 ? ra : rb;
+          const bool valid = row < kv.n_rows;
+          const __nv_bfloat16* src = c + (valid ? static_cast<int64_t>(row) * kDQK : 0) + chunk * 8;
+          const uint32_t dst = stage + r * 128 + ((chunk ^ (r & 7)) * 16);
+          for (int a = 0; a < n_atoms; ++a)
+            cp_async16(dst + a * kAtomBytes, src + a * 64, valid ? 16u : 0u);
+        }
+        cp_async_commit();
+        cp_async_wait_all();
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kKvFull + s));
       }
-      cp_async_commit();
-      cp_async_wait_all();
-      fence_proxy_async_smem();
-      mbar_arrive(bar(kKvFull + s));
+      if (!ok) break;
+      g0 += nt;
     }
     cp_async_wait_all();
     if (__any_sync(0xffffffffu, bad) && lane == 0) report_device_error(kErrBadIndex);
   } else if ((warp == kMmaWarp || warp == kMmaWarp2) && crank == 0) {
     if (lane == 0) {
       // -------------------------------------------------------------- CTA 0: QK issuers
-      // Even tiles -> S buffer 0 (warp 4), odd tiles -> S buffer 1 (warp 9). Descriptors are
-      // precomputed; each k-step only adds a constant to the encoded start address.
+      // Even global tiles -> S buffer 0 (warp 4), odd -> S buffer 1 (warp 9). Descriptors
+      // are precomputed; each k-step only adds a constant to the encoded start address.
       const int sb = warp == kMmaWarp ? 0 : 1;
       const uint32_t idesc = idesc_bf16(128, kKeys, 0, 0);
       const uint64_t desc0 = smem_desc(sbase, 16, 1024, kSwizzle128B);
       const uint32_t d_s = tmem + kColS + sb * kKeys;
-      bool ok = mbar_wait(bar(kQReady), 0, 0x22, abort_flag);
-      tc_fence_after();
-      for (int j = sb; j < n_tiles && ok; j += 2) {
-        const int s = j % kStages;
-        if (!mbar_wait(bar(kKvFull + s), (j / kStages) & 1, 0x23, abort_flag)) break;
-        if (!mbar_wait(bar(kSEmpty + sb), ((j >> 1) & 1) ^ 1, 0x24, abort_flag)) break;
+      int64_t g0 = 0;
+      bool ok = true;
+      for (int n = 0; n < n_my && ok; ++n) {
+        const int nt = meta_wait(n, false);
+        if (nt < 0) break;
+        mbar_arrive(bar(kMetaEmpty + (n & 1)));
+        if (!mbar_wait(bar(kQReady), n & 1, 0x22, abort_flag)) break;
+        mbar_arrive(bar(kQAck));                     // lets the softmax load the next Q later
         tc_fence_after();
-        const uint64_t db0 = desc0 + static_cast<uint64_t>((s * kStageS) >> 4);
+        for (int j = static_cast<int>(((sb - g0) % 2 + 2) % 2); j < nt; j += 2) {
+          const int64_t g = g0 + j;
+          const int s = static_cast<int>(g % kStages);
+          if (!mbar_wait(bar(kKvFull + s), static_cast<uint32_t>((g / kStages) & 1), 0x23, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(bar(kSEmpty + sb), static_cast<uint32_t>(((g >> 1) & 1) ^ 1), 0x24, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t db0 = desc0 + static_cast<uint64_t>((s * kStageS) >> 4);
 #pragma unroll
-        for (int g = 0; g < kDQK / 16; ++g)
-          umma_ts(d_s, tmem + kColQ + g * 8,
-                  db0 + static_cast<uint64_t>(((g >> 2) * kAtomBytes + (g & 3) * 32) >> 4), idesc,
-                  g > 0 ? 1u : 0u);
-        umma_commit(bar(kSFull + sb));
+          for (int gg = 0; gg < kDQK / 16; ++gg)
+            umma_ts(d_s, tmem + kColQ + gg * 8,
+                    db0 + static_cast<uint64_t>(((gg >> 2) * kAtomBytes + (gg & 3) * 32) >> 4),
+                    idesc, gg > 0 ? 1u : 0u);
+          umma_commit(bar(kSFull + sb));
+        }
+        g0 += nt;
       }
     }
   } else if (warp == kMmaWarp) {
@@ -618,57 +676,79 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
       const uint64_t v_desc0 = smem_desc(sbase, kAtomBytes, 1024, kSwizzle128B);
       uint32_t n_ev = 0;
       bool ok = true;
-      for (int i = 0; i < 2 && i < n_tiles; ++i)     // each P buffer expects one bulk delivery
-        mbar_expect_tx(bar(kPFull + i), kPBytes + kAFBytes);
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int s = j % kStages, pb = j & 1;
-        if (!mbar_wait(bar(kKvFull + s), (j / kStages) & 1, 0x25, abort_flag)) { ok = false; break; }
-        if (!mbar_wait(bar(kPFull + pb), (j >> 1) & 1, 0x26, abort_flag)) { ok = false; break; }
-        if (j + 2 < n_tiles) mbar_expect_tx(bar(kPFull + pb), kPBytes + kAFBytes);
-        const volatile uint32_t* flags =
-            reinterpret_cast<const volatile uint32_t*>(smem + kOffAlpha + pb * kAFStride + 512);
-        if (flags[0] | flags[1] | flags[2] | flags[3]) {
-          // some row's reference maximum moved: the row warps rescale O after PV(j-1)
-          *corr_j = j;
-          umma_commit(bar(kCorrReady));
-          mbar_arrive(bar(kCorrGo));
-          if (!mbar_wait(bar(kCorrDone), n_ev & 1u, 0x27, abort_flag)) { ok = false; break; }
-          ++n_ev;
-        }
+      // each P buffer always has one armed delivery (one bulk copy of P + alpha + flags)
+      for (int i = 0; i < 2; ++i) mbar_expect_tx(bar(kPFull + i), kPBytes + kAFBytes);
+      int64_t g0 = 0;
+      for (int n = 0; n < n_my && ok; ++n) {
+        const int nt = meta_wait(n, false);
+        if (nt < 0) break;
+        mbar_arrive(bar(kMetaEmpty + (n & 1)));
+        // O of the previous query must be drained before this query overwrites it
+        if (n > 0 && !mbar_wait(bar(kOD), (n - 1) & 1, 0x32, abort_flag)) break;
         tc_fence_after();
-        const uint64_t da0 = p_desc0 + static_cast<uint64_t>((pb * kPBytes) >> 4);
-        const uint64_t dv0 = v_desc0 + static_cast<uint64_t>((s * kStageO) >> 4);
+        for (int j = 0; j < nt && ok; ++j) {
+          const int64_t g = g0 + j;
+          const int s = static_cast<int>(g % kStages), pb = static_cast<int>(g & 1);
+          if (!mbar_wait(bar(kKvFull + s), static_cast<uint32_t>((g / kStages) & 1), 0x25, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(bar(kPFull + pb), static_cast<uint32_t>((g >> 1) & 1), 0x26, abort_flag)) { ok = false; break; }
+          mbar_expect_tx(bar(kPFull + pb), kPBytes + kAFBytes);
+          const volatile uint32_t* flags =
+              reinterpret_cast<const volatile uint32_t*>(smem + kOffAlpha + pb * kAFStride + 512);
+          if (flags[0] | flags[1] | flags[2] | flags[3]) {
+            // a row's reference maximum moved: the row warps rescale O after the previous PV
+            *corr_j = static_cast<int>(pb);
+            umma_commit(bar(kCorrReady));
+            mbar_arrive(bar(kCorrGo));
+            if (!mbar_wait(bar(kCorrDone), n_ev & 1u, 0x27, abort_flag)) { ok = false; break; }
+            ++n_ev;
+          }
+          tc_fence_after();
+          const uint64_t da0 = p_desc0 + static_cast<uint64_t>((pb * kPBytes) >> 4);
+          const uint64_t dv0 = v_desc0 + static_cast<uint64_t>((s * kStageO) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          for (int kk = 0; kk < kKeys / 16; ++kk) {
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf)
-            umma_ss(tmem + hf * 256, da0 + static_cast<uint64_t>((kk * 32) >> 4),
-                    dv0 + static_cast<uint64_t>((hf * 4 * kAtomBytes + kk * 2048) >> 4), idesc,
-                    (j > 0 || kk > 0) ? 1u : 0u);
+            for (int hf = 0; hf < 2; ++hf)
+              umma_ss(tmem + hf * 256, da0 + static_cast<uint64_t>((kk * 32) >> 4),
+                      dv0 + static_cast<uint64_t>((hf * 4 * kAtomBytes + kk * 2048) >> 4), idesc,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit_multicast(bar(kPEmpty + pb), static_cast<uint16_t>(1u << peer));
+          umma_commit(bar(kKvEmpty + s));
         }
-        umma_commit_multicast(bar(kPEmpty + pb), static_cast<uint16_t>(1u << peer));
-        umma_commit(bar(kKvEmpty + s));
+        if (!ok) break;
+        umma_commit(bar(kOFinal));                   // O of this query complete
+        *corr_j = -1;                                // end of this query's rescale requests
+        mbar_arrive(bar(kCorrGo));
+        g0 += nt;
       }
-      umma_commit(bar(kOFinal));
-      *corr_j = -1;
-      mbar_arrive(bar(kCorrGo));
     }
   } else if (warp == kCourierWarp) {
     if (lane == 0 && crank == 0) {
       // -------------------------------------------------------------- CTA 0: P courier
       // Ships each staged P tile (+ alpha, flags) to CTA 1 with two bulk copies that complete
       // on CTA 1's p_full barrier, then hands the ring slot back to its gather warp.
-      for (int j = 0; j < n_tiles; ++j) {
-        const int s = j % kStages, pb = j & 1;
-        if (!mbar_wait(bar(kPStaged + s), (j / kStages) & 1, 0x2E, abort_flag)) break;
-        if (!mbar_wait(bar(kPEmpty + pb), ((j >> 1) & 1) ^ 1, 0x2F, abort_flag)) break;
-        const uint32_t src = sbase + s * kStageS;
-        bulk_copy_to_peer(sbase + kOffP + pb * kPBytes, src, kPBytes, bar(kPFull + pb), peer);
-        bulk_copy_to_peer(sbase + kOffAlpha + pb * kAFStride, src + kPBytes, kAFBytes,
-                          bar(kPFull + pb), peer);
-        bulk_commit();
-        bulk_wait_read_all();
-        mbar_arrive(bar(kKvEmpty + s));
+      int64_t g0 = 0;
+      for (int n = 0; n < n_my; ++n) {
+        const int nt = meta_wait(n, false);
+        if (nt < 0) break;
+        mbar_arrive(bar(kMetaEmpty + (n & 1)));
+        bool ok = true;
+        for (int j = 0; j < nt; ++j) {
+          const int64_t g = g0 + j;
+          const int s = static_cast<int>(g % kStages), pb = static_cast<int>(g & 1);
+          if (!mbar_wait(bar(kPStaged + s), static_cast<uint32_t>((g / kStages) & 1), 0x2E, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(bar(kPEmpty + pb), static_cast<uint32_t>(((g >> 1) & 1) ^ 1), 0x2F, abort_flag)) { ok = false; break; }
+          const uint32_t src = sbase + s * kStageS;
+          bulk_copy_to_peer(sbase + kOffP + pb * kPBytes, src, kPBytes, bar(kPFull + pb), peer);
+          bulk_copy_to_peer(sbase + kOffAlpha + pb * kAFStride, src + kPBytes, kAFBytes,
+                            bar(kPFull + pb), peer);
+          bulk_commit();
+          bulk_wait_read_all();
+          mbar_arrive(bar(kKvEmpty + s));
+        }
+        if (!ok) break;
+        g0 += nt;
       }
       bulk_wait_read_all();
     }
@@ -676,148 +756,183 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
     // ---------------------------------------------------------------- CTA 0: softmax warps
     const int h = static_cast<int>(threadIdx.x);
     const uint32_t lane_base = (warp * 32u) << 16;
-    {
-      // Q row -> TMEM (A operand of QK): 72 loads of 16 bytes, in batches of kQBatch.
-      constexpr int kQLoads = kDQK * 2 / 16;
+    int64_t g0 = 0;
+    for (int n = 0; n < n_my; ++n) {
+      const int nt = meta_wait(n, true);
+      if (nt < 0) break;
+      const int64_t t = query(n);
+      // Q row -> TMEM (A operand of QK) once every QK of the previous query is complete (its
+      // last softmax tile saw them) and both issuers acknowledged the previous Q.
+      if (n > 0 && !warp_wait(bar(kQAck), (n - 1) & 1, 0x42, abort_flag)) break;
+      {
+        const uint4* qsrc = reinterpret_cast<const uint4*>(q + (t * kH + h) * kDQK);
+        constexpr int kQLoads = kDQK * 2 / 16;       // 72
 #pragma unroll 1
-      for (int base = 0; base < kQLoads; base += kQBatch) {
-        if (base > 0) {
+        for (int base = 0; base < kQLoads; base += kQBatch) {
+          uint4 qreg[kQBatch];
 #pragma unroll
           for (int i = 0; i < kQBatch; ++i) qreg[i] = __ldg(qsrc + base + i);
-        }
 #pragma unroll
-        for (int i = 0; i < kQBatch; i += 4) {
-          uint32_t r[16];
+          for (int i = 0; i < kQBatch; i += 4) {
+            uint32_t r[16];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            r[4 * u] = qreg[i + u].x; r[4 * u + 1] = qreg[i + u].y;
-            r[4 * u + 2] = qreg[i + u].z; r[4 * u + 3] = qreg[i + u].w;
+            for (int u = 0; u < 4; ++u) {
+              r[4 * u] = qreg[i + u].x; r[4 * u + 1] = qreg[i + u].y;
+              r[4 * u + 2] = qreg[i + u].z; r[4 * u + 3] = qreg[i + u].w;
+            }
+            tmem_st16(tmem + lane_base + kColQ + (base + i) * 4, r);
           }
-          tmem_st16(tmem + lane_base + kColQ + (base + i) * 4, r);
         }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(kQReady));
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(kQReady));
-    }
-    float m_ref = -INFINITY, l_run = 0.f;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int sb = j & 1;
-      if (!warp_wait(bar(kSFull + sb), (j >> 1) & 1, 0x28, abort_flag)) break;
-      tc_fence_after();
-      float sv[kKeys];
-      {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_base + kColS + sb * kKeys, r);
-        tmem_wait_ld();
+      const uint64_t* masks = reinterpret_cast<const uint64_t*>(smem + kOffMask) + (n & 1) * kMaxTiles;
+      float m_ref = -INFINITY, l_run = 0.f;
+      bool ok = true;
+      for (int j = 0; j < nt; ++j) {
+        const int64_t g = g0 + j;
+        const int sb = static_cast<int>(g & 1), slot_i = static_cast<int>(g % kStages);
+        if (!warp_wait(bar(kSFull + sb), static_cast<uint32_t>((g >> 1) & 1), 0x28, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        float sv[kKeys];
+        {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_base + kColS + sb * kKeys, r);
+          tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) sv[i] = __uint_as_float(r[i]);
-        tmem_ld32(tmem + lane_base + kColS + sb * kKeys + 32, r);
-        tmem_wait_ld();
+          for (int i = 0; i < 32; ++i) sv[i] = __uint_as_float(r[i]);
+          tmem_ld32(tmem + lane_base + kColS + sb * kKeys + 32, r);
+          tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) sv[32 + i] = __uint_as_float(r[i]);
+          for (int i = 0; i < 32; ++i) sv[32 + i] = __uint_as_float(r[i]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kSEmpty + sb));
+        const uint64_t mk = masks[j];
+        float mt = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kKeys; ++i) {
+          sv[i] = ((mk >> i) & 1ull) ? sv[i] * scale_log2 : -INFINITY;
+          mt = fmaxf(mt, sv[i]);
+        }
+        float alpha = 1.f;
+        if (m_ref == -INFINITY) {
+          m_ref = mt;
+        } else if (mt > m_ref + kLazyLog2) {
+          alpha = ex2_approx(m_ref - mt);
+          m_ref = mt;
+        }
+        l_run *= alpha;
+        float psum = 0.f;
+        uint32_t pk[kKeys / 2];
+#pragma unroll
+        for (int i = 0; i < kKeys; i += 2) {
+          const float p0 = m_ref == -INFINITY ? 0.f : ex2_approx(sv[i] - m_ref);
+          const float p1 = m_ref == -INFINITY ? 0.f : ex2_approx(sv[i + 1] - m_ref);
+          psum += p0 + p1;
+          pk[i / 2] = bf16x2_bits(p0, p1);
+        }
+        l_run += psum;
+        const uint32_t any = __any_sync(0xffffffffu, alpha != 1.f) ? 1u : 0u;
+        // Stage P (swizzled K-major rows), alpha and the warp flags in the ring slot of this
+        // tile, which QK no longer needs; the courier ships them and then frees the slot.
+        uint8_t* slot = smem + slot_i * kStageS;
+        uint8_t* prow = slot + (h >> 3) * 1024 + (h & 7) * 128;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          *reinterpret_cast<uint4*>(prow + ((cc ^ (h & 7)) * 16)) =
+              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+        reinterpret_cast<float*>(slot + kPBytes)[h] = alpha;
+        if (lane == 0) reinterpret_cast<uint32_t*>(slot + kPBytes + 512)[warp] = any;
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kPStaged + slot_i));
       }
-      tc_fence_before();
+      if (!ok) break;
+      // l of this query -> CTA 1 (buffer n % 2, free once CTA 1 read query n - 2's), lse
+      if (n >= 2 && !warp_wait(bar(kLEmpty + (n & 1)), ((n >> 1) & 1) ^ 1, 0x43, abort_flag)) break;
+      st_cluster_u32(sbase + kOffL + ((n & 1) * 128 + h) * 4, peer, __float_as_uint(l_run));
+      mbar_arrive_cluster(bar(kLReady + (n & 1)), peer);
+      if (lse != nullptr)
+        lse[t * kH + h] = l_run > 0.f ? (m_ref + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kSEmpty + sb));
-      const uint64_t mk = masks[j];
-      float mt = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < kKeys; ++i) {
-        sv[i] = ((mk >> i) & 1ull) ? sv[i] * scale_log2 : -INFINITY;
-        mt = fmaxf(mt, sv[i]);
-      }
-      float alpha = 1.f;
-      if (m_ref == -INFINITY) {
-        m_ref = mt;
-      } else if (mt > m_ref + kLazyLog2) {
-        alpha = ex2_approx(m_ref - mt);
-        m_ref = mt;
-      }
-      l_run *= alpha;
-      float psum = 0.f;
-      uint32_t pk[kKeys / 2];
-#pragma unroll
-      for (int i = 0; i < kKeys; i += 2) {
-        const float p0 = m_ref == -INFINITY ? 0.f : ex2_approx(sv[i] - m_ref);
-        const float p1 = m_ref == -INFINITY ? 0.f : ex2_approx(sv[i + 1] - m_ref);
-        psum += p0 + p1;
-        pk[i / 2] = bf16x2_bits(p0, p1);
-      }
-      l_run += psum;
-      const uint32_t any = __any_sync(0xffffffffu, alpha != 1.f) ? 1u : 0u;
-      // Stage P (swizzled K-major rows), alpha and the warp flags in ring slot j % 3, which
-      // QK(j) no longer needs; the courier ships them and then frees the slot.
-      uint8_t* slot = smem + (j % kStages) * kStageS;
-      uint8_t* prow = slot + (h >> 3) * 1024 + (h & 7) * 128;
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc)
-        *reinterpret_cast<uint4*>(prow + ((cc ^ (h & 7)) * 16)) =
-            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-      reinterpret_cast<float*>(slot + kPBytes)[h] = alpha;
-      if (lane == 0) reinterpret_cast<uint32_t*>(slot + kPBytes + 512)[warp] = any;
-      fence_proxy_async_smem();
-      mbar_arrive(bar(kPStaged + j % kStages));
+      if (lane == 0) mbar_arrive(bar(kMetaEmpty + (n & 1)));
+      g0 += nt;
     }
-    st_cluster_u32(sbase + kOffL + h * 4, peer, __float_as_uint(l_run));
-    mbar_arrive_cluster(bar(kLReady), peer);
-    if (lse != nullptr)
-      lse[t * kH + h] = l_run > 0.f ? (m_ref + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
   } else if (crank == 1 && warp < 4) {
     // ---------------------------------------------------------------- CTA 1: O rows
     const int h = static_cast<int>(threadIdx.x);
     const uint32_t lane_base = (warp * 32u) << 16;
     const volatile int* corr_j = reinterpret_cast<const volatile int*>(smem + kOffCorrJ);
-    bool ok = true;
-    for (uint32_t n_ev = 0;; ++n_ev) {                // rescale requests, then the end marker
-      if (!warp_wait(bar(kCorrGo), n_ev & 1u, 0x2A, abort_flag)) { ok = false; break; }
-      const int j = *corr_j;
-      if (j < 0) break;
-      if (!warp_wait(bar(kCorrReady), n_ev & 1u, 0x2B, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      const float a = reinterpret_cast<const float*>(smem + kOffAlpha + (j & 1) * kAFStride)[h];
-      if (__any_sync(0xffffffffu, a != 1.f)) {
+    uint32_t n_go = 0, n_ev = 0;                     // corr_go completions, rescale events
+    for (int n = 0; n < n_my; ++n) {
+      const int nt = meta_wait(n, true);
+      if (nt < 0) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kMetaEmpty + (n & 1)));
+      const int64_t t = query(n);
+      bool ok = true;
+      for (;;) {                                     // rescale requests, then the end marker
+        if (!warp_wait(bar(kCorrGo), n_go & 1u, 0x2A, abort_flag)) { ok = false; break; }
+        ++n_go;
+        const int pb = *corr_j;
+        if (pb < 0) break;
+        if (!warp_wait(bar(kCorrReady), n_ev & 1u, 0x2B, abort_flag)) { ok = false; break; }
+        ++n_ev;
+        tc_fence_after();
+        const float a = reinterpret_cast<const float*>(smem + kOffAlpha + pb * kAFStride)[h];
+        if (__any_sync(0xffffffffu, a != 1.f)) {
 #pragma unroll 1
-        for (int c0 = 0; c0 < kDV; c0 += 16) {
-          uint32_t r[16];
-          tmem_ld16(tmem + lane_base + c0, r);
-          tmem_wait_ld();
+          for (int c0 = 0; c0 < kDV; c0 += 16) {
+            uint32_t r[16];
+            tmem_ld16(tmem + lane_base + c0, r);
+            tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a);
-          tmem_st16(tmem + lane_base + c0, r);
+            for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a);
+            tmem_st16(tmem + lane_base + c0, r);
+          }
+          tmem_wait_st();
         }
-        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(kCorrDone));
       }
-      tc_fence_before();
-      mbar_arrive(bar(kCorrDone));
-    }
-    if (ok) ok = warp_wait_cluster(bar(kLReady), 0, 0x2C, abort_flag);
-    if (ok) ok = warp_wait(bar(kOFinal), 0, 0x2D, abort_flag);
-    tc_fence_after();
-    const float l = reinterpret_cast<const volatile float*>(smem + kOffL)[h];
-    const float inv_l = (ok && l > 0.f) ? 1.f / l : 0.f;
+      if (ok) ok = warp_wait_cluster(bar(kLReady + (n & 1)), (n >> 1) & 1, 0x2C, abort_flag);
+      if (ok) ok = warp_wait(bar(kOFinal), n & 1, 0x2D, abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      const float l = reinterpret_cast<const volatile float*>(smem + kOffL)[(n & 1) * 128 + h];
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      // the l buffer may be refilled (query n + 2) once every row read it
+      mbar_arrive_cluster(bar(kLEmpty + (n & 1)), peer);
 #pragma unroll 1
-    for (int c0 = 0; c0 < kDV; c0 += 64) {             // 64 columns per TMEM round trip
-      uint32_t r[64];
-      if (ok && n_tiles > 0) {
-        uint32_t (&ra)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
-        uint32_t (&rb)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[32]);
-        tmem_ld32(tmem + lane_base + c0, ra);
-        tmem_ld32(tmem + lane_base + c0 + 32, rb);
-        tmem_wait_ld();
-      } else {
+      for (int c0 = 0; c0 < kDV; c0 += 64) {           // 64 columns per TMEM round trip
+        uint32_t r[64];
+        if (nt > 0) {
+          uint32_t (&ra)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
+          uint32_t (&rb)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[32]);
+          tmem_ld32(tmem + lane_base + c0, ra);
+          tmem_ld32(tmem + lane_base + c0 + 32, rb);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) r[i] = 0u;
-      }
-      uint4* dst = reinterpret_cast<uint4*>(o + (t * kH + h) * kDV + c0);
+          for (int i = 0; i < 64; ++i) r[i] = 0u;
+        }
+        if (c0 + 64 == kDV) {                        // all of O read: PV may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kOD));
+        }
+        uint4* dst = reinterpret_cast<uint4*>(o + (t * kH + h) * kDV + c0);
 #pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        uint32_t pk[4];
+        for (int v = 0; v < 8; ++v) {
+          uint32_t pk[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          pk[i] = bf16x2_bits(__uint_as_float(r[8 * v + 2 * i]) * inv_l,
-                              __uint_as_float(r[8 * v + 2 * i + 1]) * inv_l);
-        dst[v] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          for (int i = 0; i < 4; ++i)
+            pk[i] = bf16x2_bits(__uint_as_float(r[8 * v + 2 * i]) * inv_l,
+                                __uint_as_float(r[8 * v + 2 * i + 1]) * inv_l);
+          dst[v] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
       }
     }
   }
@@ -836,8 +951,9 @@ int launch_mla_pair(const void* q, const void* c, int64_t n_kv_rows, const KvMap
   (void)n_kv_rows;
   DSA_CHECK_CUDA(cudaFuncSetAttribute(sparse_mla_pair_kernel,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, pair::kSmem));
+  const int64_t pairs = std::min<int64_t>(n_q, num_sms_cached() / 2);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(n_q * 2));
+  cfg.gridDim = dim3(static_cast<unsigned>(pairs * 2));
   cfg.blockDim = dim3(pair::kThreads);
   cfg.dynamicSmemBytes = pair::kSmem;
   cfg.stream = stream;
@@ -851,7 +967,7 @@ int launch_mla_pair(const void* q, const void* c, int64_t n_kv_rows, const KvMap
   const float scale_log2 = scale * 1.4426950408889634f;
   DSA_CHECK_CUDA(cudaLaunchKernelEx(&cfg, sparse_mla_pair_kernel,
                                     static_cast<const __nv_bfloat16*>(c),
-                                    static_cast<const __nv_bfloat16*>(q), bid, topk, k, kv,
+                                    static_cast<const __nv_bfloat16*>(q), bid, topk, k, n_q, kv,
                                     scale_log2, static_cast<__nv_bfloat16*>(o), lse));
   return DSA_OK;
 }
