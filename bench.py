@@ -43,6 +43,26 @@ def peaks():
     return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
 
 
+def profiled_traffic(kernel_file, summary):
+    """DRAM bytes per launch from a committed ncu summary, only while the kernel source is the
+    one that was profiled (its sha1 prefix is recorded next to the figure); else None."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "deepseek_v3_sparse_round_gb300", "csrc", kernel_file), "rb") as f:
+            sha = hashlib.sha1(f.read()).hexdigest()[:12]
+        fields = {}
+        with open(os.path.join(ROOT, "profiles", summary), encoding="utf-8") as f:
+            for line in f:
+                if ":" in line and line.split(":")[0].strip() in ("traffic_bytes_per_launch", "source_sha1"):
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        if fields.get("source_sha1") == sha:
+            return int(fields["traffic_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        pass
+    return None
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -264,9 +284,10 @@ def gpu_arm(args):
                    "queries_per_gpu": st.n_r, "kv_tokens": st.N, "topk": st.wl.topk,
                    "l2": "flushed between timed steps (256 MB write)",
                    "step": "split+gather, 2x rerange, indexer scores, top-k, sparse MLA"},
-        "roofline": {"bound": "tensor", "kernel": "sparse_mla_kernel<128,576,512>",
+        "roofline": {"bound": "tensor", "kernel": "sparse_mla_pair_kernel",
                      "achieved": round(achieved, 1), "peak": pk["bf16"], "unit": "TFLOP/s",
-                     "frac": round(achieved / pk["bf16"], 4), "traffic": None,
+                     "frac": round(achieved / pk["bf16"], 4),
+                     "traffic": profiled_traffic("mla.cu", "sparse_mla_pair_varlen_rank3.md"),
                      "peak_source": f"{pk['source']} bf16 burst (MEASURED_PEAKS.json)",
                      "algorithmic_flop_per_launch": mla_flops},
         "indexer_topk": {"algorithmic_flop_per_step": idx_flops},
