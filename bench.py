@@ -63,6 +63,21 @@ def profiled_traffic(kernel_file, summary):
     return None
 
 
+def shard_for_rank(rank: int, sp: int) -> int:
+    """GPU `rank` of the job processes shard (BASE_RANK + rank) % sp of the varlen batch."""
+    return (BASE_RANK + rank) % sp
+
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """The job's time is the slowest rank's: all-reduce MAX (no-op without a process group)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -207,7 +222,7 @@ def gpu_arm(args):
     import deepseek_v3_sparse_round_gb300 as dsa
     import workloads as W
 
-    shard = (BASE_RANK + rank) % W.WORKLOADS[WORKLOAD_ID].sp
+    shard = shard_for_rank(rank, W.WORKLOADS[WORKLOAD_ID].sp)
     st = ShardStep(torch, dsa, W, shard, device)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)   # > L2
     stream = torch.cuda.current_stream()
@@ -235,11 +250,8 @@ def gpu_arm(args):
     wall = time.perf_counter() - t_wall
     step_ms = [a.elapsed_time(b) for a, b, _, _ in evs]
     mla_ms = [c.elapsed_time(d) for _, _, c, d in evs]
-    dev_s = sum(step_ms) / 1e3
+    dev_s = max_over_ranks(sum(step_ms) / 1e3, dist, device)
     if dist:
-        t = torch.tensor([dev_s], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dev_s = float(t.item())
         dist.barrier()
     torch.cuda.synchronize()
 
@@ -256,11 +268,7 @@ def gpu_arm(args):
         st.h_o.copy_(st.o, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_s = e0.elapsed_time(e1) / 1e3
-    if dist:
-        t = torch.tensor([e2e_s], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, dist, device)
 
     errors = dsa.dsa_read_device_errors()
     if rank != 0:

@@ -3,7 +3,7 @@
 // "[DeepSeek v3.2] 上下文并行详解", section 2.B: rank r keeps the flattened tokens
 // r, r+sp, r+2sp, ... and a metadata kernel recomputes cu_seqlens and batch indices after the
 // scatter. Section 4 part 3 step B: the all-gathered rows arrive rank by rank and are put back
-// in logical order. Both kernels are plain HBM streams: 16-byte vector loads and stores over
+// in logical order. Both are plain HBM streams: 16-byte vector loads and stores over
 // the flattened (row, 16-byte chunk) index space, several independent chunks in flight per
 // thread, grid sized to a multiple of the SM count.
 #include <cstdint>
@@ -41,69 +41,65 @@ __device__ __forceinline__ int find_request(const int32_t* cu, int n_req, int64_
   int lo = 0, hi = n_req - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (static_cast<int64_t>(__ldg(cu + mid)) <= g) lo = mid; else hi = mid - 1;
+    if (static_cast<int64_t>(cu[mid]) <= g) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
 
-__global__ void __launch_bounds__(kThreads)
-split_meta_kernel(const int32_t* __restrict__ cu, int n_req, int64_t n_r, int sp, int rank,
-                  int32_t* __restrict__ cu_shard, int32_t* __restrict__ pos,
-                  int32_t* __restrict__ bid, int32_t* __restrict__ gidx) {
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (int64_t i = i0; i <= n_req; i += stride)
-    cu_shard[i] = shard_count_below(__ldg(cu + i), sp, rank);
-  for (int64_t t = i0; t < n_r; t += stride) {
-    const int64_t g = rank + t * sp;
-    const int b = find_request(cu, n_req, g);
-    pos[t] = static_cast<int32_t>(g - __ldg(cu + b));
-    bid[t] = b;
-    if (gidx) gidx[t] = static_cast<int32_t>(g);
-  }
-}
-
-// Source row of destination row `r` for the two copy patterns.
+// Source row of destination row `r` for the two copy patterns; the index arithmetic runs in
+// the copy loop's index type (32-bit whenever the chunk count fits).
 struct SplitRows {
   int sp, rank;
-  __device__ __forceinline__ int64_t operator()(int64_t t) const { return rank + t * sp; }
+  template <typename I>
+  __device__ __forceinline__ int64_t operator()(I t) const {
+    return rank + static_cast<int64_t>(t) * sp;
+  }
 };
 struct RerangeRows {
   int sp;
   int64_t per_rank;   // floor(N / sp) (packed) -- unused when padded
   int64_t rem;        // N % sp (packed)
   int64_t stride;     // > 0: padded blocks
-  __device__ __forceinline__ int64_t operator()(int64_t g) const {
-    const int64_t q = g % sp, j = g / sp;
-    const int64_t off = stride > 0 ? q * stride : q * per_rank + (q < rem ? q : rem);
-    return off + j;
+  template <typename I>
+  __device__ __forceinline__ int64_t operator()(I g) const {
+    const I q = g % static_cast<I>(sp), j = g / static_cast<I>(sp);
+    const int64_t qq = static_cast<int64_t>(q);
+    const int64_t off = stride > 0 ? qq * stride : qq * per_rank + (qq < rem ? qq : rem);
+    return off + static_cast<int64_t>(j);
   }
 };
 
-template <class RowMap>
+// Copy rows of 16-byte chunks: destination chunk i = (row i / cpr, chunk i % cpr) comes from
+// source row map(row). Index math in Idx (32-bit whenever the chunk count fits), kUnroll
+// independent 16-byte loads in flight per thread before their stores.
+template <class RowMap, typename Idx>
+__device__ __forceinline__ void copy_rows_body(const int4* __restrict__ src, int4* __restrict__ dst,
+                                               Idx total, Idx cpr, RowMap map) {
+  const Idx stride = static_cast<Idx>(gridDim.x) * blockDim.x;
+  Idx i = static_cast<Idx>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + (kUnroll - 1) * stride < total; i += kUnroll * stride) {
+    int4 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const Idx cc = i + u * stride;
+      const Idx r = cc / cpr;
+      v[u] = ld_stream(src + map(r) * cpr + (cc - r * cpr));
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) st_stream(dst + (i + u * stride), v[u]);
+  }
+  for (; i < total; i += stride) {
+    const Idx r = i / cpr;
+    st_stream(dst + i, ld_stream(src + map(r) * cpr + (i - r * cpr)));
+  }
+}
+
+template <class RowMap, typename Idx>
 __global__ void __launch_bounds__(kThreads)
 copy_rows_v16_kernel(const int4* __restrict__ src, int4* __restrict__ dst, int64_t n_rows,
                      int64_t chunks_per_row, RowMap map) {
-  const int64_t total = n_rows * chunks_per_row;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (; i + (kUnroll - 1) * stride < total; i += kUnroll * stride) {
-    int4 v[kUnroll];
-    int64_t di[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t c = i + u * stride;
-      const int64_t r = c / chunks_per_row, col = c - r * chunks_per_row;
-      di[u] = c;
-      v[u] = ld_stream(src + map(r) * chunks_per_row + col);
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) st_stream(dst + di[u], v[u]);
-  }
-  for (; i < total; i += stride) {
-    const int64_t r = i / chunks_per_row, col = i - r * chunks_per_row;
-    st_stream(dst + i, ld_stream(src + map(r) * chunks_per_row + col));
-  }
+  copy_rows_body<RowMap, Idx>(src, dst, static_cast<Idx>(n_rows * chunks_per_row),
+                              static_cast<Idx>(chunks_per_row), map);
 }
 
 template <class RowMap>
@@ -116,6 +112,44 @@ copy_rows_bytes_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ ds
        i += stride) {
     const int64_t r = i / row_bytes, col = i - r * row_bytes;
     dst[i] = src[map(r) * row_bytes + col];
+  }
+}
+
+// One launch for the whole split: shard cu_seqlens (closed form), per-token metadata (the
+// request found by binary search over cu staged in shared memory) and, when asked, the 16-byte
+// row gather of the shard's tokens.
+constexpr int kCuSmem = 4096;
+template <bool kGather>
+__global__ void __launch_bounds__(kThreads)
+split_kernel(const int32_t* __restrict__ cu, int n_req, int64_t n_r, int sp, int rank,
+             int32_t* __restrict__ cu_shard, int32_t* __restrict__ pos, int32_t* __restrict__ bid,
+             int32_t* __restrict__ gidx, const int4* __restrict__ src, int4* __restrict__ dst,
+             int64_t chunks_per_row) {
+  __shared__ int32_t s_cu[kCuSmem];
+  const bool staged = n_req + 1 <= kCuSmem;
+  if (staged) {
+    for (int i = threadIdx.x; i <= n_req; i += blockDim.x) s_cu[i] = __ldg(cu + i);
+    __syncthreads();
+  }
+  const int32_t* cuv = staged ? s_cu : cu;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (int64_t i = i0; i <= n_req; i += stride) cu_shard[i] = shard_count_below(cuv[i], sp, rank);
+  for (int64_t t = i0; t < n_r; t += stride) {
+    const int64_t g = rank + t * sp;
+    const int b = find_request(cuv, n_req, g);
+    pos[t] = static_cast<int32_t>(g - cuv[b]);
+    bid[t] = b;
+    if (gidx) gidx[t] = static_cast<int32_t>(g);
+  }
+  if (kGather) {
+    const int64_t total = n_r * chunks_per_row;
+    if (total < (int64_t(1) << 31))
+      copy_rows_body<SplitRows, uint32_t>(src, dst, static_cast<uint32_t>(total),
+                                          static_cast<uint32_t>(chunks_per_row),
+                                          SplitRows{sp, rank});
+    else
+      copy_rows_body<SplitRows, int64_t>(src, dst, total, chunks_per_row, SplitRows{sp, rank});
   }
 }
 
@@ -147,8 +181,14 @@ int launch_copy_rows(const void* src, void* dst, int64_t n_rows, int64_t row_byt
                    (reinterpret_cast<uintptr_t>(dst) % 16 == 0);
   if (vec) {
     const int64_t cpr = row_bytes / 16;
-    copy_rows_v16_kernel<RowMap><<<grid_for(n_rows * cpr, kUnroll), kThreads, 0, stream>>>(
-        static_cast<const int4*>(src), static_cast<int4*>(dst), n_rows, cpr, map);
+    if (n_rows * cpr < (int64_t(1) << 31))
+      copy_rows_v16_kernel<RowMap, uint32_t><<<grid_for(n_rows * cpr, kUnroll), kThreads, 0,
+                                               stream>>>(
+          static_cast<const int4*>(src), static_cast<int4*>(dst), n_rows, cpr, map);
+    else
+      copy_rows_v16_kernel<RowMap, int64_t><<<grid_for(n_rows * cpr, kUnroll), kThreads, 0,
+                                              stream>>>(
+          static_cast<const int4*>(src), static_cast<int4*>(dst), n_rows, cpr, map);
   } else {
     copy_rows_bytes_kernel<RowMap><<<grid_for(n_rows * row_bytes, 4), kThreads, 0, stream>>>(
         static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), n_rows, row_bytes, map);
@@ -180,8 +220,20 @@ int split_metadata(const int32_t* cu, int n_req, int64_t n_tokens, int sp, int r
   if (src_rows && (!dst_rows || row_bytes <= 0))
     return fail(DSA_ERR_INVALID, "split: a row gather needs dst_rows and row_bytes > 0");
   const int64_t meta_items = (n_r > n_req + 1) ? n_r : n_req + 1;
-  split_meta_kernel<<<grid_for(meta_items, 1), kThreads, 0, stream>>>(cu, n_req, n_r, sp, rank,
-                                                                      cu_shard, pos, bid, gidx);
+  const bool vec = src_rows && (row_bytes % 16 == 0) &&
+                   (reinterpret_cast<uintptr_t>(src_rows) % 16 == 0) &&
+                   (reinterpret_cast<uintptr_t>(dst_rows) % 16 == 0);
+  if (vec) {                                       // metadata + row gather in one launch
+    const int64_t cpr = row_bytes / 16;
+    const int64_t items = n_r * cpr > meta_items ? n_r * cpr : meta_items;
+    split_kernel<true><<<grid_for(items, kUnroll), kThreads, 0, stream>>>(
+        cu, n_req, n_r, sp, rank, cu_shard, pos, bid, gidx, static_cast<const int4*>(src_rows),
+        static_cast<int4*>(dst_rows), cpr);
+    DSA_CHECK_CUDA(cudaGetLastError());
+    return DSA_OK;
+  }
+  split_kernel<false><<<grid_for(meta_items, 1), kThreads, 0, stream>>>(
+      cu, n_req, n_r, sp, rank, cu_shard, pos, bid, gidx, nullptr, nullptr, 0);
   DSA_CHECK_CUDA(cudaGetLastError());
   if (src_rows) return launch_copy_rows(src_rows, dst_rows, n_r, row_bytes, SplitRows{sp, rank},
                                         stream);
