@@ -403,61 +403,71 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16*
 // =============================================================================================
 // H = 128, dqk = 576, dv = 512: a cluster of two CTAs per query with split roles.
 //   CTA 0 ("S side"): Q (128 x 576 bf16) in TMEM as the A operand (288 columns) and two S tiles
-//     of 128 x 64 fp32 (128 columns), so QK(j+1) runs while the softmax of tile j runs. Its
-//     softmax warps write P (bf16) straight into CTA 1's shared memory, with the per-row
-//     rescale factors, then arrive on CTA 1's barrier.
+//     of 128 x 48 fp32, so QK(j+1) runs while the softmax of tile j runs. Its softmax warps
+//     stage P (bf16), the per-row rescale factors and flags in the ring slot that QK has just
+//     consumed; a courier warp ships them to CTA 1 with bulk DSMEM copies and frees the slot.
 //   CTA 1 ("O side"): O (128 x 512 fp32) fills its TMEM; it accumulates O += P . V with two
 //     N = 256 MMAs per 16 keys and writes o = O / l at the end.
-// Each CTA gathers the selected rows it needs into its own 3-stage ring (CTA 0: all 576 columns,
-// CTA 1: the 512 latent columns), so the two rings advance independently. The running maximum
-// is lazy: O is rescaled only when a row's maximum grows by more than 2^16 (rare; then CTA 1's
-// four row warps rescale O between two PV steps).
+// Each CTA gathers the selected rows it needs into its own 4-slot ring of 48-key tiles (CTA 0:
+// all 576 columns, CTA 1: the 512 latent columns). A CTA 0 slot is held from its gather
+// through QK, softmax and the P shipment, so the ring has four slots of 48 keys rather than
+// three of 64 (the shared memory is the same). The running maximum is lazy: O is rescaled only
+// when a row's maximum grows by more than 2^16 (rare; then CTA 1's four row warps rescale O
+// between two PV steps).
 namespace pair {
 constexpr int kH = 128, kDQK = 576, kDV = 512;
-constexpr int kKeys = 64;                       // keys per tile
-constexpr int kStages = 3;
-constexpr int kMaxTiles = kMaxK / kKeys;        // 64
-constexpr int kAtomBytes = kKeys * 128;         // one 64-column swizzle atom of a tile: 8 KB
+constexpr int kKeys = 48;                       // keys per tile
+constexpr int kStages = 4;
+// validity bits of one query's top-k entries, up to the end of its last tile (+1 word so the
+// two-word read of a tile's bits stays inside the buffer)
+constexpr int kMaskWords = ((kMaxK + kKeys - 1) / kKeys * kKeys + 31) / 32 + 1;
+constexpr int kAtomBytes = kKeys * 128;         // one 64-column swizzle atom of a tile: 6 KB
 constexpr int kAtomsS = 9;                      // CTA 0: dims 0..575
 constexpr int kAtomsO = 8;                      // CTA 1: dims 0..511
-constexpr int kStageS = kAtomsS * kAtomBytes;   // 72 KB
-constexpr int kStageO = kAtomsO * kAtomBytes;   // 64 KB
-constexpr int kPBytes = 128 * 128;              // 128 rows x 64 keys bf16, SW128 K-major
+constexpr int kStageS = kAtomsS * kAtomBytes;   // 54 KB
+constexpr int kStageO = kAtomsO * kAtomBytes;   // 48 KB
+constexpr int kPBytes = 128 * 128;              // 128 rows x 64 keys bf16 (48 used), SW128 K-major
 constexpr int kAFBytes = 128 * 4 + 16;          // alpha[128] fp32 + flags[4] u32 (528 bytes)
 constexpr int kAFStride = 544;
 constexpr int kOffP = kStages * kStageO;        // CTA 1: two P buffers
 constexpr int kRegion = (kStages * kStageS > kOffP + 2 * kPBytes) ? kStages * kStageS
                                                                    : kOffP + 2 * kPBytes;
-constexpr int kOffMask = kStages * kStageS;     // CTA 0: u64 [2][kMaxTiles] (spare 8 KB)
+constexpr int kOffMask = kStages * kStageS;     // CTA 0: u32 [2][kMaskWords] (spare 8 KB)
 constexpr int kOffAlpha = kRegion;              // CTA 1: [2][kAFStride] alpha + flags
 constexpr int kOffL = kOffAlpha + 2 * kAFStride;  // CTA 1: fp32 [2][128]
 constexpr int kOffNT = kOffL + 2 * 128 * 4;     // both: int [2] tiles of the query
 constexpr int kOffBar = kOffNT + 8;
-constexpr int kNumBars = 31;
+constexpr int kNumBars = 3 * kStages + 22;
 constexpr int kOffTmem = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmem + 4;
 constexpr int kOffCorrJ = kOffAbort + 4;
 constexpr int kSmem = kOffCorrJ + 4;
 constexpr int kColQ = 0, kQCols = kDQK / 2;     // CTA 0 TMEM: Q, then two 64-column S tiles
-constexpr int kColS = kQCols;
-constexpr int kThreads = 352;
+constexpr int kColS = 384, kSStride = 64;       // S tiles at 64-column aligned TMEM offsets
+constexpr int kThreads = 32 * (kStages + 8);
 // warp roles: 0-3 row warps (TMEM lane quadrants); 4 MMA issuer (CTA 0: QK of even tiles,
-// CTA 1: PV); 5-7 row gather (warp 5 + s owns ring slot s); 8 P courier (CTA 0); 9 QK issuer
-// of odd tiles (CTA 0); 10 query metadata (both). One thread issues a 64-column MMA in ~54
-// cycles against 32 cycles of tensor work, so QK needs two issuers to keep the pipe busy.
-constexpr int kMmaWarp = 4, kGatherWarp0 = 5, kCourierWarp = 8, kMmaWarp2 = 9, kMetaWarp = 10;
+// CTA 1: PV); 5..4+kStages row gather (warp 5 + s owns ring slot s); then the P courier
+// (CTA 0), the QK issuer of odd tiles (CTA 0) and the query metadata warp (both). One thread
+// issues a QK MMA in ~54 cycles against 24-32 cycles of tensor work, so QK needs two issuers
+// to keep the pipe busy.
+constexpr int kMmaWarp = 4, kGatherWarp0 = 5, kCourierWarp = kGatherWarp0 + kStages,
+              kMmaWarp2 = kCourierWarp + 1, kMetaWarp = kCourierWarp + 2;
 constexpr float kLazyLog2 = 16.f;               // rescale O only when the max grows by > 2^16
 constexpr int kQBatch = 36;                     // 16-byte Q loads in flight per thread
 // barrier indices
-constexpr int kKvFull = 0, kKvEmpty = 3, kPStaged = 6, kSFull = 9, kSEmpty = 11, kPFull = 13,
-              kPEmpty = 15, kMetaFull = 17, kMetaEmpty = 19, kLReady = 21, kLEmpty = 23,
-              kQReady = 25, kQAck = 26, kCorrGo = 27, kCorrReady = 28, kCorrDone = 29,
-              kOFinal = 30;
-constexpr int kODrained = kOFinal;              // see below: CTA 1 reuses index 30 pairs
+constexpr int kKvFull = 0, kKvEmpty = kStages, kPStaged = 2 * kStages, kSFull = 3 * kStages,
+              kSEmpty = kSFull + 2, kPFull = kSFull + 4, kPEmpty = kSFull + 6,
+              kMetaFull = kSFull + 8, kMetaEmpty = kSFull + 10, kLReady = kSFull + 12,
+              kLEmpty = kSFull + 14, kQReady = kSFull + 16, kQAck = kSFull + 17,
+              kCorrGo = kSFull + 18, kCorrReady = kSFull + 19, kCorrDone = kSFull + 20,
+              kOFinal = kSFull + 21;
+static_assert(kOFinal + 1 == kNumBars, "barrier count");
 static_assert(kSmem <= 232448, "smem budget");
-static_assert(kOffMask + 2 * kMaxTiles * 8 <= kRegion, "masks fit in CTA 0's spare region");
-static_assert(kColS + 2 * kKeys <= 512, "TMEM budget");
-static_assert(kAFBytes % 16 == 0 && kPBytes + kAFBytes <= 3 * kAtomBytes, "P staging");
+static_assert(kOffMask + 2 * kMaskWords * 4 <= kRegion, "masks fit in CTA 0's spare region");
+static_assert(kColS >= kColQ + kQCols && kColS + kSStride + kKeys <= 512, "TMEM budget");
+static_assert(kAFBytes % 16 == 0 && kPBytes + kAFBytes <= kStageS, "P staging");
+static_assert(kKeys == 48, "the gather and softmax split a tile into 32 + 16 entries");
+static_assert(kStageS % 1024 == 0 && kStageO % 1024 == 0 && kAtomBytes % 1024 == 0, "SW128");
 }  // namespace pair
 
 // Persistent: cluster i of n processes queries i, i + n, i + 2n, ... Every role walks the same
@@ -481,8 +491,7 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffAbort);
   volatile int* nt_buf = reinterpret_cast<volatile int*>(smem + kOffNT);
   auto bar = [&](int i) { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
-  // CTA 1 has no S tiles, Q or courier: it reuses barrier slots 9..12 for its own per-query
-  // barriers (o_drained at 9, o_final at 30).
+  // CTA 1 has no S tiles, Q or courier: it reuses the first S barrier as its o_drained.
   const int kOD = kSFull;
 
   const bool aligned = (sbase & 1023u) == 0;
@@ -498,7 +507,7 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
       mbar_init(bar(kPFull + i), 1);
       mbar_init(bar(kPEmpty + i), 1);
       mbar_init(bar(kMetaFull + i), 1);
-      mbar_init(bar(kMetaEmpty + i), crank == 0 ? 10 : 8);
+      mbar_init(bar(kMetaEmpty + i), crank == 0 ? kStages + 7 : kStages + 5);
       mbar_init(bar(kLReady + i), 128);
       mbar_init(bar(kLEmpty + i), 128);
     }
@@ -518,8 +527,9 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmem);
 
-  // meta_empty arrivals per query: CTA 0: 3 gather + 2 QK + courier + 4 softmax warps (at the
-  // end of the query: they read the masks until then); CTA 1: 3 gather + PV + 4 row warps.
+  // meta_empty arrivals per query: CTA 0: kStages gather + 2 QK + courier + 4 softmax warps
+  // (at the end of the query: they read the masks until then); CTA 1: kStages gather + PV +
+  // 4 row warps.
   auto meta_wait = [&](int n, bool warp_uniform) -> int {
     const uint32_t mb = bar(kMetaFull + (n & 1)), par = (n >> 1) & 1;
     const bool ok = warp_uniform ? warp_wait(mb, par, 0x40, abort_flag)
@@ -540,7 +550,7 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
         for (int off = static_cast<int>(lane) * 128; off < kH * kDQK * 2; off += 32 * 128)
           asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow + off));
       }
-      uint32_t* mwords = reinterpret_cast<uint32_t*>(smem + kOffMask) + (n & 1) * kMaxTiles * 2;
+      uint32_t* mwords = reinterpret_cast<uint32_t*>(smem + kOffMask) + (n & 1) * kMaskWords;
       const int n_tiles_max = (k + kKeys - 1) / kKeys;
       int last = 0;
       for (int base = 0; base < n_tiles_max * kKeys; base += 32 * 8) {
@@ -561,7 +571,7 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
         const uint32_t word = w2 | __shfl_xor_sync(0xffffffffu, w2, 2);
         if ((lane & 3) == 0 && e0 < n_tiles_max * kKeys) {
           if (crank == 0) mwords[e0 / 32] = word;
-          if (word) last = e0 / kKeys + 1;
+          if (word) last = (e0 + 31 - __clz(word)) / kKeys + 1;
         }
       }
       last = __reduce_max_sync(0xffffffffu, last);
@@ -573,7 +583,7 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
     }
   } else if (warp >= kGatherWarp0 && warp < kGatherWarp0 + kStages) {
     // ---------------------------------------------------------------- row gather (both CTAs)
-    // Warp 5 + s fills ring slot s with the global tiles g = s (mod 3): 16-byte cp.async
+    // Warp 5 + s fills ring slot s with the global tiles g = s (mod kStages): 16-byte cp.async
     // copies into the 128B-swizzled K-major layout (row r of atom a at a * 8 KB + r * 128,
     // 16-byte chunk c at (c ^ (r % 8)) * 16), then waits for its own copies, fences them for
     // the tensor core (async proxy) and arrives.
@@ -598,7 +608,7 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
       auto fetch = [&](int j, int& s0, int& s1) {
         const int e0 = j * kKeys + static_cast<int>(lane);
         s0 = (j < nt && e0 < k && b_ok) ? __ldg(trow + e0) : -1;
-        s1 = (j < nt && e0 + 32 < k && b_ok) ? __ldg(trow + e0 + 32) : -1;
+        s1 = (j < nt && lane < kKeys - 32 && e0 + 32 < k && b_ok) ? __ldg(trow + e0 + 32) : -1;
       };
       int s0, s1;
       fetch(j_first, s0, s1);
@@ -618,7 +628,7 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
           const int32_t row = r < 32 ? ra : rb;
           const bool valid = row < kv.n_rows;
           const __nv_bfloat16* src = c + (valid ? static_cast<int64_t>(row) * kDQK : 0) + chunk * 8;
-          const uint32_t dst = stage + r * 128 + ((chunk ^ (r & 7)) * 16);
+          const uint32_t dst = stage + r * 128 + ((chunk ^ (r & 7)) * 16);   // r & 7: atoms are 1 KB aligned
           for (int a = 0; a < n_atoms; ++a)
             cp_async16(dst + a * kAtomBytes, src + a * 64, valid ? 16u : 0u);
         }
@@ -633,39 +643,43 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
     cp_async_wait_all();
     if (__any_sync(0xffffffffu, bad) && lane == 0) report_device_error(kErrBadIndex);
   } else if ((warp == kMmaWarp || warp == kMmaWarp2) && crank == 0) {
-    if (lane == 0) {
-      // -------------------------------------------------------------- CTA 0: QK issuers
-      // Even global tiles -> S buffer 0 (warp 4), odd -> S buffer 1 (warp 9). Descriptors
-      // are precomputed; each k-step only adds a constant to the encoded start address.
-      const int sb = warp == kMmaWarp ? 0 : 1;
-      const uint32_t idesc = idesc_bf16(128, kKeys, 0, 0);
-      const uint64_t desc0 = smem_desc(sbase, 16, 1024, kSwizzle128B);
-      const uint32_t d_s = tmem + kColS + sb * kKeys;
-      int64_t g0 = 0;
-      bool ok = true;
-      for (int n = 0; n < n_my && ok; ++n) {
-        const int nt = meta_wait(n, false);
-        if (nt < 0) break;
-        mbar_arrive(bar(kMetaEmpty + (n & 1)));
-        if (!mbar_wait(bar(kQReady), n & 1, 0x22, abort_flag)) break;
-        mbar_arrive(bar(kQAck));                     // lets the softmax load the next Q later
+    // ---------------------------------------------------------------- CTA 0: QK issuers
+    // Even global tiles -> S buffer 0 (warp 4), odd -> S buffer 1. The whole warp runs the
+    // loop (waits and descriptor arithmetic stay warp-uniform) and one elected lane issues:
+    // an MMA issued this way leaves the issuing thread at the tensor pipe's own rate, about
+    // twice as fast as from a single-lane branch.
+    const bool leader = elect_one();
+    const int sb = warp == kMmaWarp ? 0 : 1;
+    const uint32_t idesc = idesc_bf16(128, kKeys, 0, 0);
+    const uint64_t desc0 = smem_desc(sbase, 16, 1024, kSwizzle128B);
+    const uint32_t d_s = tmem + kColS + sb * kSStride;
+    int64_t g0 = 0;
+    bool ok = true;
+    for (int n = 0; n < n_my && ok; ++n) {
+      const int nt = meta_wait(n, true);
+      if (nt < 0) break;
+      __syncwarp();
+      if (leader) mbar_arrive(bar(kMetaEmpty + (n & 1)));
+      if (!warp_wait(bar(kQReady), n & 1, 0x22, abort_flag)) break;
+      if (leader) mbar_arrive(bar(kQAck));         // lets the softmax load the next Q later
+      tc_fence_after();
+      for (int j = static_cast<int>(((sb - g0) % 2 + 2) % 2); j < nt; j += 2) {
+        const int64_t g = g0 + j;
+        const int s = static_cast<int>(g % kStages);
+        if (!warp_wait(bar(kKvFull + s), static_cast<uint32_t>((g / kStages) & 1), 0x23, abort_flag)) { ok = false; break; }
+        if (!warp_wait(bar(kSEmpty + sb), static_cast<uint32_t>(((g >> 1) & 1) ^ 1), 0x24, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        for (int j = static_cast<int>(((sb - g0) % 2 + 2) % 2); j < nt; j += 2) {
-          const int64_t g = g0 + j;
-          const int s = static_cast<int>(g % kStages);
-          if (!mbar_wait(bar(kKvFull + s), static_cast<uint32_t>((g / kStages) & 1), 0x23, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(bar(kSEmpty + sb), static_cast<uint32_t>(((g >> 1) & 1) ^ 1), 0x24, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t db0 = desc0 + static_cast<uint64_t>((s * kStageS) >> 4);
+        const uint64_t db0 = desc0 + static_cast<uint64_t>((s * kStageS) >> 4);
 #pragma unroll
-          for (int gg = 0; gg < kDQK / 16; ++gg)
-            umma_ts(d_s, tmem + kColQ + gg * 8,
-                    db0 + static_cast<uint64_t>(((gg >> 2) * kAtomBytes + (gg & 3) * 32) >> 4),
-                    idesc, gg > 0 ? 1u : 0u);
-          umma_commit(bar(kSFull + sb));
+        for (int gg = 0; gg < kDQK / 16; ++gg) {
+          const uint64_t db =
+              db0 + static_cast<uint64_t>(((gg >> 2) * kAtomBytes + (gg & 3) * 32) >> 4);
+          if (leader) umma_ts(d_s, tmem + kColQ + gg * 8, db, idesc, gg > 0 ? 1u : 0u);
         }
-        g0 += nt;
+        if (leader) umma_commit(bar(kSFull + sb));
+        __syncwarp();
       }
+      g0 += nt;
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
@@ -787,7 +801,7 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
         tc_fence_before();
         mbar_arrive(bar(kQReady));
       }
-      const uint64_t* masks = reinterpret_cast<const uint64_t*>(smem + kOffMask) + (n & 1) * kMaxTiles;
+      const uint32_t* mwords = reinterpret_cast<const uint32_t*>(smem + kOffMask) + (n & 1) * kMaskWords;
       float m_ref = -INFINITY, l_run = 0.f;
       bool ok = true;
       for (int j = 0; j < nt; ++j) {
@@ -798,19 +812,22 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
         float sv[kKeys];
         {
           uint32_t r[32];
-          tmem_ld32(tmem + lane_base + kColS + sb * kKeys, r);
+          tmem_ld32(tmem + lane_base + kColS + sb * kSStride, r);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) sv[i] = __uint_as_float(r[i]);
-          tmem_ld32(tmem + lane_base + kColS + sb * kKeys + 32, r);
+          uint32_t (&r16)[16] = *reinterpret_cast<uint32_t(*)[16]>(&r[0]);
+          tmem_ld16(tmem + lane_base + kColS + sb * kSStride + 32, r16);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) sv[32 + i] = __uint_as_float(r[i]);
+          for (int i = 0; i < kKeys - 32; ++i) sv[32 + i] = __uint_as_float(r16[i]);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kSEmpty + sb));
-        const uint64_t mk = masks[j];
+        const int e0 = j * kKeys;                    // validity bits of this tile's entries
+        const uint64_t mk = ((static_cast<uint64_t>(mwords[(e0 >> 5) + 1]) << 32) |
+                             mwords[e0 >> 5]) >> (e0 & 31);
         float mt = -INFINITY;
 #pragma unroll
         for (int i = 0; i < kKeys; ++i) {
@@ -841,7 +858,7 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
         uint8_t* slot = smem + slot_i * kStageS;
         uint8_t* prow = slot + (h >> 3) * 1024 + (h & 7) * 128;
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
+        for (int cc = 0; cc < kKeys / 8; ++cc)
           *reinterpret_cast<uint4*>(prow + ((cc ^ (h & 7)) * 16)) =
               make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
         reinterpret_cast<float*>(slot + kPBytes)[h] = alpha;
