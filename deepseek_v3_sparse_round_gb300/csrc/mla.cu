@@ -402,22 +402,24 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16*
 
 // =============================================================================================
 // H = 128, dqk = 576, dv = 512: a cluster of two CTAs per query with split roles.
-//   CTA 0 ("S side"): Q (128 x 576 bf16) in TMEM as the A operand (288 columns) and two S tiles
-//     of 128 x 48 fp32, so QK(j+1) runs while the softmax of tile j runs. Its softmax warps
-//     stage P (bf16), the per-row rescale factors and flags in the ring slot that QK has just
-//     consumed; a courier warp ships them to CTA 1 with bulk DSMEM copies and frees the slot.
+//   CTA 0 ("S side"): Q (128 x 576 bf16) in TMEM as the A operand (288 columns) and one S tile
+//     of 128 x 48 fp32 per ring slot, so QK(j+1) runs while the softmax of tile j runs. Each
+//     slot has its own QK issuer warp, so every waiter sees every phase of its barriers in
+//     order (an issuer that skipped the phases of another issuer's tiles could take a parity
+//     two phases ahead for the current one). Its softmax warps
+//     stage P (bf16), the per-row rescale factors and flags in one of two staging buffers; a
+//     courier warp ships each to CTA 1 with bulk DSMEM copies (one bulk copy moves a tile far
+//     faster than per-thread DSMEM stores). A ring slot is free as soon as its QK MMAs finish.
 //   CTA 1 ("O side"): O (128 x 512 fp32) fills its TMEM; it accumulates O += P . V with two
 //     N = 256 MMAs per 16 keys and writes o = O / l at the end.
-// Each CTA gathers the selected rows it needs into its own 4-slot ring of 48-key tiles (CTA 0:
-// all 576 columns, CTA 1: the 512 latent columns). A CTA 0 slot is held from its gather
-// through QK, softmax and the P shipment, so the ring has four slots of 48 keys rather than
-// three of 64 (the shared memory is the same). The running maximum is lazy: O is rescaled only
+// Each CTA gathers the selected rows it needs into its own 3-slot ring of 48-key tiles (CTA 0:
+// all 576 columns, CTA 1: the 512 latent columns). The running maximum is lazy: O is rescaled only
 // when a row's maximum grows by more than 2^16 (rare; then CTA 1's four row warps rescale O
 // between two PV steps).
 namespace pair {
 constexpr int kH = 128, kDQK = 576, kDV = 512;
 constexpr int kKeys = 48;                       // keys per tile
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 // validity bits of one query's top-k entries, up to the end of its last tile (+1 word so the
 // two-word read of a tile's bits stays inside the buffer)
 constexpr int kMaskWords = ((kMaxK + kKeys - 1) / kKeys * kKeys + 31) / 32 + 1;
@@ -430,42 +432,43 @@ constexpr int kPBytes = 128 * 128;              // 128 rows x 64 keys bf16 (48 u
 constexpr int kAFBytes = 128 * 4 + 16;          // alpha[128] fp32 + flags[4] u32 (528 bytes)
 constexpr int kAFStride = 544;
 constexpr int kOffP = kStages * kStageO;        // CTA 1: two P buffers
-constexpr int kRegion = (kStages * kStageS > kOffP + 2 * kPBytes) ? kStages * kStageS
-                                                                   : kOffP + 2 * kPBytes;
-constexpr int kOffMask = kStages * kStageS;     // CTA 0: u32 [2][kMaskWords] (spare 8 KB)
+constexpr int kPSStride = kPBytes + kAFBytes;   // CTA 0: staged P + alpha + flags
+constexpr int kOffPS = kStages * kStageS;       // CTA 0: two P staging buffers
+constexpr int kOffMask = kOffPS + 2 * kPSStride;  // CTA 0: u32 [2][kMaskWords]
+constexpr int kEndS = kOffMask + 2 * kMaskWords * 4, kEndO = kOffP + 2 * kPBytes;
+constexpr int kRegion = ((kEndS > kEndO ? kEndS : kEndO) + 15) / 16 * 16;
 constexpr int kOffAlpha = kRegion;              // CTA 1: [2][kAFStride] alpha + flags
 constexpr int kOffL = kOffAlpha + 2 * kAFStride;  // CTA 1: fp32 [2][128]
 constexpr int kOffNT = kOffL + 2 * 128 * 4;     // both: int [2] tiles of the query
 constexpr int kOffBar = kOffNT + 8;
-constexpr int kNumBars = 3 * kStages + 22;
+constexpr int kNumBars = 4 * kStages + 22;
 constexpr int kOffTmem = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmem + 4;
 constexpr int kOffCorrJ = kOffAbort + 4;
 constexpr int kSmem = kOffCorrJ + 4;
 constexpr int kColQ = 0, kQCols = kDQK / 2;     // CTA 0 TMEM: Q, then two 64-column S tiles
-constexpr int kColS = 384, kSStride = 64;       // S tiles at 64-column aligned TMEM offsets
-constexpr int kThreads = 32 * (kStages + 8);
-// warp roles: 0-3 row warps (TMEM lane quadrants); 4 MMA issuer (CTA 0: QK of even tiles,
-// CTA 1: PV); 5..4+kStages row gather (warp 5 + s owns ring slot s); then the P courier
-// (CTA 0), the QK issuer of odd tiles (CTA 0) and the query metadata warp (both). One thread
-// issues a QK MMA in ~54 cycles against 24-32 cycles of tensor work, so QK needs two issuers
-// to keep the pipe busy.
+constexpr int kColS = 288, kSStride = 64;       // S tile of slot s at kColS + 64 s
+constexpr int kThreads = 32 * (2 * kStages + 6);
+// warp roles: 0-3 row warps (TMEM lane quadrants); 4 MMA issuer (CTA 0: QK of slot 0, CTA 1:
+// PV); 5..4+kStages row gather (warp 5 + s owns ring slot s); the P courier (CTA 0); the QK
+// issuers of slots 1..kStages-1 (CTA 0); the query metadata warp (both).
 constexpr int kMmaWarp = 4, kGatherWarp0 = 5, kCourierWarp = kGatherWarp0 + kStages,
-              kMmaWarp2 = kCourierWarp + 1, kMetaWarp = kCourierWarp + 2;
+              kQKWarp1 = kCourierWarp + 1, kMetaWarp = kQKWarp1 + kStages - 1;
 constexpr float kLazyLog2 = 16.f;               // rescale O only when the max grows by > 2^16
 constexpr int kQBatch = 36;                     // 16-byte Q loads in flight per thread
 // barrier indices
-constexpr int kKvFull = 0, kKvEmpty = kStages, kPStaged = 2 * kStages, kSFull = 3 * kStages,
-              kSEmpty = kSFull + 2, kPFull = kSFull + 4, kPEmpty = kSFull + 6,
-              kMetaFull = kSFull + 8, kMetaEmpty = kSFull + 10, kLReady = kSFull + 12,
-              kLEmpty = kSFull + 14, kQReady = kSFull + 16, kQAck = kSFull + 17,
-              kCorrGo = kSFull + 18, kCorrReady = kSFull + 19, kCorrDone = kSFull + 20,
-              kOFinal = kSFull + 21;
+constexpr int kKvFull = 0, kKvEmpty = kStages, kPStaged = 2 * kStages, kPSEmpty = kPStaged + 2,
+              kSFull = kPStaged + 4, kSEmpty = kSFull + kStages, kPFull = kSEmpty + kStages,
+              kPEmpty = kPFull + 2, kMetaFull = kPEmpty + 2, kMetaEmpty = kMetaFull + 2,
+              kLReady = kMetaEmpty + 2, kLEmpty = kLReady + 2, kQReady = kLEmpty + 2,
+              kQAck = kQReady + 1, kCorrGo = kQReady + 2, kCorrReady = kQReady + 3,
+              kCorrDone = kQReady + 4, kOFinal = kQReady + 5;
 static_assert(kOFinal + 1 == kNumBars, "barrier count");
 static_assert(kSmem <= 232448, "smem budget");
-static_assert(kOffMask + 2 * kMaskWords * 4 <= kRegion, "masks fit in CTA 0's spare region");
-static_assert(kColS >= kColQ + kQCols && kColS + kSStride + kKeys <= 512, "TMEM budget");
-static_assert(kAFBytes % 16 == 0 && kPBytes + kAFBytes <= kStageS, "P staging");
+static_assert(kOffPS % 16 == 0 && kPSStride % 16 == 0, "bulk copy sources are 16-byte aligned");
+static_assert(kColS >= kColQ + kQCols && kColS + (kStages - 1) * kSStride + kKeys <= 512,
+              "TMEM budget");
+static_assert(kAFBytes % 16 == 0, "P staging");
 static_assert(kKeys == 48, "the gather and softmax split a tile into 32 + 16 entries");
 static_assert(kStageS % 1024 == 0 && kStageO % 1024 == 0 && kAtomBytes % 1024 == 0, "SW128");
 }  // namespace pair
@@ -499,20 +502,23 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
     for (int i = 0; i < kStages; ++i) {
       mbar_init(bar(kKvFull + i), 32);
       mbar_init(bar(kKvEmpty + i), 1);
-      mbar_init(bar(kPStaged + i), 128);
+    }
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(bar(kSFull + i), (crank == 0 || i > 0) ? 1 : 4);  // CTA 1: first = o_drained
+      mbar_init(bar(kSEmpty + i), 4);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(kSFull + i), crank == 0 ? 1 : 4);      // CTA 1: [9] = o_drained (4 warps)
-      mbar_init(bar(kSEmpty + i), 4);
+      mbar_init(bar(kPStaged + i), 128);
+      mbar_init(bar(kPSEmpty + i), 1);
       mbar_init(bar(kPFull + i), 1);
       mbar_init(bar(kPEmpty + i), 1);
       mbar_init(bar(kMetaFull + i), 1);
-      mbar_init(bar(kMetaEmpty + i), crank == 0 ? kStages + 7 : kStages + 5);
+      mbar_init(bar(kMetaEmpty + i), crank == 0 ? 2 * kStages + 5 : kStages + 5);
       mbar_init(bar(kLReady + i), 128);
       mbar_init(bar(kLEmpty + i), 128);
     }
     mbar_init(bar(kQReady), 128);
-    mbar_init(bar(kQAck), 2);
+    mbar_init(bar(kQAck), kStages);
     mbar_init(bar(kCorrGo), 1);
     mbar_init(bar(kCorrReady), 1);
     mbar_init(bar(kCorrDone), 128);
@@ -527,9 +533,9 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmem);
 
-  // meta_empty arrivals per query: CTA 0: kStages gather + 2 QK + courier + 4 softmax warps
-  // (at the end of the query: they read the masks until then); CTA 1: kStages gather + PV +
-  // 4 row warps.
+  // meta_empty arrivals per query: CTA 0: kStages gather + kStages QK + courier + 4 softmax
+  // warps (at the end of the query: they read the masks until then); CTA 1: kStages gather +
+  // PV + 4 row warps.
   auto meta_wait = [&](int n, bool warp_uniform) -> int {
     const uint32_t mb = bar(kMetaFull + (n & 1)), par = (n >> 1) & 1;
     const bool ok = warp_uniform ? warp_wait(mb, par, 0x40, abort_flag)
@@ -642,14 +648,15 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
     }
     cp_async_wait_all();
     if (__any_sync(0xffffffffu, bad) && lane == 0) report_device_error(kErrBadIndex);
-  } else if ((warp == kMmaWarp || warp == kMmaWarp2) && crank == 0) {
+  } else if ((warp == kMmaWarp || (warp >= kQKWarp1 && warp < kQKWarp1 + kStages - 1)) &&
+             crank == 0) {
     // ---------------------------------------------------------------- CTA 0: QK issuers
-    // Even global tiles -> S buffer 0 (warp 4), odd -> S buffer 1. The whole warp runs the
-    // loop (waits and descriptor arithmetic stay warp-uniform) and one elected lane issues:
-    // an MMA issued this way leaves the issuing thread at the tensor pipe's own rate, about
-    // twice as fast as from a single-lane branch.
+    // Issuer sb takes the global tiles g = sb (mod kStages): ring slot sb -> S buffer sb. The
+    // whole warp runs the loop (waits and descriptor arithmetic stay warp-uniform) and one
+    // elected lane issues: an MMA issued this way leaves the issuing thread at the tensor
+    // pipe's own rate, about twice as fast as from a single-lane branch.
     const bool leader = elect_one();
-    const int sb = warp == kMmaWarp ? 0 : 1;
+    const int sb = warp == kMmaWarp ? 0 : static_cast<int>(warp) - kQKWarp1 + 1;
     const uint32_t idesc = idesc_bf16(128, kKeys, 0, 0);
     const uint64_t desc0 = smem_desc(sbase, 16, 1024, kSwizzle128B);
     const uint32_t d_s = tmem + kColS + sb * kSStride;
@@ -663,11 +670,13 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
       if (!warp_wait(bar(kQReady), n & 1, 0x22, abort_flag)) break;
       if (leader) mbar_arrive(bar(kQAck));         // lets the softmax load the next Q later
       tc_fence_after();
-      for (int j = static_cast<int>(((sb - g0) % 2 + 2) % 2); j < nt; j += 2) {
+      for (int j = static_cast<int>(((sb - g0) % kStages + kStages) % kStages); j < nt;
+           j += kStages) {
         const int64_t g = g0 + j;
-        const int s = static_cast<int>(g % kStages);
-        if (!warp_wait(bar(kKvFull + s), static_cast<uint32_t>((g / kStages) & 1), 0x23, abort_flag)) { ok = false; break; }
-        if (!warp_wait(bar(kSEmpty + sb), static_cast<uint32_t>(((g >> 1) & 1) ^ 1), 0x24, abort_flag)) { ok = false; break; }
+        const int s = sb;                              // == g % kStages
+        const uint32_t ph = static_cast<uint32_t>((g / kStages) & 1);
+        if (!warp_wait(bar(kKvFull + s), ph, 0x23, abort_flag)) { ok = false; break; }
+        if (!warp_wait(bar(kSEmpty + sb), ph ^ 1, 0x24, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint64_t db0 = desc0 + static_cast<uint64_t>((s * kStageS) >> 4);
 #pragma unroll
@@ -741,7 +750,7 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
     if (lane == 0 && crank == 0) {
       // -------------------------------------------------------------- CTA 0: P courier
       // Ships each staged P tile (+ alpha, flags) to CTA 1 with two bulk copies that complete
-      // on CTA 1's p_full barrier, then hands the ring slot back to its gather warp.
+      // on CTA 1's p_full barrier, then hands the staging buffer back to the softmax warps.
       int64_t g0 = 0;
       for (int n = 0; n < n_my; ++n) {
         const int nt = meta_wait(n, false);
@@ -750,16 +759,16 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
         bool ok = true;
         for (int j = 0; j < nt; ++j) {
           const int64_t g = g0 + j;
-          const int s = static_cast<int>(g % kStages), pb = static_cast<int>(g & 1);
-          if (!mbar_wait(bar(kPStaged + s), static_cast<uint32_t>((g / kStages) & 1), 0x2E, abort_flag)) { ok = false; break; }
+          const int pb = static_cast<int>(g & 1);
+          if (!mbar_wait(bar(kPStaged + pb), static_cast<uint32_t>((g >> 1) & 1), 0x2E, abort_flag)) { ok = false; break; }
           if (!mbar_wait(bar(kPEmpty + pb), static_cast<uint32_t>(((g >> 1) & 1) ^ 1), 0x2F, abort_flag)) { ok = false; break; }
-          const uint32_t src = sbase + s * kStageS;
+          const uint32_t src = sbase + kOffPS + pb * kPSStride;
           bulk_copy_to_peer(sbase + kOffP + pb * kPBytes, src, kPBytes, bar(kPFull + pb), peer);
           bulk_copy_to_peer(sbase + kOffAlpha + pb * kAFStride, src + kPBytes, kAFBytes,
                             bar(kPFull + pb), peer);
           bulk_commit();
           bulk_wait_read_all();
-          mbar_arrive(bar(kKvEmpty + s));
+          mbar_arrive(bar(kPSEmpty + pb));
         }
         if (!ok) break;
         g0 += nt;
@@ -806,8 +815,8 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
       bool ok = true;
       for (int j = 0; j < nt; ++j) {
         const int64_t g = g0 + j;
-        const int sb = static_cast<int>(g & 1), slot_i = static_cast<int>(g % kStages);
-        if (!warp_wait(bar(kSFull + sb), static_cast<uint32_t>((g >> 1) & 1), 0x28, abort_flag)) { ok = false; break; }
+        const int sb = static_cast<int>(g % kStages), psb = static_cast<int>(g & 1);
+        if (!warp_wait(bar(kSFull + sb), static_cast<uint32_t>((g / kStages) & 1), 0x28, abort_flag)) { ok = false; break; }
         tc_fence_after();
         float sv[kKeys];
         {
@@ -825,6 +834,8 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kSEmpty + sb));
+        // S full means this tile's QK MMAs have finished reading its ring slot
+        if (threadIdx.x == 0) mbar_arrive(bar(kKvEmpty + sb));
         const int e0 = j * kKeys;                    // validity bits of this tile's entries
         const uint64_t mk = ((static_cast<uint64_t>(mwords[(e0 >> 5) + 1]) << 32) |
                              mwords[e0 >> 5]) >> (e0 & 31);
@@ -853,9 +864,10 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
         }
         l_run += psum;
         const uint32_t any = __any_sync(0xffffffffu, alpha != 1.f) ? 1u : 0u;
-        // Stage P (swizzled K-major rows), alpha and the warp flags in the ring slot of this
-        // tile, which QK no longer needs; the courier ships them and then frees the slot.
-        uint8_t* slot = smem + slot_i * kStageS;
+        // Stage P (swizzled K-major rows), alpha and the warp flags in staging buffer g % 2
+        // once the courier has shipped its previous contents.
+        if (!warp_wait(bar(kPSEmpty + psb), static_cast<uint32_t>(((g >> 1) & 1) ^ 1), 0x29, abort_flag)) { ok = false; break; }
+        uint8_t* slot = smem + kOffPS + psb * kPSStride;
         uint8_t* prow = slot + (h >> 3) * 1024 + (h & 7) * 128;
 #pragma unroll
         for (int cc = 0; cc < kKeys / 8; ++cc)
@@ -864,7 +876,7 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
         reinterpret_cast<float*>(slot + kPBytes)[h] = alpha;
         if (lane == 0) reinterpret_cast<uint32_t*>(slot + kPBytes + 512)[warp] = any;
         fence_proxy_async_smem();
-        mbar_arrive(bar(kPStaged + slot_i));
+        mbar_arrive(bar(kPStaged + psb));
       }
       if (!ok) break;
       // l of this query -> CTA 1 (buffer n % 2, free once CTA 1 read query n - 2's), lse
