@@ -437,7 +437,11 @@ constexpr int kOffPS = kStages * kStageS;       // CTA 0: two P staging buffers
 constexpr int kOffMask = kOffPS + 2 * kPSStride;  // CTA 0: u32 [2][kMaskWords]
 constexpr int kEndS = kOffMask + 2 * kMaskWords * 4, kEndO = kOffP + 2 * kPBytes;
 constexpr int kRegion = ((kEndS > kEndO ? kEndS : kEndO) + 15) / 16 * 16;
-constexpr int kOffAlpha = kRegion;              // CTA 1: [2][kAFStride] alpha + flags
+// 32 rows x 128 B per row warp, 1 KB aligned (128B swizzle): CTA 0 transposes Q rows through
+// it on their way to TMEM, CTA 1 stages bf16 o for TMA stores.
+constexpr int kOffX = (kRegion + 1023) / 1024 * 1024;
+constexpr int kXBytes = 4 * 32 * 128;
+constexpr int kOffAlpha = kOffX + kXBytes;      // CTA 1: [2][kAFStride] alpha + flags
 constexpr int kOffL = kOffAlpha + 2 * kAFStride;  // CTA 1: fp32 [2][128]
 constexpr int kOffNT = kOffL + 2 * 128 * 4;     // both: int [2] tiles of the query
 constexpr int kOffBar = kOffNT + 8;
@@ -478,10 +482,10 @@ static_assert(kStageS % 1024 == 0 && kStageO % 1024 == 0 && kAtomBytes % 1024 ==
 // included), so ring slots, S/P buffers and their barrier phases continue across queries.
 // Every role waits for every per-query phase in order, also for queries where it has no tile.
 __global__ void __launch_bounds__(pair::kThreads, 1)
-sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16* __restrict__ q,
+sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
+                       const __nv_bfloat16* __restrict__ c, const __nv_bfloat16* __restrict__ q,
                        const int32_t* __restrict__ bid, const int32_t* __restrict__ topk, int k,
-                       int64_t n_q, KvMap kv, float scale_log2, __nv_bfloat16* __restrict__ o,
-                       float* __restrict__ lse) {
+                       int64_t n_q, KvMap kv, float scale_log2, float* __restrict__ lse) {
   using namespace pair;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -788,22 +792,46 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
       // last softmax tile saw them) and both issuers acknowledged the previous Q.
       if (n > 0 && !warp_wait(bar(kQAck), (n - 1) & 1, 0x42, abort_flag)) break;
       {
-        const uint4* qsrc = reinterpret_cast<const uint4*>(q + (t * kH + h) * kDQK);
-        constexpr int kQLoads = kDQK * 2 / 16;       // 72
-#pragma unroll 1
-        for (int base = 0; base < kQLoads; base += kQBatch) {
-          uint4 qreg[kQBatch];
+        // Coalesced: each warp-wide load covers 4 rows x 128 B of the warp's 32 Q rows; the
+        // rows are transposed through the warp's swizzled staging tile so that lane i ends up
+        // holding row i (its TMEM lane), one 64-dim atom (32 TMEM columns) at a time.
+        const char* qw = reinterpret_cast<const char*>(q + (t * kH + warp * 32) * kDQK);
+        uint8_t* xw = smem + kOffX + warp * (32 * 128);
+        const int lrow = static_cast<int>(lane >> 3), lchunk = static_cast<int>(lane & 7);
+        constexpr int kQAtoms = kDQK / 64;           // 9
+        uint4 qa[8], qb[8];
+        auto ldg_atom = [&](int a, uint4 (&v)[8]) {
 #pragma unroll
-          for (int i = 0; i < kQBatch; ++i) qreg[i] = __ldg(qsrc + base + i);
+          for (int i = 0; i < 8; ++i)
+            v[i] = __ldg(reinterpret_cast<const uint4*>(qw + (4 * i + lrow) * (kDQK * 2) + a * 128 +
+                                                        lchunk * 16));
+        };
+        auto put_atom = [&](int a, const uint4 (&v)[8]) {
 #pragma unroll
-          for (int i = 0; i < kQBatch; i += 4) {
-            uint32_t r[16];
+          for (int i = 0; i < 8; ++i) {
+            const int row = 4 * i + lrow;
+            *reinterpret_cast<uint4*>(xw + row * 128 + ((lchunk ^ (row & 7)) * 16)) = v[i];
+          }
+          __syncwarp();
+          uint32_t r[32];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              r[4 * u] = qreg[i + u].x; r[4 * u + 1] = qreg[i + u].y;
-              r[4 * u + 2] = qreg[i + u].z; r[4 * u + 3] = qreg[i + u].w;
-            }
-            tmem_st16(tmem + lane_base + kColQ + (base + i) * 4, r);
+          for (int cc = 0; cc < 8; ++cc) {
+            const uint4 u = *reinterpret_cast<const uint4*>(xw + lane * 128 + ((cc ^ (lane & 7)) * 16));
+            r[4 * cc] = u.x; r[4 * cc + 1] = u.y; r[4 * cc + 2] = u.z; r[4 * cc + 3] = u.w;
+          }
+          __syncwarp();                              // the tile is rewritten by the next atom
+          tmem_st16(tmem + lane_base + kColQ + a * 32, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
+          tmem_st16(tmem + lane_base + kColQ + a * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
+        };
+        ldg_atom(0, qa);
+#pragma unroll
+        for (int a = 0; a < kQAtoms; ++a) {
+          if ((a & 1) == 0) {
+            if (a + 1 < kQAtoms) ldg_atom(a + 1, qb);
+            put_atom(a, qa);
+          } else {
+            if (a + 1 < kQAtoms) ldg_atom(a + 1, qa);
+            put_atom(a, qb);
           }
         }
         tmem_wait_st();
@@ -934,8 +962,12 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       // the l buffer may be refilled (query n + 2) once every row read it
       mbar_arrive_cluster(bar(kLEmpty + (n & 1)), peer);
+      // o = O / l in bf16, 64 columns per round: TMEM -> registers -> the warp's swizzled
+      // staging tile -> one TMA store of 32 rows x 128 B (coalesced, asynchronous).
+      const uint32_t xw = sbase + kOffX + warp * (32 * 128);
+      uint8_t* xrow = smem + kOffX + warp * (32 * 128) + lane * 128;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kDV; c0 += 64) {           // 64 columns per TMEM round trip
+      for (int c0 = 0; c0 < kDV; c0 += 64) {
         uint32_t r[64];
         if (nt > 0) {
           uint32_t (&ra)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
@@ -952,7 +984,8 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kOD));
         }
-        uint4* dst = reinterpret_cast<uint4*>(o + (t * kH + h) * kDV + c0);
+        if (lane == 0) bulk_wait_read_all();         // the previous store has read the tile
+        __syncwarp();
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
           uint32_t pk[4];
@@ -960,10 +993,18 @@ sparse_mla_pair_kernel(const __nv_bfloat16* __restrict__ c, const __nv_bfloat16*
           for (int i = 0; i < 4; ++i)
             pk[i] = bf16x2_bits(__uint_as_float(r[8 * v + 2 * i]) * inv_l,
                                 __uint_as_float(r[8 * v + 2 * i + 1]) * inv_l);
-          dst[v] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(xrow + ((v ^ (lane & 7)) * 16)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+        fence_proxy_async_smem();                    // the tile is read by the TMA unit
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tm_o, xw, c0, static_cast<int32_t>(t * kH + warp * 32));
+          bulk_commit();
         }
       }
     }
+    if (lane == 0) bulk_wait_all();                  // stores complete before the CTA exits
   }
 
   __syncthreads();
@@ -978,6 +1019,10 @@ int launch_mla_pair(const void* q, const void* c, int64_t n_kv_rows, const KvMap
                     const int32_t* bid, const int32_t* topk, int64_t n_q, int k, float scale,
                     void* o, float* lse, cudaStream_t stream) {
   (void)n_kv_rows;
+  CUtensorMap tm_o;                                  // o as [n_q * 128 rows, 512 columns]
+  int rc = make_tmap_bf16_2d(&tm_o, o, static_cast<uint64_t>(n_q) * pair::kH, pair::kDV,
+                             pair::kDV * 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc) return rc;
   DSA_CHECK_CUDA(cudaFuncSetAttribute(sparse_mla_pair_kernel,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, pair::kSmem));
   const int64_t pairs = std::min<int64_t>(n_q, num_sms_cached() / 2);
@@ -994,10 +1039,10 @@ int launch_mla_pair(const void* q, const void* c, int64_t n_kv_rows, const KvMap
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const float scale_log2 = scale * 1.4426950408889634f;
-  DSA_CHECK_CUDA(cudaLaunchKernelEx(&cfg, sparse_mla_pair_kernel,
+  DSA_CHECK_CUDA(cudaLaunchKernelEx(&cfg, sparse_mla_pair_kernel, tm_o,
                                     static_cast<const __nv_bfloat16*>(c),
                                     static_cast<const __nv_bfloat16*>(q), bid, topk, k, n_q, kv,
-                                    scale_log2, static_cast<__nv_bfloat16*>(o), lse));
+                                    scale_log2, lse));
   return DSA_OK;
 }
 
