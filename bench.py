@@ -87,34 +87,50 @@ def dist_env():
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
+    """nvidia-smi clock / throttle samples every INTERVAL_MS, each stamped with its arrival time
+    so that only the samples taken inside the timed window are summarised."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 50
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
+        self.stamped = []
+        self.window = (0.0, float("inf"))
+
+    def _reader(self):
+        for ln in self.proc.stdout:
+            if ln.strip():
+                self.stamped.append((time.perf_counter(), ln))
 
     def __enter__(self):
+        import threading
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._reader, daemon=True)
+            self.thread.start()
         except OSError:
             self.proc = None
         return self
 
+    def mark(self, t0, t1):
+        self.window = (t0, t1 + self.INTERVAL_MS / 1e3)
+
     def __exit__(self, *a):
-        self.lines = []
         if self.proc is not None:
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+            self.thread.join(timeout=5)
+        t0, t1 = self.window
+        self.lines = [ln for t, ln in self.stamped if t0 <= t <= t1]
 
     def summary(self):
         sm, mx, reasons = [], None, set()
@@ -227,6 +243,7 @@ def gpu_arm(args):
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)   # > L2
     stream = torch.cuda.current_stream()
 
+    clk = ClockSampler(local).__enter__()            # running before the timed window opens
     for _ in range(args.warmup):
         st.run()
     torch.cuda.synchronize()
@@ -240,14 +257,16 @@ def gpu_arm(args):
         dist.barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    with ClockSampler(local) as clk:
-        for i in range(args.steps):
-            flush.fill_(float(i))
-            evs[i][0].record(stream)
-            st.run(ev=(evs[i][2], evs[i][3]))
-            evs[i][1].record(stream)
-        torch.cuda.synchronize()
-    wall = time.perf_counter() - t_wall
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        evs[i][0].record(stream)
+        st.run(ev=(evs[i][2], evs[i][3]))
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    t_end = time.perf_counter()
+    wall = t_end - t_wall
+    clk.mark(t_wall, t_end)
+    clk.__exit__(None, None, None)
     step_ms = [a.elapsed_time(b) for a, b, _, _ in evs]
     mla_ms = [c.elapsed_time(d) for _, _, c, d in evs]
     dev_s = max_over_ranks(sum(step_ms) / 1e3, dist, device)
@@ -404,7 +423,7 @@ def reference_arm(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-sample", type=int, default=96, help="queries per reference-arm step")
