@@ -403,10 +403,10 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16*
 // =============================================================================================
 // H = 128, dqk = 576, dv = 512: a cluster of two CTAs per query with split roles.
 //   CTA 0 ("S side"): Q (128 x 576 bf16) in TMEM as the A operand (288 columns) and one S tile
-//     of 128 x 48 fp32 per ring slot, so QK(j+1) runs while the softmax of tile j runs. Each
-//     slot has its own QK issuer warp, so every waiter sees every phase of its barriers in
-//     order (an issuer that skipped the phases of another issuer's tiles could take a parity
-//     two phases ahead for the current one). Its softmax warps
+//     of 128 x 48 fp32 per ring slot, so QK(j+1) runs while the softmax of tile j runs. One
+//     warp-uniform QK issuer takes every tile in order, so it sees every phase of the barriers
+//     it waits on (an issuer skipping another issuer's tiles on a 3-slot ring could take a
+//     parity two phases ahead). Its softmax warps
 //     stage P (bf16), the per-row rescale factors and flags in one of two staging buffers; a
 //     courier warp ships each to CTA 1 with bulk DSMEM copies (one bulk copy moves a tile far
 //     faster than per-thread DSMEM stores). A ring slot is free as soon as its QK MMAs finish.
@@ -441,6 +441,7 @@ constexpr int kRegion = ((kEndS > kEndO ? kEndS : kEndO) + 15) / 16 * 16;
 // it on their way to TMEM, CTA 1 stages bf16 o for TMA stores.
 constexpr int kOffX = (kRegion + 1023) / 1024 * 1024;
 constexpr int kXBytes = 4 * 32 * 128;
+constexpr int kOffXO1 = kEndO;                  // CTA 1: second o staging tile per row warp
 constexpr int kOffAlpha = kOffX + kXBytes;      // CTA 1: [2][kAFStride] alpha + flags
 constexpr int kOffL = kOffAlpha + 2 * kAFStride;  // CTA 1: fp32 [2][128]
 constexpr int kOffNT = kOffL + 2 * 128 * 4;     // both: int [2] tiles of the query
@@ -452,12 +453,12 @@ constexpr int kOffCorrJ = kOffAbort + 4;
 constexpr int kSmem = kOffCorrJ + 4;
 constexpr int kColQ = 0, kQCols = kDQK / 2;     // CTA 0 TMEM: Q, then two 64-column S tiles
 constexpr int kColS = 288, kSStride = 64;       // S tile of slot s at kColS + 64 s
-constexpr int kThreads = 32 * (2 * kStages + 6);
-// warp roles: 0-3 row warps (TMEM lane quadrants); 4 MMA issuer (CTA 0: QK of slot 0, CTA 1:
-// PV); 5..4+kStages row gather (warp 5 + s owns ring slot s); the P courier (CTA 0); the QK
-// issuers of slots 1..kStages-1 (CTA 0); the query metadata warp (both).
+constexpr int kThreads = 32 * (kStages + 7);
+// warp roles: 0-3 row warps (TMEM lane quadrants); 4 MMA issuer (CTA 0: QK, CTA 1: PV);
+// 5..4+kStages row gather (warp 5 + s owns ring slot s); the P courier (CTA 0); the query
+// metadata warp (both).
 constexpr int kMmaWarp = 4, kGatherWarp0 = 5, kCourierWarp = kGatherWarp0 + kStages,
-              kQKWarp1 = kCourierWarp + 1, kMetaWarp = kQKWarp1 + kStages - 1;
+              kMetaWarp = kCourierWarp + 1;
 constexpr float kLazyLog2 = 16.f;               // rescale O only when the max grows by > 2^16
 constexpr int kQBatch = 36;                     // 16-byte Q loads in flight per thread
 // barrier indices
@@ -473,6 +474,7 @@ static_assert(kOffPS % 16 == 0 && kPSStride % 16 == 0, "bulk copy sources are 16
 static_assert(kColS >= kColQ + kQCols && kColS + (kStages - 1) * kSStride + kKeys <= 512,
               "TMEM budget");
 static_assert(kAFBytes % 16 == 0, "P staging");
+static_assert(kOffXO1 % 1024 == 0 && kOffXO1 + kXBytes <= kRegion, "CTA 1's second o tiles");
 static_assert(kKeys == 48, "the gather and softmax split a tile into 32 + 16 entries");
 static_assert(kStageS % 1024 == 0 && kStageO % 1024 == 0 && kAtomBytes % 1024 == 0, "SW128");
 }  // namespace pair
@@ -517,12 +519,12 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
       mbar_init(bar(kPFull + i), 1);
       mbar_init(bar(kPEmpty + i), 1);
       mbar_init(bar(kMetaFull + i), 1);
-      mbar_init(bar(kMetaEmpty + i), crank == 0 ? 2 * kStages + 5 : kStages + 5);
-      mbar_init(bar(kLReady + i), 128);
+      mbar_init(bar(kMetaEmpty + i), crank == 0 ? kStages + 6 : kStages + 5);
+      mbar_init(bar(kLReady + i), 1);               // CTA 1: armed with 512 tx bytes per query
       mbar_init(bar(kLEmpty + i), 128);
     }
     mbar_init(bar(kQReady), 128);
-    mbar_init(bar(kQAck), kStages);
+    mbar_init(bar(kQAck), 1);
     mbar_init(bar(kCorrGo), 1);
     mbar_init(bar(kCorrReady), 1);
     mbar_init(bar(kCorrDone), 128);
@@ -537,9 +539,9 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmem);
 
-  // meta_empty arrivals per query: CTA 0: kStages gather + kStages QK + courier + 4 softmax
-  // warps (at the end of the query: they read the masks until then); CTA 1: kStages gather +
-  // PV + 4 row warps.
+  // meta_empty arrivals per query: CTA 0: kStages gather + QK + courier + 4 softmax warps (at
+  // the end of the query: they read the masks until then); CTA 1: kStages gather + PV + 4 row
+  // warps.
   auto meta_wait = [&](int n, bool warp_uniform) -> int {
     const uint32_t mb = bar(kMetaFull + (n & 1)), par = (n >> 1) & 1;
     const bool ok = warp_uniform ? warp_wait(mb, par, 0x40, abort_flag)
@@ -652,18 +654,15 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
     }
     cp_async_wait_all();
     if (__any_sync(0xffffffffu, bad) && lane == 0) report_device_error(kErrBadIndex);
-  } else if ((warp == kMmaWarp || (warp >= kQKWarp1 && warp < kQKWarp1 + kStages - 1)) &&
-             crank == 0) {
-    // ---------------------------------------------------------------- CTA 0: QK issuers
-    // Issuer sb takes the global tiles g = sb (mod kStages): ring slot sb -> S buffer sb. The
-    // whole warp runs the loop (waits and descriptor arithmetic stay warp-uniform) and one
-    // elected lane issues: an MMA issued this way leaves the issuing thread at the tensor
-    // pipe's own rate, about twice as fast as from a single-lane branch.
+  } else if (warp == kMmaWarp && crank == 0) {
+    // ---------------------------------------------------------------- CTA 0: QK issuer
+    // Tile g: ring slot g % kStages -> S buffer g % kStages. The whole warp runs the loop
+    // (waits and descriptor arithmetic stay warp-uniform) and one elected lane issues: an MMA
+    // issued this way leaves the issuing thread at the tensor pipe's own rate, about twice as
+    // fast as from a single-lane branch.
     const bool leader = elect_one();
-    const int sb = warp == kMmaWarp ? 0 : static_cast<int>(warp) - kQKWarp1 + 1;
     const uint32_t idesc = idesc_bf16(128, kKeys, 0, 0);
     const uint64_t desc0 = smem_desc(sbase, 16, 1024, kSwizzle128B);
-    const uint32_t d_s = tmem + kColS + sb * kSStride;
     int64_t g0 = 0;
     bool ok = true;
     for (int n = 0; n < n_my && ok; ++n) {
@@ -674,10 +673,10 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
       if (!warp_wait(bar(kQReady), n & 1, 0x22, abort_flag)) break;
       if (leader) mbar_arrive(bar(kQAck));         // lets the softmax load the next Q later
       tc_fence_after();
-      for (int j = static_cast<int>(((sb - g0) % kStages + kStages) % kStages); j < nt;
-           j += kStages) {
+      for (int j = 0; j < nt; ++j) {
         const int64_t g = g0 + j;
-        const int s = sb;                              // == g % kStages
+        const int s = static_cast<int>(g % kStages), sb = s;
+        const uint32_t d_s = tmem + kColS + sb * kSStride;
         const uint32_t ph = static_cast<uint32_t>((g / kStages) & 1);
         if (!warp_wait(bar(kKvFull + s), ph, 0x23, abort_flag)) { ok = false; break; }
         if (!warp_wait(bar(kSEmpty + sb), ph ^ 1, 0x24, abort_flag)) { ok = false; break; }
@@ -907,10 +906,12 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
         mbar_arrive(bar(kPStaged + psb));
       }
       if (!ok) break;
-      // l of this query -> CTA 1 (buffer n % 2, free once CTA 1 read query n - 2's), lse
+      // l of this query -> CTA 1 (buffer n % 2, free once CTA 1 read query n - 2's) as an
+      // asynchronous store that completes on CTA 1's l_ready barrier (no release fence, which
+      // would first wait for every earlier memory operation of the thread), then lse
       if (n >= 2 && !warp_wait(bar(kLEmpty + (n & 1)), ((n >> 1) & 1) ^ 1, 0x43, abort_flag)) break;
-      st_cluster_u32(sbase + kOffL + ((n & 1) * 128 + h) * 4, peer, __float_as_uint(l_run));
-      mbar_arrive_cluster(bar(kLReady + (n & 1)), peer);
+      st_async_u32(sbase + kOffL + ((n & 1) * 128 + h) * 4, bar(kLReady + (n & 1)), peer,
+                   __float_as_uint(l_run));
       if (lse != nullptr)
         lse[t * kH + h] = l_run > 0.f ? (m_ref + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
       __syncwarp();
@@ -929,6 +930,7 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kMetaEmpty + (n & 1)));
       const int64_t t = query(n);
+      if (threadIdx.x == 0) mbar_expect_tx(bar(kLReady + (n & 1)), 128 * 4);   // l of query n
       bool ok = true;
       for (;;) {                                     // rescale requests, then the end marker
         if (!warp_wait(bar(kCorrGo), n_go & 1u, 0x2A, abort_flag)) { ok = false; break; }
@@ -960,14 +962,16 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
       tc_fence_after();
       const float l = reinterpret_cast<const volatile float*>(smem + kOffL)[(n & 1) * 128 + h];
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      // the l buffer may be refilled (query n + 2) once every row read it
-      mbar_arrive_cluster(bar(kLEmpty + (n & 1)), peer);
       // o = O / l in bf16, 64 columns per round: TMEM -> registers -> the warp's swizzled
       // staging tile -> one TMA store of 32 rows x 128 B (coalesced, asynchronous).
-      const uint32_t xw = sbase + kOffX + warp * (32 * 128);
-      uint8_t* xrow = smem + kOffX + warp * (32 * 128) + lane * 128;
+      // Two staging tiles per warp, alternating, so a store can still be reading one tile
+      // while the next round fills the other.
+      const uint32_t xo[2] = {static_cast<uint32_t>(kOffX + warp * (32 * 128)),
+                              static_cast<uint32_t>(kOffXO1 + warp * (32 * 128))};
 #pragma unroll 1
       for (int c0 = 0; c0 < kDV; c0 += 64) {
+        const uint32_t xoff = xo[(c0 >> 6) & 1];
+        uint8_t* xrow = smem + xoff + lane * 128;
         uint32_t r[64];
         if (nt > 0) {
           uint32_t (&ra)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
@@ -984,7 +988,7 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kOD));
         }
-        if (lane == 0) bulk_wait_read_all();         // the previous store has read the tile
+        if (lane == 0) bulk_wait_read_but_one();     // the store of two rounds ago read this tile
         __syncwarp();
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
@@ -999,10 +1003,12 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
         fence_proxy_async_smem();                    // the tile is read by the TMA unit
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&tm_o, xw, c0, static_cast<int32_t>(t * kH + warp * 32));
+          tma_store_2d(&tm_o, sbase + xoff, c0, static_cast<int32_t>(t * kH + warp * 32));
           bulk_commit();
         }
       }
+      // the l buffer may be refilled (query n + 2): every row read it; off the critical path
+      mbar_arrive_cluster(bar(kLEmpty + (n & 1)), peer);
     }
     if (lane == 0) bulk_wait_all();                  // stores complete before the CTA exits
   }

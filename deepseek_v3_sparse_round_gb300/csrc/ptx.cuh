@@ -155,6 +155,17 @@ __device__ __forceinline__ void st_cluster_v4u(uint32_t local_addr, uint32_t cta
 }
 // Order this thread's generic-proxy writes to shared memory anywhere in the cluster before
 // later async-proxy (TMA / tensor core) accesses.
+// Asynchronous 4-byte store into a peer CTA's shared memory; its completion counts 4 transaction
+// bytes on the peer's mbarrier `bar_local` (both addresses given as this CTA's offsets).
+__device__ __forceinline__ void st_async_u32(uint32_t local_addr, uint32_t bar_local,
+                                             uint32_t cta_rank, uint32_t v) {
+  asm volatile(
+      "{\n .reg .b32 ra, rb;\n mapa.shared::cluster.u32 ra, %0, %2;\n"
+      " mapa.shared::cluster.u32 rb, %1, %2;\n"
+      " st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [ra], %3, [rb];\n}\n"
+      ::"r"(local_addr), "r"(bar_local), "r"(cta_rank), "r"(v)
+      : "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_cluster() {
   asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
@@ -177,6 +188,11 @@ __device__ __forceinline__ void bulk_commit() {
 // Wait until every committed bulk copy of this thread has finished reading its source.
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until all but the most recent committed bulk copy group of this thread have finished
+// reading their sources.
+__device__ __forceinline__ void bulk_wait_read_but_one() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 // Wait until every committed bulk copy of this thread has completed (writes included).
 __device__ __forceinline__ void bulk_wait_all() {
