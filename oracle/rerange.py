@@ -46,3 +46,22 @@ def rerange(gathered: np.ndarray, n_tokens: int, sp: int, stride: int = 0) -> np
         tokens = shard_tokens(n_tokens, sp, q)
         out[tokens] = gathered[off[q]:off[q] + len(tokens)]
     return out
+
+
+def rerange_into_pages(gathered: np.ndarray, cu, sp: int, stride: int, block_table,
+                       page_size: int, pool: np.ndarray) -> np.ndarray:
+    """The rerange fused with the write of the KV cache: logical token g of request b (position
+    s = g - cu[b]) goes straight to pool row block_table[b, s // page_size] * page_size +
+    s % page_size instead of row g of a contiguous buffer. Rows of the pool that no token maps to
+    keep their contents. ("[RFC]: Parallel strategy for Deepseek v3.2 like models", "New
+    proposal": the KV is all-gathered before the KV-cache update step; "[DeepSeek v3.2]
+    上下文并行详解", section 4 part 3 step B for the rerange.)"""
+    cu = np.asarray(cu, dtype=np.int64)
+    table = np.asarray(block_table, dtype=np.int64)
+    logical = rerange(gathered, int(cu[-1]), sp, stride)
+    out = pool.copy()
+    for b in range(len(cu) - 1):
+        for s in range(int(cu[b + 1] - cu[b])):
+            page = table[b, s // page_size]
+            out[page * page_size + s % page_size] = logical[cu[b] + s]
+    return out

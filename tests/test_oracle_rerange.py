@@ -48,3 +48,63 @@ def test_padded_offsets():
     assert orr.rank_offsets(11, 4, 3).tolist() == [0, 3, 6, 9]
     assert orr.rank_offsets(11, 4, 0).tolist() == [0, 3, 6, 9]
     assert orr.rank_offsets(10, 4, 0).tolist() == [0, 3, 6, 8]
+
+
+def test_rerange_into_pages_hand_example():
+    # 6 tokens (values 0..5), requests of 4 and 2 tokens, sp = 2 (gathered T0,T2,T4,T1,T3,T5),
+    # pages of 2 rows; request 0 uses pages 3 then 0, request 1 uses page 1. By hand: tokens 0,1
+    # -> rows 6,7; tokens 2,3 -> rows 0,1; tokens 4,5 -> rows 2,3; rows 4,5 untouched (-1).
+    gathered = np.array([0, 2, 4, 1, 3, 5])
+    pool = np.full(8, -1)
+    out = orr.rerange_into_pages(gathered, [0, 4, 6], 2, 0, [[3, 0], [1, -1]], 2, pool)
+    assert out.tolist() == [2, 3, 4, 5, -1, -1, 0, 1]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_rerange_into_pages_contiguous_pages_is_the_rerange(seed):
+    # request lengths that are whole pages and a block table of consecutive pages in request
+    # order: the pool is exactly the logical buffer
+    rng = np.random.default_rng(seed)
+    ps, sp = int(rng.choice([2, 4, 8])), int(rng.integers(1, 6))
+    pages = rng.integers(1, 4, size=int(rng.integers(1, 5)))
+    cu = np.concatenate([[0], np.cumsum(pages * ps)])
+    n = int(cu[-1])
+    table = np.full((len(pages), int(pages.max())), -1)
+    at = 0
+    for b, p in enumerate(pages):
+        table[b, :p] = np.arange(at, at + p)
+        at += p
+    x = rng.integers(0, 1 << 30, size=(n, 3))
+    gathered = orr.all_gather([osplit.split_rows(x, sp, r) for r in range(sp)])
+    out = orr.rerange_into_pages(gathered, cu, sp, 0, table, ps, np.zeros_like(x))
+    assert np.array_equal(out, x)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_rerange_into_pages_reads_back_through_the_page_map(seed):
+    from oracle.kv import PagedKV
+    rng = np.random.default_rng(100 + seed)
+    ps, sp = int(rng.choice([2, 3, 64])), int(rng.integers(1, 9))
+    lengths = rng.integers(0, 200, size=int(rng.integers(1, 6)))
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    need = [-(-int(L) // ps) for L in lengths]
+    perm = rng.permutation(sum(need) + 3)             # a few spare pages stay untouched
+    table = np.full((len(lengths), max(max(need), 1)), -1)
+    at = 0
+    for b, p in enumerate(need):
+        table[b, :p] = perm[at:at + p]
+        at += p
+    n = int(cu[-1])
+    x = rng.integers(0, 1 << 30, size=(n, 2))
+    stride = -(-n // sp) + 1
+    gathered = orr.all_gather([osplit.split_rows(x, sp, r) for r in range(sp)], stride)
+    pool0 = np.full(((sum(need) + 3) * ps, 2), -7)
+    pool = orr.rerange_into_pages(gathered, cu, sp, stride, table, ps, pool0)
+    kv = PagedKV(table, ps)
+    for b in range(len(lengths)):
+        s = np.arange(lengths[b])
+        assert np.array_equal(pool[kv.rows(b, s)], x[cu[b] + s])
+    written = np.zeros(len(pool), bool)
+    for b in range(len(lengths)):
+        written[kv.rows(b, np.arange(lengths[b]))] = True
+    assert (pool[~written] == -7).all()
