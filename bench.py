@@ -223,6 +223,38 @@ class ShardStep:
         return idx_flops, mla_flops
 
 
+def shard_balance(torch, dsa, W, device, wid=3):
+    """Per-shard work of the many-request batch (32 requests, N = 71,014, sp = 4): queries and
+    causal (query, key) pairs under the round-robin split, read from the library's split
+    metadata on the GPU, and for comparison under the contiguous in-sequence split that cuts
+    every request into sp chunks of ceil(L / sp) tokens. spread = (max - min) / mean."""
+    wl = W.WORKLOADS[wid]
+    cu_np = W.cu_seqlens(wl.lengths)
+    n = int(cu_np[-1])
+    cu = torch.as_tensor(cu_np, device=device)
+    rr_q, rr_p = [], []
+    for r in range(wl.sp):
+        n_r = dsa.dsa_rr_shard_len(n, wl.sp, r)
+        e = lambda m: torch.empty(m, dtype=torch.int32, device=device)
+        pos = e(n_r)
+        dsa.dsa_rr_split_metadata(cu, n, wl.sp, r, e(len(cu_np)), pos, e(n_r), e(n_r))
+        p = pos.cpu().numpy().astype(np.int64)
+        rr_q.append(int(n_r))
+        rr_p.append(int(np.sum(p + 1)))
+    is_q, is_p = [0] * wl.sp, [0] * wl.sp
+    for length in wl.lengths:
+        c = -(-int(length) // wl.sp)
+        for q in range(wl.sp):
+            lo, hi = q * c, min((q + 1) * c, int(length))
+            if hi > lo:
+                is_q[q] += hi - lo
+                is_p[q] += (lo + 1 + hi) * (hi - lo) // 2      # sum of (p + 1) over [lo, hi)
+    spread = lambda v: round((max(v) - min(v)) / (sum(v) / len(v)), 5)
+    return {"workload": "many_req: 32 requests U[128,4096] (N=71,014), sp=4",
+            "round_robin": {"queries": rr_q, "causal_pairs": rr_p, "pair_spread": spread(rr_p)},
+            "in_seq": {"queries": is_q, "causal_pairs": is_p, "pair_spread": spread(is_p)}}
+
+
 def gpu_arm(args):
     import torch
     ws, rank, local = dist_env()
@@ -326,6 +358,7 @@ def gpu_arm(args):
         "device_errors": errors,
         "wall_s_timed_region": round(wall, 4),
         "cpu_baseline": cpu,
+        "shard_balance": shard_balance(torch, dsa, W, device),
     }
     print(json.dumps(line), flush=True)
     if dist:

@@ -16,6 +16,7 @@ from . import _native
 
 __all__ = [
     "DsaError", "dsa_version", "dsa_rr_shard_len", "dsa_rr_split_metadata", "dsa_rr_rerange",
+    "dsa_rr_rerange_paged",
     "dsa_indexer_topk_workspace_size", "dsa_score_row_stride", "dsa_indexer_scores",
     "dsa_topk_select", "dsa_indexer_topk", "dsa_indexer_topk_noalloc", "dsa_sparse_mla", "dsa_read_device_errors",
     "DEVERR_TIMEOUT", "DEVERR_BAD_INDEX", "DEVERR_BAD_LENGTH",
@@ -115,6 +116,20 @@ def dsa_rr_rerange(gathered, out, n_tokens, sp, rank_stride_rows=0, stream=None)
     row_bytes = _row_bytes(out)
     _check(_lib().dsa_rr_rerange(_ptr(gathered), _ptr(out), n_tokens, sp, rank_stride_rows,
                                  row_bytes, _stream(stream)))
+
+
+def dsa_rr_rerange_paged(gathered, pool, n_tokens, sp, cu, block_table, rank_stride_rows=0,
+                         page_size=64, stream=None):
+    """pool[page row of (b, s)] = gathered[off[g % sp] + g // sp] for every logical token g
+    (request b, position s = g - cu[b]); n_tokens = cu[-1], passed from the host."""
+    _dev(gathered, None, "gathered")
+    _dev(pool, gathered.dtype, "pool")
+    _dev(cu, torch.int32, "cu"); _dev(block_table, torch.int32, "block_table")
+    row_bytes = _row_bytes(pool)
+    _check(_lib().dsa_rr_rerange_paged(
+        _ptr(gathered), _ptr(pool), pool.shape[0], n_tokens, sp, rank_stride_rows, row_bytes,
+        _ptr(cu), cu.numel() - 1, _ptr(block_table), block_table.shape[1], page_size,
+        _stream(stream)))
 
 
 def dsa_indexer_scores(q_idx, w, k_idx, cu, n_req, pos, bid, max_ctx, scores, workspace,

@@ -29,6 +29,9 @@ int sparse_mla(const void* q, const void* c, int64_t n_kv_rows, const int32_t* c
                float scale, const int32_t* block_table, int max_pages, int page_size, void* o,
                float* lse, cudaStream_t stream);
 cudaError_t split_read_errors(uint32_t* flags);
+int rerange_paged(const void* gathered, void* pool, int64_t pool_rows, int64_t n_tokens, int sp,
+                  int64_t rank_stride_rows, int64_t row_bytes, const int32_t* cu, int n_req,
+                  const int32_t* block_table, int max_pages, int page_size, cudaStream_t stream);
 cudaError_t topk_read_errors(uint32_t* flags);
 cudaError_t indexer_read_errors(uint32_t* flags);
 cudaError_t mla_read_errors(uint32_t* flags);
@@ -105,6 +108,16 @@ DSA_EXPORT int dsa_rr_rerange(const void* gathered, void* out, int64_t n_tokens,
                    int64_t rank_stride_rows, int64_t row_bytes, dsa_stream_t stream) {
   return dsa::rerange(gathered, out, n_tokens, sp, rank_stride_rows, row_bytes,
                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+DSA_EXPORT int dsa_rr_rerange_paged(const void* gathered, void* pool, int64_t pool_rows,
+                                    int64_t n_tokens, int sp, int64_t rank_stride_rows,
+                                    int64_t row_bytes, const int32_t* cu, int n_req,
+                                    const int32_t* block_table, int max_pages, int page_size,
+                                    dsa_stream_t stream) {
+  return dsa::rerange_paged(gathered, pool, pool_rows, n_tokens, sp, rank_stride_rows, row_bytes,
+                            cu, n_req, block_table, max_pages, page_size,
+                            reinterpret_cast<cudaStream_t>(stream));
 }
 
 DSA_EXPORT int64_t dsa_score_row_stride(int max_ctx) {

@@ -5,23 +5,17 @@
 //   S[h, j] = scale * q[t, h, :] . c[row_j, :]          (dqk = 576 = 512 latent + 64 rope)
 //   o[t, h, :] = sum_j softmax_j(S[h, :]) c[row_j, 0:dv]  (dv = 512), lse[t, h] = ln sum exp S
 //
-// GB300 mapping (H = 128, dqk = 576, dv = 512): the fp32 output block O = 128 x 512 alone fills
-// a whole SM's tensor memory (128 lanes x 512 columns), so each query runs on a cluster of two
-// CTAs. CTA c owns
-//   * half of the QK contraction: dims [288c, 288c + 288) -- its slice of Q lives in TMEM
-//     (144 columns, the MMA's A operand) and its slice of every gathered key row in smem,
-//   * half of the output: dims [256c, 256c + 256) of O (256 TMEM columns).
-// Each 64-key tile: TMA tile::gather4 brings the selected rows (5 swizzled 64-column atoms per
-// CTA, 40 KB) into a 4-stage ring; one MMA chain computes the CTA's partial S (128 x 64 fp32,
-// 64 TMEM columns); the softmax warps swap partial tiles with the peer CTA through distributed
-// shared memory, add them (both CTAs obtain bit-identical S), run the online softmax (exp2,
-// running maximum, rescaling O only when the maximum grows by more than 2^8), write P as bf16
-// into a swizzled smem tile and the MMA warp accumulates O += P . V, where V is the same
-// gathered tile read MN-major. QK(j+1) is issued before PV(j) so the tensor pipe works while
-// the softmax of tile j runs.
-//
-// Small heads (H <= 128 with dv <= 256, e.g. H = 8, dqk = 80, dv = 64) run the same code on a
-// single CTA that owns the whole contraction and output.
+// Two kernels:
+//   * sparse_mla_pair_kernel (H = 128, dqk = 576, dv = 512): a persistent grid of CTA pairs;
+//     see the comment above it.
+//   * sparse_mla_kernel (small heads, H <= 128 with dv <= 256; built for H = 8, dqk = 80,
+//     dv = 64): one CTA per query owns the whole contraction and output. Each 64-key tile:
+//     TMA tile::gather4 brings the selected rows into a 4-stage ring; one MMA chain computes S
+//     (128 x 64 fp32) in TMEM; the softmax warps run the online softmax (exp2, running
+//     maximum, rescaling O only when the maximum grows by more than 2^8), write P as bf16 into
+//     a swizzled smem tile and the MMA warp accumulates O += P . V, where V is the same
+//     gathered tile read MN-major. QK(j+1) is issued before PV(j) so the tensor pipe works
+//     while the softmax of tile j runs.
 #include <algorithm>
 #include <cstdint>
 #include <cuda.h>
@@ -41,26 +35,17 @@ constexpr int kPageRows = 64;
 
 template <int H, int DQK, int DV>
 struct MlaShape {
-  static constexpr int kSplit = DV > 256 ? 2 : 1;           // CTAs per query
-  static constexpr int kAtomsTotal = (DQK + 63) / 64;        // 64-column swizzle atoms per row
-  static constexpr int kQKSteps = DQK / 16 / kSplit;         // k-steps (16 dims) per CTA
-  static constexpr int kQDims = kQKSteps * 16;               // dims of Q per CTA
-  static constexpr int kQCols = ((kQDims / 2) + 15) / 16 * 16;  // TMEM columns for Q
-  static constexpr int kDVc = DV / kSplit;                   // output dims per CTA
-  static constexpr int kVAtoms = (kDVc + 63) / 64;
-  // Atoms a CTA gathers: enough to cover its QK dims and its V dims.
-  // (CTA 1's slice starts kQDims % 64 columns into an atom; both CTAs need the same count.)
-  static constexpr int kGAtoms =
-      kSplit == 2 ? ((kQDims % 64) + kQDims + 63) / 64 : kAtomsTotal;
+  static constexpr int kGAtoms = (DQK + 63) / 64;            // 64-column swizzle atoms per row
+  static constexpr int kQKSteps = DQK / 16;                  // k-steps (16 dims)
+  static constexpr int kQCols = ((DQK / 2) + 15) / 16 * 16;  // TMEM columns for Q
+  static constexpr int kDVc = DV;                            // output dims (one CTA)
   static constexpr int kAtomBytes = kTileKeys * 128;         // 64 rows x 128 B
   static constexpr int kStageBytes = kGAtoms * kAtomBytes;
   static constexpr int kStages = 4;
   static constexpr int kPBytes = 128 * 128;                  // 128 rows x 64 keys bf16
-  static constexpr int kXBytes = kSplit == 2 ? 128 * kTileKeys * 4 : 0;
   static constexpr int kOffKV = 0;
   static constexpr int kOffP = kStages * kStageBytes;
-  static constexpr int kOffX = kOffP + 2 * kPBytes;
-  static constexpr int kOffMask = kOffX + kXBytes;
+  static constexpr int kOffMask = kOffP + 2 * kPBytes;
   static constexpr int kOffBar = kOffMask + (kMaxK / kTileKeys) * 8;
   static constexpr int kNumBars = 2 * kStages + 12;
   static constexpr int kOffTmem = kOffBar + kNumBars * 8;
@@ -74,12 +59,10 @@ struct MlaShape {
   static constexpr int kTmemCols = (kColQ + kQCols) <= 256 ? 256 : 512;
   static constexpr int kThreads = 192;                       // 4 softmax warps + TMA + MMA
   static_assert(H <= 128, "heads per CTA");
-  static_assert(DQK % (16 * kSplit) == 0, "qk split");
+  static_assert(DQK % 16 == 0, "qk k-steps");
   static_assert(kColQ + kQCols <= 512, "TMEM budget");
   static_assert(kSmem <= 232448, "smem budget");
-  static_assert(kDVc % 16 == 0 && kDVc <= 256, "PV N");
-  // For the split case, CTA 1's V atoms must start where its gathered atoms start.
-  static_assert(kSplit == 1 || (kDVc % 64 == 0 && kQDims / 64 == kDVc / 64), "layout");
+  static_assert(kDVc % 16 == 0 && kDVc <= 256, "PV N: one CTA holds O");
 };
 
 struct KvMap {
@@ -115,16 +98,13 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16*
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   const uint32_t warp = warp_id(), lane = lane_id();
-  const uint32_t crank = S::kSplit == 2 ? cluster_ctarank() : 0u;
-  const uint32_t peer = crank ^ 1u;
-  const int64_t t = blockIdx.x / S::kSplit;
+  const int64_t t = blockIdx.x;
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + S::kOffAbort);
   uint64_t* masks = reinterpret_cast<uint64_t*>(smem + S::kOffMask);
   auto bar = [&](int i) { return sbase + S::kOffBar + 8u * static_cast<uint32_t>(i); };
   const int kKvFull = 0, kKvEmpty = S::kStages, kQReady = 2 * S::kStages, kSFull = kQReady + 1,
             kSEmpty = kQReady + 2, kPFull = kQReady + 3, kPEmpty = kQReady + 5,
-            kOReady = kQReady + 7, kXFull = kQReady + 8, kXFree = kQReady + 9,
-            kOFinal = kQReady + 10;
+            kOReady = kQReady + 7, kOFinal = kQReady + 8;
 
   const bool aligned = (sbase & 1023u) == 0;
   if (threadIdx.x == 0) {
@@ -134,8 +114,6 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16*
     mbar_init(bar(kSEmpty), 4);
     for (int i = 0; i < 2; ++i) { mbar_init(bar(kPFull + i), 128); mbar_init(bar(kPEmpty + i), 1); }
     mbar_init(bar(kOReady), 1);
-    mbar_init(bar(kXFull), 128);
-    mbar_init(bar(kXFree), 128);
     mbar_init(bar(kOFinal), 1);
     *abort_flag = aligned ? 0u : 1u;
     if (!aligned) report_device_error(kErrBadIndex | 0xB1u);
@@ -158,7 +136,6 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16*
   }
   if (warp == 0) tmem_alloc<S::kTmemCols>(sbase + S::kOffTmem);
   __syncthreads();
-  if (S::kSplit == 2) cluster_sync();                  // the peer's barriers exist from here on
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + S::kOffTmem);
   const int n_tiles = *reinterpret_cast<volatile int*>(smem + S::kOffNTiles);
@@ -168,7 +145,6 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16*
   if (warp == 4) {
     // ------------------------------------------------------------------ TMA gather producer
     if (lane == 0) tma_prefetch_desc(&tm_c);
-    const int atom0 = S::kSplit == 2 ? static_cast<int>(crank) * (S::kQKSteps * 16 / 64) : 0;
     bool bad = !b_ok;
     int stage = 0, issued = 0;
     uint32_t phase = 0;
@@ -189,8 +165,8 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16*
         const uint32_t dst = sbase + S::kOffKV + stage * S::kStageBytes + lane * 4 * 128;
 #pragma unroll
         for (int a = 0; a < S::kGAtoms; ++a)
-          tma_gather4(dst + a * S::kAtomBytes, &tm_c, (atom0 + a) * 64, rows[0], rows[1], rows[2],
-                      rows[3], bar(kKvFull + stage));
+          tma_gather4(dst + a * S::kAtomBytes, &tm_c, a * 64, rows[0], rows[1], rows[2], rows[3],
+                      bar(kKvFull + stage));
       }
       ++issued;
       if (++stage == S::kStages) { stage = 0; phase ^= 1u; }
@@ -210,8 +186,6 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16*
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_bf16(128, kTileKeys, 0, 0);
       const uint32_t idesc_pv = idesc_bf16(128, S::kDVc, 0, 1);
-      const int kstep0 = S::kSplit == 2 ? static_cast<int>(crank) * S::kQKSteps : 0;
-      const int atom0 = S::kSplit == 2 ? static_cast<int>(crank) * (S::kQKSteps * 16 / 64) : 0;
       auto pv = [&](int j) -> bool {
         if (!mbar_wait(bar(kPFull + (j & 1)), (j >> 1) & 1, 0x12, abort_flag)) return false;
         tc_fence_after();
@@ -239,8 +213,7 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16*
         const uint32_t kv_base = sbase + S::kOffKV + st * S::kStageBytes;
 #pragma unroll
         for (int kk = 0; kk < S::kQKSteps; ++kk) {
-          const int g = kstep0 + kk;                   // global 16-dim step
-          const int a = g / 4 - atom0, off = (g % 4) * 32;
+          const int a = kk / 4, off = (kk % 4) * 32;
           const uint64_t db = smem_desc(kv_base + a * S::kAtomBytes + off, 16, 1024, kSwizzle128B);
           umma_ts(tmem + S::kColS, tmem + S::kColQ + kk * 8, db, idesc_qk, kk > 0 ? 1u : 0u);
         }
@@ -255,8 +228,7 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16*
     const uint32_t lane_base = (warp * 32u) << 16;
     // Q slice -> TMEM (A operand of QK).
     {
-      const int d0 = S::kSplit == 2 ? static_cast<int>(crank) * S::kQDims : 0;
-      const uint4* src = reinterpret_cast<const uint4*>(q + (t * H + (h < H ? h : 0)) * DQK + d0);
+      const uint4* src = reinterpret_cast<const uint4*>(q + (t * H + (h < H ? h : 0)) * DQK);
 #pragma unroll
       for (int c0 = 0; c0 < S::kQCols; c0 += 16) {
         uint32_t r[16];
@@ -264,7 +236,7 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16*
         for (int i = 0; i < 4; ++i) {
           const int e = (c0 + 4 * i) * 2;              // first element of this 16-byte chunk
           uint4 v = make_uint4(0, 0, 0, 0);
-          if (h < H && e < S::kQDims) v = __ldg(src + e / 8);
+          if (h < H && e < DQK) v = __ldg(src + e / 8);
           r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
         }
         tmem_st16(tmem + lane_base + S::kColQ + c0, r);
@@ -274,7 +246,6 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16*
       mbar_arrive(bar(kQReady));
     }
     float m_run = -INFINITY, l_run = 0.f;
-    const uint32_t x_row = sbase + S::kOffX + static_cast<uint32_t>(h) * 16u;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
       if (!warp_wait(bar(kSFull), j & 1, 0x16, abort_flag)) { ok = false; break; }
@@ -294,23 +265,6 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16*
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kSEmpty));
-      if (S::kSplit == 2) {
-        // partial tile -> peer, then add the peer's partial tile (identical sum on both CTAs)
-        if (!warp_wait(bar(kXFree), (j & 1) ^ 1, 0x17, abort_flag)) { ok = false; break; }
-#pragma unroll
-        for (int c = 0; c < kTileKeys / 4; ++c)
-          st_cluster_v4(x_row + c * 128 * 16, peer, sv[4 * c], sv[4 * c + 1], sv[4 * c + 2],
-                        sv[4 * c + 3]);
-        mbar_arrive_cluster(bar(kXFull), peer);
-        if (!warp_wait_cluster(bar(kXFull), j & 1, 0x18, abort_flag)) { ok = false; break; }
-        const float4* xr = reinterpret_cast<const float4*>(smem + S::kOffX) + h;
-#pragma unroll
-        for (int c = 0; c < kTileKeys / 4; ++c) {
-          const float4 v = xr[c * 128];
-          sv[4 * c] += v.x; sv[4 * c + 1] += v.y; sv[4 * c + 2] += v.z; sv[4 * c + 3] += v.w;
-        }
-        mbar_arrive_cluster(bar(kXFree), peer);
-      }
       // online softmax in the log2 domain
       const uint64_t mk = masks[j];
       float mt = -INFINITY;
@@ -367,7 +321,6 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16*
     if (ok && n_tiles > 0) ok = warp_wait(bar(kOFinal), 0, 0x1B, abort_flag);
     tc_fence_after();
     const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-    const int dv0 = S::kSplit == 2 ? static_cast<int>(crank) * S::kDVc : 0;
 #pragma unroll 1
     for (int c0 = 0; c0 < S::kDVc; c0 += 16) {
       uint32_t r[16];
@@ -383,12 +336,12 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16*
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           pk[i] = bf16x2_bits(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
-        uint4* dst = reinterpret_cast<uint4*>(o + (t * H + h) * DV + dv0 + c0);
+        uint4* dst = reinterpret_cast<uint4*>(o + (t * H + h) * DV + c0);
         dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
       }
     }
-    if (lse != nullptr && h < H && crank == 0)
+    if (lse != nullptr && h < H)
       lse[t * H + h] = l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
   }
 
@@ -397,7 +350,6 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16*
     tc_fence_after();
     tmem_dealloc<S::kTmemCols>(tmem);
   }
-  if (S::kSplit == 2) cluster_sync();                 // no CTA leaves while its peer may write
 }
 
 // =============================================================================================
@@ -1064,17 +1016,10 @@ int launch_mla(const void* q, const void* c, int64_t n_kv_rows, const KvMap& kv,
   auto kern = sparse_mla_kernel<H, DQK, DV>;
   DSA_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmem));
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(n_q * S::kSplit));
+  cfg.gridDim = dim3(static_cast<unsigned>(n_q));
   cfg.blockDim = dim3(S::kThreads);
   cfg.dynamicSmemBytes = S::kSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = S::kSplit;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   const float scale_log2 = scale * 1.4426950408889634f;
   DSA_CHECK_CUDA(cudaLaunchKernelEx(&cfg, kern, tc, static_cast<const __nv_bfloat16*>(q), bid, topk,
                                     k, kv, scale_log2, static_cast<__nv_bfloat16*>(o), lse));

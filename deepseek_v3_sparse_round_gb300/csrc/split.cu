@@ -7,6 +7,7 @@
 // the flattened (row, 16-byte chunk) index space, several independent chunks in flight per
 // thread, grid sized to a multiple of the SM count.
 #include <cstdint>
+#include <type_traits>
 #include <cuda_runtime.h>
 
 #include "status.cuh"
@@ -153,6 +154,74 @@ split_kernel(const int32_t* __restrict__ cu, int n_req, int64_t n_r, int sp, int
   }
 }
 
+// The rerange fused with the KV-cache write: logical token g (request b, position s = g -
+// cu[b]) lands in pool row block_table[b][s / page_size] * page_size + s % page_size. Chunks of
+// the flattened (token, 16-byte chunk) space, kUnroll loads in flight per thread; the request
+// of a token comes from a binary search over cu staged in shared memory. A token whose page is
+// missing (negative entry, beyond max_pages or outside the pool) is skipped and recorded in the
+// device error word.
+struct PagedPool {
+  const int32_t* table;
+  int max_pages, page_size;
+  int64_t pool_rows;
+};
+
+__device__ __forceinline__ int64_t paged_row(const int32_t* cuv, int n_req, const PagedPool& pp,
+                                             int64_t g) {
+  const int b = find_request(cuv, n_req, g);
+  const int64_t s = g - cuv[b];
+  const int64_t pi = s / pp.page_size;
+  const int page = pi < pp.max_pages ? __ldg(pp.table + static_cast<int64_t>(b) * pp.max_pages + pi) : -1;
+  const int64_t r = page < 0 ? -1 : static_cast<int64_t>(page) * pp.page_size + (s - pi * pp.page_size);
+  return (r >= 0 && r < pp.pool_rows) ? r : -1;
+}
+
+template <typename Idx, int kBytes>
+__global__ void __launch_bounds__(kThreads)
+rerange_paged_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ pool, Idx total,
+                     Idx cpr, RerangeRows map, const int32_t* __restrict__ cu, int n_req,
+                     PagedPool pp) {
+  using V = typename std::conditional<kBytes == 16, int4, uint8_t>::type;
+  __shared__ int32_t s_cu[kCuSmem];
+  const bool staged = n_req + 1 <= kCuSmem;
+  if (staged) {
+    for (int i = threadIdx.x; i <= n_req; i += blockDim.x) s_cu[i] = __ldg(cu + i);
+    __syncthreads();
+  }
+  const int32_t* cuv = staged ? s_cu : cu;
+  const V* vs = reinterpret_cast<const V*>(src);
+  V* vp = reinterpret_cast<V*>(pool);
+  const Idx stride = static_cast<Idx>(gridDim.x) * blockDim.x;
+  bool bad = false;
+  for (Idx i = static_cast<Idx>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += kUnroll * stride) {
+    V v[kUnroll];
+    int64_t dst[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const Idx cc = i + u * stride;
+      dst[u] = -1;
+      if (cc < total) {
+        const Idx g = cc / cpr, c = cc - g * cpr;
+        const int64_t r = paged_row(cuv, n_req, pp, static_cast<int64_t>(g));
+        bad |= r < 0;
+        if (r >= 0) {
+          dst[u] = r * cpr + c;
+          if constexpr (kBytes == 16) v[u] = ld_stream(vs + map(g) * cpr + c);
+          else v[u] = vs[map(g) * cpr + c];
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (dst[u] < 0) continue;
+      if constexpr (kBytes == 16) st_stream(vp + dst[u], v[u]);
+      else vp[dst[u]] = v[u];
+    }
+  }
+  if (bad) report_device_error(kErrBadIndex);
+}
+
 int num_sms() {
   static int sms = 0;
   if (sms == 0) {
@@ -252,6 +321,45 @@ int rerange(const void* gathered, void* out, int64_t n_tokens, int sp, int64_t r
                 static_cast<long long>(rank_stride_rows), static_cast<long long>(need));
   RerangeRows map{sp, n_tokens / sp, n_tokens % sp, rank_stride_rows};
   return launch_copy_rows(gathered, out, n_tokens, row_bytes, map, stream);
+}
+
+int rerange_paged(const void* gathered, void* pool, int64_t pool_rows, int64_t n_tokens, int sp,
+                  int64_t rank_stride_rows, int64_t row_bytes, const int32_t* cu, int n_req,
+                  const int32_t* block_table, int max_pages, int page_size,
+                  cudaStream_t stream) {
+  if (sp < 1 || n_tokens < 0 || row_bytes <= 0 || rank_stride_rows < 0 || n_req < 1 ||
+      page_size < 1 || max_pages < 1 || pool_rows < 0)
+    return fail(DSA_ERR_INVALID,
+                "rerange_paged: need sp >= 1, n_tokens >= 0, row_bytes > 0, n_req >= 1, "
+                "page_size >= 1, max_pages >= 1");
+  if (n_tokens > INT32_MAX) return fail(DSA_ERR_INVALID, "rerange_paged: n_tokens >= 2^31");
+  if (n_tokens == 0) return DSA_OK;
+  if (!gathered || !pool || !cu || !block_table)
+    return fail(DSA_ERR_INVALID, "rerange_paged: null pointer");
+  const int64_t need = (n_tokens + sp - 1) / sp;
+  if (rank_stride_rows > 0 && rank_stride_rows < need)
+    return fail(DSA_ERR_INVALID, "rerange_paged: rank_stride_rows %lld < ceil(N/sp) = %lld",
+                static_cast<long long>(rank_stride_rows), static_cast<long long>(need));
+  RerangeRows map{sp, n_tokens / sp, n_tokens % sp, rank_stride_rows};
+  PagedPool pp{block_table, max_pages, page_size, pool_rows};
+  const bool vec = (row_bytes % 16 == 0) && (reinterpret_cast<uintptr_t>(gathered) % 16 == 0) &&
+                   (reinterpret_cast<uintptr_t>(pool) % 16 == 0);
+  const int64_t cpr = vec ? row_bytes / 16 : row_bytes;
+  const int64_t total = n_tokens * cpr;
+  const int grid = grid_for(total, kUnroll);
+  const auto* src = static_cast<const uint8_t*>(gathered);
+  auto* dst = static_cast<uint8_t*>(pool);
+  if (vec && total < (int64_t(1) << 31))
+    rerange_paged_kernel<uint32_t, 16><<<grid, kThreads, 0, stream>>>(
+        src, dst, static_cast<uint32_t>(total), static_cast<uint32_t>(cpr), map, cu, n_req, pp);
+  else if (vec)
+    rerange_paged_kernel<int64_t, 16><<<grid, kThreads, 0, stream>>>(src, dst, total, cpr, map, cu,
+                                                                      n_req, pp);
+  else
+    rerange_paged_kernel<int64_t, 1><<<grid, kThreads, 0, stream>>>(src, dst, total, cpr, map, cu,
+                                                                     n_req, pp);
+  DSA_CHECK_CUDA(cudaGetLastError());
+  return DSA_OK;
 }
 
 cudaError_t split_read_errors(uint32_t* flags) { return read_and_clear_device_error(flags); }

@@ -6,6 +6,7 @@
  *
  *   dsa_rr_split_metadata  shard token list, batch ids, positions, shard cu_seqlens, row gather
  *   dsa_rr_rerange         all-gathered (rank-major) KV rows -> logical token order
+ *   dsa_rr_rerange_paged   the same rows straight into a paged KV cache (rerange + cache write)
  *   dsa_indexer_topk       lightning-indexer scores over the causal history + per-query top-k
  *     (= dsa_indexer_scores followed by dsa_topk_select, also exported on their own)
  *   dsa_sparse_mla         sparse MLA of every shard query over its top-k latent rows
@@ -109,6 +110,31 @@ int dsa_rr_split_metadata(const int32_t* cu, int n_req, int64_t n_tokens, int sp
  */
 int dsa_rr_rerange(const void* gathered, void* out, int64_t n_tokens, int sp,
                    int64_t rank_stride_rows, int64_t row_bytes, dsa_stream_t stream);
+
+/*
+ * Rerange fused with the write of a paged KV cache.
+ * Source: "[RFC]: Parallel strategy for Deepseek v3.2 like models", "New proposal" (the KV is
+ * all-gathered before the KV-cache update step) and "[DeepSeek v3.2] 上下文并行详解", section 4
+ * part 3 step B (rank-major gathered rows back to logical order). Reading: the two steps are
+ * one pass, so the logical rows never exist as a separate buffer.
+ *
+ * For every logical token g < n_tokens with request b (the largest b with cu[b] <= g) and
+ * position s = g - cu[b]:
+ *   pool[block_table[b * max_pages + s / page_size] * page_size + s % page_size, :] =
+ *       gathered[off[g % sp] + g / sp, :]
+ * with off[] as in dsa_rr_rerange (rank_stride_rows > 0: padded blocks; 0: packed). Rows of
+ * row_bytes bytes. cu [n_req+1] int32 device (cu[0] = 0, non-decreasing, cu[n_req] =
+ * n_tokens); block_table [n_req, max_pages] int32 device; pool [pool_rows, row_bytes] device,
+ * caller-owned; pool rows that no token maps to are not written. A token whose page entry is
+ * negative, beyond max_pages or outside the pool is skipped and sets DSA_DEVERR_BAD_INDEX.
+ * 16-byte vectors when both buffers and row_bytes are multiples of 16, else byte copies.
+ * Errors: DSA_ERR_INVALID for sp < 1, n_tokens < 0 or >= 2^31, row_bytes <= 0, n_req < 1,
+ * page_size < 1, max_pages < 1, a stride smaller than ceil(n_tokens / sp) or null pointers.
+ */
+int dsa_rr_rerange_paged(const void* gathered, void* pool, int64_t pool_rows, int64_t n_tokens,
+                         int sp, int64_t rank_stride_rows, int64_t row_bytes, const int32_t* cu,
+                         int n_req, const int32_t* block_table, int max_pages, int page_size,
+                         dsa_stream_t stream);
 
 /*
  * Bytes of scratch dsa_indexer_topk needs: the fp32 score rows [n_q, stride(max_ctx)] plus a

@@ -70,3 +70,15 @@ def test_invalid_arguments_rejected_before_any_launch(lib):
     assert lib.dsa_topk_select(fake, 3, fake, 4, 8, 10, fake, null) == -1    # stride < max_ctx
     assert lib.dsa_indexer_scores(fake, fake, fake, 10, fake, 1, fake, fake, 4, 32, 128, 10, null,
                                   0, 0, fake, 12, fake, 1 << 20, null) == -2
+
+
+def test_rerange_paged_arguments_rejected(lib):
+    null = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(4096)
+    f = lib.dsa_rr_rerange_paged
+    assert f(fake, fake, 64, 10, 0, 0, 16, fake, 1, fake, 1, 64, null) == -1     # sp = 0
+    assert f(fake, fake, 64, 10, 4, 1, 16, fake, 1, fake, 1, 64, null) == -1     # stride < ceil(N/sp)
+    assert f(fake, fake, 64, 10, 4, 0, 16, fake, 1, fake, 1, 0, null) == -1      # page_size 0
+    assert f(fake, fake, 64, 10, 4, 0, 16, fake, 0, fake, 1, 64, null) == -1     # n_req 0
+    assert f(null, fake, 64, 10, 4, 0, 16, fake, 1, fake, 1, 64, null) == -1     # null gathered
+    assert f(null, null, 0, 0, 4, 0, 16, null, 1, null, 1, 64, null) == 0        # empty no-op

@@ -64,3 +64,86 @@ def test_rerange_of_oracle_gather_odd_rows(row_bytes):
     import deepseek_v3_sparse_round_gb300 as dsa
     dsa.dsa_rr_rerange(torch.as_tensor(gathered).cuda(), out, n, sp, 0)
     assert np.array_equal(out.cpu().numpy(), x)
+
+
+def _paged_case(lengths, sp, ps, seed, width, dtype=torch.bfloat16, spare_pages=3):
+    """Logical rows x (seeded), the rank-major gathered buffer, a random block table and a pool
+    pre-filled with a sentinel."""
+    rng = np.random.default_rng(seed)
+    cu = W.cu_seqlens(lengths)
+    n = int(cu[-1])
+    need = [-(-int(L) // ps) for L in lengths]
+    n_pages = sum(need) + spare_pages
+    perm = rng.permutation(n_pages)
+    table = np.full((len(lengths), max(max(need), 1)), -1, dtype=np.int32)
+    at = 0
+    for b, p in enumerate(need):
+        table[b, :p] = perm[at:at + p]
+        at += p
+    x = W.normal_bf16((n, width), seed=seed, device="cuda") if dtype == torch.bfloat16 \
+        else W.int_uniform((n, width), 0, 254, seed, dtype=torch.uint8, device="cuda")
+    pool0 = torch.full((n_pages * ps, width), 7, dtype=x.dtype, device="cuda")
+    return cu, n, table, x, pool0
+
+
+def _oracle_pool(gathered, cu, sp, stride, table, ps, pool0):
+    g = gathered.cpu().view(torch.uint8).numpy() if gathered.dtype == torch.bfloat16 else gathered.cpu().numpy()
+    p = pool0.cpu().view(torch.uint8).numpy() if pool0.dtype == torch.bfloat16 else pool0.cpu().numpy()
+    return orr.rerange_into_pages(g, cu, sp, stride, table, ps, p)
+
+
+@pytest.mark.parametrize("wid", [1, 3])
+@pytest.mark.parametrize("padded", [False, True])
+@pytest.mark.parametrize("width", [576, 128])
+def test_rerange_paged_workloads(wid, padded, width):
+    from dsa_cases import dsa, i32
+    wl = W.WORKLOADS[wid]
+    cu, n, table, x, pool0 = _paged_case(wl.lengths, wl.sp, 64, 11 + wid, width)
+    gathered, _ = gpu_gather_and_rerange(x, cu, wl.sp, padded)
+    stride = (-(-n // wl.sp)) if padded else 0
+    pool = pool0.clone()
+    dsa().dsa_rr_rerange_paged(gathered, pool, n, wl.sp, i32(cu), i32(table), stride, 64)
+    want = _oracle_pool(gathered, cu, wl.sp, stride, table, 64, pool0)
+    got = pool.cpu().view(torch.uint8).numpy()
+    assert np.array_equal(got, want)
+    assert dsa().dsa_read_device_errors() == 0
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_rerange_paged_edge_cases(seed):
+    """Odd page sizes, empty requests, byte rows (row size not a multiple of 16), sp = 1."""
+    from dsa_cases import dsa, i32
+    rng = np.random.default_rng(seed)
+    lengths = [int(v) for v in rng.integers(0, 300, int(rng.integers(1, 9)))]
+    lengths[0] = 0
+    sp = int(rng.integers(1, 9))
+    ps = int(rng.choice([1, 3, 16, 64]))
+    width = int(rng.choice([7, 32]))                       # 7-byte rows: byte path
+    cu, n, table, x, pool0 = _paged_case(lengths, sp, ps, 50 + seed, width, dtype=torch.uint8)
+    shards = [gpu_split(cu, sp, r, src=x)["rows"] for r in range(sp)]
+    gathered = torch.cat(shards)
+    pool = pool0.clone()
+    dsa().dsa_rr_rerange_paged(gathered, pool, n, sp, i32(cu), i32(table), 0, ps)
+    want = orr.rerange_into_pages(gathered.cpu().numpy(), cu, sp, 0, table, ps, pool0.cpu().numpy())
+    assert np.array_equal(pool.cpu().numpy(), want)
+    assert dsa().dsa_read_device_errors() == 0
+
+
+def test_rerange_paged_missing_page_is_skipped_and_flagged():
+    from dsa_cases import dsa, i32
+    lengths = [130, 70]
+    cu, n, table, x, pool0 = _paged_case(lengths, 4, 64, 3, 128)
+    table = table.copy()
+    lost = int(table[0, 1])
+    table[0, 1] = -1                                       # request 0, positions 64..127
+    gathered, _ = gpu_gather_and_rerange(x, cu, 4, False)
+    pool = pool0.clone()
+    dsa().dsa_rr_rerange_paged(gathered, pool, n, 4, i32(cu), i32(table), 0, 64)
+    assert dsa().dsa_read_device_errors() & dsa().DEVERR_BAD_INDEX
+    got = pool.cpu()
+    assert torch.equal(got[lost * 64:(lost + 1) * 64], pool0.cpu()[lost * 64:(lost + 1) * 64])
+    keep = table.copy()
+    keep[0, 1] = lost
+    kv_rows = [int(keep[0, 0]) * 64 + s for s in range(64)] + [int(keep[1, 0]) * 64 + s for s in range(64)]
+    src_rows = list(range(64)) + [130 + s for s in range(64)]
+    assert torch.equal(got[kv_rows], x.cpu()[src_rows])
