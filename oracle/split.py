@@ -45,3 +45,16 @@ def round_robin_split(cu, sp: int, rank: int) -> dict:
 def split_rows(src: np.ndarray, sp: int, rank: int) -> np.ndarray:
     """The rank's rows of a per-token tensor: src[arange(rank, N, sp)] (section 2.B)."""
     return src[shard_tokens(src.shape[0], sp, rank)]
+
+
+def round_robin_split_decode(cu_new, pos_base, sp: int, rank: int) -> dict:
+    """Round-robin split of a decode step's new tokens ("[RFC]: Parallel strategy for Deepseek
+    v3.2 like models", "New proposal": sequence parallel over the token dimension for both
+    prefill and decode). The flattened batch is the new tokens only (cu_new); a new token's
+    logical position is its request's earlier context pos_base[b] plus its index among the
+    request's new tokens. Reading: the same dealing as prefill (section 2.B of "[DeepSeek v3.2]
+    上下文并行详解"), applied to the decode batch."""
+    out = round_robin_split(cu_new, sp, rank)
+    base = np.asarray(pos_base, dtype=np.int64)
+    out["pos"] = out["pos"] + base[out["bid"]]
+    return out

@@ -105,3 +105,39 @@ def test_split_rows_gathers_rows():
 
 def test_random_lengths_generator_is_seeded():
     assert random_lengths(5, 1, 9, 3) == random_lengths(5, 1, 9, 3)
+
+
+def test_decode_split_positions_continue_the_context():
+    # two requests with contexts of 10 and 5 tokens before this step, 2 and 3 new tokens;
+    # sp = 2: flattened new tokens 0..4 -> rank 0 gets 0, 2, 4; rank 1 gets 1, 3.
+    # request 0's new tokens sit at positions 10, 11; request 1's at 5, 6, 7.
+    r0 = osplit.round_robin_split_decode([0, 2, 5], [10, 5], 2, 0)
+    r1 = osplit.round_robin_split_decode([0, 2, 5], [10, 5], 2, 1)
+    assert r0["bid"].tolist() == [0, 1, 1] and r0["pos"].tolist() == [10, 5, 7]
+    assert r1["bid"].tolist() == [0, 1] and r1["pos"].tolist() == [11, 6]
+    assert r0["cu_shard"].tolist() == [0, 1, 3] and r1["cu_shard"].tolist() == [0, 1, 2]
+
+
+def test_decode_split_with_one_shard_is_the_decode_batch():
+    # sp = 1 keeps every new token: the positions are the last q tokens of each context, the
+    # layout of the decode workload (its queries at C - 2 and C - 1)
+    import workloads as W
+    wl = W.WORKLOADS[4]
+    q = wl.decode_queries
+    ctx = np.asarray(wl.lengths, dtype=np.int64)
+    cu_new = np.arange(len(ctx) + 1, dtype=np.int64) * q
+    out = osplit.round_robin_split_decode(cu_new, ctx - q, 1, 0)
+    bid, pos = W.decode_queries(wl.lengths, q)
+    assert np.array_equal(out["bid"], bid) and np.array_equal(out["pos"], pos)
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_decode_split_zero_base_is_the_prefill_split(seed):
+    rng = np.random.default_rng(seed)
+    cu = np.concatenate([[0], np.cumsum(rng.integers(0, 5, int(rng.integers(1, 9))))])
+    sp = int(rng.integers(1, 6))
+    for r in range(sp):
+        a = osplit.round_robin_split(cu, sp, r)
+        b = osplit.round_robin_split_decode(cu, np.zeros(len(cu) - 1), sp, r)
+        for k in a:
+            assert np.array_equal(a[k], b[k])
