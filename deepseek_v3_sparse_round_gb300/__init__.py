@@ -16,7 +16,7 @@ from . import _native
 
 __all__ = [
     "DsaError", "dsa_version", "dsa_rr_shard_len", "dsa_rr_split_metadata", "dsa_rr_rerange",
-    "dsa_rr_rerange_paged",
+    "dsa_rr_rerange_paged", "dsa_rr_split_decode_metadata",
     "dsa_indexer_topk_workspace_size", "dsa_score_row_stride", "dsa_indexer_scores",
     "dsa_topk_select", "dsa_indexer_topk", "dsa_indexer_topk_noalloc", "dsa_sparse_mla", "dsa_read_device_errors",
     "DEVERR_TIMEOUT", "DEVERR_BAD_INDEX", "DEVERR_BAD_LENGTH",
@@ -107,6 +107,23 @@ def dsa_rr_split_metadata(cu, n_tokens, sp, rank, cu_shard, pos, bid, gidx=None,
                                         _ptr(cu_shard), _ptr(pos), _ptr(bid), _ptr(gidx),
                                         _ptr(src_rows), _ptr(dst_rows), row_bytes,
                                         _stream(stream)))
+
+
+def dsa_rr_split_decode_metadata(cu_new, pos_base, n_tokens, sp, rank, cu_shard, pos, bid,
+                                 gidx=None, src_rows=None, dst_rows=None, stream=None):
+    """As dsa_rr_split_metadata over a decode step's new tokens; pos = pos_base[b] + index."""
+    for name, t in (("cu_new", cu_new), ("pos_base", pos_base), ("cu_shard", cu_shard),
+                    ("pos", pos), ("bid", bid), ("gidx", gidx)):
+        _dev(t, torch.int32, name)
+    row_bytes = 0
+    if src_rows is not None:
+        _dev(src_rows, None, "src_rows")
+        _dev(dst_rows, src_rows.dtype, "dst_rows")
+        row_bytes = _row_bytes(src_rows)
+    _check(_lib().dsa_rr_split_decode_metadata(
+        _ptr(cu_new), _ptr(pos_base), cu_new.numel() - 1, n_tokens, sp, rank, _ptr(cu_shard),
+        _ptr(pos), _ptr(bid), _ptr(gidx), _ptr(src_rows), _ptr(dst_rows), row_bytes,
+        _stream(stream)))
 
 
 def dsa_rr_rerange(gathered, out, n_tokens, sp, rank_stride_rows=0, stream=None):

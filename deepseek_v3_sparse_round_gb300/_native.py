@@ -19,6 +19,8 @@ SIGNATURES = {
     "dsa_rr_shard_len": (c_i64, [c_i64, c_int, c_int]),
     "dsa_rr_split_metadata": (c_int, [c_vp, c_int, c_i64, c_int, c_int, c_vp, c_vp, c_vp, c_vp,
                                       c_vp, c_vp, c_i64, c_vp]),
+    "dsa_rr_split_decode_metadata": (c_int, [c_vp, c_vp, c_int, c_i64, c_int, c_int, c_vp, c_vp,
+                                             c_vp, c_vp, c_vp, c_vp, c_i64, c_vp]),
     "dsa_rr_rerange": (c_int, [c_vp, c_vp, c_i64, c_int, c_i64, c_i64, c_vp]),
     "dsa_rr_rerange_paged": (c_int, [c_vp, c_vp, c_i64, c_i64, c_int, c_i64, c_i64, c_vp, c_int,
                                      c_vp, c_int, c_int, c_vp]),

@@ -11,8 +11,8 @@ namespace dsa {
 
 // ---- defined in the kernel translation units ----
 int64_t shard_len(int64_t n_tokens, int sp, int rank);
-int split_metadata(const int32_t* cu, int n_req, int64_t n_tokens, int sp, int rank,
-                   int32_t* cu_shard, int32_t* pos, int32_t* bid, int32_t* gidx,
+int split_metadata(const int32_t* cu, const int32_t* pos_base, int n_req, int64_t n_tokens,
+                   int sp, int rank, int32_t* cu_shard, int32_t* pos, int32_t* bid, int32_t* gidx,
                    const void* src_rows, void* dst_rows, int64_t row_bytes, cudaStream_t stream);
 int rerange(const void* gathered, void* out, int64_t n_tokens, int sp, int64_t rank_stride_rows,
             int64_t row_bytes, cudaStream_t stream);
@@ -100,8 +100,19 @@ DSA_EXPORT int dsa_rr_split_metadata(const int32_t* cu, int n_req, int64_t n_tok
                           int32_t* cu_shard, int32_t* pos, int32_t* bid, int32_t* gidx,
                           const void* src_rows, void* dst_rows, int64_t row_bytes,
                           dsa_stream_t stream) {
-  return dsa::split_metadata(cu, n_req, n_tokens, sp, rank, cu_shard, pos, bid, gidx, src_rows,
-                             dst_rows, row_bytes, reinterpret_cast<cudaStream_t>(stream));
+  return dsa::split_metadata(cu, nullptr, n_req, n_tokens, sp, rank, cu_shard, pos, bid, gidx,
+                             src_rows, dst_rows, row_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+DSA_EXPORT int dsa_rr_split_decode_metadata(const int32_t* cu_new, const int32_t* pos_base,
+                                            int n_req, int64_t n_tokens, int sp, int rank,
+                                            int32_t* cu_shard, int32_t* pos, int32_t* bid,
+                                            int32_t* gidx, const void* src_rows, void* dst_rows,
+                                            int64_t row_bytes, dsa_stream_t stream) {
+  if (!pos_base) return dsa::fail(DSA_ERR_INVALID, "split_decode: pos_base is required");
+  return dsa::split_metadata(cu_new, pos_base, n_req, n_tokens, sp, rank, cu_shard, pos, bid,
+                             gidx, src_rows, dst_rows, row_bytes,
+                             reinterpret_cast<cudaStream_t>(stream));
 }
 
 DSA_EXPORT int dsa_rr_rerange(const void* gathered, void* out, int64_t n_tokens, int sp,

@@ -117,15 +117,16 @@ copy_rows_bytes_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ ds
 }
 
 // One launch for the whole split: shard cu_seqlens (closed form), per-token metadata (the
-// request found by binary search over cu staged in shared memory) and, when asked, the 16-byte
-// row gather of the shard's tokens.
+// request found by binary search over cu staged in shared memory; positions offset by
+// pos_base[b] when given, for a decode step's new tokens) and, when asked, the 16-byte row
+// gather of the shard's tokens.
 constexpr int kCuSmem = 4096;
 template <bool kGather>
 __global__ void __launch_bounds__(kThreads)
-split_kernel(const int32_t* __restrict__ cu, int n_req, int64_t n_r, int sp, int rank,
-             int32_t* __restrict__ cu_shard, int32_t* __restrict__ pos, int32_t* __restrict__ bid,
-             int32_t* __restrict__ gidx, const int4* __restrict__ src, int4* __restrict__ dst,
-             int64_t chunks_per_row) {
+split_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ pos_base, int n_req,
+             int64_t n_r, int sp, int rank, int32_t* __restrict__ cu_shard,
+             int32_t* __restrict__ pos, int32_t* __restrict__ bid, int32_t* __restrict__ gidx,
+             const int4* __restrict__ src, int4* __restrict__ dst, int64_t chunks_per_row) {
   __shared__ int32_t s_cu[kCuSmem];
   const bool staged = n_req + 1 <= kCuSmem;
   if (staged) {
@@ -139,7 +140,7 @@ split_kernel(const int32_t* __restrict__ cu, int n_req, int64_t n_r, int sp, int
   for (int64_t t = i0; t < n_r; t += stride) {
     const int64_t g = rank + t * sp;
     const int b = find_request(cuv, n_req, g);
-    pos[t] = static_cast<int32_t>(g - cuv[b]);
+    pos[t] = static_cast<int32_t>(g - cuv[b] + (pos_base ? __ldg(pos_base + b) : 0));
     bid[t] = b;
     if (gidx) gidx[t] = static_cast<int32_t>(g);
   }
@@ -273,9 +274,9 @@ int64_t shard_len(int64_t n_tokens, int sp, int rank) {
   return n_tokens > rank ? (n_tokens - rank + sp - 1) / sp : 0;
 }
 
-int split_metadata(const int32_t* cu, int n_req, int64_t n_tokens, int sp, int rank,
-                   int32_t* cu_shard, int32_t* pos, int32_t* bid, int32_t* gidx,
-                   const void* src_rows, void* dst_rows, int64_t row_bytes,
+int split_metadata(const int32_t* cu, const int32_t* pos_base, int n_req, int64_t n_tokens,
+                   int sp, int rank, int32_t* cu_shard, int32_t* pos, int32_t* bid,
+                   int32_t* gidx, const void* src_rows, void* dst_rows, int64_t row_bytes,
                    cudaStream_t stream) {
   if (sp < 1 || rank < 0 || rank >= sp)
     return fail(DSA_ERR_INVALID, "split: need sp >= 1 and 0 <= rank < sp (sp=%d rank=%d)", sp,
@@ -296,13 +297,13 @@ int split_metadata(const int32_t* cu, int n_req, int64_t n_tokens, int sp, int r
     const int64_t cpr = row_bytes / 16;
     const int64_t items = n_r * cpr > meta_items ? n_r * cpr : meta_items;
     split_kernel<true><<<grid_for(items, kUnroll), kThreads, 0, stream>>>(
-        cu, n_req, n_r, sp, rank, cu_shard, pos, bid, gidx, static_cast<const int4*>(src_rows),
+        cu, pos_base, n_req, n_r, sp, rank, cu_shard, pos, bid, gidx, static_cast<const int4*>(src_rows),
         static_cast<int4*>(dst_rows), cpr);
     DSA_CHECK_CUDA(cudaGetLastError());
     return DSA_OK;
   }
   split_kernel<false><<<grid_for(meta_items, 1), kThreads, 0, stream>>>(
-      cu, n_req, n_r, sp, rank, cu_shard, pos, bid, gidx, nullptr, nullptr, 0);
+      cu, pos_base, n_req, n_r, sp, rank, cu_shard, pos, bid, gidx, nullptr, nullptr, 0);
   DSA_CHECK_CUDA(cudaGetLastError());
   if (src_rows) return launch_copy_rows(src_rows, dst_rows, n_r, row_bytes, SplitRows{sp, rank},
                                         stream);

@@ -5,6 +5,8 @@
  * over `sp` sequence shards (flattened token g goes to shard g % sp):
  *
  *   dsa_rr_split_metadata  shard token list, batch ids, positions, shard cu_seqlens, row gather
+ *   dsa_rr_split_decode_metadata  the same for a decode step's new tokens (positions continue
+ *                          each request's context)
  *   dsa_rr_rerange         all-gathered (rank-major) KV rows -> logical token order
  *   dsa_rr_rerange_paged   the same rows straight into a paged KV cache (rerange + cache write)
  *   dsa_indexer_topk       lightning-indexer scores over the causal history + per-query top-k
@@ -93,6 +95,27 @@ int dsa_rr_split_metadata(const int32_t* cu, int n_req, int64_t n_tokens, int sp
                           int32_t* cu_shard, int32_t* pos, int32_t* bid, int32_t* gidx,
                           const void* src_rows, void* dst_rows, int64_t row_bytes,
                           dsa_stream_t stream);
+
+/*
+ * Round-robin split of a decode step's new tokens.
+ * Source: "[RFC]: Parallel strategy for Deepseek v3.2 like models", "New proposal" (sequence
+ * parallel over the token dimension for both prefill and decode); the dealing itself is the
+ * prefill one ("[DeepSeek v3.2] 上下文并行详解", section 2.B). Reading: the flattened batch is
+ * the step's new tokens, and a new token's position continues its request's context.
+ *
+ * Identical to dsa_rr_split_metadata over cu_new [n_req+1] (offsets of each request's new
+ * tokens, cu_new[n_req] = n_tokens) except that
+ *   pos[t] = pos_base[bid_t] + (g_t - cu_new[bid_t])
+ * where pos_base [n_req] int32 device = the number of tokens of request b already in the KV
+ * cache before this step. The outputs feed dsa_indexer_topk / dsa_sparse_mla with a block
+ * table. Every argument is a device pointer or a host scalar, nothing is read back, so a decode
+ * step built from these calls can be captured in a CUDA graph and replayed.
+ * Errors: as dsa_rr_split_metadata; DSA_ERR_INVALID when pos_base is NULL.
+ */
+int dsa_rr_split_decode_metadata(const int32_t* cu_new, const int32_t* pos_base, int n_req,
+                                 int64_t n_tokens, int sp, int rank, int32_t* cu_shard,
+                                 int32_t* pos, int32_t* bid, int32_t* gidx, const void* src_rows,
+                                 void* dst_rows, int64_t row_bytes, dsa_stream_t stream);
 
 /*
  * Rerange an all-gathered buffer to logical token order.

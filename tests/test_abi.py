@@ -82,3 +82,12 @@ def test_rerange_paged_arguments_rejected(lib):
     assert f(fake, fake, 64, 10, 4, 0, 16, fake, 0, fake, 1, 64, null) == -1     # n_req 0
     assert f(null, fake, 64, 10, 4, 0, 16, fake, 1, fake, 1, 64, null) == -1     # null gathered
     assert f(null, null, 0, 0, 4, 0, 16, null, 1, null, 1, 64, null) == 0        # empty no-op
+
+
+def test_split_decode_needs_pos_base(lib):
+    null = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(4096)
+    f = lib.dsa_rr_split_decode_metadata
+    assert f(fake, null, 1, 10, 4, 0, fake, fake, fake, null, null, null, 0, null) == -1
+    assert b"pos_base" in lib.dsa_last_error_string()
+    assert f(fake, fake, 1, 10, 0, 0, fake, fake, fake, null, null, null, 0, null) == -1   # sp = 0
