@@ -383,15 +383,22 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         float acc[S::kQPA];
 #pragma unroll
         for (int q = 0; q < S::kQPA; ++q) acc[q] = 0.f;
+        // 64 columns per TMEM round trip; w read four columns at a time (broadcast LDS.128)
+        static_assert((S::kQPA * HI) % 64 == 0, "epilogue chunks");
 #pragma unroll
-        for (int c0 = 0; c0 < S::kQPA * HI; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(t_acc + static_cast<uint32_t>(c0), v);
+        for (int c0 = 0; c0 < S::kQPA * HI; c0 += 64) {
+          uint32_t v[64];
+          tmem_ld32(t_acc + static_cast<uint32_t>(c0), *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          tmem_ld32(t_acc + static_cast<uint32_t>(c0 + 32), *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
+          for (int j = 0; j < 64; j += 4) {
             const int col = c0 + j, q = col / HI;
-            acc[q] = fmaf(sw[col], fmaxf(__uint_as_float(v[j]), 0.f), acc[q]);
+            const float4 w4 = *reinterpret_cast<const float4*>(sw + col);
+            acc[q] = fmaf(w4.x, fmaxf(__uint_as_float(v[j]), 0.f), acc[q]);
+            acc[q] = fmaf(w4.y, fmaxf(__uint_as_float(v[j + 1]), 0.f), acc[q]);
+            acc[q] = fmaf(w4.z, fmaxf(__uint_as_float(v[j + 2]), 0.f), acc[q]);
+            acc[q] = fmaf(w4.w, fmaxf(__uint_as_float(v[j + 3]), 0.f), acc[q]);
           }
         }
         tc_fence_before();
