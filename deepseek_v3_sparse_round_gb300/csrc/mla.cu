@@ -640,7 +640,10 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
               db0 + static_cast<uint64_t>(((gg >> 2) * kAtomBytes + (gg & 3) * 32) >> 4);
           if (leader) umma_ts(d_s, tmem + kColQ + gg * 8, db, idesc, gg > 0 ? 1u : 0u);
         }
-        if (leader) umma_commit(bar(kSFull + sb));
+        if (leader) {
+          umma_commit(bar(kSFull + sb));
+          umma_commit(bar(kKvEmpty + s));          // the slot is free once these MMAs finish
+        }
         __syncwarp();
       }
       g0 += nt;
@@ -813,8 +816,6 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kSEmpty + sb));
-        // S full means this tile's QK MMAs have finished reading its ring slot
-        if (threadIdx.x == 0) mbar_arrive(bar(kKvEmpty + sb));
         const int e0 = j * kKeys;                    // validity bits of this tile's entries
         const uint64_t mk = ((static_cast<uint64_t>(mwords[(e0 >> 5) + 1]) << 32) |
                              mwords[e0 >> 5]) >> (e0 & 31);
