@@ -802,14 +802,12 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
         tc_fence_after();
         float sv[kKeys];
         {
-          uint32_t r[32];
+          uint32_t r[32], r16[16];                   // both loads in flight, one wait
           tmem_ld32(tmem + lane_base + kColS + sb * kSStride, r);
+          tmem_ld16(tmem + lane_base + kColS + sb * kSStride + 32, r16);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) sv[i] = __uint_as_float(r[i]);
-          uint32_t (&r16)[16] = *reinterpret_cast<uint32_t(*)[16]>(&r[0]);
-          tmem_ld16(tmem + lane_base + kColS + sb * kSStride + 32, r16);
-          tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < kKeys - 32; ++i) sv[32 + i] = __uint_as_float(r16[i]);
         }
@@ -819,11 +817,21 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
         const int e0 = j * kKeys;                    // validity bits of this tile's entries
         const uint64_t mk = ((static_cast<uint64_t>(mwords[(e0 >> 5) + 1]) << 32) |
                              mwords[e0 >> 5]) >> (e0 & 31);
+        const uint32_t mlo = static_cast<uint32_t>(mk), mhi = static_cast<uint32_t>(mk >> 32);
         float mt = -INFINITY;
+        if (mlo == 0xFFFFFFFFu && (mhi & 0xFFFFu) == 0xFFFFu) {   // every entry valid (common)
 #pragma unroll
-        for (int i = 0; i < kKeys; ++i) {
-          sv[i] = ((mk >> i) & 1ull) ? sv[i] * scale_log2 : -INFINITY;
-          mt = fmaxf(mt, sv[i]);
+          for (int i = 0; i < kKeys; ++i) {
+            sv[i] *= scale_log2;
+            mt = fmaxf(mt, sv[i]);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < kKeys; ++i) {
+            const bool v = i < 32 ? ((mlo >> i) & 1u) : ((mhi >> (i - 32)) & 1u);
+            sv[i] = v ? sv[i] * scale_log2 : -INFINITY;
+            mt = fmaxf(mt, sv[i]);
+          }
         }
         float alpha = 1.f;
         if (m_ref == -INFINITY) {
