@@ -818,35 +818,46 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
         const uint64_t mk = ((static_cast<uint64_t>(mwords[(e0 >> 5) + 1]) << 32) |
                              mwords[e0 >> 5]) >> (e0 & 31);
         const uint32_t mlo = static_cast<uint32_t>(mk), mhi = static_cast<uint32_t>(mk >> 32);
-        float mt = -INFINITY;
-        if (mlo == 0xFFFFFFFFu && (mhi & 0xFFFFu) == 0xFFFFu) {   // every entry valid (common)
+        const bool full = mlo == 0xFFFFFFFFu && (mhi & 0xFFFFu) == 0xFFFFu;   // common case
+        auto valid_at = [&](int i) {
+          return full || (i < 32 ? ((mlo >> i) & 1u) != 0u : ((mhi >> (i - 32)) & 1u) != 0u);
+        };
+        // x_i = scale * s_i - m_ref in the log2 domain (one FMA); masked entries -inf, whose
+        // ex2 is 0. m_ref moves only when a row's maximum grows by more than 2^kLazyLog2.
+        float alpha = 1.f;
+        if (m_ref == -INFINITY) {                    // no valid entry in this row so far
+          float mt = -INFINITY;
 #pragma unroll
           for (int i = 0; i < kKeys; ++i) {
-            sv[i] *= scale_log2;
+            sv[i] = valid_at(i) ? sv[i] * scale_log2 : -INFINITY;
             mt = fmaxf(mt, sv[i]);
+          }
+          m_ref = mt;
+          if (mt != -INFINITY) {
+#pragma unroll
+            for (int i = 0; i < kKeys; ++i) sv[i] -= mt;
           }
         } else {
+          const float nm = -m_ref;
+          float xm = -INFINITY;
 #pragma unroll
           for (int i = 0; i < kKeys; ++i) {
-            const bool v = i < 32 ? ((mlo >> i) & 1u) : ((mhi >> (i - 32)) & 1u);
-            sv[i] = v ? sv[i] * scale_log2 : -INFINITY;
-            mt = fmaxf(mt, sv[i]);
+            sv[i] = valid_at(i) ? fmaf(sv[i], scale_log2, nm) : -INFINITY;
+            xm = fmaxf(xm, sv[i]);
           }
-        }
-        float alpha = 1.f;
-        if (m_ref == -INFINITY) {
-          m_ref = mt;
-        } else if (mt > m_ref + kLazyLog2) {
-          alpha = ex2_approx(m_ref - mt);
-          m_ref = mt;
+          if (xm > kLazyLog2) {                      // rare: move the reference maximum
+            alpha = ex2_approx(-xm);
+            m_ref += xm;
+#pragma unroll
+            for (int i = 0; i < kKeys; ++i) sv[i] -= xm;
+          }
         }
         l_run *= alpha;
         float psum = 0.f;
         uint32_t pk[kKeys / 2];
 #pragma unroll
         for (int i = 0; i < kKeys; i += 2) {
-          const float p0 = m_ref == -INFINITY ? 0.f : ex2_approx(sv[i] - m_ref);
-          const float p1 = m_ref == -INFINITY ? 0.f : ex2_approx(sv[i + 1] - m_ref);
+          const float p0 = ex2_approx(sv[i]), p1 = ex2_approx(sv[i + 1]);
           psum += p0 + p1;
           pk[i / 2] = bf16x2_bits(p0, p1);
         }
