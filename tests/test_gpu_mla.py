@@ -100,3 +100,17 @@ def test_large_logits_trigger_rescale(gain):
     assert np.all(np.abs(og - ref_o) <= bound), float(np.max(np.abs(og - ref_o) / bound))
     assert np.linalg.norm(og - ref_o) / np.linalg.norm(ref_o) <= 5e-3
     assert np.allclose(lse.cpu().numpy(), ref_lse, atol=1e-3, rtol=1e-4)
+
+
+@pytest.mark.parametrize("k", [1, 47, 49, 96, 4096])
+def test_unusual_k(k):
+    """Top-k widths that do not fill whole 48-key tiles (1, 47, 49, 96) and the largest k the
+    pair kernel takes (4096, which sizes its per-query validity-mask buffer)."""
+    sh = Shard(W.WORKLOADS[1], 3)
+    rng = np.random.default_rng(k)
+    sel = np.flatnonzero(sh.pos > 7000)[:4]
+    topk = np.full((len(sel), k), -1, dtype=np.int64)
+    for i, t in enumerate(sel):
+        n_pick = min(k, int(sh.pos[t]) + 1)
+        topk[i, :n_pick] = np.sort(rng.choice(int(sh.pos[t]) + 1, n_pick, replace=False))
+    _check(sh, sel, topk)
