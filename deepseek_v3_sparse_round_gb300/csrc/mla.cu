@@ -746,47 +746,55 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
       // last softmax tile saw them) and both issuers acknowledged the previous Q.
       if (n > 0 && !warp_wait(bar(kQAck), (n - 1) & 1, 0x42, abort_flag)) break;
       {
-        // Coalesced: each warp-wide load covers 4 rows x 128 B of the warp's 32 Q rows; the
-        // rows are transposed through the warp's swizzled staging tile so that lane i ends up
-        // holding row i (its TMEM lane), one 64-dim atom (32 TMEM columns) at a time.
+        // Coalesced: each warp-wide cp.async covers 4 rows x 128 B of the warp's 32 Q rows; the
+        // rows are transposed through swizzled 4 KB staging tiles so that lane i ends up holding
+        // row i (its TMEM lane), one 64-dim atom (32 TMEM columns) at a time, three atoms in
+        // flight. The tiles are the warp's slice of the Q staging region and of the two P
+        // staging buffers, which stay idle between the last P shipment of the previous query
+        // and this query's first softmax tile: wait until the courier has shipped them.
+        if (g0 >= 1 && !warp_wait(bar(kPSEmpty + static_cast<int>((g0 - 1) & 1)),
+                                  static_cast<uint32_t>(((g0 - 1) >> 1) & 1), 0x44, abort_flag)) break;
+        if (g0 >= 2 && !warp_wait(bar(kPSEmpty + static_cast<int>((g0 - 2) & 1)),
+                                  static_cast<uint32_t>(((g0 - 2) >> 1) & 1), 0x45, abort_flag)) break;
         const char* qw = reinterpret_cast<const char*>(q + (t * kH + warp * 32) * kDQK);
-        uint8_t* xw = smem + kOffX + warp * (32 * 128);
+        const uint32_t xoff[3] = {static_cast<uint32_t>(kOffX + warp * (32 * 128)),
+                                  static_cast<uint32_t>(kOffPS + warp * (32 * 128)),
+                                  static_cast<uint32_t>(kOffPS + kPSStride + warp * (32 * 128))};
         const int lrow = static_cast<int>(lane >> 3), lchunk = static_cast<int>(lane & 7);
         constexpr int kQAtoms = kDQK / 64;           // 9
-        uint4 qa[8], qb[8];
-        auto ldg_atom = [&](int a, uint4 (&v)[8]) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            v[i] = __ldg(reinterpret_cast<const uint4*>(qw + (4 * i + lrow) * (kDQK * 2) + a * 128 +
-                                                        lchunk * 16));
-        };
-        auto put_atom = [&](int a, const uint4 (&v)[8]) {
+        auto issue_atom = [&](int a) {
+          const uint32_t x = sbase + xoff[a % 3];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int row = 4 * i + lrow;
-            *reinterpret_cast<uint4*>(xw + row * 128 + ((lchunk ^ (row & 7)) * 16)) = v[i];
+            cp_async16(x + row * 128 + ((lchunk ^ (row & 7)) * 16),
+                       qw + row * (kDQK * 2) + a * 128 + lchunk * 16, 16u);
           }
-          __syncwarp();
-          uint32_t r[32];
-#pragma unroll
-          for (int cc = 0; cc < 8; ++cc) {
-            const uint4 u = *reinterpret_cast<const uint4*>(xw + lane * 128 + ((cc ^ (lane & 7)) * 16));
-            r[4 * cc] = u.x; r[4 * cc + 1] = u.y; r[4 * cc + 2] = u.z; r[4 * cc + 3] = u.w;
-          }
-          __syncwarp();                              // the tile is rewritten by the next atom
-          tmem_st16(tmem + lane_base + kColQ + a * 32, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
-          tmem_st16(tmem + lane_base + kColQ + a * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
+          cp_async_commit();
         };
-        ldg_atom(0, qa);
+        issue_atom(0);
+        issue_atom(1);
+        issue_atom(2);
 #pragma unroll
         for (int a = 0; a < kQAtoms; ++a) {
-          if ((a & 1) == 0) {
-            if (a + 1 < kQAtoms) ldg_atom(a + 1, qb);
-            put_atom(a, qa);
-          } else {
-            if (a + 1 < kQAtoms) ldg_atom(a + 1, qa);
-            put_atom(a, qb);
+          if (a + 2 < kQAtoms) cp_async_wait_group<2>();
+          else if (a + 1 < kQAtoms) cp_async_wait_group<1>();
+          else cp_async_wait_group<0>();
+          __syncwarp();                              // every lane's copies of atom a landed
+          const uint8_t* xr = smem + xoff[a % 3] + lane * 128;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {     // 16 TMEM columns (32 dims) at a time
+            uint32_t r[16];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const int cc = 4 * half + q4;
+              const uint4 u = *reinterpret_cast<const uint4*>(xr + ((cc ^ (lane & 7)) * 16));
+              r[4 * q4] = u.x; r[4 * q4 + 1] = u.y; r[4 * q4 + 2] = u.z; r[4 * q4 + 3] = u.w;
+            }
+            tmem_st16(tmem + lane_base + kColQ + a * 32 + half * 16, r);
           }
+          __syncwarp();                              // the tile is refilled with atom a + 3
+          if (a + 3 < kQAtoms) issue_atom(a + 3);
         }
         tmem_wait_st();
         tc_fence_before();
