@@ -405,13 +405,14 @@ constexpr int kOffCorrJ = kOffAbort + 4;
 constexpr int kSmem = kOffCorrJ + 4;
 constexpr int kColQ = 0, kQCols = kDQK / 2;     // CTA 0 TMEM: Q, then two 64-column S tiles
 constexpr int kColS = 288, kSStride = 64;       // S tile of slot s at kColS + 64 s
-constexpr int kThreads = 32 * (2 * kStages + 7);
+constexpr int kGatherPerSlot = 3;               // gather warps per ring slot
+constexpr int kThreads = 32 * (kGatherPerSlot * kStages + 7);
 // warp roles: 0-3 row warps (TMEM lane quadrants); 4 MMA issuer (CTA 0: QK, CTA 1: PV);
-// 5..4+kStages and 10..9+kStages row gather (warps 5 + s and 10 + s fill ring slot s
-// together); 8 the P courier (CTA 0); 9 the query metadata warp (both).
+// 5..4+kStages and 10.. row gather (warps 5 + s, 10 + s, 13 + s fill ring slot s together);
+// 8 the P courier (CTA 0); 9 the query metadata warp (both).
 constexpr int kMmaWarp = 4, kGatherWarp0 = 5, kCourierWarp = kGatherWarp0 + kStages,
               kMetaWarp = kCourierWarp + 1, kGatherWarp1 = kMetaWarp + 1;
-static_assert(kGatherWarp1 + kStages == kThreads / 32, "warp roles");
+static_assert(kGatherWarp1 + (kGatherPerSlot - 1) * kStages == kThreads / 32, "warp roles");
 constexpr float kLazyLog2 = 16.f;               // rescale O only when the max grows by > 2^16
 constexpr int kQBatch = 36;                     // 16-byte Q loads in flight per thread
 // barrier indices
@@ -459,7 +460,7 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
   const bool aligned = (sbase & 1023u) == 0;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(bar(kKvFull + i), 64);             // both gather warps of the slot
+      mbar_init(bar(kKvFull + i), 32 * kGatherPerSlot);   // every gather warp of the slot
       mbar_init(bar(kKvEmpty + i), 1);
     }
     for (int i = 0; i < kStages; ++i) {
@@ -472,7 +473,8 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
       mbar_init(bar(kPFull + i), 1);
       mbar_init(bar(kPEmpty + i), 1);
       mbar_init(bar(kMetaFull + i), 1);
-      mbar_init(bar(kMetaEmpty + i), crank == 0 ? 2 * kStages + 6 : 2 * kStages + 5);
+      mbar_init(bar(kMetaEmpty + i),
+                crank == 0 ? kGatherPerSlot * kStages + 6 : kGatherPerSlot * kStages + 5);
       mbar_init(bar(kLReady + i), 1);               // CTA 1: armed with 512 tx bytes per query
       mbar_init(bar(kLEmpty + i), 128);
     }
@@ -492,8 +494,8 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmem);
 
-  // meta_empty arrivals per query: CTA 0: 2 kStages gather + QK + courier + 4 softmax warps
-  // (at the end of the query: they read the masks until then); CTA 1: 2 kStages gather + PV +
+  // meta_empty arrivals per query: CTA 0: every gather warp + QK + courier + 4 softmax warps
+  // (at the end of the query: they read the masks until then); CTA 1: every gather warp + PV +
   // 4 row warps.
   auto meta_wait = [&](int n, bool warp_uniform) -> int {
     const uint32_t mb = bar(kMetaFull + (n & 1)), par = (n >> 1) & 1;
@@ -547,14 +549,16 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
       __syncwarp();
     }
   } else if ((warp >= kGatherWarp0 && warp < kGatherWarp0 + kStages) ||
-             (warp >= kGatherWarp1 && warp < kGatherWarp1 + kStages)) {
+             (warp >= kGatherWarp1 && warp < kGatherWarp1 + (kGatherPerSlot - 1) * kStages)) {
     // ---------------------------------------------------------------- row gather (both CTAs)
-    // Warps 5 + s and 10 + s fill ring slot s with the global tiles g = s (mod kStages), half
-    // of the rows each: 16-byte cp.async copies into the 128B-swizzled K-major layout (row r of
-    // atom a at a * kAtomBytes + r * 128, 16-byte chunk c at (c ^ (r % 8)) * 16); each waits
-    // for its own copies, fences them for the tensor core (async proxy) and arrives.
-    const int half = warp >= kGatherWarp1 ? 1 : 0;
-    const int s = static_cast<int>(warp) - (half ? kGatherWarp1 : kGatherWarp0);
+    // kGatherPerSlot warps fill ring slot s with the global tiles g = s (mod kStages), an equal
+    // share of the rows each: 16-byte cp.async copies into the 128B-swizzled K-major layout (row
+    // r of atom a at a * kAtomBytes + r * 128, 16-byte chunk c at (c ^ (r % 8)) * 16); each
+    // waits for its own copies, fences them for the tensor core (async proxy) and arrives.
+    const int gi = warp >= kGatherWarp1 ? static_cast<int>(warp) - kGatherWarp1 + kStages
+                                        : static_cast<int>(warp) - kGatherWarp0;
+    const int half = gi / kStages;                   // this warp's share of the slot's rows
+    const int s = gi % kStages;
     const int n_atoms = crank == 0 ? kAtomsS : kAtomsO;
     const uint32_t stage = sbase + s * (crank == 0 ? kStageS : kStageO);
     const int chunk = static_cast<int>(lane & 7);
@@ -587,8 +591,8 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
         const int32_t r0 = kv_row(kv, bb, s0, &bad);
         const int32_t r1 = kv_row(kv, bb, s1, &bad);
         fetch(j + kStages, s0, s1);
-#pragma unroll 3
-        for (int i = half; i < kKeys / 4; i += 2) {
+#pragma unroll
+        for (int i = half; i < kKeys / 4; i += kGatherPerSlot) {
           const int r = static_cast<int>(lane >> 3) + 4 * i;        // tile row of this lane
           const int32_t ra = __shfl_sync(0xffffffffu, r0, r & 31);
           const int32_t rb = __shfl_sync(0xffffffffu, r1, r & 31);
