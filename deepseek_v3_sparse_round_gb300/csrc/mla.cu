@@ -358,16 +358,18 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16*
 //     of 128 x 48 fp32 per ring slot, so QK(j+1) runs while the softmax of tile j runs. One
 //     warp-uniform QK issuer takes every tile in order, so it sees every phase of the barriers
 //     it waits on (an issuer skipping another issuer's tiles on a 3-slot ring could take a
-//     parity two phases ahead). Its softmax warps
-//     stage P (bf16), the per-row rescale factors and flags in one of two staging buffers; a
-//     courier warp ships each to CTA 1 with bulk DSMEM copies (one bulk copy moves a tile far
-//     faster than per-thread DSMEM stores). A ring slot is free as soon as its QK MMAs finish.
+//     parity two phases ahead). Its softmax warps stage P (bf16), the per-row rescale factors
+//     and flags in one of two staging buffers; a courier warp ships each to CTA 1 with bulk
+//     DSMEM copies (one bulk copy moves a tile far faster than per-thread DSMEM stores). A ring
+//     slot is free as soon as its QK MMAs finish.
 //   CTA 1 ("O side"): O (128 x 512 fp32) fills its TMEM; it accumulates O += P . V with two
-//     N = 256 MMAs per 16 keys and writes o = O / l at the end.
+//     N = 256 MMAs per 16 keys and writes o = O / l at the end (TMA stores).
 // Each CTA gathers the selected rows it needs into its own 3-slot ring of 48-key tiles (CTA 0:
-// all 576 columns, CTA 1: the 512 latent columns). The running maximum is lazy: O is rescaled only
-// when a row's maximum grows by more than 2^16 (rare; then CTA 1's four row warps rescale O
-// between two PV steps).
+// all 576 columns, CTA 1: the 512 latent columns), three gather warps per slot. At a query
+// boundary CTA 0 brings the next Q into TMEM through shared-memory staging tiles (the Q region
+// and the then idle P staging buffers). The running maximum is lazy: O is rescaled only when a
+// row's maximum grows by more than 2^16 (rare; then CTA 1's four row warps rescale O between
+// two PV steps).
 namespace pair {
 constexpr int kH = 128, kDQK = 576, kDV = 512;
 constexpr int kKeys = 48;                       // keys per tile
@@ -414,7 +416,6 @@ constexpr int kMmaWarp = 4, kGatherWarp0 = 5, kCourierWarp = kGatherWarp0 + kSta
               kMetaWarp = kCourierWarp + 1, kGatherWarp1 = kMetaWarp + 1;
 static_assert(kGatherWarp1 + (kGatherPerSlot - 1) * kStages == kThreads / 32, "warp roles");
 constexpr float kLazyLog2 = 16.f;               // rescale O only when the max grows by > 2^16
-constexpr int kQBatch = 36;                     // 16-byte Q loads in flight per thread
 // barrier indices
 constexpr int kKvFull = 0, kKvEmpty = kStages, kPStaged = 2 * kStages, kPSEmpty = kPStaged + 2,
               kSFull = kPStaged + 4, kSEmpty = kSFull + kStages, kPFull = kSEmpty + kStages,
