@@ -397,12 +397,16 @@ def _oracle_inputs(n_sample):
     return W, wl, sh, n_r
 
 
-def cpu_baseline(sample_queries=12, steps=1):
+def cpu_baseline(sample_queries=12, min_seconds=10.0, max_passes=6):
+    """Passes of the oracle over the sample until at least `min_seconds` of CPU work (bounded
+    by `max_passes`), so the figure rests on 10-30 s of work without stretching the bench."""
     W, wl, sh, n_r = _oracle_inputs(sample_queries)
     sel = np.arange(len(sh["pos"]))
+    steps = 0
     t0 = time.perf_counter()
-    for _ in range(steps):
+    while steps < max_passes and (steps == 0 or time.perf_counter() - t0 < min_seconds):
         _oracle_step(W, wl, sh, sel)
+        steps += 1
     dt = time.perf_counter() - t0
     cores = _blas_threads()
     return {"value": round(len(sel) * steps / dt, 4), "unit": "tokens/s", "cores": cores,
