@@ -457,6 +457,101 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
+def next_rows(args):
+    """Separate measurements of the two widened rows (not part of the step): the rerange fused
+    with the paged KV-cache write (HBM roofline, algorithmic bytes = 2 x rows x row bytes) and
+    the decode-step split (launch bound). One JSON line per case; `--next-rows large` runs only
+    the 1,048,576-row case (the one captured under ncu)."""
+    import torch
+    import __graft_entry__ as ge
+    ge.build()
+    import deepseek_v3_sparse_round_gb300 as dsa
+    import workloads as W
+    hbm = peaks()["hbm"]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def timeit(fn, reps, do_flush):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for i in range(reps):
+            if do_flush:
+                flush.fill_(i & 255)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return float(np.median(ts))
+
+    rng = np.random.default_rng(0)
+
+    def paged_case(lengths, sp, width, page=64):
+        cu = W.cu_seqlens(lengths)
+        n = int(cu[-1])
+        per = [(int(x) + page - 1) // page for x in lengths]
+        total = sum(per)
+        perm = rng.permutation(total + 8)[:total]          # pages scattered over the pool
+        table = np.full((len(lengths), max(per)), -1, np.int32)
+        k = 0
+        for b, m in enumerate(per):
+            table[b, :m] = perm[k:k + m]
+            k += m
+        gathered = torch.randn(n, width, device="cuda").to(torch.bfloat16)
+        pool = torch.zeros((total + 8) * page, width, dtype=torch.bfloat16, device="cuda")
+        dcu, dt = torch.as_tensor(cu, device="cuda"), torch.as_tensor(table, device="cuda")
+        out = torch.empty_like(gathered)
+        return (n, lambda: dsa.dsa_rr_rerange_paged(gathered, pool, n, sp, dcu, dt, 0, page),
+                lambda: dsa.dsa_rr_rerange(gathered, out, n, sp, 0), 2 * n * width * 2)
+
+    large = args.next_rows == "large"
+    cases = [] if large else [("varlen {8000,800,5,3000}, sp=8", W.WORKLOADS[1].lengths, 8),
+                              ("many_req (32 requests), sp=4", W.WORKLOADS[3].lengths, 4)]
+    cases.append(("64 requests x 16384 tokens, sp=8", (16384,) * 64, 8))
+    for name, lengths, sp in cases:
+        for width in ((576,) if large else (576, 128)):
+            n, f_paged, f_plain, nbytes = paged_case(lengths, sp, width)
+            for kind, fn in (("rerange_paged", f_paged), ("rerange", f_plain))[:1 if large else 2]:
+                ms = timeit(fn, 20, True)
+                gbs = nbytes / ms / 1e6
+                print(json.dumps({"kernel": kind, "workload": name, "row_bytes": width * 2,
+                                  "rows": n, "us": round(ms * 1e3, 1), "GB/s": round(gbs),
+                                  "frac_of_measured_hbm": round(gbs / hbm, 3),
+                                  "l2": "flushed between launches"}), flush=True)
+            torch.cuda.empty_cache()
+    if not large:
+        wl = W.WORKLOADS[4]
+        q = wl.decode_queries
+        ctx = np.asarray(wl.lengths, dtype=np.int64)
+        cu_new = torch.as_tensor((np.arange(len(ctx) + 1) * q).astype(np.int32), device="cuda")
+        base = torch.as_tensor((ctx - q).astype(np.int32), device="cuda")
+        n = int(len(ctx) * q)
+        for sp in (1, 8):
+            n_r = dsa.dsa_rr_shard_len(n, sp, 0)
+            e = lambda m: torch.empty(m, dtype=torch.int32, device="cuda")
+            cs, p, b, g = e(len(ctx) + 1), e(n_r), e(n_r), e(n_r)
+            src = torch.randn(n, 576, device="cuda").to(torch.bfloat16)
+            dst = torch.empty(n_r, 576, dtype=torch.bfloat16, device="cuda")
+            f = lambda: dsa.dsa_rr_split_decode_metadata(cu_new, base, n, sp, 0, cs, p, b, g, src, dst)
+            eager = timeit(f, 100, False)
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                f()
+            torch.cuda.current_stream().wait_stream(side)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                f()
+            replay = timeit(graph.replay, 100, False)
+            print(json.dumps({"kernel": "split_decode (metadata + row gather)",
+                              "workload": f"decode batch: {len(ctx)} requests x {q} new tokens, sp={sp}",
+                              "rows_gathered": n_r, "us_eager": round(eager * 1e3, 2),
+                              "us_graph_replay": round(replay * 1e3, 2)}), flush=True)
+    print(json.dumps({"device_errors": dsa.dsa_read_device_errors()}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -466,7 +561,12 @@ def main():
     ap.add_argument("--cpu-sample", type=int, default=96, help="queries per reference-arm step")
     ap.add_argument("--cpu-baseline-queries", type=int, default=1476)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--next-rows", nargs="?", const="all", default=None,
+                    help="measure the widened rows (paged rerange, decode split) and exit")
     args = ap.parse_args()
+    if args.next_rows:
+        next_rows(args)
+        return
     if args.warmup < 3 and args.impl == "native":
         args.warmup = 3
     if args.impl == "reference":

@@ -167,18 +167,8 @@ struct PagedPool {
   int64_t pool_rows;
 };
 
-__device__ __forceinline__ int64_t paged_row(const int32_t* cuv, int n_req, const PagedPool& pp,
-                                             int64_t g) {
-  const int b = find_request(cuv, n_req, g);
-  const int64_t s = g - cuv[b];
-  const int64_t pi = s / pp.page_size;
-  const int page = pi < pp.max_pages ? __ldg(pp.table + static_cast<int64_t>(b) * pp.max_pages + pi) : -1;
-  const int64_t r = page < 0 ? -1 : static_cast<int64_t>(page) * pp.page_size + (s - pi * pp.page_size);
-  return (r >= 0 && r < pp.pool_rows) ? r : -1;
-}
-
 template <typename Idx, int kBytes>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)   // 4 CTAs per SM: enough loads in flight
 rerange_paged_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ pool, Idx total,
                      Idx cpr, RerangeRows map, const int32_t* __restrict__ cu, int n_req,
                      PagedPool pp) {
@@ -190,28 +180,57 @@ rerange_paged_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ pool
     __syncthreads();
   }
   const int32_t* cuv = staged ? s_cu : cu;
+  // largest power of two <= n_req - 1: the first step of the request search below
+  int step0 = 0;
+  if (n_req > 1) {
+    step0 = 1;
+    while (2 * step0 <= n_req - 1) step0 <<= 1;
+  }
   const V* vs = reinterpret_cast<const V*>(src);
   V* vp = reinterpret_cast<V*>(pool);
   const Idx stride = static_cast<Idx>(gridDim.x) * blockDim.x;
   bool bad = false;
   for (Idx i = static_cast<Idx>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += kUnroll * stride) {
+    // The source chunks do not depend on the page map: their loads go out first and are in
+    // flight while the destinations are worked out.
+    Idx g[kUnroll], c[kUnroll];
+    bool in[kUnroll];
     V v[kUnroll];
-    int64_t dst[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const Idx cc = i + u * stride;
-      dst[u] = -1;
-      if (cc < total) {
-        const Idx g = cc / cpr, c = cc - g * cpr;
-        const int64_t r = paged_row(cuv, n_req, pp, static_cast<int64_t>(g));
-        bad |= r < 0;
-        if (r >= 0) {
-          dst[u] = r * cpr + c;
-          if constexpr (kBytes == 16) v[u] = ld_stream(vs + map(g) * cpr + c);
-          else v[u] = vs[map(g) * cpr + c];
-        }
+      in[u] = cc < total;
+      const Idx ci = in[u] ? cc : 0;
+      g[u] = ci / cpr;
+      c[u] = ci - g[u] * cpr;
+      if constexpr (kBytes == 16) v[u] = ld_stream(vs + map(g[u]) * cpr + c[u]);
+      else v[u] = vs[map(g[u]) * cpr + c[u]];
+    }
+    // Request of each chunk: the largest b < n_req with cu[b] <= g, by a fixed sequence of
+    // halving steps (the same count for every thread), the kUnroll searches side by side.
+    int b[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) b[u] = 0;
+    for (int step = step0; step > 0; step >>= 1) {
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int t = b[u] + step;
+        if (t < n_req && static_cast<int64_t>(cuv[t]) <= static_cast<int64_t>(g[u])) b[u] = t;
       }
+    }
+    int64_t dst[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      // position in the request (cu is int32, so it fits 32 bits), its page and row
+      const int s = static_cast<int>(static_cast<int64_t>(g[u]) - cuv[b[u]]);
+      const int pi = s / pp.page_size;
+      const int page = (in[u] && pi < pp.max_pages)
+                           ? __ldg(pp.table + static_cast<int64_t>(b[u]) * pp.max_pages + pi)
+                           : -1;
+      const int64_t r = page < 0 ? -1 : static_cast<int64_t>(page) * pp.page_size + (s - pi * pp.page_size);
+      dst[u] = (r >= 0 && r < pp.pool_rows) ? r * static_cast<int64_t>(cpr) + c[u] : -1;
+      bad |= in[u] && dst[u] < 0;
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
