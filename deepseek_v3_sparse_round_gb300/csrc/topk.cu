@@ -8,6 +8,10 @@
 // index entries with key == T, in ascending index order, using block-wide prefix counts.
 // Rows up to kStashKeys entries are read from global memory once and kept in shared memory;
 // longer rows are re-read from global memory (L2) in every pass.
+// Shared-memory access: the histogram passes read the stash with consecutive lanes on
+// consecutive words (order does not matter for a histogram); the ordered pass gives each thread
+// one contiguous, odd-length segment of the row, so a single block-wide scan orders the output
+// and the lanes' reads still fall in distinct banks.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -22,6 +26,7 @@ constexpr int kPerThread = 8;                       // consecutive entries per t
 constexpr int kChunk = kThreads * kPerThread;       // 4096 entries
 constexpr int kBins = 2048;                         // 11-bit digits
 constexpr int kStashKeys = 40960;                   // 160 KB of keys in shared memory
+constexpr int kShortRow = 16384;                    // rows up to this length: kIn = 2
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -63,10 +68,19 @@ __device__ __forceinline__ void load_keys(const float* __restrict__ row, const u
                                           bool (&valid)[kPerThread]) {
   const int i0 = base + threadIdx.x * kPerThread;
   if (kStash) {
+    if (i0 + kPerThread <= L) {                     // two 16-byte reads (i0 is a multiple of 8)
+      const uint4 a = *reinterpret_cast<const uint4*>(stash + i0);
+      const uint4 b = *reinterpret_cast<const uint4*>(stash + i0 + 4);
+      key[0] = a.x; key[1] = a.y; key[2] = a.z; key[3] = a.w;
+      key[4] = b.x; key[5] = b.y; key[6] = b.z; key[7] = b.w;
 #pragma unroll
-    for (int j = 0; j < kPerThread; ++j) {
-      valid[j] = i0 + j < L;
-      key[j] = valid[j] ? stash[i0 + j] : 0u;
+      for (int j = 0; j < kPerThread; ++j) valid[j] = true;
+    } else {
+#pragma unroll
+      for (int j = 0; j < kPerThread; ++j) {
+        valid[j] = i0 + j < L;
+        key[j] = valid[j] ? stash[i0 + j] : 0u;
+      }
     }
   } else {
     if (i0 + kPerThread <= L) {
@@ -85,8 +99,31 @@ __device__ __forceinline__ void load_keys(const float* __restrict__ row, const u
   }
 }
 
+// The histogram passes do not depend on which thread sees which entry: from the stash they read
+// entry base + j * kThreads + threadIdx.x, so the 32 lanes of a warp read 32 consecutive words
+// (no bank conflicts); from global memory they use the blocked layout (16-byte loads).
 template <bool kStash>
-__global__ void __launch_bounds__(kThreads)
+__device__ __forceinline__ void load_keys_any_order(const float* __restrict__ row,
+                                                    const uint32_t* stash, int L, int base,
+                                                    uint32_t (&key)[kPerThread],
+                                                    bool (&valid)[kPerThread]) {
+  if (kStash) {
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) {
+      const int i = base + j * kThreads + static_cast<int>(threadIdx.x);
+      valid[j] = i < L;
+      key[j] = valid[j] ? stash[i] : 0u;
+    }
+  } else {
+    load_keys<false>(row, stash, L, base, key, valid);
+  }
+}
+
+// kIn: 16-byte loads in flight per thread while the stash fills. Short rows (several CTAs per SM)
+// take 2 and keep the registers for three CTAs per SM; long rows (one CTA per SM: the stash
+// takes most of shared memory) take 4.
+template <bool kStash, int kIn>
+__global__ void __launch_bounds__(kThreads, kIn <= 2 ? 3 : 1)
 topk_kernel(const float* __restrict__ scores, int64_t stride, const int32_t* __restrict__ pos,
             int k, int max_ctx, int32_t* __restrict__ topk) {
   extern __shared__ __align__(16) uint32_t stash[];
@@ -109,13 +146,23 @@ topk_kernel(const float* __restrict__ scores, int64_t stride, const int32_t* __r
   const float* row = scores + t * stride;
 
   if (kStash) {                                     // keys of the whole row into shared memory
-    for (int i = threadIdx.x * 4; i < L; i += kThreads * 4) {
-      if (i + 4 <= L) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(row + i));
-        *reinterpret_cast<uint4*>(stash + i) =
-            make_uint4(order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w));
-      } else {
-        for (int j = i; j < L; ++j) stash[j] = order_key(__ldcg(row + j));
+    // four 16-byte loads in flight per thread, then their stores
+    for (int i0 = threadIdx.x * 4; i0 < L; i0 += kThreads * 4 * kIn) {
+      float4 v[kIn];
+#pragma unroll
+      for (int u = 0; u < kIn; ++u) {
+        const int i = i0 + u * kThreads * 4;
+        if (i + 4 <= L) v[u] = __ldcg(reinterpret_cast<const float4*>(row + i));
+      }
+#pragma unroll
+      for (int u = 0; u < kIn; ++u) {
+        const int i = i0 + u * kThreads * 4;
+        if (i + 4 <= L) {
+          *reinterpret_cast<uint4*>(stash + i) =
+              make_uint4(order_key(v[u].x), order_key(v[u].y), order_key(v[u].z), order_key(v[u].w));
+        } else {
+          for (int j = i; j < L; ++j) stash[j] = order_key(__ldcg(row + j));
+        }
       }
     }
   }
@@ -131,7 +178,7 @@ topk_kernel(const float* __restrict__ scores, int64_t stride, const int32_t* __r
     for (int base = 0; base < L; base += kChunk) {
       uint32_t key[kPerThread];
       bool valid[kPerThread];
-      load_keys<kStash>(row, stash, L, base, key, valid);
+      load_keys_any_order<kStash>(row, stash, L, base, key, valid);
 #pragma unroll
       for (int j = 0; j < kPerThread; ++j)
         if (valid[j] && (key[j] & prefix_mask) == prefix) atomicAdd(&hist[(key[j] >> sh) & dm], 1u);
@@ -164,6 +211,33 @@ topk_kernel(const float* __restrict__ scores, int64_t stride, const int32_t* __r
   const uint32_t n_gt = static_cast<uint32_t>(k) - remaining;
 
   // ---- ordered emission ----
+  if (kStash) {
+    // One contiguous segment of the row per thread (odd length, so the lanes' reads fall in
+    // distinct banks), one block-wide scan of the per-thread counts, then every thread writes
+    // its selected indices in order.
+    const int seg = ((L + kThreads - 1) / kThreads) | 1;
+    const int lo = min(static_cast<int>(threadIdx.x) * seg, L), hi = min(lo + seg, L);
+    uint32_t n_g = 0, n_e = 0;
+    for (int i = lo; i < hi; ++i) {
+      const uint32_t key = stash[i];
+      n_g += key > T;
+      n_e += key == T;
+    }
+    uint32_t tot;                                   // counts < 2^16: L <= kStashKeys
+    const uint32_t before = block_exclusive_scan((n_g << 16) | n_e, warp_tot, &tot);
+    uint32_t g_before = before >> 16, e_before = before & 0xFFFFu;
+    for (int i = lo; i < hi; ++i) {
+      const uint32_t key = stash[i];
+      if (key > T) {
+        out[g_before + (e_before < need_eq ? e_before : need_eq)] = i;
+        ++g_before;
+      } else if (key == T) {
+        if (e_before < need_eq) out[g_before + e_before] = i;
+        ++e_before;
+      }
+    }
+    return;
+  }
   uint32_t gt_done = 0, eq_done = 0;
   for (int base = 0; base < L && (gt_done < n_gt || eq_done < need_eq); base += kChunk) {
     uint32_t key[kPerThread];
@@ -210,13 +284,20 @@ int topk_select(const float* scores, int64_t score_stride, const int32_t* pos, i
   if (n_q > INT32_MAX) return fail(DSA_ERR_UNSUPPORTED, "topk: n_q too large");
   if (max_ctx <= kStashKeys) {
     const size_t smem = static_cast<size_t>(((max_ctx + 3) / 4) * 4) * sizeof(uint32_t);
-    DSA_CHECK_CUDA(cudaFuncSetAttribute(topk_kernel<true>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kStashKeys * static_cast<int>(sizeof(uint32_t))));
-    topk_kernel<true><<<static_cast<unsigned>(n_q), kThreads, smem, stream>>>(
-        scores, score_stride, pos, k, max_ctx, topk);
+    const int max_smem = kStashKeys * static_cast<int>(sizeof(uint32_t));
+    if (max_ctx <= kShortRow) {
+      DSA_CHECK_CUDA(cudaFuncSetAttribute(topk_kernel<true, 2>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem));
+      topk_kernel<true, 2><<<static_cast<unsigned>(n_q), kThreads, smem, stream>>>(
+          scores, score_stride, pos, k, max_ctx, topk);
+    } else {
+      DSA_CHECK_CUDA(cudaFuncSetAttribute(topk_kernel<true, 4>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem));
+      topk_kernel<true, 4><<<static_cast<unsigned>(n_q), kThreads, smem, stream>>>(
+          scores, score_stride, pos, k, max_ctx, topk);
+    }
   } else {
-    topk_kernel<false><<<static_cast<unsigned>(n_q), kThreads, 0, stream>>>(
+    topk_kernel<false, 2><<<static_cast<unsigned>(n_q), kThreads, 0, stream>>>(
         scores, score_stride, pos, k, max_ctx, topk);
   }
   DSA_CHECK_CUDA(cudaGetLastError());

@@ -41,6 +41,19 @@ def test_long_rows_shared_and_global_paths(L):
         assert np.array_equal(got[i], topk_indices(r, 2048))
 
 
+@pytest.mark.parametrize("L", [16383, 16384, 16385, 20003])
+def test_rows_around_the_short_and_long_row_kernels(L):
+    """Row lengths on both sides of the switch between the short-row and long-row kernels, with
+    ragged tails (L not a multiple of 4 or of the 512-thread segment count) and heavy ties."""
+    rng = np.random.default_rng(L)
+    rows = [rng.integers(-20, 21, L).astype(np.float32), rng.normal(size=L).astype(np.float32),
+            np.full(L, -1.25, np.float32), rng.normal(size=L - 2049).astype(np.float32)]
+    for k in (2048, 1):
+        got = _run(rows, k)
+        for i, r in enumerate(rows):
+            assert np.array_equal(got[i], topk_indices(r, k)), (L, i, k)
+
+
 def test_signed_zero_and_constant_rows():
     z = np.array([-0.0, 0.0] * 50, dtype=np.float32)
     neg = -np.abs(np.random.default_rng(1).normal(size=300)).astype(np.float32)
