@@ -380,9 +380,13 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (!warp_wait(bar(kAccFull + h), acc_uses & 1u, 0x06, abort_flag)) { ok = false; break; }
         ++acc_uses;
         tc_fence_after();
-        float acc[S::kQPA];
+        // Four partial sums per query (heads h with h % 4 == 0, 1, 2, 3): chains of HI / 4
+        // dependent FMAs instead of HI, added at the end.
+        float accp[S::kQPA][4];
 #pragma unroll
-        for (int q = 0; q < S::kQPA; ++q) acc[q] = 0.f;
+        for (int q = 0; q < S::kQPA; ++q)
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) accp[q][k4] = 0.f;
         // 64 columns per TMEM round trip; w read four columns at a time (broadcast LDS.128)
         static_assert((S::kQPA * HI) % 64 == 0, "epilogue chunks");
 #pragma unroll
@@ -395,12 +399,15 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           for (int j = 0; j < 64; j += 4) {
             const int col = c0 + j, q = col / HI;
             const float4 w4 = *reinterpret_cast<const float4*>(sw + col);
-            acc[q] = fmaf(w4.x, fmaxf(__uint_as_float(v[j]), 0.f), acc[q]);
-            acc[q] = fmaf(w4.y, fmaxf(__uint_as_float(v[j + 1]), 0.f), acc[q]);
-            acc[q] = fmaf(w4.z, fmaxf(__uint_as_float(v[j + 2]), 0.f), acc[q]);
-            acc[q] = fmaf(w4.w, fmaxf(__uint_as_float(v[j + 3]), 0.f), acc[q]);
+            accp[q][0] = fmaf(w4.x, fmaxf(__uint_as_float(v[j]), 0.f), accp[q][0]);
+            accp[q][1] = fmaf(w4.y, fmaxf(__uint_as_float(v[j + 1]), 0.f), accp[q][1]);
+            accp[q][2] = fmaf(w4.z, fmaxf(__uint_as_float(v[j + 2]), 0.f), accp[q][2]);
+            accp[q][3] = fmaf(w4.w, fmaxf(__uint_as_float(v[j + 3]), 0.f), accp[q][3]);
           }
         }
+        float acc[S::kQPA];
+#pragma unroll
+        for (int q = 0; q < S::kQPA; ++q) acc[q] = (accp[q][0] + accp[q][1]) + (accp[q][2] + accp[q][3]);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kAccEmpty + h));
