@@ -380,13 +380,15 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (!warp_wait(bar(kAccFull + h), acc_uses & 1u, 0x06, abort_flag)) { ok = false; break; }
         ++acc_uses;
         tc_fence_after();
-        // Four partial sums per query (heads h with h % 4 == 0, 1, 2, 3): chains of HI / 4
-        // dependent FMAs instead of HI, added at the end.
-        float accp[S::kQPA][4];
+        // Four partial sums per query (heads h with h % 4 == 0, 1, 2, 3), held as two packed
+        // pairs so that one two-wide FMA serves two heads: chains of HI / 4 dependent FMAs
+        // instead of HI, added at the end.
+        float2 accp[S::kQPA][2];
 #pragma unroll
-        for (int q = 0; q < S::kQPA; ++q)
-#pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) accp[q][k4] = 0.f;
+        for (int q = 0; q < S::kQPA; ++q) {
+          accp[q][0] = make_float2(0.f, 0.f);
+          accp[q][1] = make_float2(0.f, 0.f);
+        }
         // 64 columns per TMEM round trip; w read four columns at a time (broadcast LDS.128)
         static_assert((S::kQPA * HI) % 64 == 0, "epilogue chunks");
 #pragma unroll
@@ -399,15 +401,18 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           for (int j = 0; j < 64; j += 4) {
             const int col = c0 + j, q = col / HI;
             const float4 w4 = *reinterpret_cast<const float4*>(sw + col);
-            accp[q][0] = fmaf(w4.x, fmaxf(__uint_as_float(v[j]), 0.f), accp[q][0]);
-            accp[q][1] = fmaf(w4.y, fmaxf(__uint_as_float(v[j + 1]), 0.f), accp[q][1]);
-            accp[q][2] = fmaf(w4.z, fmaxf(__uint_as_float(v[j + 2]), 0.f), accp[q][2]);
-            accp[q][3] = fmaf(w4.w, fmaxf(__uint_as_float(v[j + 3]), 0.f), accp[q][3]);
+            const float2 r01 = make_float2(fmaxf(__uint_as_float(v[j]), 0.f),
+                                           fmaxf(__uint_as_float(v[j + 1]), 0.f));
+            const float2 r23 = make_float2(fmaxf(__uint_as_float(v[j + 2]), 0.f),
+                                           fmaxf(__uint_as_float(v[j + 3]), 0.f));
+            accp[q][0] = __ffma2_rn(make_float2(w4.x, w4.y), r01, accp[q][0]);
+            accp[q][1] = __ffma2_rn(make_float2(w4.z, w4.w), r23, accp[q][1]);
           }
         }
         float acc[S::kQPA];
 #pragma unroll
-        for (int q = 0; q < S::kQPA; ++q) acc[q] = (accp[q][0] + accp[q][1]) + (accp[q][2] + accp[q][3]);
+        for (int q = 0; q < S::kQPA; ++q)
+          acc[q] = (accp[q][0].x + accp[q][0].y) + (accp[q][1].x + accp[q][1].y);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kAccEmpty + h));
