@@ -18,9 +18,11 @@
 //  * Warp roles: warps 0-3 and 4-7 are the epilogues of accumulators 0 and 1 (TMEM lane
 //    quadrant = warp % 4), warp 8 issues TMA, warp 9 issues tcgen05.mma.
 //  * Persistent grid (one CTA per SM). A one-CTA planning kernel cuts the queries into groups
-//    (never across a request, at most 8 queries) and each group's causal key range into
-//    chunks of whole 128-key tiles; CTA i takes chunks i, i + grid, ... Only tiles that hold
-//    some causal key are computed; keys past a query's position are masked in the epilogue.
+//    (never across a request, at most 8 queries) and counts each group's causal 128-key tiles;
+//    the groups' tiles, concatenated in order, are split into equal contiguous ranges, one per
+//    CTA (a range covers one or a few groups, so each CTA loads few Q blocks). Only tiles that
+//    hold some causal key are computed; keys past a query's position are masked in the
+//    epilogue.
 //  * Key rows: contiguous (cu[b] + s, the logical order after the rerange) or paged
 //    (block_table, 64-token pages, one TMA box per page).
 #include <cstdint>
@@ -39,8 +41,8 @@ constexpr int kKeysPerTile = 128;
 constexpr int kPageRows = 64;          // TMA box height for keys (also the page size)
 
 struct Plan {
-  int total_units;
-  int chunk_tiles;
+  int total_tiles;   // key tiles of all groups
+  int pad;
   int n_groups;
   int error;
 };
@@ -93,7 +95,7 @@ struct Shape {
 };
 
 // ------------------------------------------------------------------------------------------
-// Planning: groups of <= GQ consecutive queries of one request, chunks of whole key tiles.
+// Planning: groups of <= GQ consecutive queries of one request, and their key-tile counts.
 __device__ __forceinline__ uint32_t plan_scan(uint32_t v, uint32_t* wt, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   constexpr int kW = kPlanThreads / 32;
@@ -125,6 +127,7 @@ __global__ void __launch_bounds__(kPlanThreads)
 indexer_plan_kernel(const int32_t* __restrict__ pos, const int32_t* __restrict__ bid, int n_q,
                     int n_req, int max_ctx, int gq, int n_ctas, Plan* plan, int4* groups,
                     int32_t* unit_start, int32_t* t0_list) {
+  (void)n_ctas;
   __shared__ uint32_t wt[32];
   const int per = (n_q + kPlanThreads - 1) / kPlanThreads;
   const int lo = min(static_cast<int>(threadIdx.x) * per, n_q), hi = min(lo + per, n_q);
@@ -156,41 +159,30 @@ indexer_plan_kernel(const int32_t* __restrict__ pos, const int32_t* __restrict__
     tiles_sum += tiles;
   }
   if (bad) report_device_error(kErrBadIndex);
+  // Tile prefix per group: the indexer hands each CTA an equal, contiguous range of the
+  // concatenated tile sequence (all groups, in order).
   uint32_t total_tiles;
-  plan_scan(tiles_sum, wt, &total_tiles);
-  // Chunk size: about six chunks per CTA, between 1 and 64 tiles.
-  int chunk = static_cast<int>((total_tiles + static_cast<uint32_t>(n_ctas) * 6 - 1) /
-                               (static_cast<uint32_t>(n_ctas) * 6));
-  chunk = max(1, min(chunk, 64));
-  uint32_t units = 0;
+  uint32_t ts = plan_scan(tiles_sum, wt, &total_tiles);
   for (int gi = glo; gi < ghi; ++gi) {
+    unit_start[gi] = static_cast<int32_t>(ts);
     const int pmax = groups[gi].w;
-    const int tiles = pmax >= 0 ? pmax / kKeysPerTile + 1 : 0;
-    units += (tiles + chunk - 1) / chunk;
-  }
-  uint32_t total_units;
-  uint32_t u = plan_scan(units, wt, &total_units);
-  for (int gi = glo; gi < ghi; ++gi) {
-    unit_start[gi] = static_cast<int32_t>(u);
-    const int pmax = groups[gi].w;
-    const int tiles = pmax >= 0 ? pmax / kKeysPerTile + 1 : 0;
-    u += (tiles + chunk - 1) / chunk;
+    ts += pmax >= 0 ? static_cast<uint32_t>(pmax / kKeysPerTile + 1) : 0u;
   }
   if (threadIdx.x == 0) {
-    unit_start[G] = static_cast<int32_t>(total_units);
-    plan->total_units = static_cast<int>(total_units);
-    plan->chunk_tiles = chunk;
+    unit_start[G] = static_cast<int32_t>(total_tiles);
+    plan->total_tiles = static_cast<int>(total_tiles);
+    plan->pad = 0;
     plan->n_groups = G;
     plan->error = 0;
   }
 }
 
-// The unit's group: largest g with unit_start[g] <= u (unit_start non-decreasing, size G+1).
-__device__ __forceinline__ int find_group(const int32_t* __restrict__ unit_start, int G, int u) {
+// Largest g < G with tile_start[g] <= t (tile_start non-decreasing, size G + 1).
+__device__ __forceinline__ int find_group(const int32_t* __restrict__ tile_start, int G, int t) {
   int lo = 0, hi = G - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(unit_start + mid) <= u) lo = mid; else hi = mid - 1;
+    if (__ldg(tile_start + mid) <= t) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
@@ -199,18 +191,19 @@ struct Unit {
   int t0, count, b, pmax, tile_begin, tile_end;
 };
 
-__device__ __forceinline__ Unit load_unit(const Plan* plan, const int4* groups,
-                                          const int32_t* unit_start, int u) {
-  const int G = plan->n_groups, chunk = plan->chunk_tiles;
-  const int g = find_group(unit_start, G, u);
+// Next piece of this CTA's tile range [cur, t_hi): the part that falls in one group (a unit:
+// that group's queries against a run of its key tiles). Every role walks the same sequence.
+__device__ __forceinline__ bool next_unit(const int4* groups, const int32_t* tile_start, int G,
+                                          int& g, int& cur, int t_hi, Unit& x) {
+  if (cur >= t_hi) return false;
+  while (g < G - 1 && __ldg(tile_start + g + 1) <= cur) ++g;   // also skips empty groups
   const int4 rec = __ldg(groups + g);
-  const int c = u - __ldg(unit_start + g);
-  const int tiles = rec.w / kKeysPerTile + 1;
-  Unit x;
+  const int base = __ldg(tile_start + g);
   x.t0 = rec.x; x.count = rec.y; x.b = rec.z; x.pmax = rec.w;
-  x.tile_begin = c * chunk;
-  x.tile_end = min(tiles, x.tile_begin + chunk);
-  return x;
+  x.tile_begin = cur - base;
+  x.tile_end = min(t_hi, __ldg(tile_start + g + 1)) - base;
+  cur = base + x.tile_end;
+  return true;
 }
 
 struct KeyRows {
@@ -270,7 +263,11 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + S::kOffTmem);
-  const int total_units = plan->total_units;
+  // This CTA's share of the concatenated tile sequence: an equal contiguous range.
+  const int n_tiles = plan->total_tiles, n_groups = plan->n_groups;
+  const int t_lo = static_cast<int>(static_cast<int64_t>(n_tiles) * blockIdx.x / gridDim.x);
+  const int t_hi = static_cast<int>(static_cast<int64_t>(n_tiles) * (blockIdx.x + 1) / gridDim.x);
+  const int g_lo = t_lo < t_hi ? find_group(unit_start, n_groups, t_lo) : 0;
 
   if (warp == 8) {
     // ------------------------------------------------------------------ TMA producer
@@ -279,8 +276,9 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       tma_prefetch_desc(&tm_q);
       int stage = 0;
       uint32_t phase = 0, b_uses = 0;
-      for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-        const Unit un = load_unit(plan, groups, unit_start, u);
+      int ug = g_lo, ucur = t_lo;
+      Unit un;
+      while (next_unit(groups, unit_start, n_groups, ug, ucur, t_hi, un)) {
         if (!mbar_wait(bar(kBEmpty), (b_uses & 1u) ^ 1u, 0x01, abort_flag)) break;
         ++b_uses;
         mbar_expect_tx(bar(kBFull), S::kBBytes);
@@ -309,8 +307,9 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0, b_uses = 0, acc_uses[2] = {0u, 0u};
-      for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
-        const Unit un = load_unit(plan, groups, unit_start, u);
+      int ug = g_lo, ucur = t_lo;
+      Unit un;
+      while (!*abort_flag && next_unit(groups, unit_start, n_groups, ug, ucur, t_hi, un)) {
         if (!mbar_wait(bar(kBFull), b_uses & 1u, 0x03, abort_flag)) break;
         ++b_uses;
         tc_fence_after();
@@ -358,8 +357,9 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     float* sw = reinterpret_cast<float*>(smem + S::kOffW) + h * S::kQPA * HI;
     int* spos = reinterpret_cast<int*>(smem + S::kOffPos) + h * S::kQPA;
     uint32_t acc_uses = 0, w_uses = 0;
-    for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
-      const Unit un = load_unit(plan, groups, unit_start, u);
+    int ug = g_lo, ucur = t_lo;
+    Unit un;
+    while (!*abort_flag && next_unit(groups, unit_start, n_groups, ug, ucur, t_hi, un)) {
       const int nq = max(0, min(un.count - h * S::kQPA, S::kQPA));
       if (nq == 0) continue;
       const int tq0 = un.t0 + h * S::kQPA;
