@@ -9,9 +9,10 @@ The other shards' rows are inputs (one GPU, no collective). With --gpus N (torch
 takes shard (3 + i) % 8 of the same batch: independent problems, weak scaling.
 
 value = shard queries processed / device time of the timed steps (CUDA events on the launch
-stream, L2 flushed between steps); e2e = the same through host buffers (pinned H2D of the
-step's inputs + D2H of o inside the timed region). --impl reference times the fp64 CPU oracle
-on a bounded sample of the same workload.
+stream, L2 flushed between steps); e2e = the same through host buffers: every step copies its
+inputs from pinned host memory and reads o back, inside the timed region, pipelined over two
+buffer sets and three streams (upload of step i + 1 and download of step i - 1 overlap step i).
+--impl reference times the fp64 CPU oracle on a bounded sample of the same workload.
 """
 from __future__ import annotations
 
@@ -189,10 +190,13 @@ class ShardStep:
         self.o = e(self.n_r, wl.H, wl.dv, dt=torch.bfloat16)
         self.lse = e(self.n_r, wl.H, dt=torch.float32)
         self.launches_per_step = 8   # split meta + gather, 2 reranges, plan + indexer + top-k, MLA
-        self.h_o = torch.empty(self.o.shape, dtype=torch.bfloat16).pin_memory()
+        self.h_o = [torch.empty(self.o.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        # second input / output set for the end-to-end pipeline (step i + 1 uploads while step i runs)
+        self.d_sets = [self.d, {k: torch.empty_like(v) for k, v in self.d.items()}]
+        self.o_sets = [self.o, torch.empty_like(self.o)]
 
-    def run(self, ev=None):
-        dsa, wl, d = self.dsa, self.wl, self.d
+    def run(self, ev=None, b=0):
+        dsa, wl, d = self.dsa, self.wl, self.d_sets[b]
         dsa.dsa_rr_split_metadata(d["cu"], self.N, wl.sp, self.rank, self.cu_shard, self.pos,
                                   self.bid, self.gidx, src_rows=d["c_log"], dst_rows=self.c_local)
         dsa.dsa_rr_rerange(d["k_gath"], self.k_idx, self.N, wl.sp, 0)
@@ -202,13 +206,13 @@ class ShardStep:
         if ev is not None:
             ev[0].record()
         dsa.dsa_sparse_mla(d["q"], self.c, d["cu"], self.n_req, self.bid, self.topk, wl.scale,
-                           self.o, self.lse)
+                           self.o_sets[b], self.lse)
         if ev is not None:
             ev[1].record()
 
-    def upload(self):
+    def upload(self, b=0):
         for k in ("cu", "q_idx", "w", "q", "k_gath", "c_gath", "c_log"):
-            self.d[k].copy_(self.h[k], non_blocking=True)
+            self.d_sets[b][k].copy_(self.h[k], non_blocking=True)
 
     def h2d_bytes(self):
         return sum(self.h[k].numel() * self.h[k].element_size()
@@ -306,18 +310,38 @@ def gpu_arm(args):
         dist.barrier()
     torch.cuda.synchronize()
 
-    # ---- end to end through host buffers: H2D inputs, step, D2H of o ----
-    e2e_steps = max(1, min(args.steps, 10))
+    # ---- end to end through host buffers: every step uploads its inputs from pinned host memory
+    # and reads o back. Pipelined over two input/output sets and three streams (upload, compute,
+    # download), so step i + 1's upload and step i - 1's download overlap step i.
+    e2e_steps = max(2, min(args.steps, 20))
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
+    s_in, s_run, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device), torch.cuda.Stream(device)
+    mk = lambda: torch.cuda.Event()
+    ev_in, ev_run, ev_out = ([mk() for _ in range(e2e_steps)] for _ in range(3))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        st.upload()
-        st.run()
-        st.h_o.copy_(st.o, non_blocking=True)
-    e1.record(stream)
+    e0.record(s_in)
+    s_run.wait_event(e0)
+    s_out.wait_event(e0)
+    for i in range(e2e_steps):
+        b = i % 2
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev_run[i - 2])       # step i - 2 is done reading input set b
+            st.upload(b)
+            ev_in[i].record(s_in)
+        with torch.cuda.stream(s_run):
+            s_run.wait_event(ev_in[i])
+            if i >= 2:
+                s_run.wait_event(ev_out[i - 2])      # o of step i - 2 has been read back
+            st.run(b=b)
+            ev_run[i].record(s_run)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_run[i])
+            st.h_o[b].copy_(st.o_sets[b], non_blocking=True)
+            ev_out[i].record(s_out)
+    e1.record(s_out)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, dist, device)
 
