@@ -189,7 +189,9 @@ class ShardStep:
         self.topk = e(self.n_r, wl.topk)
         self.o = e(self.n_r, wl.H, wl.dv, dt=torch.bfloat16)
         self.lse = e(self.n_r, wl.H, dt=torch.float32)
-        self.launches_per_step = 8   # split meta + gather, 2 reranges, plan + indexer + top-k, MLA
+        self.mla_ws = e(dsa.dsa_sparse_mla_workspace_size(self.n_r), dt=torch.uint8)
+        # split meta + gather, 2 reranges, plan + indexer + top-k, MLA schedule + MLA
+        self.launches_per_step = 9
         self.h_o = [torch.empty(self.o.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
         # second input / output set for the end-to-end pipeline (step i + 1 uploads while step i runs)
         self.d_sets = [self.d, {k: torch.empty_like(v) for k, v in self.d.items()}]
@@ -205,8 +207,9 @@ class ShardStep:
                              self.bid, wl.topk, self.max_ctx, self.topk, self.ws)
         if ev is not None:
             ev[0].record()
-        dsa.dsa_sparse_mla(d["q"], self.c, d["cu"], self.n_req, self.bid, self.topk, wl.scale,
-                           self.o_sets[b], self.lse)
+        dsa.dsa_sparse_mla_balanced(d["q"], self.c, d["cu"], self.n_req, self.bid, self.pos,
+                                    self.topk, wl.scale, self.o_sets[b], self.mla_ws,
+                                    lse=self.lse)
         if ev is not None:
             ev[1].record()
 

@@ -18,7 +18,8 @@ __all__ = [
     "DsaError", "dsa_version", "dsa_rr_shard_len", "dsa_rr_split_metadata", "dsa_rr_rerange",
     "dsa_rr_rerange_paged", "dsa_rr_split_decode_metadata",
     "dsa_indexer_topk_workspace_size", "dsa_score_row_stride", "dsa_indexer_scores",
-    "dsa_topk_select", "dsa_indexer_topk", "dsa_indexer_topk_noalloc", "dsa_sparse_mla", "dsa_read_device_errors",
+    "dsa_topk_select", "dsa_indexer_topk", "dsa_indexer_topk_noalloc", "dsa_sparse_mla",
+    "dsa_sparse_mla_workspace_size", "dsa_sparse_mla_balanced", "dsa_read_device_errors",
     "DEVERR_TIMEOUT", "DEVERR_BAD_INDEX", "DEVERR_BAD_LENGTH",
 ]
 
@@ -215,4 +216,28 @@ def dsa_sparse_mla(q, c, cu, n_req, bid, topk, scale, o, lse=None, block_table=N
     _check(_lib().dsa_sparse_mla(
         _ptr(q), _ptr(c), c.shape[0], _ptr(cu), n_req, _ptr(bid), _ptr(topk), n_q, H, dqk, dv,
         topk.shape[1], float(scale), _ptr(block_table), max_pages, page_size, _ptr(o), _ptr(lse),
+        _stream(stream)))
+
+
+def dsa_sparse_mla_workspace_size(n_q: int) -> int:
+    return int(_lib().dsa_sparse_mla_workspace_size(n_q))
+
+
+def dsa_sparse_mla_balanced(q, c, cu, n_req, bid, pos, topk, scale, o, workspace, lse=None,
+                            block_table=None, page_size=64, stream=None):
+    """dsa_sparse_mla with the persistent pairs' work ordered by min(pos + 1, k) (same result)."""
+    _dev(q, torch.bfloat16, "q"); _dev(c, torch.bfloat16, "c"); _dev(o, torch.bfloat16, "o")
+    _dev(bid, torch.int32, "bid"); _dev(pos, torch.int32, "pos"); _dev(topk, torch.int32, "topk")
+    _dev(cu, torch.int32, "cu"); _dev(lse, torch.float32, "lse")
+    _dev(block_table, torch.int32, "block_table")
+    if workspace is None:
+        raise ValueError("workspace is required (dsa_sparse_mla_workspace_size bytes)")
+    _dev(workspace, None, "workspace")
+    n_q, H, dqk = q.shape
+    dv = o.shape[2]
+    max_pages = block_table.shape[1] if block_table is not None else 0
+    _check(_lib().dsa_sparse_mla_balanced(
+        _ptr(q), _ptr(c), c.shape[0], _ptr(cu), n_req, _ptr(bid), _ptr(pos), _ptr(topk), n_q, H,
+        dqk, dv, topk.shape[1], float(scale), _ptr(block_table), max_pages, page_size, _ptr(o),
+        _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))

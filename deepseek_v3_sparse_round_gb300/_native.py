@@ -37,6 +37,10 @@ SIGNATURES = {
                                          c_vp]),
     "dsa_sparse_mla": (c_int, [c_vp, c_vp, c_i64, c_vp, c_int, c_vp, c_vp, c_i64, c_int, c_int,
                                c_int, c_int, c_f, c_vp, c_int, c_int, c_vp, c_vp, c_vp]),
+    "dsa_sparse_mla_workspace_size": (c_sz, [c_i64]),
+    "dsa_sparse_mla_balanced": (c_int, [c_vp, c_vp, c_i64, c_vp, c_int, c_vp, c_vp, c_vp, c_i64,
+                                        c_int, c_int, c_int, c_int, c_f, c_vp, c_int, c_int, c_vp,
+                                        c_vp, c_vp, c_sz, c_vp]),
 }
 
 _lib = None

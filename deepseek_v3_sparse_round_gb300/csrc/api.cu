@@ -27,7 +27,8 @@ int topk_select(const float* scores, int64_t score_stride, const int32_t* pos, i
 int sparse_mla(const void* q, const void* c, int64_t n_kv_rows, const int32_t* cu, int n_req,
                const int32_t* bid, const int32_t* topk, int64_t n_q, int H, int dqk, int dv, int k,
                float scale, const int32_t* block_table, int max_pages, int page_size, void* o,
-               float* lse, cudaStream_t stream);
+               float* lse, const int32_t* pos, void* ws, size_t ws_bytes, cudaStream_t stream);
+size_t sparse_mla_workspace_bytes(int64_t n_q);
 cudaError_t split_read_errors(uint32_t* flags);
 int rerange_paged(const void* gathered, void* pool, int64_t pool_rows, int64_t n_tokens, int sp,
                   int64_t rank_stride_rows, int64_t row_bytes, const int32_t* cu, int n_req,
@@ -193,8 +194,25 @@ DSA_EXPORT int dsa_sparse_mla(const void* q, const void* c, int64_t n_kv_rows, c
                    int k, float scale, const int32_t* block_table, int max_pages, int page_size,
                    void* o, float* lse, dsa_stream_t stream) {
   return dsa::sparse_mla(q, c, n_kv_rows, cu, n_req, bid, topk, n_q, H, dqk, dv, k, scale,
-                         block_table, max_pages, page_size, o, lse,
+                         block_table, max_pages, page_size, o, lse, nullptr, nullptr, 0,
                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+DSA_EXPORT size_t dsa_sparse_mla_workspace_size(int64_t n_q) {
+  return dsa::sparse_mla_workspace_bytes(n_q);
+}
+
+DSA_EXPORT int dsa_sparse_mla_balanced(const void* q, const void* c, int64_t n_kv_rows,
+                                       const int32_t* cu, int n_req, const int32_t* bid,
+                                       const int32_t* pos, const int32_t* topk, int64_t n_q, int H,
+                                       int dqk, int dv, int k, float scale,
+                                       const int32_t* block_table, int max_pages, int page_size,
+                                       void* o, float* lse, void* workspace,
+                                       size_t workspace_bytes, dsa_stream_t stream) {
+  if (pos == nullptr) return dsa::fail(DSA_ERR_INVALID, "mla: pos is required");
+  return dsa::sparse_mla(q, c, n_kv_rows, cu, n_req, bid, topk, n_q, H, dqk, dv, k, scale,
+                         block_table, max_pages, page_size, o, lse, pos, workspace,
+                         workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

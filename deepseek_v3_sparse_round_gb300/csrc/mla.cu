@@ -442,7 +442,8 @@ __global__ void __launch_bounds__(pair::kThreads, 1)
 sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
                        const __nv_bfloat16* __restrict__ c, const __nv_bfloat16* __restrict__ q,
                        const int32_t* __restrict__ bid, const int32_t* __restrict__ topk, int k,
-                       int64_t n_q, KvMap kv, float scale_log2, float* __restrict__ lse) {
+                       int64_t n_q, KvMap kv, float scale_log2, float* __restrict__ lse,
+                       const int32_t* __restrict__ order) {
   using namespace pair;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -451,7 +452,12 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
   const uint32_t peer = crank ^ 1u;
   const int64_t cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
   const int n_my = static_cast<int>((n_q - cluster + n_clusters - 1) / n_clusters);  // queries
-  auto query = [&](int n) { return cluster + static_cast<int64_t>(n) * n_clusters; };
+  // Query of this pair's n-th slot: slot cluster + n * n_clusters of the schedule (`order`, a
+  // permutation of the queries; the identity when null).
+  auto query = [&](int n) {
+    const int64_t i = cluster + static_cast<int64_t>(n) * n_clusters;
+    return order != nullptr ? static_cast<int64_t>(__ldg(order + i)) : i;
+  };
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffAbort);
   volatile int* nt_buf = reinterpret_cast<volatile int*>(smem + kOffNT);
   auto bar = [&](int i) { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
@@ -1009,9 +1015,46 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
   cluster_sync();                                    // no CTA leaves while its peer may write
 }
 
+// Schedule for the persistent pairs: queries sorted by their number of key tiles, largest
+// first (counting sort; a query at position p selects min(p + 1, k) keys), and dealt to the
+// pairs in rounds whose direction alternates, so that the pairs' total work evens out. Slot i of
+// the schedule is processed by pair i % n_pairs.
+constexpr int kOrderThreads = 1024;
+constexpr int kOrderBuckets = (kMaxK + pair::kKeys - 1) / pair::kKeys + 1;
+__global__ void __launch_bounds__(kOrderThreads)
+mla_order_kernel(const int32_t* __restrict__ pos, int k, int n_q, int n_pairs,
+                 int32_t* __restrict__ order) {
+  __shared__ uint32_t hist[kOrderBuckets], next[kOrderBuckets];
+  for (int b = threadIdx.x; b < kOrderBuckets; b += blockDim.x) hist[b] = 0;
+  __syncthreads();
+  auto tiles_of = [&](int t) {
+    const int p = __ldg(pos + t);
+    const int sel = p < 0 ? 0 : (p >= k ? k : p + 1);
+    return (sel + pair::kKeys - 1) / pair::kKeys;
+  };
+  for (int t = threadIdx.x; t < n_q; t += blockDim.x) atomicAdd(&hist[tiles_of(t)], 1u);
+  __syncthreads();
+  if (threadIdx.x == 0) {                            // bucket b starts after every larger bucket
+    uint32_t run = 0;
+    for (int b = kOrderBuckets - 1; b >= 0; --b) {
+      next[b] = run;
+      run += hist[b];
+    }
+  }
+  __syncthreads();
+  for (int t = threadIdx.x; t < n_q; t += blockDim.x) {
+    const int p = static_cast<int>(atomicAdd(&next[tiles_of(t)], 1u));   // rank, largest first
+    const int r = p / n_pairs;
+    int j = p - r * n_pairs;
+    if ((r & 1) && (r + 1) * n_pairs <= n_q) j = n_pairs - 1 - j;          // full rounds snake
+    order[r * n_pairs + j] = t;
+  }
+}
+
 int launch_mla_pair(const void* q, const void* c, int64_t n_kv_rows, const KvMap& kv,
                     const int32_t* bid, const int32_t* topk, int64_t n_q, int k, float scale,
-                    void* o, float* lse, cudaStream_t stream) {
+                    void* o, float* lse, const int32_t* pos, int32_t* order_ws,
+                    cudaStream_t stream) {
   (void)n_kv_rows;
   CUtensorMap tm_o;                                  // o as [n_q * 128 rows, 512 columns]
   int rc = make_tmap_bf16_2d(&tm_o, o, static_cast<uint64_t>(n_q) * pair::kH, pair::kDV,
@@ -1020,6 +1063,13 @@ int launch_mla_pair(const void* q, const void* c, int64_t n_kv_rows, const KvMap
   DSA_CHECK_CUDA(cudaFuncSetAttribute(sparse_mla_pair_kernel,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, pair::kSmem));
   const int64_t pairs = std::min<int64_t>(n_q, num_sms_cached() / 2);
+  const int32_t* order = nullptr;
+  if (pos != nullptr && order_ws != nullptr) {
+    mla_order_kernel<<<1, kOrderThreads, 0, stream>>>(pos, k, static_cast<int>(n_q),
+                                                      static_cast<int>(pairs), order_ws);
+    DSA_CHECK_CUDA(cudaGetLastError());
+    order = order_ws;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(pairs * 2));
   cfg.blockDim = dim3(pair::kThreads);
@@ -1036,7 +1086,7 @@ int launch_mla_pair(const void* q, const void* c, int64_t n_kv_rows, const KvMap
   DSA_CHECK_CUDA(cudaLaunchKernelEx(&cfg, sparse_mla_pair_kernel, tm_o,
                                     static_cast<const __nv_bfloat16*>(c),
                                     static_cast<const __nv_bfloat16*>(q), bid, topk, k, n_q, kv,
-                                    scale_log2, lse));
+                                    scale_log2, lse, order));
   return DSA_OK;
 }
 
@@ -1064,10 +1114,14 @@ int launch_mla(const void* q, const void* c, int64_t n_kv_rows, const KvMap& kv,
 
 }  // namespace
 
+size_t sparse_mla_workspace_bytes(int64_t n_q) {
+  return n_q > 0 ? static_cast<size_t>(n_q) * sizeof(int32_t) : 0;
+}
+
 int sparse_mla(const void* q, const void* c, int64_t n_kv_rows, const int32_t* cu, int n_req,
                const int32_t* bid, const int32_t* topk, int64_t n_q, int H, int dqk, int dv, int k,
                float scale, const int32_t* block_table, int max_pages, int page_size, void* o,
-               float* lse, cudaStream_t stream) {
+               float* lse, const int32_t* pos, void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (n_q < 0 || k < 1 || n_kv_rows < 0 || n_req < 1)
     return fail(DSA_ERR_INVALID, "mla: need n_q >= 0, k >= 1, n_kv_rows >= 0, n_req >= 1");
   if (n_q == 0) return DSA_OK;
@@ -1080,9 +1134,15 @@ int sparse_mla(const void* q, const void* c, int64_t n_kv_rows, const int32_t* c
     return fail(DSA_ERR_UNSUPPORTED, "mla: sizes beyond 32-bit TMA coordinates");
   if (reinterpret_cast<uintptr_t>(q) % 16 || reinterpret_cast<uintptr_t>(o) % 16)
     return fail(DSA_ERR_INVALID, "mla: q and o must be 16-byte aligned");
+  if (pos != nullptr && (ws == nullptr || ws_bytes < sparse_mla_workspace_bytes(n_q)))
+    return fail(DSA_ERR_WORKSPACE, "mla: workspace of %zu bytes < %zu", ws_bytes,
+                sparse_mla_workspace_bytes(n_q));
+  if (ws != nullptr && reinterpret_cast<uintptr_t>(ws) % 16 != 0)
+    return fail(DSA_ERR_INVALID, "mla: workspace must be 16-byte aligned");
   KvMap kv{cu, block_table, max_pages, n_req, n_kv_rows};
   if (H == 128 && dqk == 576 && dv == 512)
-    return launch_mla_pair(q, c, n_kv_rows, kv, bid, topk, n_q, k, scale, o, lse, stream);
+    return launch_mla_pair(q, c, n_kv_rows, kv, bid, topk, n_q, k, scale, o, lse, pos,
+                           static_cast<int32_t*>(ws), stream);
   if (H == 8 && dqk == 80 && dv == 64)
     return launch_mla<8, 80, 64>(q, c, n_kv_rows, kv, bid, topk, n_q, k, scale, o, lse, stream);
   return fail(DSA_ERR_UNSUPPORTED, "mla: (H, dqk, dv) = (%d, %d, %d) not built; supported "

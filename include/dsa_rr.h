@@ -241,6 +241,28 @@ int dsa_sparse_mla(const void* q, const void* c, int64_t n_kv_rows, const int32_
                    void* o, float* lse, dsa_stream_t stream);
 
 /*
+ * dsa_sparse_mla with a schedule for the persistent CTA pairs (H = 128 path). The pages have no
+ * counterpart: this orders the work, the result is the same.
+ *
+ * Arguments and results are those of dsa_sparse_mla, plus pos (int32 [n_q], device): the query
+ * positions, used only to estimate each query's work (a query at position p selects
+ * min(p + 1, k) keys). Queries are sorted by that estimate, largest first, and dealt to the
+ * pairs in rounds of alternating direction, so that the pairs finish together; o and lse are
+ * bit-identical to dsa_sparse_mla's (each query's arithmetic does not depend on its pair).
+ * workspace: device, 16-byte aligned, >= dsa_sparse_mla_workspace_size(n_q) bytes (the
+ * schedule, int32 [n_q]); owned by the caller, not read before it is written. Errors as
+ * dsa_sparse_mla, plus DSA_ERR_WORKSPACE for a short workspace and DSA_ERR_INVALID for a null
+ * pos or a misaligned workspace. The (8, 80, 64) path checks the workspace but runs unscheduled.
+ */
+size_t dsa_sparse_mla_workspace_size(int64_t n_q);
+int dsa_sparse_mla_balanced(const void* q, const void* c, int64_t n_kv_rows, const int32_t* cu,
+                            int n_req, const int32_t* bid, const int32_t* pos,
+                            const int32_t* topk, int64_t n_q, int H, int dqk, int dv, int k,
+                            float scale, const int32_t* block_table, int max_pages,
+                            int page_size, void* o, float* lse, void* workspace,
+                            size_t workspace_bytes, dsa_stream_t stream);
+
+/*
  * Allocation-free variant of dsa_indexer_topk. (The pages have no counterpart: this is a
  * convenience of the library, not a step of the method.)
  *
