@@ -579,6 +579,115 @@ def next_rows(args):
     print(json.dumps({"device_errors": dsa.dsa_read_device_errors()}), flush=True)
 
 
+def config_rows(args):
+    """The metric's steps (indexer + top-k + sparse MLA) on every workload config, one JSON line
+    each: shard queries / device time (per shard the median of 20 launches after 3 warm-up, L2
+    flushed before each; the shards of a config back to back), and the indexer's and the MLA's
+    algorithmic TFLOP/s against the measured bf16 peak. For the paged decode batch also their
+    algorithmic bytes (k_idx read once per request; the selected latent rows) against the
+    measured copy bandwidth. Inputs are generated on the device; positions of prefill shards come
+    from the library's own split."""
+    import torch
+    import __graft_entry__ as ge
+    ge.build()
+    import deepseek_v3_sparse_round_gb300 as dsa
+    import workloads as W
+    pk = peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def timed(parts, reps=20):
+        for _ in range(3):
+            for f in parts:
+                f()
+        t = [[] for _ in parts]
+        for i in range(reps):
+            flush.fill_(i & 255)
+            es = [ev() for _ in range(len(parts) + 1)]
+            es[0].record()
+            for j, f in enumerate(parts):
+                f()
+                es[j + 1].record()
+            torch.cuda.synchronize()
+            for j in range(len(parts)):
+                t[j].append(es[j].elapsed_time(es[j + 1]))
+        return [float(np.median(x)) for x in t]
+
+    def shard_inputs(wl, rank):
+        if wl.decode_queries:
+            table, n_pages = W.random_block_table(wl.lengths, wl.page_size,
+                                                  W.seed_of(wl, "block_table"))
+            bid, pos = W.decode_queries(wl.lengths, wl.decode_queries)
+            n_rows = n_pages * wl.page_size
+            cu = torch.zeros(len(wl.lengths) + 1, dtype=torch.int32, device="cuda")
+            return dict(n_rows=n_rows, cu=cu, bt=torch.as_tensor(table, device="cuda"),
+                        bid=torch.as_tensor(np.asarray(bid, np.int32), device="cuda"),
+                        pos=torch.as_tensor(np.asarray(pos, np.int32), device="cuda"),
+                        max_ctx=int(max(wl.lengths)))
+        cu_np = W.cu_seqlens(wl.lengths)
+        n_tok = int(cu_np[-1])
+        n_r = dsa.dsa_rr_shard_len(n_tok, wl.sp, rank)
+        cu = torch.as_tensor(cu_np, device="cuda")
+        e = lambda m: torch.empty(m, dtype=torch.int32, device="cuda")
+        cs, pos, bid, gidx = e(len(cu_np)), e(n_r), e(n_r), e(n_r)
+        dsa.dsa_rr_split_metadata(cu, n_tok, wl.sp, rank, cs, pos, bid, gidx)
+        return dict(n_rows=n_tok, cu=cu, bt=None, bid=bid, pos=pos, max_ctx=int(max(wl.lengths)))
+
+    for wid in (1, 2, 3, 4):
+        wl = W.WORKLOADS[wid]
+        ranks = (0,) if wl.decode_queries else wl.ranks
+        tot_q = tot_idx = tot_mla = 0.0
+        idx_flop = mla_flop = idx_bytes = mla_bytes = 0.0
+        for rank in ranks:
+            si = shard_inputs(wl, rank)
+            n_q = si["pos"].numel()
+            idx = W.indexer_inputs(wl, n_q, si["n_rows"], rank, device="cuda")
+            mi = W.mla_inputs(wl, n_q, si["n_rows"], rank, device="cuda")
+            ws = torch.empty(dsa.dsa_indexer_topk_workspace_size(n_q, si["max_ctx"], wl.topk),
+                             dtype=torch.uint8, device="cuda")
+            mws = torch.empty(dsa.dsa_sparse_mla_workspace_size(n_q), dtype=torch.uint8,
+                              device="cuda")
+            topk = torch.empty((n_q, wl.topk), dtype=torch.int32, device="cuda")
+            o = torch.empty((n_q, wl.H, wl.dv), dtype=torch.bfloat16, device="cuda")
+            lse = torch.empty((n_q, wl.H), device="cuda")
+            n_req = len(wl.lengths)
+            f_idx = lambda: dsa.dsa_indexer_topk(idx.q_idx, idx.w, idx.k_idx, si["cu"], n_req,
+                                                 si["pos"], si["bid"], wl.topk, si["max_ctx"],
+                                                 topk, ws, block_table=si["bt"])
+            f_mla = lambda: dsa.dsa_sparse_mla_balanced(mi.q, mi.c, si["cu"], n_req, si["bid"],
+                                                        si["pos"], topk, wl.scale, o, mws,
+                                                        lse=lse, block_table=si["bt"])
+            t_idx, t_mla = timed([f_idx, f_mla])
+            p = si["pos"].cpu().numpy().astype(np.int64)
+            tot_q += n_q
+            tot_idx += t_idx
+            tot_mla += t_mla
+            idx_flop += 2.0 * wl.Hi * wl.Di * float(np.sum(p + 1))
+            sel = float(np.sum(np.minimum(p + 1, wl.topk)))
+            mla_flop += 2.0 * wl.H * (wl.dqk + wl.dv) * sel
+            if wl.decode_queries:
+                idx_bytes = float(sum(wl.lengths)) * wl.Di * 2
+                mla_bytes += sel * wl.dqk * 2
+            del idx, mi, ws, mws, topk, o, lse, si
+            torch.cuda.empty_cache()
+        ms = tot_idx + tot_mla
+        line = {"config": wid, "workload": wl.name, "shards": len(ranks), "queries": int(tot_q),
+                "ms": round(ms, 4), "tokens_per_s": round(tot_q / (ms * 1e-3), 1),
+                "indexer_topk_ms": round(tot_idx, 4), "mla_ms": round(tot_mla, 4),
+                "indexer_topk_tflops": round(idx_flop / (tot_idx * 1e-3) / 1e12, 1),
+                "indexer_topk_frac_bf16": round(idx_flop / (tot_idx * 1e-3) / 1e12 / pk["bf16"], 3),
+                "mla_tflops": round(mla_flop / (tot_mla * 1e-3) / 1e12, 1),
+                "mla_frac_bf16": round(mla_flop / (tot_mla * 1e-3) / 1e12 / pk["bf16"], 3),
+                "runs": "median of 20 per shard, L2 flushed before each"}
+        if wl.decode_queries:
+            line["indexer_topk_gbs"] = round(idx_bytes / (tot_idx * 1e-3) / 1e9, 1)
+            line["indexer_topk_frac_hbm"] = round(idx_bytes / (tot_idx * 1e-3) / 1e9 / pk["hbm"], 3)
+            line["mla_gbs"] = round(mla_bytes / (tot_mla * 1e-3) / 1e9, 1)
+            line["mla_frac_hbm"] = round(mla_bytes / (tot_mla * 1e-3) / 1e9 / pk["hbm"], 3)
+        print(json.dumps(line), flush=True)
+    print(json.dumps({"device_errors": dsa.dsa_read_device_errors()}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -590,7 +699,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--next-rows", nargs="?", const="all", default=None,
                     help="measure the widened rows (paged rerange, decode split) and exit")
+    ap.add_argument("--configs", action="store_true",
+                    help="indexer + top-k + sparse MLA on every workload config, then exit")
     args = ap.parse_args()
+    if args.configs:
+        config_rows(args)
+        return
     if args.next_rows:
         next_rows(args)
         return
