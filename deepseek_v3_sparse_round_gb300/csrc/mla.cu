@@ -434,9 +434,10 @@ static_assert(kKeys == 48, "the gather and softmax split a tile into 32 + 16 ent
 static_assert(kStageS % 1024 == 0 && kStageO % 1024 == 0 && kAtomBytes % 1024 == 0, "SW128");
 }  // namespace pair
 
-// Persistent: cluster i of n processes queries i, i + n, i + 2n, ... Every role walks the same
-// query sequence and, inside it, the same global tile sequence (tiles of earlier queries
-// included), so ring slots, S/P buffers and their barrier phases continue across queries.
+// Persistent: cluster i of n processes the queries in slots i, i + n, i + 2n, ... of `order` (the
+// identity when null). Every role walks the same query sequence and, inside it, the same global
+// tile sequence (tiles of earlier queries included), so ring slots, S/P buffers and their
+// barrier phases continue across queries.
 // Every role waits for every per-query phase in order, also for queries where it has no tile.
 __global__ void __launch_bounds__(pair::kThreads, 1)
 sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
