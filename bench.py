@@ -668,6 +668,8 @@ def config_rows(args):
             if wl.decode_queries:
                 idx_bytes = float(sum(wl.lengths)) * wl.Di * 2
                 mla_bytes += sel * wl.dqk * 2
+            if args.with_oracle and rank == ranks[-1]:
+                or_q, or_s = _oracle_sample_time(W, wl, si, idx, mi, 4 if wl.decode_queries else 8)
             del idx, mi, ws, mws, topk, o, lse, si
             torch.cuda.empty_cache()
         ms = tot_idx + tot_mla
@@ -679,6 +681,11 @@ def config_rows(args):
                 "mla_tflops": round(mla_flop / (tot_mla * 1e-3) / 1e12, 1),
                 "mla_frac_bf16": round(mla_flop / (tot_mla * 1e-3) / 1e12 / pk["bf16"], 3),
                 "runs": "median of 20 per shard, L2 flushed before each"}
+        if args.with_oracle:
+            line["oracle"] = {"tokens_per_s": round(or_q / or_s, 3), "kind": "oracle",
+                              "cores": _blas_threads(),
+                              "sample": f"{or_q} evenly spaced queries of one shard (the longest "
+                                        f"included), {or_s:.1f} s, extrapolated per query"}
         if wl.decode_queries:
             line["indexer_topk_gbs"] = round(idx_bytes / (tot_idx * 1e-3) / 1e9, 1)
             line["indexer_topk_frac_hbm"] = round(idx_bytes / (tot_idx * 1e-3) / 1e9 / pk["hbm"], 3)
@@ -686,6 +693,41 @@ def config_rows(args):
             line["mla_frac_hbm"] = round(mla_bytes / (tot_mla * 1e-3) / 1e9 / pk["hbm"], 3)
         print(json.dumps(line), flush=True)
     print(json.dumps({"device_errors": dsa.dsa_read_device_errors()}), flush=True)
+
+
+def _oracle_sample_time(W, wl, si, idx, mi, n_sample):
+    """fp64 oracle (indexer, full-sort top-k, sparse MLA) on `n_sample` queries of a shard whose
+    inputs live on the device; returns (queries, seconds). Only the sampled queries' requests are
+    copied to the host, as one compact contiguous KV (a paged cache is read through its table)."""
+    from oracle.kv import ContiguousKV
+    pos = si["pos"].cpu().numpy().astype(np.int64)
+    bid = si["bid"].cpu().numpy().astype(np.int64)
+    sel = np.unique(np.concatenate([np.linspace(0, len(pos) - 1, n_sample).round(),
+                                    [int(np.argmax(pos))]]).astype(np.int64))
+    reqs = sorted(set(int(b) for b in bid[sel]))
+    need = {b: int(pos[sel][bid[sel] == b].max()) + 1 for b in reqs}
+    if si["bt"] is not None:
+        table = si["bt"].cpu().numpy().astype(np.int64)
+        rows = np.concatenate([table[b, np.arange(need[b]) // wl.page_size] * wl.page_size
+                               + np.arange(need[b]) % wl.page_size for b in reqs])
+    else:
+        cu = si["cu"].cpu().numpy().astype(np.int64)
+        rows = np.concatenate([cu[b] + np.arange(need[b]) for b in reqs])
+    import torch
+    r_dev = torch.as_tensor(rows, device=idx.k_idx.device)
+    k64 = idx.k_idx[r_dev].float().cpu().numpy().astype(np.float64)
+    c64 = mi.c[r_dev].float().cpu().numpy().astype(np.float64)
+    cu2 = np.concatenate([[0], np.cumsum([need[b] for b in reqs])]).astype(np.int64)
+    remap = {b: i for i, b in enumerate(reqs)}
+    s_dev = torch.as_tensor(sel, device=idx.k_idx.device)
+    sh = {"cu": cu2, "q_idx": idx.q_idx[s_dev].float().cpu().numpy().astype(np.float64),
+          "w": idx.w[s_dev].cpu().numpy().astype(np.float64), "k_idx": k64,
+          "q": mi.q[s_dev].float().cpu().numpy().astype(np.float64), "c": c64,
+          "pos": pos[sel], "bid": np.asarray([remap[int(b)] for b in bid[sel]], dtype=np.int64)}
+    loc = np.arange(len(sel))
+    t0 = time.perf_counter()
+    _oracle_step(W, wl, sh, loc)
+    return len(sel), time.perf_counter() - t0
 
 
 def main():
@@ -701,6 +743,8 @@ def main():
                     help="measure the widened rows (paged rerange, decode split) and exit")
     ap.add_argument("--configs", action="store_true",
                     help="indexer + top-k + sparse MLA on every workload config, then exit")
+    ap.add_argument("--with-oracle", action="store_true",
+                    help="with --configs: also time the fp64 oracle on a sample of each config")
     args = ap.parse_args()
     if args.configs:
         config_rows(args)
