@@ -669,7 +669,7 @@ def config_rows(args):
                 idx_bytes = float(sum(wl.lengths)) * wl.Di * 2
                 mla_bytes += sel * wl.dqk * 2
             if args.with_oracle and rank == ranks[-1]:
-                or_q, or_s = _oracle_sample_time(W, wl, si, idx, mi, 4 if wl.decode_queries else 8)
+                or_q, or_s = _oracle_sample_time(W, wl, si, idx, mi, 16 if wl.decode_queries else 64)
             del idx, mi, ws, mws, topk, o, lse, si
             torch.cuda.empty_cache()
         ms = tot_idx + tot_mla
@@ -685,7 +685,7 @@ def config_rows(args):
             line["oracle"] = {"tokens_per_s": round(or_q / or_s, 3), "kind": "oracle",
                               "cores": _blas_threads(),
                               "sample": f"{or_q} evenly spaced queries of one shard (the longest "
-                                        f"included), {or_s:.1f} s, extrapolated per query"}
+                                        f"included), {or_s:.2f} s, extrapolated per query"}
         if wl.decode_queries:
             line["indexer_topk_gbs"] = round(idx_bytes / (tot_idx * 1e-3) / 1e9, 1)
             line["indexer_topk_frac_hbm"] = round(idx_bytes / (tot_idx * 1e-3) / 1e9 / pk["hbm"], 3)
