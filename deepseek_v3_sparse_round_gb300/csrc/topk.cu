@@ -131,7 +131,9 @@ topk_kernel(const float* __restrict__ scores, int64_t stride, const int32_t* __r
   __shared__ uint32_t warp_tot[kWarps];
   __shared__ uint32_t s_digit, s_above;
 
-  const int64_t t = blockIdx.x;
+  // Rows in reverse order: within a request of a round-robin shard, later rows are longer, so
+  // the longest rows start first and the last CTAs to be scheduled get short ones.
+  const int64_t t = static_cast<int64_t>(gridDim.x) - 1 - blockIdx.x;
   int32_t* out = topk + t * k;
   const int L = __ldg(pos + t) + 1;
   if (L < 1 || L > max_ctx) {
