@@ -91,3 +91,18 @@ def test_split_decode_needs_pos_base(lib):
     assert f(fake, null, 1, 10, 4, 0, fake, fake, fake, null, null, null, 0, null) == -1
     assert b"pos_base" in lib.dsa_last_error_string()
     assert f(fake, fake, 1, 10, 0, 0, fake, fake, fake, null, null, null, 0, null) == -1   # sp = 0
+
+
+def test_sparse_mla_balanced_arguments_rejected(lib):
+    null = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(4096)
+    f = lib.dsa_sparse_mla_balanced
+    args = lambda pos, ws, ws_bytes: (fake, fake, 10, fake, 1, fake, pos, fake, 4, 128, 576, 512,
+                                      2048, 0.1, null, 0, 0, fake, null, ws, ws_bytes, null)
+    assert f(*args(null, fake, 16)) == -1                              # pos is required
+    assert b"pos" in lib.dsa_last_error_string()
+    assert f(*args(fake, fake, 8)) == -3                               # 4 queries need 16 bytes
+    assert f(*args(fake, null, 16)) == -3                              # no workspace
+    assert f(*args(fake, ctypes.c_void_p(4100), 16)) == -1             # not 16-byte aligned
+    assert lib.dsa_sparse_mla_workspace_size(1476) == 1476 * 4
+    assert lib.dsa_sparse_mla_workspace_size(0) == 0
