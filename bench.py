@@ -190,8 +190,9 @@ class ShardStep:
         self.o = e(self.n_r, wl.H, wl.dv, dt=torch.bfloat16)
         self.lse = e(self.n_r, wl.H, dt=torch.float32)
         self.mla_ws = e(dsa.dsa_sparse_mla_workspace_size(self.n_r), dt=torch.uint8)
-        # split meta + gather, 2 reranges, plan + indexer + top-k, MLA schedule + MLA
-        self.launches_per_step = 9
+        # split (metadata + row gather: one launch), 2 reranges, indexer plan + indexer, top-k,
+        # MLA schedule + MLA (as the ncu launch list of a step shows)
+        self.launches_per_step = 8
         self.h_o = [torch.empty(self.o.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
         # second input / output set for the end-to-end pipeline (step i + 1 uploads while step i runs)
         self.d_sets = [self.d, {k: torch.empty_like(v) for k, v in self.d.items()}]
