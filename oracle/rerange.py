@@ -65,3 +65,24 @@ def rerange_into_pages(gathered: np.ndarray, cu, sp: int, stride: int, block_tab
             page = table[b, s // page_size]
             out[page * page_size + s % page_size] = logical[cu[b] + s]
     return out
+
+
+def cache_local_into_pages(local_rows: np.ndarray, cu, sp: int, rank: int, block_table,
+                           page_size: int, pool: np.ndarray) -> np.ndarray:
+    """After attention a rank drops the global KV and its cache keeps only the tokens it owns
+    ("[DeepSeek v3.2] 上下文并行详解", section 4 part 3 step D: with CP = 4, rank 1 stores only
+    K1 and K5 in its cache pool for the decode steps). local_rows[t] is the rank's t-th token,
+    flattened index g = rank + t*sp. Reading taken where the page is silent: the rank's cache of
+    request b lists that request's tokens on this rank in order, the j-th of them in slot j, and
+    slot j lives in row block_table[b, j // page_size] * page_size + j % page_size of the rank's
+    pool. Rows of the pool that no token maps to keep their contents."""
+    cu = np.asarray(cu, dtype=np.int64)
+    table = np.asarray(block_table, dtype=np.int64)
+    tokens = shard_tokens(int(cu[-1]), sp, rank)
+    out = pool.copy()
+    for b in range(len(cu) - 1):
+        mine = [t for t, g in enumerate(tokens) if cu[b] <= g < cu[b + 1]]
+        for j, t in enumerate(mine):
+            page = table[b, j // page_size]
+            out[page * page_size + j % page_size] = local_rows[t]
+    return out

@@ -108,3 +108,70 @@ def test_rerange_into_pages_reads_back_through_the_page_map(seed):
     for b in range(len(lengths)):
         written[kv.rows(b, np.arange(lengths[b]))] = True
     assert (pool[~written] == -7).all()
+
+
+def test_local_cache_worked_example():
+    # CP = 4, one request [T0 .. T7]: each rank's cache keeps exactly the tokens the page names
+    # for it (rank 1: K1 then K5). Pages of 2 rows; every rank's request uses its page 5.
+    g = read_golden("local_cache_cp4.txt")
+    sp, n = int(g[0][0].split()[1]), int(g[1][0].split()[1])
+    x = np.arange(n) * 10                                  # K_g = 10 g
+    for key, vals in g[2:]:
+        r = int(key.split()[1])
+        local = osplit.split_rows(x, sp, r)
+        pool = orr.cache_local_into_pages(local, [0, n], sp, r, [[5]], 2, np.full(12, -1))
+        assert pool[10:12].tolist() == [10 * int(v) for v in vals]
+        assert (pool[:10] == -1).all()
+
+
+def test_local_cache_one_shard_is_the_paged_rerange():
+    # sp = 1: the rank owns every token, so its cache is the full paged write of the batch
+    rng = np.random.default_rng(5)
+    lengths = [7, 3, 12]
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    ps = 4
+    need = [-(-L // ps) for L in lengths]
+    perm = rng.permutation(sum(need))
+    table = np.full((3, max(need)), -1)
+    at = 0
+    for b, p in enumerate(need):
+        table[b, :p] = perm[at:at + p]
+        at += p
+    x = rng.integers(0, 1 << 30, size=(int(cu[-1]), 2))
+    pool0 = np.zeros((sum(need) * ps, 2), dtype=x.dtype)
+    a = orr.cache_local_into_pages(x, cu, 1, 0, table, ps, pool0)
+    b = orr.rerange_into_pages(x, cu, 1, 0, table, ps, pool0)
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_local_caches_partition_the_batch(seed):
+    # Every logical token lands in exactly one rank's cache, at its index among the request's
+    # tokens on that rank; read back through each rank's page map it is the split's row.
+    from oracle.kv import PagedKV
+    rng = np.random.default_rng(200 + seed)
+    sp, ps = int(rng.integers(1, 9)), int(rng.choice([1, 3, 64]))
+    lengths = rng.integers(0, 150, size=int(rng.integers(1, 6)))
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    n = int(cu[-1])
+    x = rng.integers(0, 1 << 30, size=(n, 2))
+    seen = np.zeros(n, dtype=np.int64)
+    for r in range(sp):
+        tokens = osplit.shard_tokens(n, sp, r)
+        counts = [int(np.sum((tokens >= cu[b]) & (tokens < cu[b + 1]))) for b in range(len(lengths))]
+        need = [-(-c // ps) for c in counts]
+        perm = rng.permutation(sum(need) + 2)
+        table = np.full((len(lengths), max(max(need), 1)), -1)
+        at = 0
+        for b, p in enumerate(need):
+            table[b, :p] = perm[at:at + p]
+            at += p
+        pool = orr.cache_local_into_pages(osplit.split_rows(x, sp, r), cu, sp, r, table, ps,
+                                          np.full(((sum(need) + 2) * ps, 2), -7))
+        kv = PagedKV(table, ps)
+        for b in range(len(lengths)):
+            mine = tokens[(tokens >= cu[b]) & (tokens < cu[b + 1])]
+            assert np.array_equal(pool[kv.rows(b, np.arange(len(mine)))], x[mine])
+            assert np.all(mine % sp == r)
+            seen[mine] += 1
+    assert (seen == 1).all()
