@@ -1,22 +1,27 @@
-"""Benchmark: one shard of round-robin sequence-sharded DSA prefill attention on GB300.
+"""Benchmark: round-robin sequence-sharded DSA prefill attention on one GB300.
 
-Workload (default): the varlen batch {8000, 800, 5, 3000} tokens, sp = 8, shard rank 3
-(1,476 queries); indexer 64 heads x 128, top-k 2048; MLA 128 heads, qk 576 / v 512, bf16.
-A step is one pass of the whole shard path through the C ABI:
+Workload (default): the many-request batch -- 32 requests with lengths U[128, 4096] (seed 0,
+N = 71,014 tokens), sp = 4, all four shards processed back to back on one GPU (17,753-17,754
+queries each, 71,014 in total); indexer 64 heads x 128, top-k 2048; MLA 128 heads, qk 576 /
+v 512, bf16. A step is the whole shard path of every shard through the C ABI:
   split metadata + the shard's row gather -> rerange of the all-gathered k_idx and latent rows
   -> indexer scores + top-k -> sparse MLA.
-The other shards' rows are inputs (one GPU, no collective). With --gpus N (torchrun), GPU i
-takes shard (3 + i) % 8 of the same batch: independent problems, weak scaling.
+The other shards' rows are inputs (one GPU, no collective). The long single prompt (32,768
+tokens, sp = 8, all eight shards) is timed the same way and reported under "config_long".
+With --gpus N (torchrun) every GPU runs an independent replica of the same batch: weak scaling,
+no collective on the data path.
 
-value = shard queries processed / device time of the timed steps (CUDA events on the launch
+value = query tokens processed / device time of the timed steps (CUDA events on the launch
 stream, L2 flushed between steps); e2e = the same through host buffers: every step copies its
-inputs from pinned host memory and reads o back, inside the timed region, pipelined over two
-buffer sets and three streams (upload of step i + 1 and download of step i - 1 overlap step i).
+inputs from pinned host memory and reads o back inside the timed region, pipelined shard by
+shard over two buffer sets and three streams (the upload of the next shard and the download of
+the previous one overlap the current shard's kernels).
 --impl reference times the fp64 CPU oracle on a bounded sample of the same workload.
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -30,8 +35,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "shard prefill query tokens/s (indexer+top-k+sparse MLA); % of BF16 TC roofline"
-WORKLOAD_ID = 1
-BASE_RANK = 3
+WORKLOAD_ID = 3          # many-request batch, all shards (the largest single-GPU prefill config)
+LONG_ID = 2              # long single prompt, all shards (reported beside it)
+NOMINAL = {"bf16": 2250.0, "hbm": 7900.0}   # GB300 dense bf16 TFLOP/s and HBM3e GB/s, nominal
 
 
 def peaks():
@@ -44,29 +50,26 @@ def peaks():
     return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
 
 
-def profiled_traffic(kernel_file, summary):
-    """DRAM bytes per launch from a committed ncu summary, only while the kernel source is the
-    one that was profiled (its sha1 prefix is recorded next to the figure); else None."""
-    import hashlib
+def profiled_traffic(kernel):
+    """DRAM bytes per unit of work from profiles/traffic.json (written from an ncu capture),
+    only while the kernel's source file still has the hash recorded there; else None."""
     try:
-        with open(os.path.join(ROOT, "deepseek_v3_sparse_round_gb300", "csrc", kernel_file), "rb") as f:
+        with open(os.path.join(ROOT, "profiles", "traffic.json"), encoding="utf-8") as f:
+            rec = json.load(f)[kernel]
+        with open(os.path.join(ROOT, "deepseek_v3_sparse_round_gb300", "csrc", rec["source"]), "rb") as f:
             sha = hashlib.sha1(f.read()).hexdigest()[:12]
-        fields = {}
-        with open(os.path.join(ROOT, "profiles", summary), encoding="utf-8") as f:
-            for line in f:
-                if ":" in line and line.split(":")[0].strip() in ("traffic_bytes_per_launch", "source_sha1"):
-                    k, v = line.split(":", 1)
-                    fields[k.strip()] = v.strip()
-        if fields.get("source_sha1") == sha:
-            return int(fields["traffic_bytes_per_launch"])
+        if rec.get("source_sha1") == sha:
+            return rec
     except (OSError, KeyError, ValueError):
         pass
     return None
 
 
-def shard_for_rank(rank: int, sp: int) -> int:
-    """GPU `rank` of the job processes shard (BASE_RANK + rank) % sp of the varlen batch."""
-    return (BASE_RANK + rank) % sp
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
 
 
 def max_over_ranks(value: float, dist, device) -> float:
@@ -79,11 +82,11 @@ def max_over_ranks(value: float, dist, device) -> float:
     return float(t.item())
 
 
-def dist_env():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
+def shards_for_rank(rank: int, world: int, sp: int) -> list:
+    """Every GPU runs an independent replica of the whole batch: all sp shards of it. The job
+    processes world x (all queries of the batch); no shard is shared between GPUs."""
+    del rank, world
+    return list(range(sp))
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -155,80 +158,171 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- GPU arm
-class ShardStep:
-    """Device buffers and the launches of one step for shard `rank` of the varlen workload."""
+class ConfigStep:
+    """Device buffers and the launches of one step of a prefill workload: every shard of the
+    batch, back to back. Inputs are drawn on the device (seeded); `host()` makes pinned host
+    copies for the end-to-end run."""
 
-    def __init__(self, torch, dsa, W, rank, device):
-        self.torch, self.dsa = torch, dsa
-        wl = W.WORKLOADS[WORKLOAD_ID]
-        self.wl, self.rank, self.dev = wl, rank, device
+    LAUNCHES_PER_SHARD = 8   # split (+gather), 2 reranges, indexer plan, indexer, top-k,
+    #                          MLA schedule, MLA -- as the ncu launch list of a step shows
+
+    def __init__(self, torch, dsa, W, wid, device):
+        self.torch, self.dsa, self.W = torch, dsa, W
+        wl = W.WORKLOADS[wid]
+        self.wl, self.wid, self.dev = wl, wid, device
         cu_np = W.cu_seqlens(wl.lengths)
+        self.cu_np = cu_np
         self.N = int(cu_np[-1])
         self.n_req = len(wl.lengths)
-        self.n_r = dsa.dsa_rr_shard_len(self.N, wl.sp, rank)
         self.max_ctx = int(max(wl.lengths))
-        idx = W.indexer_inputs(wl, self.n_r, self.N, rank)
-        mi = W.mla_inputs(wl, self.n_r, self.N, rank)
-        # host inputs (pinned): the shard's queries, and the all-gathered (rank-major) KV rows
-        # that the other shards contribute; built by plain indexing of the logical rows.
-        perm = np.concatenate([np.arange(q, self.N, wl.sp) for q in range(wl.sp)])
-        self.h = {
-            "cu": torch.as_tensor(cu_np).pin_memory(),
-            "q_idx": idx.q_idx.pin_memory(), "w": idx.w.pin_memory(), "q": mi.q.pin_memory(),
-            "k_gath": idx.k_idx[torch.as_tensor(perm)].contiguous().pin_memory(),
-            "c_gath": mi.c[torch.as_tensor(perm)].contiguous().pin_memory(),
-            "c_log": mi.c.pin_memory(),
-        }
-        self.d = {k: v.to(device) for k, v in self.h.items()}
-        e = lambda *s, dt=torch.int32: torch.empty(*s, dtype=dt, device=device)
-        self.cu_shard, self.pos, self.bid, self.gidx = e(self.n_req + 1), e(self.n_r), e(self.n_r), e(self.n_r)
-        self.c_local = e(self.n_r, wl.dqk, dt=torch.bfloat16)
+        self.ranks = list(wl.ranks)
+        e = lambda *sh, dt=torch.int32: torch.empty(*sh, dtype=dt, device=device)
+        self.n_r = {r: dsa.dsa_rr_shard_len(self.N, wl.sp, r) for r in self.ranks}
+        # shared inputs: request offsets, the logical latent rows (each shard gathers its own
+        # rows from them), and the all-gathered (rank-major, packed) k_idx and latent rows that
+        # every shard reranges
+        idx0 = W.indexer_inputs(wl, 1, self.N, 0, device=device)
+        mi0 = W.mla_inputs(wl, 1, self.N, 0, device=device)
+        perm = torch.as_tensor(np.concatenate([np.arange(q, self.N, wl.sp) for q in range(wl.sp)]),
+                               device=device)
+        self.shared = {"cu": torch.as_tensor(cu_np, device=device), "c_log": mi0.c,
+                       "k_gath": idx0.k_idx[perm].contiguous(), "c_gath": mi0.c[perm].contiguous()}
+        del idx0, mi0
+        # per-shard inputs and outputs
+        self.inp, self.out = {}, {}
+        for r in self.ranks:
+            n = self.n_r[r]
+            idx = W.indexer_inputs(wl, n, 1, r, device=device)
+            mi = W.mla_inputs(wl, n, 1, r, device=device)
+            self.inp[r] = {"q_idx": idx.q_idx, "w": idx.w, "q": mi.q}
+            self.out[r] = {"cu_shard": e(self.n_req + 1), "pos": e(n), "bid": e(n), "gidx": e(n),
+                           "c_local": e(n, wl.dqk, dt=torch.bfloat16),
+                           "o": e(n, wl.H, wl.dv, dt=torch.bfloat16),
+                           "lse": e(n, wl.H, dt=torch.float32)}
+        n_max = max(self.n_r.values())
+        # one rank's working buffers, reused shard after shard (the shards run in order)
         self.k_idx = e(self.N, wl.Di, dt=torch.bfloat16)
         self.c = e(self.N, wl.dqk, dt=torch.bfloat16)
-        self.ws = e(dsa.dsa_indexer_topk_workspace_size(self.n_r, self.max_ctx, wl.topk), dt=torch.uint8)
-        self.topk = e(self.n_r, wl.topk)
-        self.o = e(self.n_r, wl.H, wl.dv, dt=torch.bfloat16)
-        self.lse = e(self.n_r, wl.H, dt=torch.float32)
-        self.mla_ws = e(dsa.dsa_sparse_mla_workspace_size(self.n_r), dt=torch.uint8)
-        # split (metadata + row gather: one launch), 2 reranges, indexer plan + indexer, top-k,
-        # MLA schedule + MLA (as the ncu launch list of a step shows)
-        self.launches_per_step = 8
-        self.h_o = [torch.empty(self.o.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-        # second input / output set for the end-to-end pipeline (step i + 1 uploads while step i runs)
-        self.d_sets = [self.d, {k: torch.empty_like(v) for k, v in self.d.items()}]
-        self.o_sets = [self.o, torch.empty_like(self.o)]
+        self.ws = e(dsa.dsa_indexer_topk_workspace_size(n_max, self.max_ctx, wl.topk), dt=torch.uint8)
+        self.topk = e(n_max, wl.topk)
+        self.mla_ws = e(dsa.dsa_sparse_mla_workspace_size(n_max), dt=torch.uint8)
+        self.launches_per_step = self.LAUNCHES_PER_SHARD * len(self.ranks)
 
-    def run(self, ev=None, b=0):
-        dsa, wl, d = self.dsa, self.wl, self.d_sets[b]
-        dsa.dsa_rr_split_metadata(d["cu"], self.N, wl.sp, self.rank, self.cu_shard, self.pos,
-                                  self.bid, self.gidx, src_rows=d["c_log"], dst_rows=self.c_local)
-        dsa.dsa_rr_rerange(d["k_gath"], self.k_idx, self.N, wl.sp, 0)
-        dsa.dsa_rr_rerange(d["c_gath"], self.c, self.N, wl.sp, 0)
-        dsa.dsa_indexer_topk(d["q_idx"], d["w"], self.k_idx, d["cu"], self.n_req, self.pos,
-                             self.bid, wl.topk, self.max_ctx, self.topk, self.ws)
+    def run_shard(self, r, inp=None, shared=None, o=None, ev=None):
+        """One shard's path. ev: optional 4 events recorded after split+reranges, after
+        indexer+top-k and after the MLA (and before the split)."""
+        dsa, wl = self.dsa, self.wl
+        inp = self.inp[r] if inp is None else inp
+        sh = self.shared if shared is None else shared
+        out = self.out[r]
+        n = self.n_r[r]
         if ev is not None:
             ev[0].record()
-        dsa.dsa_sparse_mla_balanced(d["q"], self.c, d["cu"], self.n_req, self.bid, self.pos,
-                                    self.topk, wl.scale, self.o_sets[b], self.mla_ws,
-                                    lse=self.lse)
+        dsa.dsa_rr_split_metadata(sh["cu"], self.N, wl.sp, r, out["cu_shard"], out["pos"],
+                                  out["bid"], out["gidx"], src_rows=sh["c_log"],
+                                  dst_rows=out["c_local"])
+        dsa.dsa_rr_rerange(sh["k_gath"], self.k_idx, self.N, wl.sp, 0)
+        dsa.dsa_rr_rerange(sh["c_gath"], self.c, self.N, wl.sp, 0)
         if ev is not None:
             ev[1].record()
+        topk = self.topk[:n]
+        dsa.dsa_indexer_topk(inp["q_idx"], inp["w"], self.k_idx, sh["cu"], self.n_req, out["pos"],
+                             out["bid"], wl.topk, self.max_ctx, topk, self.ws)
+        if ev is not None:
+            ev[2].record()
+        dsa.dsa_sparse_mla_balanced(inp["q"], self.c, sh["cu"], self.n_req, out["bid"],
+                                    out["pos"], topk, wl.scale, out["o"] if o is None else o,
+                                    self.mla_ws, lse=out["lse"])
+        if ev is not None:
+            ev[3].record()
 
-    def upload(self, b=0):
-        for k in ("cu", "q_idx", "w", "q", "k_gath", "c_gath", "c_log"):
-            self.d_sets[b][k].copy_(self.h[k], non_blocking=True)
-
-    def h2d_bytes(self):
-        return sum(self.h[k].numel() * self.h[k].element_size()
-                   for k in ("cu", "q_idx", "w", "q", "k_gath", "c_gath", "c_log"))
+    def run(self):
+        for r in self.ranks:
+            self.run_shard(r)
 
     def work(self):
-        pos = self.pos.cpu().numpy().astype(np.int64)
+        """Algorithmic work of one step: indexer flop (causal pairs), MLA flop (selected
+        pairs), bytes moved by the split gather and the two reranges."""
         wl = self.wl
-        sel = np.minimum(pos + 1, wl.topk)
-        idx_flops = 2.0 * wl.Hi * wl.Di * float(np.sum(pos + 1))
-        mla_flops = 2.0 * wl.H * (wl.dqk + wl.dv) * float(np.sum(sel))
-        return idx_flops, mla_flops
+        idx = mla = 0.0
+        pairs_c = pairs_s = 0
+        for r in self.ranks:
+            pos = self.out[r]["pos"].cpu().numpy().astype(np.int64)
+            pairs_c += int(np.sum(pos + 1))
+            pairs_s += int(np.sum(np.minimum(pos + 1, wl.topk)))
+        idx = 2.0 * wl.Hi * wl.Di * pairs_c
+        mla = 2.0 * wl.H * (wl.dqk + wl.dv) * pairs_s
+        nbytes = sum(2 * self.n_r[r] * wl.dqk * 2 + 2 * self.N * (wl.Di + wl.dqk) * 2
+                     for r in self.ranks)
+        return {"indexer_flop": idx, "mla_flop": mla, "causal_pairs": pairs_c,
+                "selected_pairs": pairs_s, "copy_bytes": nbytes}
+
+    def queries(self):
+        return sum(self.n_r.values())
+
+    def host(self):
+        """Pinned host copies of every input, and pinned host outputs (o per shard)."""
+        torch = self.torch
+        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+        self.h_shared = {k: pin(v) for k, v in self.shared.items()}
+        self.h_inp = {r: {k: pin(v) for k, v in d.items()} for r, d in self.inp.items()}
+        self.h_o = {r: torch.empty(self.out[r]["o"].shape, dtype=torch.bfloat16, pin_memory=True)
+                    for r in self.ranks}
+        n_max = max(self.n_r.values())
+        wl = self.wl
+        mk = lambda *sh, dt: torch.empty(*sh, dtype=dt, device=self.dev)
+        # two device sets for the pipeline: shared inputs, one shard's inputs and its o
+        self.d_shared = [{k: torch.empty_like(v) for k, v in self.shared.items()} for _ in range(2)]
+        self.d_inp = [{"q_idx": mk(n_max, wl.Hi, wl.Di, dt=torch.bfloat16),
+                       "w": mk(n_max, wl.Hi, dt=torch.float32),
+                       "q": mk(n_max, wl.H, wl.dqk, dt=torch.bfloat16)} for _ in range(2)]
+        self.d_o = [mk(n_max, wl.H, wl.dv, dt=torch.bfloat16) for _ in range(2)]
+
+    def h2d_bytes(self):
+        b = sum(v.numel() * v.element_size() for v in self.h_shared.values())
+        for d in self.h_inp.values():
+            b += sum(v.numel() * v.element_size() for v in d.values())
+        return b
+
+    def d2h_bytes(self):
+        return sum(v.numel() * v.element_size() for v in self.h_o.values())
+
+
+def time_steps(torch, st, steps, flush, stream):
+    """Device time of `steps` steps, L2 flushed before each; per-shard events split each step
+    into split+reranges, indexer+top-k and MLA. Returns (total seconds, per-part seconds)."""
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    evs = []
+    for i in range(steps):
+        flush.fill_(float(i))
+        e0 = mk()
+        e0.record(stream)
+        per = []
+        for r in st.ranks:
+            ev = (mk(), mk(), mk(), mk())
+            st.run_shard(r, ev=ev)
+            per.append(ev)
+        e1 = mk()
+        e1.record(stream)
+        evs.append((e0, e1, per))
+    torch.cuda.synchronize()
+    total = sum(a.elapsed_time(b) for a, b, _ in evs) / 1e3
+    parts = {"split_rerange": 0.0, "indexer_topk": 0.0, "mla": 0.0}
+    for _, _, per in evs:
+        for ev in per:
+            parts["split_rerange"] += ev[0].elapsed_time(ev[1]) / 1e3
+            parts["indexer_topk"] += ev[1].elapsed_time(ev[2]) / 1e3
+            parts["mla"] += ev[2].elapsed_time(ev[3]) / 1e3
+    return total, parts
+
+
+def roofline_obj(kernel, bound, achieved, peak, unit, nominal, traffic, extra):
+    d = {"bound": bound, "kernel": kernel, "achieved": round(achieved, 1), "peak": peak,
+         "unit": unit, "frac": round(achieved / peak, 4),
+         "nominal_peak": nominal, "frac_of_nominal": round(achieved / nominal, 4),
+         "traffic": traffic}
+    d.update(extra)
+    return d
 
 
 def shard_balance(torch, dsa, W, device, wid=3):
@@ -278,8 +372,8 @@ def gpu_arm(args):
     import deepseek_v3_sparse_round_gb300 as dsa
     import workloads as W
 
-    shard = shard_for_rank(rank, W.WORKLOADS[WORKLOAD_ID].sp)
-    st = ShardStep(torch, dsa, W, shard, device)
+    pk = peaks()
+    st = ConfigStep(torch, dsa, W, WORKLOAD_ID, device)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)   # > L2
     stream = torch.cuda.current_stream()
 
@@ -287,63 +381,92 @@ def gpu_arm(args):
     for _ in range(args.warmup):
         st.run()
     torch.cuda.synchronize()
-    idx_flops, mla_flops = st.work()
+    work = st.work()
 
     # ---- device-timed steps (inputs resident in HBM), L2 flushed between steps ----
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-            torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    for i in range(args.steps):
-        flush.fill_(float(i))
-        evs[i][0].record(stream)
-        st.run(ev=(evs[i][2], evs[i][3]))
-        evs[i][1].record(stream)
-    torch.cuda.synchronize()
+    dev_s, parts = time_steps(torch, st, args.steps, flush, stream)
     t_end = time.perf_counter()
-    wall = t_end - t_wall
     clk.mark(t_wall, t_end)
     clk.__exit__(None, None, None)
-    step_ms = [a.elapsed_time(b) for a, b, _, _ in evs]
-    mla_ms = [c.elapsed_time(d) for _, _, c, d in evs]
-    dev_s = max_over_ranks(sum(step_ms) / 1e3, dist, device)
+    dev_s = max_over_ranks(dev_s, dist, device)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
 
-    # ---- end to end through host buffers: every step uploads its inputs from pinned host memory
-    # and reads o back. Pipelined over two input/output sets and three streams (upload, compute,
-    # download), so step i + 1's upload and step i - 1's download overlap step i.
-    e2e_steps = max(2, min(args.steps, 20))
+    # ---- the long single prompt (8 shards of 4,096 queries), timed the same way ----
+    long_line = None
+    if not args.no_long:
+        st2 = ConfigStep(torch, dsa, W, LONG_ID, device)
+        for _ in range(args.warmup):
+            st2.run()
+        torch.cuda.synchronize()
+        work2 = st2.work()
+        steps2 = max(3, args.steps // 2)
+        if dist:
+            dist.barrier()
+        l_s, l_parts = time_steps(torch, st2, steps2, flush, stream)
+        l_s = max_over_ranks(l_s, dist, device)
+        q2 = st2.queries() * ws
+        mla2 = work2["mla_flop"] / (l_parts["mla"] / steps2) / 1e12
+        idx2 = work2["indexer_flop"] / (l_parts["indexer_topk"] / steps2) / 1e12
+        long_line = {
+            "workload": "long: 1 request of 32,768 tokens, sp=8, all 8 shards back to back "
+                        "(4,096 queries each)",
+            "value": round(q2 * steps2 / l_s, 2), "unit": "tokens/s", "steps": steps2,
+            "ms_per_step": round(l_s * 1e3 / steps2, 4),
+            "ms_split_rerange": round(l_parts["split_rerange"] * 1e3 / steps2, 4),
+            "ms_indexer_topk": round(l_parts["indexer_topk"] * 1e3 / steps2, 4),
+            "ms_mla": round(l_parts["mla"] * 1e3 / steps2, 4),
+            "mla_tflops": round(mla2, 1), "mla_frac": round(mla2 / pk["bf16"], 4),
+            "mla_frac_of_nominal": round(mla2 / NOMINAL["bf16"], 4),
+            "indexer_topk_tflops": round(idx2, 1), "indexer_topk_frac": round(idx2 / pk["bf16"], 4),
+            "indexer_topk_frac_of_nominal": round(idx2 / NOMINAL["bf16"], 4)}
+        del st2
+        torch.cuda.empty_cache()
+
+    # ---- end to end through host buffers, pipelined shard by shard ----
+    st.host()
+    n_units = len(st.ranks)
+    e2e_steps = max(2, min(args.e2e_steps, args.steps))
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     s_in, s_run, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device), torch.cuda.Stream(device)
-    mk = lambda: torch.cuda.Event()
-    ev_in, ev_run, ev_out = ([mk() for _ in range(e2e_steps)] for _ in range(3))
+    total_units = e2e_steps * n_units
+    ev_in, ev_run, ev_out = ([torch.cuda.Event() for _ in range(total_units)] for _ in range(3))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s_in)
     s_run.wait_event(e0)
     s_out.wait_event(e0)
-    for i in range(e2e_steps):
-        b = i % 2
+    for i in range(total_units):
+        step, r = divmod(i, n_units)
+        r = st.ranks[r]
+        b, sb = i % 2, step % 2
+        n = st.n_r[r]
         with torch.cuda.stream(s_in):
             if i >= 2:
-                s_in.wait_event(ev_run[i - 2])       # step i - 2 is done reading input set b
-            st.upload(b)
+                s_in.wait_event(ev_run[i - 2])       # unit i - 2 is done reading set b
+            if r == st.ranks[0]:                     # the step's shared inputs (set sb)
+                for k, v in st.h_shared.items():
+                    st.d_shared[sb][k].copy_(v, non_blocking=True)
+            for k, v in st.h_inp[r].items():
+                st.d_inp[b][k][:n].copy_(v, non_blocking=True)
             ev_in[i].record(s_in)
         with torch.cuda.stream(s_run):
             s_run.wait_event(ev_in[i])
             if i >= 2:
-                s_run.wait_event(ev_out[i - 2])      # o of step i - 2 has been read back
-            st.run(b=b)
+                s_run.wait_event(ev_out[i - 2])      # o of unit i - 2 has been read back
+            d = st.d_inp[b]
+            st.run_shard(r, inp={k: v[:n] for k, v in d.items()}, shared=st.d_shared[sb],
+                         o=st.d_o[b][:n])
             ev_run[i].record(s_run)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_run[i])
-            st.h_o[b].copy_(st.o_sets[b], non_blocking=True)
+            st.h_o[r].copy_(st.d_o[b][:n], non_blocking=True)
             ev_out[i].record(s_out)
     e1.record(s_out)
     torch.cuda.synchronize()
@@ -354,37 +477,70 @@ def gpu_arm(args):
         if dist:
             dist.destroy_process_group()
         return
-    pk = peaks()
-    queries = st.n_r * ws
+    queries = st.queries() * ws
     value = queries * args.steps / dev_s
-    mla_avg_s = float(np.mean(mla_ms)) / 1e3
-    achieved = mla_flops / mla_avg_s / 1e12
-    cpu = cpu_baseline(sample_queries=args.cpu_baseline_queries) if not args.no_cpu_baseline else None
+    mla_s = parts["mla"] / args.steps
+    idx_s = parts["indexer_topk"] / args.steps
+    cp_s = parts["split_rerange"] / args.steps
+    mla_ach = work["mla_flop"] / mla_s / 1e12
+    idx_ach = work["indexer_flop"] / idx_s / 1e12
+    cp_ach = work["copy_bytes"] / cp_s / 1e9
+    mla_tr = profiled_traffic("sparse_mla_pair_kernel")
+    traffic = None
+    if mla_tr is not None:    # DRAM bytes per selected pair from a capture, scaled to a launch
+        traffic = int(mla_tr["dram_bytes_per_unit"] * work["selected_pairs"] / len(st.ranks))
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.cpu_baseline_queries)
+    wl = st.wl
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dev_s * 1e3 / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded bf16 N(0,1) queries/keys/latents; no weights needed)",
-        "config": {"workload": "varlen {8000,800,5,3000} tokens, sp=8, shard rank 3 (+i per GPU): "
-                               "1476 queries, indexer 64x128 top-2048, MLA 128 heads 576/512",
-                   "queries_per_gpu": st.n_r, "kv_tokens": st.N, "topk": st.wl.topk,
+        "config": {"workload": "many_req: 32 requests, lengths U[128,4096] (seed 0, N=71,014), "
+                               "sp=4, all 4 shards back to back (71,014 queries); indexer 64x128 "
+                               "top-2048; MLA 128 heads 576/512",
+                   "queries_per_gpu": st.queries(), "kv_tokens": st.N, "topk": wl.topk,
+                   "shard_queries": [st.n_r[r] for r in st.ranks],
                    "l2": "flushed between timed steps (256 MB write)",
-                   "step": "split+gather, 2x rerange, indexer scores, top-k, sparse MLA"},
-        "roofline": {"bound": "tensor", "kernel": "sparse_mla_pair_kernel",
-                     "achieved": round(achieved, 1), "peak": pk["bf16"], "unit": "TFLOP/s",
-                     "frac": round(achieved / pk["bf16"], 4),
-                     "traffic": profiled_traffic("mla.cu", "sparse_mla_pair_varlen_rank3.md"),
-                     "peak_source": f"{pk['source']} bf16 burst (MEASURED_PEAKS.json)",
-                     "algorithmic_flop_per_launch": mla_flops},
-        "indexer_topk": {"algorithmic_flop_per_step": idx_flops},
+                   "step": "per shard: split+gather, 2x rerange, indexer scores, top-k, sparse MLA",
+                   "multi_gpu": "independent replicas of the whole batch (no collective)"},
+        "roofline": roofline_obj(
+            "sparse_mla_pair_kernel", "tensor", mla_ach, pk["bf16"], "TFLOP/s", NOMINAL["bf16"],
+            traffic,
+            {"peak_source": f"{pk['source']} bf16 burst (MEASURED_PEAKS.json)",
+             "algorithmic_flop_per_launch": work["mla_flop"] / len(st.ranks),
+             "unit_of_work": "selected (query, key) pair: 2*128*(576+512) = 278,528 flop",
+             "launches_per_step": len(st.ranks),
+             "timing": "CUDA events around each MLA call (schedule kernel + MLA) on the launch "
+                       "stream, mean over the timed steps",
+             "traffic_note": None if traffic is None else
+             f"ncu DRAM bytes per selected pair x pairs per launch ({mla_tr['workload']})"}),
+        "roofline_indexer": roofline_obj(
+            "indexer_kernel<64,128> + topk_kernel", "tensor", idx_ach, pk["bf16"], "TFLOP/s",
+            NOMINAL["bf16"], None,
+            {"algorithmic_flop_per_step": work["indexer_flop"],
+             "unit_of_work": "causal (query, key) pair: 2*64*128 = 16,384 flop",
+             "timing": "CUDA events around each indexer+top-k call (plan, indexer, top-k)"}),
+        "roofline_split_rerange": roofline_obj(
+            "split_kernel + copy_rows_v16_kernel", "hbm", cp_ach, pk["hbm"], "GB/s",
+            NOMINAL["hbm"], None,
+            {"algorithmic_bytes_per_step": work["copy_bytes"],
+             "unit_of_work": "row moved: 2 x row bytes (read + write)"}),
+        "ms_split_rerange": round(cp_s * 1e3, 4), "ms_indexer_topk": round(idx_s * 1e3, 4),
+        "ms_mla": round(mla_s * 1e3, 4),
         "e2e": {"value": round(queries * e2e_steps / e2e_s, 2), "unit": "tokens/s",
-                "h2d_bytes_per_step": st.h2d_bytes(),
-                "d2h_bytes_per_step": st.o.numel() * st.o.element_size()},
+                "steps": e2e_steps, "h2d_bytes_per_step": st.h2d_bytes(),
+                "d2h_bytes_per_step": st.d2h_bytes(),
+                "how": "pinned host inputs uploaded and o read back every step, pipelined per "
+                       "shard over 2 buffer sets and 3 streams"},
         "gpu_launches": st.launches_per_step * args.steps,
         "clocks": clk.summary(),
         "device_errors": errors,
-        "wall_s_timed_region": round(wall, 4),
+        "wall_s_timed_region": round(t_end - t_wall, 4),
+        "config_long": long_line,
         "cpu_baseline": cpu,
         "shard_balance": shard_balance(torch, dsa, W, device),
     }
@@ -405,30 +561,48 @@ def _oracle_step(W, wl, sh, sel):
 
 
 def _oracle_inputs(n_sample):
+    """fp64 inputs of a bounded sample of the many-request batch: n_sample queries spread
+    evenly over every shard (all requests, short and long histories), with the whole logical KV.
+    Values come from the same seeded generators as the GPU arm (on the GPU when there is one, so
+    the sampled rows are the very values the GPU path consumes)."""
+    import torch
     import workloads as W
     from oracle import split as osplit
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
     wl = W.WORKLOADS[WORKLOAD_ID]
     cu = W.cu_seqlens(wl.lengths)
-    meta = osplit.round_robin_split(cu, wl.sp, BASE_RANK)
-    n_r = len(meta["pos"])
-    idx = W.indexer_inputs(wl, n_r, int(cu[-1]), BASE_RANK)
-    mi = W.mla_inputs(wl, n_r, int(cu[-1]), BASE_RANK)
-    # a bounded sample spread over the shard (every request, short and long histories)
-    sel = np.unique(np.linspace(0, n_r - 1, n_sample).round().astype(np.int64))
-    sh = {"cu": cu, "pos": meta["pos"], "bid": meta["bid"],
-          "q_idx": idx.q_idx.float().numpy().astype(np.float64)[sel],
-          "w": idx.w.numpy().astype(np.float64)[sel],
-          "k_idx": idx.k_idx.float().numpy().astype(np.float64),
-          "q": mi.q[sel].float().numpy().astype(np.float64),
-          "c": mi.c.float().numpy().astype(np.float64)}
-    sh["pos"], sh["bid"] = sh["pos"][sel], sh["bid"][sel]
-    return W, wl, sh, n_r
+    n = int(cu[-1])
+    f64 = lambda t: t.float().cpu().numpy().astype(np.float64)
+    k_all = W.indexer_inputs(wl, 1, n, 0, device=dev).k_idx
+    c_all = W.mla_inputs(wl, 1, n, 0, device=dev).c
+    parts = {"q_idx": [], "w": [], "q": [], "pos": [], "bid": []}
+    per = max(1, n_sample // len(wl.ranks))
+    n_total = 0
+    for r in wl.ranks:
+        meta = osplit.round_robin_split(cu, wl.sp, r)
+        n_r = len(meta["pos"])
+        n_total += n_r
+        sel = np.unique(np.linspace(0, n_r - 1, per).round().astype(np.int64))
+        idx = W.indexer_inputs(wl, n_r, 1, r, device=dev)
+        mi = W.mla_inputs(wl, n_r, 1, r, device=dev)
+        st = torch.as_tensor(sel, device=dev)
+        parts["q_idx"].append(f64(idx.q_idx[st]))
+        parts["w"].append(f64(idx.w[st]))
+        parts["q"].append(f64(mi.q[st]))
+        parts["pos"].append(meta["pos"][sel])
+        parts["bid"].append(meta["bid"][sel])
+        del idx, mi
+    sh = {k: np.concatenate(v) for k, v in parts.items()}
+    sh["cu"] = cu
+    sh["k_idx"] = f64(k_all)
+    sh["c"] = f64(c_all)
+    return W, wl, sh, n_total
 
 
-def cpu_baseline(sample_queries=12, min_seconds=10.0, max_passes=6):
+def cpu_baseline(sample_queries=1024, min_seconds=10.0, max_passes=6):
     """Passes of the oracle over the sample until at least `min_seconds` of CPU work (bounded
     by `max_passes`), so the figure rests on 10-30 s of work without stretching the bench."""
-    W, wl, sh, n_r = _oracle_inputs(sample_queries)
+    W, wl, sh, n_total = _oracle_inputs(sample_queries)
     sel = np.arange(len(sh["pos"]))
     steps = 0
     t0 = time.perf_counter()
@@ -439,9 +613,9 @@ def cpu_baseline(sample_queries=12, min_seconds=10.0, max_passes=6):
     cores = _blas_threads()
     return {"value": round(len(sel) * steps / dt, 4), "unit": "tokens/s", "cores": cores,
             "kind": "oracle",
-            "sample": f"{len(sel)} of the {n_r} rank-3 queries (evenly spaced, all requests), "
-                      f"fp64 NumPy indexer + full-sort top-k + sparse MLA, {steps} pass(es), "
-                      f"{dt:.1f} s"}
+            "sample": f"{len(sel)} of the {n_total} queries of the many-request batch (evenly "
+                      f"spaced over all 4 shards), fp64 NumPy indexer + full-sort top-k + sparse "
+                      f"MLA, {steps} pass(es), {dt:.1f} s"}
 
 
 def _blas_threads():
@@ -459,7 +633,7 @@ def reference_arm(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return
-    W, wl, sh, n_r = _oracle_inputs(args.cpu_sample)
+    W, wl, sh, n_total = _oracle_inputs(args.cpu_sample)
     sel = np.arange(len(sh["pos"]))
     for _ in range(args.warmup):
         _oracle_step(W, wl, sh, sel[:1])
@@ -474,11 +648,12 @@ def reference_arm(args):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3 / args.steps, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "varlen {8000,800,5,3000} tokens, sp=8, shard rank 3: a bounded "
-                               f"sample of {len(sel)} of its {n_r} queries per step"},
+        "config": {"workload": "many_req: 32 requests, lengths U[128,4096] (seed 0, N=71,014), "
+                               "sp=4, all 4 shards: a bounded sample of "
+                               f"{len(sel)} of its {n_total} queries per step"},
         "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores,
                          "kind": "oracle",
-                         "sample": f"{len(sel)} evenly spaced queries of the rank-3 shard per step"},
+                         "sample": f"{len(sel)} queries per step, evenly spaced over the 4 shards"},
         "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -731,22 +906,90 @@ def _oracle_sample_time(W, wl, si, idx, mi, n_sample):
     return len(sel), time.perf_counter() - t0
 
 
+def profile_run(args):
+    """Small, fixed launch sequences for ncu (no timing, no flush, nothing else on the GPU):
+    --profile-steps K: the default workload's whole step, 1 untimed step then K more (32
+      launches per step: the launch list);
+    --profile-case: one shard of the many-request batch (rank 1) cut to an evenly spaced
+      subset of 2,048 of its queries (every request, short and long histories; about 0.7 GB on
+      the device), indexer + top-k and balanced sparse MLA run twice (one kernel capture)."""
+    import torch
+    import __graft_entry__ as ge
+    ge.build()
+    import deepseek_v3_sparse_round_gb300 as dsa
+    import workloads as W
+    dev = torch.device("cuda", 0)
+    if args.profile_steps:
+        st = ConfigStep(torch, dsa, W, WORKLOAD_ID, dev)
+        torch.cuda.synchronize()
+        for _ in range(1 + args.profile_steps):
+            st.run()
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_steps": args.profile_steps, "launches_per_step":
+                          st.launches_per_step, "device_errors": dsa.dsa_read_device_errors()}))
+        return
+    wl = W.WORKLOADS[WORKLOAD_ID]
+    r = 1
+    cu_np = W.cu_seqlens(wl.lengths)
+    n_tok = int(cu_np[-1])
+    n_r = dsa.dsa_rr_shard_len(n_tok, wl.sp, r)
+    cu = torch.as_tensor(cu_np, device=dev)
+    e = lambda *sh, dt=torch.int32: torch.empty(*sh, dtype=dt, device=dev)
+    pos, bid = e(n_r), e(n_r)
+    dsa.dsa_rr_split_metadata(cu, n_tok, wl.sp, r, e(len(cu_np)), pos, bid)
+    sel = torch.as_tensor(np.unique(np.linspace(0, n_r - 1, 2048).round().astype(np.int64)), device=dev)
+    idx = W.indexer_inputs(wl, n_r, n_tok, r, device=dev)
+    mi = W.mla_inputs(wl, n_r, n_tok, r, device=dev)
+    q_idx, w, q = idx.q_idx[sel].contiguous(), idx.w[sel].contiguous(), mi.q[sel].contiguous()
+    k_idx, c = idx.k_idx, mi.c
+    del idx, mi
+    pos, bid = pos[sel].contiguous(), bid[sel].contiguous()
+    n = int(sel.numel())
+    torch.cuda.empty_cache()
+    max_ctx = int(max(wl.lengths))
+    ws = e(dsa.dsa_indexer_topk_workspace_size(n, max_ctx, wl.topk), dt=torch.uint8)
+    topk = e(n, wl.topk)
+    o = e(n, wl.H, wl.dv, dt=torch.bfloat16)
+    lse = e(n, wl.H, dt=torch.float32)
+    mws = e(dsa.dsa_sparse_mla_workspace_size(n), dt=torch.uint8)
+    for _ in range(2):
+        dsa.dsa_indexer_topk(q_idx, w, k_idx, cu, len(wl.lengths), pos, bid, wl.topk, max_ctx,
+                             topk, ws)
+        dsa.dsa_sparse_mla_balanced(q, c, cu, len(wl.lengths), bid, pos, topk, wl.scale, o, mws,
+                                    lse=lse)
+    torch.cuda.synchronize()
+    p = pos.cpu().numpy().astype(np.int64)
+    print(json.dumps({"profile_case": "many_req rank 1, 2048 evenly spaced queries",
+                      "queries": n, "causal_pairs": int(np.sum(p + 1)),
+                      "selected_pairs": int(np.sum(np.minimum(p + 1, wl.topk))),
+                      "device_errors": dsa.dsa_read_device_errors()}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--cpu-sample", type=int, default=96, help="queries per reference-arm step")
-    ap.add_argument("--cpu-baseline-queries", type=int, default=1476)
+    ap.add_argument("--cpu-sample", type=int, default=128, help="queries per reference-arm step")
+    ap.add_argument("--cpu-baseline-queries", type=int, default=1024)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-long", action="store_true", help="skip the long-prompt line")
+    ap.add_argument("--e2e-steps", type=int, default=4)
     ap.add_argument("--next-rows", nargs="?", const="all", default=None,
                     help="measure the widened rows (paged rerange, decode split) and exit")
     ap.add_argument("--configs", action="store_true",
                     help="indexer + top-k + sparse MLA on every workload config, then exit")
     ap.add_argument("--with-oracle", action="store_true",
                     help="with --configs: also time the fp64 oracle on a sample of each config")
+    ap.add_argument("--profile-steps", type=int, default=0,
+                    help="ncu launch list: 1 + K default-workload steps, nothing else, then exit")
+    ap.add_argument("--profile-case", action="store_true",
+                    help="ncu capture: one 2,048-query cut of a many-request shard, then exit")
     args = ap.parse_args()
+    if args.profile_steps or args.profile_case:
+        profile_run(args)
+        return
     if args.configs:
         config_rows(args)
         return

@@ -20,6 +20,7 @@ __all__ = [
     "dsa_indexer_topk_workspace_size", "dsa_score_row_stride", "dsa_indexer_scores",
     "dsa_topk_select", "dsa_indexer_topk", "dsa_indexer_topk_noalloc", "dsa_sparse_mla",
     "dsa_sparse_mla_workspace_size", "dsa_sparse_mla_balanced", "dsa_read_device_errors",
+    "dsa_rr_cache_local_paged", "dsa_selftest_bounded_wait",
     "DEVERR_TIMEOUT", "DEVERR_BAD_INDEX", "DEVERR_BAD_LENGTH",
 ]
 
@@ -62,6 +63,16 @@ def _dev(t, dtype=None, name="tensor"):
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+def _shape(t, want, name):
+    """Raise ValueError unless t's shape matches `want` (None entries match any size). The C ABI
+    takes bare pointers and cannot check sizes, so the binding does, before any launch."""
+    if t is None:
+        return
+    got = tuple(t.shape)
+    if len(got) != len(want) or any(w is not None and g != w for g, w in zip(got, want)):
+        raise ValueError(f"{name} has shape {got}, expected {tuple('*' if w is None else w for w in want)}")
+
+
 def _row_bytes(t):
     return math.prod(t.shape[1:]) * t.element_size()
 
@@ -94,15 +105,29 @@ def dsa_read_device_errors() -> int:
     return int(flags.value)
 
 
+def dsa_selftest_bounded_wait(limit_cycles: int, stream=None):
+    """One kernel waits, with the library's bounded wait, on a phase nothing completes; after
+    limit_cycles the wait gives up and sets DEVERR_TIMEOUT | 0xEE (read it with
+    dsa_read_device_errors)."""
+    _check(_lib().dsa_selftest_bounded_wait(int(limit_cycles), _stream(stream)))
+
+
 def dsa_rr_split_metadata(cu, n_tokens, sp, rank, cu_shard, pos, bid, gidx=None,
                           src_rows=None, dst_rows=None, stream=None):
     """cu int32 [B+1] -> cu_shard [B+1], pos/bid/gidx [n_r]; optional dst_rows = src_rows[g_t]."""
     for name, t in (("cu", cu), ("cu_shard", cu_shard), ("pos", pos), ("bid", bid), ("gidx", gidx)):
         _dev(t, torch.int32, name)
+    n_r = max(0, int(_lib().dsa_rr_shard_len(n_tokens, sp, rank)))
+    _shape(cu_shard, (cu.numel(),), "cu_shard")
+    for name, t in (("pos", pos), ("bid", bid), ("gidx", gidx)):
+        _shape(t, (n_r,), name)
     row_bytes = 0
     if src_rows is not None:
         _dev(src_rows, None, "src_rows")
         _dev(dst_rows, src_rows.dtype, "dst_rows")
+        if src_rows.shape[0] < n_tokens or dst_rows.shape[0] < n_r or \
+                tuple(dst_rows.shape[1:]) != tuple(src_rows.shape[1:]):
+            raise ValueError("src_rows needs n_tokens rows and dst_rows n_r rows of the same width")
         row_bytes = _row_bytes(src_rows)
     _check(_lib().dsa_rr_split_metadata(_ptr(cu), cu.numel() - 1, n_tokens, sp, rank,
                                         _ptr(cu_shard), _ptr(pos), _ptr(bid), _ptr(gidx),
@@ -116,10 +141,18 @@ def dsa_rr_split_decode_metadata(cu_new, pos_base, n_tokens, sp, rank, cu_shard,
     for name, t in (("cu_new", cu_new), ("pos_base", pos_base), ("cu_shard", cu_shard),
                     ("pos", pos), ("bid", bid), ("gidx", gidx)):
         _dev(t, torch.int32, name)
+    n_r = max(0, int(_lib().dsa_rr_shard_len(n_tokens, sp, rank)))
+    _shape(cu_shard, (cu_new.numel(),), "cu_shard")
+    _shape(pos_base, (cu_new.numel() - 1,), "pos_base")
+    for name, t in (("pos", pos), ("bid", bid), ("gidx", gidx)):
+        _shape(t, (n_r,), name)
     row_bytes = 0
     if src_rows is not None:
         _dev(src_rows, None, "src_rows")
         _dev(dst_rows, src_rows.dtype, "dst_rows")
+        if src_rows.shape[0] < n_tokens or dst_rows.shape[0] < n_r or \
+                tuple(dst_rows.shape[1:]) != tuple(src_rows.shape[1:]):
+            raise ValueError("src_rows needs n_tokens rows and dst_rows n_r rows of the same width")
         row_bytes = _row_bytes(src_rows)
     _check(_lib().dsa_rr_split_decode_metadata(
         _ptr(cu_new), _ptr(pos_base), cu_new.numel() - 1, n_tokens, sp, rank, _ptr(cu_shard),
@@ -131,6 +164,11 @@ def dsa_rr_rerange(gathered, out, n_tokens, sp, rank_stride_rows=0, stream=None)
     """out[g] = gathered[off[g % sp] + g // sp] (padded blocks if rank_stride_rows > 0)."""
     _dev(gathered, None, "gathered")
     _dev(out, gathered.dtype, "out")
+    need = sp * rank_stride_rows if rank_stride_rows > 0 else n_tokens
+    if out.shape[0] < n_tokens or gathered.shape[0] < need or \
+            tuple(out.shape[1:]) != tuple(gathered.shape[1:]):
+        raise ValueError(f"rerange needs gathered with >= {need} rows and out with >= {n_tokens} "
+                         "rows of the same width")
     row_bytes = _row_bytes(out)
     _check(_lib().dsa_rr_rerange(_ptr(gathered), _ptr(out), n_tokens, sp, rank_stride_rows,
                                  row_bytes, _stream(stream)))
@@ -143,9 +181,30 @@ def dsa_rr_rerange_paged(gathered, pool, n_tokens, sp, cu, block_table, rank_str
     _dev(gathered, None, "gathered")
     _dev(pool, gathered.dtype, "pool")
     _dev(cu, torch.int32, "cu"); _dev(block_table, torch.int32, "block_table")
+    need = sp * rank_stride_rows if rank_stride_rows > 0 else n_tokens
+    if gathered.shape[0] < need or tuple(pool.shape[1:]) != tuple(gathered.shape[1:]):
+        raise ValueError(f"gathered needs >= {need} rows of the pool's width")
+    _shape(block_table, (cu.numel() - 1, None), "block_table")
     row_bytes = _row_bytes(pool)
     _check(_lib().dsa_rr_rerange_paged(
         _ptr(gathered), _ptr(pool), pool.shape[0], n_tokens, sp, rank_stride_rows, row_bytes,
+        _ptr(cu), cu.numel() - 1, _ptr(block_table), block_table.shape[1], page_size,
+        _stream(stream)))
+
+
+def dsa_rr_cache_local_paged(local_rows, pool, n_tokens, sp, rank, cu, block_table, page_size=64,
+                             stream=None):
+    """This rank's own tokens only: pool[page row of (b, j)] = local_rows[t], j = t - cu_shard[b]
+    (the token's index among request b's tokens on this rank); n_tokens = cu[-1]."""
+    _dev(local_rows, None, "local_rows")
+    _dev(pool, local_rows.dtype, "pool")
+    _dev(cu, torch.int32, "cu"); _dev(block_table, torch.int32, "block_table")
+    n_r = max(0, int(_lib().dsa_rr_shard_len(n_tokens, sp, rank)))
+    if local_rows.shape[0] < n_r or tuple(pool.shape[1:]) != tuple(local_rows.shape[1:]):
+        raise ValueError(f"local_rows needs >= {n_r} rows of the pool's width")
+    _shape(block_table, (cu.numel() - 1, None), "block_table")
+    _check(_lib().dsa_rr_cache_local_paged(
+        _ptr(local_rows), _ptr(pool), pool.shape[0], n_tokens, sp, rank, _row_bytes(pool),
         _ptr(cu), cu.numel() - 1, _ptr(block_table), block_table.shape[1], page_size,
         _stream(stream)))
 
@@ -158,6 +217,8 @@ def dsa_indexer_scores(q_idx, w, k_idx, cu, n_req, pos, bid, max_ctx, scores, wo
     _dev(pos, torch.int32, "pos"); _dev(bid, torch.int32, "bid"); _dev(cu, torch.int32, "cu")
     _dev(block_table, torch.int32, "block_table")
     n_q, Hi, Di = q_idx.shape
+    _indexer_shapes(q_idx, w, pos, bid, block_table, n_req)
+    _shape(scores, (n_q, None), "scores")
     max_pages = block_table.shape[1] if block_table is not None else 0
     _check(_lib().dsa_indexer_scores(
         _ptr(q_idx), _ptr(w), _ptr(k_idx), k_idx.shape[0], _ptr(cu), n_req, _ptr(pos), _ptr(bid),
@@ -166,9 +227,19 @@ def dsa_indexer_scores(q_idx, w, k_idx, cu, n_req, pos, bid, max_ctx, scores, wo
         _stream(stream)))
 
 
+def _indexer_shapes(q_idx, w, pos, bid, block_table, n_req):
+    n_q, Hi, _ = q_idx.shape
+    _shape(w, (n_q, Hi), "w")
+    _shape(pos, (n_q,), "pos")
+    _shape(bid, (n_q,), "bid")
+    _shape(block_table, (n_req, None), "block_table")
+
+
 def dsa_topk_select(scores, pos, k, max_ctx, topk, stream=None):
     _dev(scores, torch.float32, "scores"); _dev(pos, torch.int32, "pos")
     _dev(topk, torch.int32, "topk")
+    _shape(pos, (scores.shape[0],), "pos")
+    _shape(topk, (scores.shape[0], k), "topk")
     _check(_lib().dsa_topk_select(_ptr(scores), scores.shape[1], _ptr(pos), pos.numel(), k,
                                   max_ctx, _ptr(topk), _stream(stream)))
 
@@ -181,6 +252,8 @@ def dsa_indexer_topk(q_idx, w, k_idx, cu, n_req, pos, bid, k, max_ctx, topk, wor
     _dev(pos, torch.int32, "pos"); _dev(bid, torch.int32, "bid"); _dev(cu, torch.int32, "cu")
     _dev(block_table, torch.int32, "block_table")
     n_q, Hi, Di = q_idx.shape
+    _indexer_shapes(q_idx, w, pos, bid, block_table, n_req)
+    _shape(topk, (n_q, k), "topk")
     max_pages = block_table.shape[1] if block_table is not None else 0
     _check(_lib().dsa_indexer_topk(
         _ptr(q_idx), _ptr(w), _ptr(k_idx), k_idx.shape[0], _ptr(cu), n_req, _ptr(pos), _ptr(bid),
@@ -197,6 +270,8 @@ def dsa_indexer_topk_noalloc(q_idx, w, k_idx, cu, n_req, pos, bid, k, max_ctx, t
     _dev(pos, torch.int32, "pos"); _dev(bid, torch.int32, "bid"); _dev(cu, torch.int32, "cu")
     _dev(block_table, torch.int32, "block_table")
     n_q, Hi, Di = q_idx.shape
+    _indexer_shapes(q_idx, w, pos, bid, block_table, n_req)
+    _shape(topk, (n_q, k), "topk")
     max_pages = block_table.shape[1] if block_table is not None else 0
     _check(_lib().dsa_indexer_topk_noalloc(
         _ptr(q_idx), _ptr(w), _ptr(k_idx), k_idx.shape[0], _ptr(cu), n_req, _ptr(pos), _ptr(bid),
@@ -212,11 +287,23 @@ def dsa_sparse_mla(q, c, cu, n_req, bid, topk, scale, o, lse=None, block_table=N
     _dev(lse, torch.float32, "lse"); _dev(block_table, torch.int32, "block_table")
     n_q, H, dqk = q.shape
     dv = o.shape[2]
+    _mla_shapes(q, c, o, lse, bid, None, topk, block_table, n_req)
     max_pages = block_table.shape[1] if block_table is not None else 0
     _check(_lib().dsa_sparse_mla(
         _ptr(q), _ptr(c), c.shape[0], _ptr(cu), n_req, _ptr(bid), _ptr(topk), n_q, H, dqk, dv,
         topk.shape[1], float(scale), _ptr(block_table), max_pages, page_size, _ptr(o), _ptr(lse),
         _stream(stream)))
+
+
+def _mla_shapes(q, c, o, lse, bid, pos, topk, block_table, n_req):
+    n_q, H, dqk = q.shape
+    _shape(c, (None, dqk), "c")
+    _shape(o, (n_q, H, None), "o")
+    _shape(lse, (n_q, H), "lse")
+    _shape(bid, (n_q,), "bid")
+    _shape(pos, (n_q,), "pos")
+    _shape(topk, (n_q, None), "topk")
+    _shape(block_table, (n_req, None), "block_table")
 
 
 def dsa_sparse_mla_workspace_size(n_q: int) -> int:
@@ -235,6 +322,7 @@ def dsa_sparse_mla_balanced(q, c, cu, n_req, bid, pos, topk, scale, o, workspace
     _dev(workspace, None, "workspace")
     n_q, H, dqk = q.shape
     dv = o.shape[2]
+    _mla_shapes(q, c, o, lse, bid, pos, topk, block_table, n_req)
     max_pages = block_table.shape[1] if block_table is not None else 0
     _check(_lib().dsa_sparse_mla_balanced(
         _ptr(q), _ptr(c), c.shape[0], _ptr(cu), n_req, _ptr(bid), _ptr(pos), _ptr(topk), n_q, H,

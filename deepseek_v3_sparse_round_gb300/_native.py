@@ -16,6 +16,7 @@ SIGNATURES = {
     "dsa_last_error_string": (ctypes.c_char_p, []),
     "dsa_version": (c_int, []),
     "dsa_read_device_errors": (c_int, [c_u32p]),
+    "dsa_selftest_bounded_wait": (c_int, [c_i64, c_vp]),
     "dsa_rr_shard_len": (c_i64, [c_i64, c_int, c_int]),
     "dsa_rr_split_metadata": (c_int, [c_vp, c_int, c_i64, c_int, c_int, c_vp, c_vp, c_vp, c_vp,
                                       c_vp, c_vp, c_i64, c_vp]),
@@ -24,6 +25,8 @@ SIGNATURES = {
     "dsa_rr_rerange": (c_int, [c_vp, c_vp, c_i64, c_int, c_i64, c_i64, c_vp]),
     "dsa_rr_rerange_paged": (c_int, [c_vp, c_vp, c_i64, c_i64, c_int, c_i64, c_i64, c_vp, c_int,
                                      c_vp, c_int, c_int, c_vp]),
+    "dsa_rr_cache_local_paged": (c_int, [c_vp, c_vp, c_i64, c_i64, c_int, c_int, c_i64, c_vp,
+                                         c_int, c_vp, c_int, c_int, c_vp]),
     "dsa_indexer_topk_workspace_size": (c_sz, [c_i64, c_int, c_int]),
     "dsa_score_row_stride": (c_i64, [c_int]),
     "dsa_indexer_scores": (c_int, [c_vp, c_vp, c_vp, c_i64, c_vp, c_int, c_vp, c_vp, c_i64, c_int,

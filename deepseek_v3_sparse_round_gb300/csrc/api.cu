@@ -1,5 +1,6 @@
 // extern "C" entry points declared in include/dsa_rr.h: argument checks, error text, workspace
 // sizing, and dispatch to the kernels of split.cu, topk.cu, indexer.cu and mla.cu.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -21,7 +22,10 @@ int indexer_scores(const void* q_idx, const float* w, const void* k_idx, int64_t
                    const int32_t* cu, const int32_t* pos, const int32_t* bid, int64_t n_q, int n_req,
                    int Hi, int Di, int max_ctx, const int32_t* block_table, int max_pages,
                    int page_size, float* scores, int64_t stride, void* ws, size_t ws_bytes,
-                   cudaStream_t stream);
+                   uint32_t* hist, cudaStream_t stream);
+int topk_select_hist(const float* scores, int64_t score_stride, const int32_t* pos, int64_t n_q,
+                     int k, int max_ctx, const uint32_t* hist_rows, int32_t* topk,
+                     cudaStream_t stream);
 int topk_select(const float* scores, int64_t score_stride, const int32_t* pos, int64_t n_q, int k,
                 int max_ctx, int32_t* topk, cudaStream_t stream);
 int sparse_mla(const void* q, const void* c, int64_t n_kv_rows, const int32_t* cu, int n_req,
@@ -33,6 +37,12 @@ cudaError_t split_read_errors(uint32_t* flags);
 int rerange_paged(const void* gathered, void* pool, int64_t pool_rows, int64_t n_tokens, int sp,
                   int64_t rank_stride_rows, int64_t row_bytes, const int32_t* cu, int n_req,
                   const int32_t* block_table, int max_pages, int page_size, cudaStream_t stream);
+int cache_local_paged(const void* local_rows, void* pool, int64_t pool_rows, int64_t n_tokens,
+                      int sp, int rank, int64_t row_bytes, const int32_t* cu, int n_req,
+                      const int32_t* block_table, int max_pages, int page_size,
+                      cudaStream_t stream);
+int selftest_bounded_wait(long long limit_cycles, cudaStream_t stream);
+cudaError_t selftest_read_errors(uint32_t* flags);
 cudaError_t topk_read_errors(uint32_t* flags);
 cudaError_t indexer_read_errors(uint32_t* flags);
 cudaError_t mla_read_errors(uint32_t* flags);
@@ -62,15 +72,36 @@ int cuda_fail(cudaError_t e, const char* what) {
   return DSA_ERR_CUDA;
 }
 
+// SM count of the current device, looked up once per device ordinal (grids and persistent
+// pairs are sized from it). Concurrent first calls may both query; they store the same value.
 int num_sms_cached() {
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     return 148;
+  if (dev >= 0 && dev < kMaxDevices) cache[dev].store(sms, std::memory_order_relaxed);
   return sms;
 }
 
 static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// dsa_indexer_topk fuses the two steps (the indexer histograms the first radix digit of every
+// score it writes; the top-k reads each row once) when a row can be longer than this: shorter
+// rows are selected from a shared-memory copy of the row at least as fast, without the
+// histogram's memset and atomics.
+constexpr int kFuseMinCtx = 8192;
+constexpr size_t kHistRowBytes = 2048 * sizeof(uint32_t);
+
+static size_t hist_bytes(int64_t n_q, int max_ctx) {
+  return max_ctx > kFuseMinCtx ? static_cast<size_t>(n_q) * kHistRowBytes : 0;
+}
 
 }  // namespace dsa
 
@@ -90,7 +121,15 @@ DSA_EXPORT int dsa_read_device_errors(uint32_t* flags) {
   DSA_CHECK_CUDA(dsa::topk_read_errors(flags));
   DSA_CHECK_CUDA(dsa::indexer_read_errors(flags));
   DSA_CHECK_CUDA(dsa::mla_read_errors(flags));
+  DSA_CHECK_CUDA(dsa::selftest_read_errors(flags));
   return DSA_OK;
+}
+
+DSA_EXPORT int dsa_selftest_bounded_wait(int64_t limit_cycles, dsa_stream_t stream) {
+  if (limit_cycles < 1 || limit_cycles > (1ll << 40))
+    return dsa::fail(DSA_ERR_INVALID, "selftest: limit_cycles must be in [1, 2^40]");
+  return dsa::selftest_bounded_wait(static_cast<long long>(limit_cycles),
+                                    reinterpret_cast<cudaStream_t>(stream));
 }
 
 DSA_EXPORT int64_t dsa_rr_shard_len(int64_t n_tokens, int sp, int rank) {
@@ -132,6 +171,15 @@ DSA_EXPORT int dsa_rr_rerange_paged(const void* gathered, void* pool, int64_t po
                             reinterpret_cast<cudaStream_t>(stream));
 }
 
+DSA_EXPORT int dsa_rr_cache_local_paged(const void* local_rows, void* pool, int64_t pool_rows,
+                                        int64_t n_tokens, int sp, int rank, int64_t row_bytes,
+                                        const int32_t* cu, int n_req, const int32_t* block_table,
+                                        int max_pages, int page_size, dsa_stream_t stream) {
+  return dsa::cache_local_paged(local_rows, pool, pool_rows, n_tokens, sp, rank, row_bytes, cu,
+                                n_req, block_table, max_pages, page_size,
+                                reinterpret_cast<cudaStream_t>(stream));
+}
+
 DSA_EXPORT int64_t dsa_score_row_stride(int max_ctx) {
   if (max_ctx < 1) return 0;
   return static_cast<int64_t>((max_ctx + 3) / 4) * 4;
@@ -143,7 +191,8 @@ DSA_EXPORT size_t dsa_indexer_topk_workspace_size(int64_t n_q, int max_ctx, int 
   const size_t plan = dsa::indexer_plan_bytes(n_q);
   const size_t scores = static_cast<size_t>(n_q) * static_cast<size_t>(dsa_score_row_stride(max_ctx)) *
                         sizeof(float);
-  return dsa::round_up(plan, 256) + dsa::round_up(scores, 256);
+  return dsa::round_up(plan, 256) + dsa::round_up(scores, 256) +
+         dsa::round_up(dsa::hist_bytes(n_q, max_ctx), 256);
 }
 
 DSA_EXPORT int dsa_indexer_scores(const void* q_idx, const float* w, const void* k_idx, int64_t n_kv_rows,
@@ -156,7 +205,8 @@ DSA_EXPORT int dsa_indexer_scores(const void* q_idx, const float* w, const void*
     return dsa::fail(DSA_ERR_INVALID, "indexer: score rows must be 16-byte aligned");
   return dsa::indexer_scores(q_idx, w, k_idx, n_kv_rows, cu, pos, bid, n_q, n_req, Hi, Di,
                              max_ctx, block_table, max_pages, page_size, scores, score_stride,
-                             workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+                             workspace, workspace_bytes, nullptr,
+                             reinterpret_cast<cudaStream_t>(stream));
 }
 
 DSA_EXPORT int dsa_topk_select(const float* scores, int64_t score_stride, const int32_t* pos, int64_t n_q,
@@ -182,11 +232,21 @@ DSA_EXPORT int dsa_indexer_topk(const void* q_idx, const float* w, const void* k
   const size_t plan = dsa::round_up(dsa::indexer_plan_bytes(n_q), 256);
   float* scores = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan);
   const int64_t stride = dsa_score_row_stride(max_ctx);
-  int rc = dsa_indexer_scores(q_idx, w, k_idx, n_kv_rows, cu, n_req, pos, bid, n_q, Hi, Di,
-                              max_ctx, block_table, max_pages, page_size, scores, stride,
-                              workspace, plan, stream);
+  const size_t score_bytes =
+      dsa::round_up(static_cast<size_t>(n_q) * static_cast<size_t>(stride) * sizeof(float), 256);
+  uint32_t* hist = dsa::hist_bytes(n_q, max_ctx) > 0
+                       ? reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + plan +
+                                                     score_bytes)
+                       : nullptr;
+  if (n_req < 1) return dsa::fail(DSA_ERR_INVALID, "indexer: n_req must be >= 1");
+  int rc = dsa::indexer_scores(q_idx, w, k_idx, n_kv_rows, cu, pos, bid, n_q, n_req, Hi, Di,
+                               max_ctx, block_table, max_pages, page_size, scores, stride,
+                               workspace, plan, hist, reinterpret_cast<cudaStream_t>(stream));
   if (rc) return rc;
-  return dsa_topk_select(scores, stride, pos, n_q, k, max_ctx, topk, stream);
+  if (hist == nullptr) return dsa_topk_select(scores, stride, pos, n_q, k, max_ctx, topk, stream);
+  if (!topk) return dsa::fail(DSA_ERR_INVALID, "topk: null pointer");
+  return dsa::topk_select_hist(scores, stride, pos, n_q, k, max_ctx, hist, topk,
+                               reinterpret_cast<cudaStream_t>(stream));
 }
 
 DSA_EXPORT int dsa_sparse_mla(const void* q, const void* c, int64_t n_kv_rows, const int32_t* cu, int n_req,

@@ -29,6 +29,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "keys.cuh"
 #include "ptx.cuh"
 #include "status.cuh"
 #include "tmap.cuh"
@@ -230,7 +231,7 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                const float* __restrict__ w, const int32_t* __restrict__ pos, KeyRows kr,
                const Plan* __restrict__ plan, const int4* __restrict__ groups,
                const int32_t* __restrict__ unit_start, float* __restrict__ scores,
-               int64_t stride, int max_ctx, int n_q) {
+               int64_t stride, int max_ctx, int n_q, uint32_t* __restrict__ hist) {
   using S = Shape<HI, DI>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -422,6 +423,18 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           if (q < nq && s <= spos[q] && s < max_ctx)
             scores[static_cast<int64_t>(tq0 + q) * stride + s] = acc[q];
         }
+        if (hist != nullptr) {
+          // First-digit histogram of every written score (for the top-k that follows): the
+          // warp's lanes with the same (query, digit) add their count with one atomic.
+#pragma unroll
+          for (int q = 0; q < S::kQPA; ++q) {
+            const bool v = q < nq && s <= spos[q] && s < max_ctx;
+            const uint32_t d = v ? first_digit(order_key(acc[q])) : 0xFFFFFFFFu;
+            const uint32_t peers = __match_any_sync(0xffffffffu, d);
+            if (v && static_cast<int>(lane) == __ffs(peers) - 1)
+              atomicAdd(hist + static_cast<int64_t>(tq0 + q) * kHistBins + d, __popc(peers));
+          }
+        }
       }
       mbar_arrive(bar(kWEmpty + h));                  // done reading this unit's w / pos
       if (!ok) break;
@@ -439,8 +452,12 @@ template <int HI, int DI>
 int launch_indexer(const void* q_idx, const float* w, const void* k_idx, int64_t n_kv_rows,
                    const int32_t* pos, const int32_t* bid, int64_t n_q, int n_req, int max_ctx,
                    const KeyRows& kr, float* scores, int64_t stride, Plan* plan, int4* groups,
-                   int32_t* unit_start, int32_t* t0_list, int n_ctas, cudaStream_t stream) {
+                   int32_t* unit_start, int32_t* t0_list, int n_ctas, uint32_t* hist,
+                   cudaStream_t stream) {
   using S = Shape<HI, DI>;
+  if (hist != nullptr)
+    DSA_CHECK_CUDA(cudaMemsetAsync(hist, 0, static_cast<size_t>(n_q) * kHistBins * sizeof(uint32_t),
+                                   stream));
   const int n_req_eff = kr.block_table ? n_req : n_req;
   indexer_plan_kernel<<<1, kPlanThreads, 0, stream>>>(pos, bid, static_cast<int>(n_q), n_req_eff,
                                                       max_ctx, S::kGQ, n_ctas, plan, groups,
@@ -457,7 +474,7 @@ int launch_indexer(const void* q_idx, const float* w, const void* k_idx, int64_t
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmem));
   indexer_kernel<HI, DI><<<n_ctas, S::kThreads, S::kSmem, stream>>>(
       tk, tq, w, pos, kr, plan, groups, unit_start, scores, stride, max_ctx,
-      static_cast<int>(n_q));
+      static_cast<int>(n_q), hist);
   DSA_CHECK_CUDA(cudaGetLastError());
   return DSA_OK;
 }
@@ -470,7 +487,7 @@ int indexer_scores(const void* q_idx, const float* w, const void* k_idx, int64_t
                    const int32_t* cu, const int32_t* pos, const int32_t* bid, int64_t n_q, int n_req,
                    int Hi, int Di, int max_ctx, const int32_t* block_table, int max_pages,
                    int page_size, float* scores, int64_t stride, void* ws, size_t ws_bytes,
-                   cudaStream_t stream) {
+                   uint32_t* hist, cudaStream_t stream) {
   if (n_q < 0 || max_ctx < 1 || n_kv_rows < 0)
     return fail(DSA_ERR_INVALID, "indexer: need n_q >= 0, max_ctx >= 1, n_kv_rows >= 0");
   if (n_q == 0) return DSA_OK;
@@ -497,10 +514,11 @@ int indexer_scores(const void* q_idx, const float* w, const void* k_idx, int64_t
   if (Hi == 64 && Di == 128)
     return launch_indexer<64, 128>(q_idx, w, k_idx, n_kv_rows, pos, bid, n_q, n_req, max_ctx, kr,
                                    scores, stride, plan, groups, unit_start, t0_list, n_ctas,
-                                   stream);
+                                   hist, stream);
   if (Hi == 4 && Di == 32)
     return launch_indexer<4, 32>(q_idx, w, k_idx, n_kv_rows, pos, bid, n_q, n_req, max_ctx, kr,
-                                 scores, stride, plan, groups, unit_start, t0_list, n_ctas, stream);
+                                 scores, stride, plan, groups, unit_start, t0_list, n_ctas, hist,
+                                 stream);
   return fail(DSA_ERR_UNSUPPORTED, "indexer: (Hi, Di) = (%d, %d) not built; supported (64, 128), "
                                    "(4, 32)", Hi, Di);
 }

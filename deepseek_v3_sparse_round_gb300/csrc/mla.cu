@@ -71,11 +71,30 @@ struct KvMap {
   int max_pages;
   int n_req;
   int64_t n_rows;
+  const int32_t* pos;          // query positions (nullptr: not given)
 };
 
+// Largest top-k entry query t of request b may hold: the last position of its request
+// (contiguous), the last position its block-table row can address (paged), and, when the
+// positions are given, pos_t (a key after the query is not in its causal history).
+__device__ __forceinline__ int entry_limit(const KvMap& m, int b, int64_t t) {
+  int lim;
+  if (m.block_table == nullptr) {
+    lim = __ldg(m.cu + b + 1) - __ldg(m.cu + b) - 1;
+  } else {
+    const int64_t span = static_cast<int64_t>(m.max_pages) * kPageRows - 1;
+    lim = span < 0x7FFFFFFF ? static_cast<int>(span) : 0x7FFFFFFF;
+  }
+  if (m.pos != nullptr) lim = min(lim, __ldg(m.pos + t));
+  return lim;
+}
+
 // KV row of position s in request b, or n_rows (read as zeros) when it is not addressable.
-__device__ __forceinline__ int32_t kv_row(const KvMap& m, int b, int s, bool* bad) {
+// s < 0 is padding; s > lim (past the query or its request) is an invalid index: skipped and
+// recorded in *bad.
+__device__ __forceinline__ int32_t kv_row(const KvMap& m, int b, int s, int lim, bool* bad) {
   if (s < 0) return static_cast<int32_t>(m.n_rows);
+  if (s > lim) { *bad = true; return static_cast<int32_t>(m.n_rows); }
   int64_t r;
   if (m.block_table == nullptr) {
     r = static_cast<int64_t>(__ldg(m.cu + b)) + s;
@@ -122,12 +141,16 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16*
   // Tile validity masks and the number of tiles up to the last valid entry.
   const int32_t* trow = topk + t * k;
   const int n_tiles_max = (k + kTileKeys - 1) / kTileKeys;
+  const int b = __ldg(bid + t);
+  const bool b_ok = b >= 0 && b < kv.n_req;
+  const int lim = b_ok ? entry_limit(kv, b, t) : -1;
   if (threadIdx.x == 0) *reinterpret_cast<volatile int*>(smem + S::kOffNTiles) = 0;
   __syncthreads();
   for (int tile = static_cast<int>(warp); tile < n_tiles_max; tile += S::kThreads / 32) {
     const int j0 = tile * kTileKeys + static_cast<int>(lane), j1 = j0 + 32;
-    const bool v0 = j0 < k && __ldg(trow + j0) >= 0;
-    const bool v1 = j1 < k && __ldg(trow + j1) >= 0;
+    const int e0 = j0 < k ? __ldg(trow + j0) : -1, e1 = j1 < k ? __ldg(trow + j1) : -1;
+    const bool v0 = e0 >= 0 && e0 <= lim;
+    const bool v1 = e1 >= 0 && e1 <= lim;
     const uint32_t b0 = __ballot_sync(0xffffffffu, v0), b1 = __ballot_sync(0xffffffffu, v1);
     if (lane == 0) {
       masks[tile] = static_cast<uint64_t>(b0) | (static_cast<uint64_t>(b1) << 32);
@@ -139,8 +162,6 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16*
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + S::kOffTmem);
   const int n_tiles = *reinterpret_cast<volatile int*>(smem + S::kOffNTiles);
-  const int b = __ldg(bid + t);
-  const bool b_ok = b >= 0 && b < kv.n_req;
 
   if (warp == 4) {
     // ------------------------------------------------------------------ TMA gather producer
@@ -160,7 +181,7 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16*
         for (int i = 0; i < 4; ++i) {
           const int e = j * kTileKeys + static_cast<int>(lane) * 4 + i;
           const int s = (e < k && b_ok) ? __ldg(trow + e) : -1;
-          rows[i] = kv_row(kv, b_ok ? b : 0, s, &bad);
+          rows[i] = kv_row(kv, b_ok ? b : 0, s, lim, &bad);
         }
         const uint32_t dst = sbase + S::kOffKV + stage * S::kStageBytes + lane * 4 * 128;
 #pragma unroll
@@ -520,6 +541,9 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
       if (!warp_wait(bar(kMetaEmpty + (n & 1)), ((n >> 1) & 1) ^ 1, 0x41, abort_flag)) break;
       const int64_t t = query(n);
       const int32_t* trow = topk + t * k;
+      const int bq = __ldg(bid + t);
+      const int lim = (bq >= 0 && bq < kv.n_req) ? entry_limit(kv, bq, t) : -1;
+      bool bad_entry = false;
       if (crank == 0) {
         const char* qrow = reinterpret_cast<const char*>(q + t * kH * kDQK);
         for (int off = static_cast<int>(lane) * 128; off < kH * kDQK * 2; off += 32 * 128)
@@ -533,13 +557,19 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
         uint32_t bits = 0;
         if (e0 + 8 <= k && (k & 3) == 0) {
           const int4 a = __ldg(reinterpret_cast<const int4*>(trow + e0));
-          const int4 bq = __ldg(reinterpret_cast<const int4*>(trow + e0 + 4));
-          const int v[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
+          const int4 b4 = __ldg(reinterpret_cast<const int4*>(trow + e0 + 4));
+          const int v[8] = {a.x, a.y, a.z, a.w, b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-          for (int i = 0; i < 8; ++i) bits |= (v[i] >= 0 ? 1u : 0u) << i;
+          for (int i = 0; i < 8; ++i) {
+            bits |= (v[i] >= 0 && v[i] <= lim ? 1u : 0u) << i;
+            bad_entry |= v[i] > lim;
+          }
         } else {
-          for (int i = 0; i < 8; ++i)
-            bits |= ((e0 + i < k && __ldg(trow + e0 + i) >= 0) ? 1u : 0u) << i;
+          for (int i = 0; i < 8; ++i) {
+            const int v = e0 + i < k ? __ldg(trow + e0 + i) : -1;
+            bits |= (v >= 0 && v <= lim ? 1u : 0u) << i;
+            bad_entry |= v > lim;
+          }
         }
         const uint32_t w = bits << ((lane & 3) * 8);           // 4 lanes -> one 32-bit word
         const uint32_t w2 = w | __shfl_xor_sync(0xffffffffu, w, 1);
@@ -550,6 +580,8 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
         }
       }
       last = __reduce_max_sync(0xffffffffu, last);
+      if (__any_sync(0xffffffffu, bad_entry) && lane == 0 && crank == 0)
+        report_device_error(kErrBadIndex);
       if (lane == 0) {
         nt_buf[n & 1] = last;
         mbar_arrive(bar(kMetaFull + (n & 1)));
@@ -583,6 +615,7 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
       const bool b_ok = b >= 0 && b < kv.n_req;
       bad |= !b_ok;
       const int bb = b_ok ? b : 0;
+      const int lim = b_ok ? entry_limit(kv, b, t) : -1;
       const int j_first = static_cast<int>(((s - g0) % kStages + kStages) % kStages);
       auto fetch = [&](int j, int& s0, int& s1) {
         const int e0 = j * kKeys + static_cast<int>(lane);
@@ -596,8 +629,8 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
         const int64_t g = g0 + j;
         if (!warp_wait(bar(kKvEmpty + s), static_cast<uint32_t>(((g / kStages) & 1) ^ 1), 0x21,
                        abort_flag)) { ok = false; break; }
-        const int32_t r0 = kv_row(kv, bb, s0, &bad);
-        const int32_t r1 = kv_row(kv, bb, s1, &bad);
+        const int32_t r0 = kv_row(kv, bb, s0, lim, &bad);
+        const int32_t r1 = kv_row(kv, bb, s1, lim, &bad);
         fetch(j + kStages, s0, s1);
 #pragma unroll
         for (int i = half; i < kKeys / 4; i += kGatherPerSlot) {
@@ -1140,7 +1173,7 @@ int sparse_mla(const void* q, const void* c, int64_t n_kv_rows, const int32_t* c
                 sparse_mla_workspace_bytes(n_q));
   if (ws != nullptr && reinterpret_cast<uintptr_t>(ws) % 16 != 0)
     return fail(DSA_ERR_INVALID, "mla: workspace must be 16-byte aligned");
-  KvMap kv{cu, block_table, max_pages, n_req, n_kv_rows};
+  KvMap kv{cu, block_table, max_pages, n_req, n_kv_rows, pos};
   if (H == 128 && dqk == 576 && dv == 512)
     return launch_mla_pair(q, c, n_kv_rows, kv, bid, topk, n_q, k, scale, o, lse, pos,
                            static_cast<int32_t*>(ws), stream);

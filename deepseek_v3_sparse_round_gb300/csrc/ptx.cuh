@@ -76,12 +76,13 @@ constexpr long long kWaitLimitCycles = 4000000000ll;
 // If `abort_flag` (shared memory) is set by another warp, or the time limit passes, the wait
 // gives up, sets the flag and returns false so that every role of the kernel unwinds.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t where,
-                                          volatile uint32_t* abort_flag) {
+                                          volatile uint32_t* abort_flag,
+                                          long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       report_device_error(kErrTimeout | where);
       *abort_flag = 1u;
       return false;
@@ -108,8 +109,9 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
 // phase complete (any timeout / abort makes the whole warp give up together, so no lane is left
 // behind before a warp-collective instruction).
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_t where,
-                                          volatile uint32_t* abort_flag) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, where, abort_flag));
+                                          volatile uint32_t* abort_flag,
+                                          long long limit = kWaitLimitCycles) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, where, abort_flag, limit));
 }
 __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity, uint32_t where,
                                                   volatile uint32_t* abort_flag) {

@@ -13,6 +13,10 @@
 #include "status.cuh"
 
 namespace dsa {
+
+int num_sms_cached();
+int64_t shard_len(int64_t n_tokens, int sp, int rank);
+
 namespace {
 
 constexpr int kThreads = 256;
@@ -155,23 +159,53 @@ split_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ pos_bas
   }
 }
 
-// The rerange fused with the KV-cache write: logical token g (request b, position s = g -
-// cu[b]) lands in pool row block_table[b][s / page_size] * page_size + s % page_size. Chunks of
-// the flattened (token, 16-byte chunk) space, kUnroll loads in flight per thread; the request
-// of a token comes from a binary search over cu staged in shared memory. A token whose page is
-// missing (negative entry, beyond max_pages or outside the pool) is skipped and recorded in the
-// device error word.
+// Paged KV-cache writes: row i of the source goes to the cache slot of its token. Two maps:
+//   RerangeToCache  (the rerange fused with the cache write) i = logical token g, source row
+//                   off[g % sp] + g / sp of the all-gathered buffer, slot s = g - cu[b];
+//   LocalToCache    (a rank keeps only its own tokens) i = shard token t, g = rank + t * sp,
+//                   source row t of the rank's local rows, slot j = t - cu_shard[b] (the
+//                   token's index among request b's tokens on this rank).
+// Slot x of request b is pool row block_table[b][x / page_size] * page_size + x % page_size.
+// Chunks of the flattened (row, 16-byte chunk) space, kUnroll loads in flight per thread; the
+// request of a token comes from a binary search over cu staged in shared memory. A token whose
+// page is missing (negative entry, beyond max_pages or outside the pool) is skipped and
+// recorded in the device error word.
 struct PagedPool {
   const int32_t* table;
   int max_pages, page_size;
   int64_t pool_rows;
 };
 
-template <typename Idx, int kBytes>
+struct RerangeToCache {
+  RerangeRows rows;
+  template <typename I>
+  __device__ __forceinline__ int64_t src(I i) const { return rows(i); }
+  template <typename I>
+  __device__ __forceinline__ int64_t token(I i) const { return static_cast<int64_t>(i); }
+  template <typename I>
+  __device__ __forceinline__ int64_t slot(I i, int32_t cu_b) const {
+    return static_cast<int64_t>(i) - cu_b;
+  }
+};
+
+struct LocalToCache {
+  int sp, rank;
+  template <typename I>
+  __device__ __forceinline__ int64_t src(I i) const { return static_cast<int64_t>(i); }
+  template <typename I>
+  __device__ __forceinline__ int64_t token(I i) const {
+    return rank + static_cast<int64_t>(i) * sp;
+  }
+  template <typename I>
+  __device__ __forceinline__ int64_t slot(I i, int32_t cu_b) const {
+    return static_cast<int64_t>(i) - shard_count_below(cu_b, sp, rank);
+  }
+};
+
+template <typename Idx, int kBytes, class Map>
 __global__ void __launch_bounds__(kThreads, 4)   // 4 CTAs per SM: enough loads in flight
-rerange_paged_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ pool, Idx total,
-                     Idx cpr, RerangeRows map, const int32_t* __restrict__ cu, int n_req,
-                     PagedPool pp) {
+paged_write_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ pool, Idx total,
+                   Idx cpr, Map map, const int32_t* __restrict__ cu, int n_req, PagedPool pp) {
   using V = typename std::conditional<kBytes == 16, int4, uint8_t>::type;
   __shared__ int32_t s_cu[kCuSmem];
   const bool staged = n_req + 1 <= kCuSmem;
@@ -194,7 +228,8 @@ rerange_paged_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ pool
        i += kUnroll * stride) {
     // The source chunks do not depend on the page map: their loads go out first and are in
     // flight while the destinations are worked out.
-    Idx g[kUnroll], c[kUnroll];
+    Idx r[kUnroll], c[kUnroll];
+    int64_t g[kUnroll];
     bool in[kUnroll];
     V v[kUnroll];
 #pragma unroll
@@ -202,10 +237,11 @@ rerange_paged_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ pool
       const Idx cc = i + u * stride;
       in[u] = cc < total;
       const Idx ci = in[u] ? cc : 0;
-      g[u] = ci / cpr;
-      c[u] = ci - g[u] * cpr;
-      if constexpr (kBytes == 16) v[u] = ld_stream(vs + map(g[u]) * cpr + c[u]);
-      else v[u] = vs[map(g[u]) * cpr + c[u]];
+      r[u] = ci / cpr;
+      c[u] = ci - r[u] * cpr;
+      g[u] = map.token(r[u]);
+      if constexpr (kBytes == 16) v[u] = ld_stream(vs + map.src(r[u]) * cpr + c[u]);
+      else v[u] = vs[map.src(r[u]) * cpr + c[u]];
     }
     // Request of each chunk: the largest b < n_req with cu[b] <= g, by a fixed sequence of
     // halving steps (the same count for every thread), the kUnroll searches side by side.
@@ -216,20 +252,20 @@ rerange_paged_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ pool
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int t = b[u] + step;
-        if (t < n_req && static_cast<int64_t>(cuv[t]) <= static_cast<int64_t>(g[u])) b[u] = t;
+        if (t < n_req && static_cast<int64_t>(cuv[t]) <= g[u]) b[u] = t;
       }
     }
     int64_t dst[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      // position in the request (cu is int32, so it fits 32 bits), its page and row
-      const int s = static_cast<int>(static_cast<int64_t>(g[u]) - cuv[b[u]]);
-      const int pi = s / pp.page_size;
+      // slot in the request's cache (cu is int32, so it fits 32 bits), its page and row
+      const int x = static_cast<int>(map.slot(r[u], cuv[b[u]]));
+      const int pi = x / pp.page_size;
       const int page = (in[u] && pi < pp.max_pages)
                            ? __ldg(pp.table + static_cast<int64_t>(b[u]) * pp.max_pages + pi)
                            : -1;
-      const int64_t r = page < 0 ? -1 : static_cast<int64_t>(page) * pp.page_size + (s - pi * pp.page_size);
-      dst[u] = (r >= 0 && r < pp.pool_rows) ? r * static_cast<int64_t>(cpr) + c[u] : -1;
+      const int64_t row = page < 0 ? -1 : static_cast<int64_t>(page) * pp.page_size + (x - pi * pp.page_size);
+      dst[u] = (row >= 0 && row < pp.pool_rows) ? row * static_cast<int64_t>(cpr) + c[u] : -1;
       bad |= in[u] && dst[u] < 0;
     }
 #pragma unroll
@@ -242,17 +278,7 @@ rerange_paged_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ pool
   if (bad) report_device_error(kErrBadIndex);
 }
 
-int num_sms() {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        sms <= 0)
-      sms = 148;
-  }
-  return sms;
-}
+int num_sms() { return num_sms_cached(); }
 
 int grid_for(int64_t work_items, int per_thread) {
   const int64_t want = (work_items + static_cast<int64_t>(kThreads) * per_thread - 1) /
@@ -282,6 +308,32 @@ int launch_copy_rows(const void* src, void* dst, int64_t n_rows, int64_t row_byt
     copy_rows_bytes_kernel<RowMap><<<grid_for(n_rows * row_bytes, 4), kThreads, 0, stream>>>(
         static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), n_rows, row_bytes, map);
   }
+  DSA_CHECK_CUDA(cudaGetLastError());
+  return DSA_OK;
+}
+
+// Rows 0..n_rows-1 of `src` into their cache slots (16-byte vectors when both buffers and
+// row_bytes are multiples of 16, else byte copies).
+template <class Map>
+int launch_paged_write(const void* src_rows, void* pool, int64_t n_rows, int64_t row_bytes,
+                       const Map& map, const int32_t* cu, int n_req, const PagedPool& pp,
+                       cudaStream_t stream) {
+  const bool vec = (row_bytes % 16 == 0) && (reinterpret_cast<uintptr_t>(src_rows) % 16 == 0) &&
+                   (reinterpret_cast<uintptr_t>(pool) % 16 == 0);
+  const int64_t cpr = vec ? row_bytes / 16 : row_bytes;
+  const int64_t total = n_rows * cpr;
+  const int grid = grid_for(total, kUnroll);
+  const auto* src = static_cast<const uint8_t*>(src_rows);
+  auto* dst = static_cast<uint8_t*>(pool);
+  if (vec && total < (int64_t(1) << 31))
+    paged_write_kernel<uint32_t, 16, Map><<<grid, kThreads, 0, stream>>>(
+        src, dst, static_cast<uint32_t>(total), static_cast<uint32_t>(cpr), map, cu, n_req, pp);
+  else if (vec)
+    paged_write_kernel<int64_t, 16, Map><<<grid, kThreads, 0, stream>>>(src, dst, total, cpr, map,
+                                                                        cu, n_req, pp);
+  else
+    paged_write_kernel<int64_t, 1, Map><<<grid, kThreads, 0, stream>>>(src, dst, total, cpr, map,
+                                                                       cu, n_req, pp);
   DSA_CHECK_CUDA(cudaGetLastError());
   return DSA_OK;
 }
@@ -360,26 +412,31 @@ int rerange_paged(const void* gathered, void* pool, int64_t pool_rows, int64_t n
   if (rank_stride_rows > 0 && rank_stride_rows < need)
     return fail(DSA_ERR_INVALID, "rerange_paged: rank_stride_rows %lld < ceil(N/sp) = %lld",
                 static_cast<long long>(rank_stride_rows), static_cast<long long>(need));
-  RerangeRows map{sp, n_tokens / sp, n_tokens % sp, rank_stride_rows};
+  RerangeToCache map{RerangeRows{sp, n_tokens / sp, n_tokens % sp, rank_stride_rows}};
   PagedPool pp{block_table, max_pages, page_size, pool_rows};
-  const bool vec = (row_bytes % 16 == 0) && (reinterpret_cast<uintptr_t>(gathered) % 16 == 0) &&
-                   (reinterpret_cast<uintptr_t>(pool) % 16 == 0);
-  const int64_t cpr = vec ? row_bytes / 16 : row_bytes;
-  const int64_t total = n_tokens * cpr;
-  const int grid = grid_for(total, kUnroll);
-  const auto* src = static_cast<const uint8_t*>(gathered);
-  auto* dst = static_cast<uint8_t*>(pool);
-  if (vec && total < (int64_t(1) << 31))
-    rerange_paged_kernel<uint32_t, 16><<<grid, kThreads, 0, stream>>>(
-        src, dst, static_cast<uint32_t>(total), static_cast<uint32_t>(cpr), map, cu, n_req, pp);
-  else if (vec)
-    rerange_paged_kernel<int64_t, 16><<<grid, kThreads, 0, stream>>>(src, dst, total, cpr, map, cu,
-                                                                      n_req, pp);
-  else
-    rerange_paged_kernel<int64_t, 1><<<grid, kThreads, 0, stream>>>(src, dst, total, cpr, map, cu,
-                                                                     n_req, pp);
-  DSA_CHECK_CUDA(cudaGetLastError());
-  return DSA_OK;
+  return launch_paged_write(gathered, pool, n_tokens, row_bytes, map, cu, n_req, pp, stream);
+}
+
+int cache_local_paged(const void* local_rows, void* pool, int64_t pool_rows, int64_t n_tokens,
+                      int sp, int rank, int64_t row_bytes, const int32_t* cu, int n_req,
+                      const int32_t* block_table, int max_pages, int page_size,
+                      cudaStream_t stream) {
+  if (sp < 1 || rank < 0 || rank >= sp)
+    return fail(DSA_ERR_INVALID, "cache_local_paged: need sp >= 1 and 0 <= rank < sp (sp=%d "
+                                 "rank=%d)", sp, rank);
+  if (n_tokens < 0 || row_bytes <= 0 || n_req < 1 || page_size < 1 || max_pages < 1 ||
+      pool_rows < 0)
+    return fail(DSA_ERR_INVALID,
+                "cache_local_paged: need n_tokens >= 0, row_bytes > 0, n_req >= 1, "
+                "page_size >= 1, max_pages >= 1");
+  if (n_tokens > INT32_MAX) return fail(DSA_ERR_INVALID, "cache_local_paged: n_tokens >= 2^31");
+  const int64_t n_r = shard_len(n_tokens, sp, rank);
+  if (n_r == 0) return DSA_OK;
+  if (!local_rows || !pool || !cu || !block_table)
+    return fail(DSA_ERR_INVALID, "cache_local_paged: null pointer");
+  PagedPool pp{block_table, max_pages, page_size, pool_rows};
+  return launch_paged_write(local_rows, pool, n_r, row_bytes, LocalToCache{sp, rank}, cu, n_req,
+                            pp, stream);
 }
 
 cudaError_t split_read_errors(uint32_t* flags) { return read_and_clear_device_error(flags); }

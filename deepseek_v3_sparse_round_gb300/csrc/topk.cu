@@ -15,6 +15,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "keys.cuh"
 #include "status.cuh"
 
 namespace dsa {
@@ -24,15 +25,10 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kPerThread = 8;                       // consecutive entries per thread per chunk
 constexpr int kChunk = kThreads * kPerThread;       // 4096 entries
-constexpr int kBins = 2048;                         // 11-bit digits
+constexpr int kBins = kHistBins;                    // 11-bit digits
 constexpr int kStashKeys = 40960;                   // 160 KB of keys in shared memory
 constexpr int kShortRow = 16384;                    // rows up to this length: kIn = 2
 
-__device__ __forceinline__ uint32_t order_key(float f) {
-  uint32_t u = __float_as_uint(f);
-  if (u == 0x80000000u) u = 0u;                     // -0.0 == +0.0
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
 
 // Exclusive prefix sum over threads in threadIdx order; returns the block total in *total.
 __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_tot,
@@ -119,6 +115,108 @@ __device__ __forceinline__ void load_keys_any_order(const float* __restrict__ ro
   }
 }
 
+// Digit of the bin holding the `remaining`-th largest entry of a filled histogram, and the
+// number of entries in the bins above it (written to *s_digit / *s_above; all threads see them
+// after the call). Thread j owns the 4 bins of mirror index m = kThreads-1-j, so an exclusive
+// scan in thread order counts every bin above them.
+__device__ __forceinline__ void pick_bin(const uint32_t* hist, uint32_t remaining,
+                                         uint32_t* warp_tot, uint32_t* s_digit,
+                                         uint32_t* s_above) {
+  if (threadIdx.x == 0) {          // defined even if the counts fall short of `remaining`
+    *s_digit = 0u;
+    *s_above = 0u;
+  }                                // (ordered before the writes below by the scan's barrier)
+  const int m = kThreads - 1 - threadIdx.x;
+  const uint32_t h0 = hist[4 * m], h1 = hist[4 * m + 1], h2 = hist[4 * m + 2],
+                 h3 = hist[4 * m + 3];
+  uint32_t tot;
+  uint32_t above = block_exclusive_scan(h0 + h1 + h2 + h3, warp_tot, &tot);
+  const uint32_t hs[4] = {h0, h1, h2, h3};
+#pragma unroll
+  for (int j = 3; j >= 0; --j) {
+    if (above < remaining && above + hs[j] >= remaining) {
+      *s_digit = static_cast<uint32_t>(4 * m + j);
+      *s_above = above;
+    }
+    above += hs[j];
+  }
+  __syncthreads();
+}
+
+// Radix passes (11, 11, 10 bits, most significant first) from pass `first` on, over the keys
+// whose top bits already match `prefix` under `prefix_mask`, finding the exact key T of the
+// `remaining`-th largest of them and how many entries equal to T still belong to the result.
+template <bool kStash>
+__device__ __forceinline__ void radix_threshold(const float* __restrict__ row,
+                                                const uint32_t* stash, int L, int k, int first,
+                                                uint32_t prefix, uint32_t prefix_mask,
+                                                uint32_t remaining, uint32_t* hist,
+                                                uint32_t* warp_tot, uint32_t* s_digit,
+                                                uint32_t* s_above, uint32_t* T_out,
+                                                uint32_t* need_eq_out) {
+  (void)k;
+#pragma unroll 1
+  for (int p = first; p < 3; ++p) {
+    for (int b = threadIdx.x; b < kBins; b += kThreads) hist[b] = 0;
+    __syncthreads();
+    const int sh = p == 0 ? 21 : (p == 1 ? 10 : 0);
+    const uint32_t dm = p == 2 ? 0x3FFu : 0x7FFu;
+    for (int base = 0; base < L; base += kChunk) {
+      uint32_t key[kPerThread];
+      bool valid[kPerThread];
+      load_keys_any_order<kStash>(row, stash, L, base, key, valid);
+#pragma unroll
+      for (int j = 0; j < kPerThread; ++j)
+        if (valid[j] && (key[j] & prefix_mask) == prefix) atomicAdd(&hist[(key[j] >> sh) & dm], 1u);
+    }
+    __syncthreads();
+    pick_bin(hist, remaining, warp_tot, s_digit, s_above);
+    remaining -= *s_above;
+    prefix |= *s_digit << sh;
+    prefix_mask |= dm << sh;
+    __syncthreads();
+  }
+  *T_out = prefix;
+  *need_eq_out = remaining;
+}
+
+// Ordered emission reading the row from global memory in chunks: every index with key > T and
+// the lowest-index need_eq entries with key == T, in ascending index order.
+__device__ __forceinline__ void emit_ordered_global(const float* __restrict__ row, int L,
+                                                    uint32_t T, uint32_t need_eq, uint32_t n_gt,
+                                                    int32_t* __restrict__ out,
+                                                    uint32_t* warp_tot) {
+  uint32_t gt_done = 0, eq_done = 0;
+  for (int base = 0; base < L && (gt_done < n_gt || eq_done < need_eq); base += kChunk) {
+    uint32_t key[kPerThread];
+    bool valid[kPerThread];
+    load_keys<false>(row, nullptr, L, base, key, valid);
+    uint32_t n_g = 0, n_e = 0;
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) {
+      n_g += (valid[j] && key[j] > T);
+      n_e += (valid[j] && key[j] == T);
+    }
+    uint32_t tot;
+    const uint32_t before = block_exclusive_scan((n_g << 16) | n_e, warp_tot, &tot);
+    uint32_t g_before = gt_done + (before >> 16), e_before = eq_done + (before & 0xFFFFu);
+    const int i0 = base + threadIdx.x * kPerThread;
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) {
+      if (!valid[j]) continue;
+      if (key[j] > T) {
+        out[g_before + (e_before < need_eq ? e_before : need_eq)] = i0 + j;
+        ++g_before;
+      } else if (key[j] == T) {
+        if (e_before < need_eq) out[g_before + e_before] = i0 + j;
+        ++e_before;
+      }
+    }
+    gt_done += tot >> 16;
+    eq_done += tot & 0xFFFFu;
+  }
+}
+
 // kIn: 16-byte loads in flight per thread while the stash fills. Short rows (several CTAs per SM)
 // take 2 and keep the registers for three CTAs per SM; long rows (one CTA per SM: the stash
 // takes most of shared memory) take 4.
@@ -170,47 +268,10 @@ topk_kernel(const float* __restrict__ scores, int64_t stride, const int32_t* __r
   }
 
   // ---- three radix passes: find the exact k-th largest key T ----
-  uint32_t prefix = 0, prefix_mask = 0, remaining = static_cast<uint32_t>(k);
-#pragma unroll 1
-  for (int p = 0; p < 3; ++p) {
-    for (int b = threadIdx.x; b < kBins; b += kThreads) hist[b] = 0;
-    __syncthreads();
-    const int sh = p == 0 ? 21 : (p == 1 ? 10 : 0);
-    const uint32_t dm = p == 2 ? 0x3FFu : 0x7FFu;
-    for (int base = 0; base < L; base += kChunk) {
-      uint32_t key[kPerThread];
-      bool valid[kPerThread];
-      load_keys_any_order<kStash>(row, stash, L, base, key, valid);
-#pragma unroll
-      for (int j = 0; j < kPerThread; ++j)
-        if (valid[j] && (key[j] & prefix_mask) == prefix) atomicAdd(&hist[(key[j] >> sh) & dm], 1u);
-    }
-    __syncthreads();
-    // Thread j owns the 4 bins of mirror index m = kThreads-1-j, so an exclusive scan in thread
-    // order counts every bin above them.
-    const int m = kThreads - 1 - threadIdx.x;
-    const uint32_t h0 = hist[4 * m], h1 = hist[4 * m + 1], h2 = hist[4 * m + 2],
-                   h3 = hist[4 * m + 3];
-    uint32_t tot;
-    uint32_t above = block_exclusive_scan(h0 + h1 + h2 + h3, warp_tot, &tot);
-    const uint32_t hs[4] = {h0, h1, h2, h3};
-#pragma unroll
-    for (int j = 3; j >= 0; --j) {
-      if (above < remaining && above + hs[j] >= remaining) {
-        s_digit = static_cast<uint32_t>(4 * m + j);
-        s_above = above;
-      }
-      above += hs[j];
-    }
-    __syncthreads();
-    remaining -= s_above;
-    prefix |= s_digit << sh;
-    prefix_mask |= dm << sh;
-    __syncthreads();
-  }
-  const uint32_t T = prefix;
-  const uint32_t need_eq = remaining;               // entries equal to T that are still taken
-  const uint32_t n_gt = static_cast<uint32_t>(k) - remaining;
+  uint32_t T, need_eq;
+  radix_threshold<kStash>(row, stash, L, k, 0, 0u, 0u, static_cast<uint32_t>(k), hist, warp_tot,
+                          &s_digit, &s_above, &T, &need_eq);
+  const uint32_t n_gt = static_cast<uint32_t>(k) - need_eq;
 
   // ---- ordered emission ----
   if (kStash) {
@@ -240,34 +301,179 @@ topk_kernel(const float* __restrict__ scores, int64_t stride, const int32_t* __r
     }
     return;
   }
-  uint32_t gt_done = 0, eq_done = 0;
-  for (int base = 0; base < L && (gt_done < n_gt || eq_done < need_eq); base += kChunk) {
-    uint32_t key[kPerThread];
-    bool valid[kPerThread];
-    load_keys<kStash>(row, stash, L, base, key, valid);
-    uint32_t n_g = 0, n_e = 0;
+  emit_ordered_global(row, L, T, need_eq, n_gt, out, warp_tot);
+}
+
+// ------------------------------------------------------------------------------------------
+// Top-k fed by the indexer's first-digit histograms (the fused indexer -> top-k path).
+//
+// The indexer epilogue counted, for every query, how many of its scores fall in each of the
+// kBins first-digit bins (the top 11 bits of the order key). From that row of counts the bin T0
+// holding the k-th largest score and the number of scores above it are known before the row is
+// read. One pass over the row then keeps only the entries whose digit is >= T0, compacted in
+// index order into shared memory (key and index), typically k plus the boundary bin's few
+// hundred to few thousand entries; the two remaining radix passes and the ordered emission run
+// over that short list. A row whose kept entries exceed kCap (a histogram crowded at the
+// boundary) takes the global-memory passes instead, starting from the known first digit.
+constexpr int kCap = 8192;                          // kept entries in shared memory (64 KB)
+constexpr int kCompactPerLane = 16;                 // entries per lane per compaction chunk
+constexpr int kCompactChunk = kThreads * kCompactPerLane;
+
+__global__ void __launch_bounds__(kThreads, 2)
+topk_hist_kernel(const float* __restrict__ scores, int64_t stride, const int32_t* __restrict__ pos,
+                 int k, int max_ctx, const uint32_t* __restrict__ hist_rows,
+                 int32_t* __restrict__ topk) {
+  extern __shared__ __align__(16) uint32_t kept[];   // keys [kCap], then indices [kCap]
+  __shared__ uint32_t hist[kBins];
+  __shared__ uint32_t warp_tot[kWarps];
+  __shared__ uint32_t s_digit, s_above;
+  uint32_t* ckey = kept;
+  uint32_t* cidx = kept + kCap;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+  const int64_t t = static_cast<int64_t>(gridDim.x) - 1 - blockIdx.x;   // longest rows first
+  int32_t* out = topk + t * k;
+  const int L = __ldg(pos + t) + 1;
+  if (L < 1 || L > max_ctx) {
+    if (threadIdx.x == 0) report_device_error(kErrBadLength);
+    for (int j = threadIdx.x; j < k; j += kThreads) out[j] = -1;
+    return;
+  }
+  if (L <= k) {
+    for (int j = threadIdx.x; j < k; j += kThreads) out[j] = j < L ? j : -1;
+    return;
+  }
+  const float* row = scores + t * stride;
+  {
+    const uint4* h = reinterpret_cast<const uint4*>(hist_rows + t * kBins);
+    for (int i = threadIdx.x; i < kBins / 4; i += kThreads)
+      reinterpret_cast<uint4*>(hist)[i] = __ldcg(h + i);
+  }
+  __syncthreads();
+  pick_bin(hist, static_cast<uint32_t>(k), warp_tot, &s_digit, &s_above);
+  const uint32_t T0 = s_digit;
+  const uint32_t above = s_above;
+  const uint32_t n_keep = above + hist[T0];
+  __syncthreads();
+  const uint32_t prefix0 = T0 << kHistShift, mask0 = 0x7FFu << kHistShift;
+  uint32_t T, need_eq;
+  if (n_keep > static_cast<uint32_t>(kCap)) {
+    radix_threshold<false>(row, nullptr, L, k, 1, prefix0, mask0, static_cast<uint32_t>(k) - above,
+                           hist, warp_tot, &s_digit, &s_above, &T, &need_eq);
+    emit_ordered_global(row, L, T, need_eq, static_cast<uint32_t>(k) - need_eq, out, warp_tot);
+    return;
+  }
+
+  // ---- compaction: entries with digit >= T0, in index order. Warp w reads the 1,024 entries
+  // [base + 1024 w, base + 1024 (w + 1)) of a chunk as 8 coalesced rounds of 32 lanes x 4; the
+  // per-warp counts are scanned across the block, then each round is placed by a warp scan.
+  uint32_t kept_so_far = 0;
+  for (int base = 0; base < L; base += kCompactChunk) {
+    const int wb = base + warp * (kCompactPerLane * 32);
+    uint32_t key[kCompactPerLane / 4][4];
+    uint32_t keepm[kCompactPerLane / 4];
+    uint32_t cnt = 0;
 #pragma unroll
-    for (int j = 0; j < kPerThread; ++j) {
-      n_g += (valid[j] && key[j] > T);
-      n_e += (valid[j] && key[j] == T);
-    }
-    uint32_t tot;
-    const uint32_t before = block_exclusive_scan((n_g << 16) | n_e, warp_tot, &tot);
-    uint32_t g_before = gt_done + (before >> 16), e_before = eq_done + (before & 0xFFFFu);
-    const int i0 = base + threadIdx.x * kPerThread;
+    for (int j = 0; j < kCompactPerLane / 4; ++j) {
+      const int i = wb + 128 * j + 4 * lane;
+      float f[4] = {0.f, 0.f, 0.f, 0.f};
+      if (i + 4 <= L) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(row + i));
+        f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+      } else {
 #pragma unroll
-    for (int j = 0; j < kPerThread; ++j) {
-      if (!valid[j]) continue;
-      if (key[j] > T) {
-        out[g_before + (e_before < need_eq ? e_before : need_eq)] = i0 + j;
-        ++g_before;
-      } else if (key[j] == T) {
-        if (e_before < need_eq) out[g_before + e_before] = i0 + j;
-        ++e_before;
+        for (int e = 0; e < 4; ++e) f[e] = i + e < L ? __ldcg(row + i + e) : 0.f;
       }
+      uint32_t m = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        key[j][e] = order_key(f[e]);
+        if (i + e < L && first_digit(key[j][e]) >= T0) m |= 1u << e;
+      }
+      keepm[j] = m;
+      cnt += __popc(m);
     }
-    gt_done += tot >> 16;
-    eq_done += tot & 0xFFFFu;
+    const uint32_t warp_cnt = __reduce_add_sync(0xffffffffu, cnt);
+    uint32_t tot;
+    const uint32_t wbefore = block_exclusive_scan(lane == 0 ? warp_cnt : 0u, warp_tot, &tot);
+    uint32_t at = kept_so_far + __shfl_sync(0xffffffffu, wbefore, 0);
+#pragma unroll
+    for (int j = 0; j < kCompactPerLane / 4; ++j) {
+      const uint32_t c = __popc(keepm[j]);
+      uint32_t incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      uint32_t dst = at + incl - c;
+      const int i = wb + 128 * j + 4 * lane;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if ((keepm[j] & (1u << e)) && dst < static_cast<uint32_t>(kCap)) {
+          ckey[dst] = key[j][e];
+          cidx[dst] = static_cast<uint32_t>(i + e);
+          ++dst;
+        }
+      }
+      at += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    kept_so_far += tot;
+  }
+  __syncthreads();
+  if (kept_so_far != n_keep) {                        // the histogram does not match the row
+    if (threadIdx.x == 0) report_device_error(kErrBadIndex | 0xC1u);
+    radix_threshold<false>(row, nullptr, L, k, 0, 0u, 0u, static_cast<uint32_t>(k), hist,
+                           warp_tot, &s_digit, &s_above, &T, &need_eq);
+    emit_ordered_global(row, L, T, need_eq, static_cast<uint32_t>(k) - need_eq, out, warp_tot);
+    return;
+  }
+  const int n = static_cast<int>(kept_so_far);
+
+  // ---- radix passes 2 and 3 over the kept entries of the boundary bin ----
+  uint32_t prefix = prefix0, prefix_mask = mask0;
+  uint32_t remaining = static_cast<uint32_t>(k) - above;
+#pragma unroll 1
+  for (int p = 1; p < 3; ++p) {
+    for (int b = threadIdx.x; b < kBins; b += kThreads) hist[b] = 0;
+    __syncthreads();
+    const int sh = p == 1 ? 10 : 0;
+    const uint32_t dm = p == 2 ? 0x3FFu : 0x7FFu;
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      const uint32_t key = ckey[i];
+      if ((key & prefix_mask) == prefix) atomicAdd(&hist[(key >> sh) & dm], 1u);
+    }
+    __syncthreads();
+    pick_bin(hist, remaining, warp_tot, &s_digit, &s_above);
+    remaining -= s_above;
+    prefix |= s_digit << sh;
+    prefix_mask |= dm << sh;
+    __syncthreads();
+  }
+  T = prefix;
+  need_eq = remaining;
+
+  // ---- ordered emission over the kept list (already in index order) ----
+  const int seg = ((n + kThreads - 1) / kThreads) | 1;
+  const int lo = min(static_cast<int>(threadIdx.x) * seg, n), hi = min(lo + seg, n);
+  uint32_t n_g = 0, n_e = 0;
+  for (int i = lo; i < hi; ++i) {
+    const uint32_t key = ckey[i];
+    n_g += key > T;
+    n_e += key == T;
+  }
+  uint32_t tot;                                       // counts < 2^16: n <= kCap
+  const uint32_t before = block_exclusive_scan((n_g << 16) | n_e, warp_tot, &tot);
+  uint32_t g_before = before >> 16, e_before = before & 0xFFFFu;
+  for (int i = lo; i < hi; ++i) {
+    const uint32_t key = ckey[i];
+    if (key > T) {
+      out[g_before + (e_before < need_eq ? e_before : need_eq)] = static_cast<int32_t>(cidx[i]);
+      ++g_before;
+    } else if (key == T) {
+      if (e_before < need_eq) out[g_before + e_before] = static_cast<int32_t>(cidx[i]);
+      ++e_before;
+    }
   }
 }
 
@@ -307,5 +513,25 @@ int topk_select(const float* scores, int64_t score_stride, const int32_t* pos, i
 }
 
 cudaError_t topk_read_errors(uint32_t* flags) { return read_and_clear_device_error(flags); }
+
+}  // namespace dsa
+
+namespace dsa {
+
+// Top-k of rows whose first-digit histograms (hist_rows [n_q, kHistBins] u32, complete counts
+// of every score s <= pos_t of the row) the indexer produced.
+int topk_select_hist(const float* scores, int64_t score_stride, const int32_t* pos, int64_t n_q,
+                     int k, int max_ctx, const uint32_t* hist_rows, int32_t* topk,
+                     cudaStream_t stream) {
+  if (n_q == 0) return DSA_OK;
+  if (n_q > INT32_MAX) return fail(DSA_ERR_UNSUPPORTED, "topk: n_q too large");
+  const int smem = 2 * kCap * static_cast<int>(sizeof(uint32_t));
+  DSA_CHECK_CUDA(cudaFuncSetAttribute(topk_hist_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+  topk_hist_kernel<<<static_cast<unsigned>(n_q), kThreads, smem, stream>>>(
+      scores, score_stride, pos, k, max_ctx, hist_rows, topk);
+  DSA_CHECK_CUDA(cudaGetLastError());
+  return DSA_OK;
+}
 
 }  // namespace dsa

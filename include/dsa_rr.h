@@ -9,6 +9,8 @@
  *                          each request's context)
  *   dsa_rr_rerange         all-gathered (rank-major) KV rows -> logical token order
  *   dsa_rr_rerange_paged   the same rows straight into a paged KV cache (rerange + cache write)
+ *   dsa_rr_cache_local_paged  a rank's own tokens only into its paged KV cache (the global KV
+ *                          is dropped after attention)
  *   dsa_indexer_topk       lightning-indexer scores over the causal history + per-query top-k
  *     (= dsa_indexer_scores followed by dsa_topk_select, also exported on their own)
  *   dsa_sparse_mla         sparse MLA of every shard query over its top-k latent rows
@@ -62,6 +64,17 @@ int dsa_version(void);
 
 /* Synchronise the device, OR every kernel's device error word into *flags and clear them. */
 int dsa_read_device_errors(uint32_t* flags);
+
+/*
+ * Self-test of the bounded in-kernel wait (the pages have no counterpart: this checks the
+ * library's failure detection). Enqueues one single-warp kernel that waits, with the same
+ * bounded wait the tcgen05 kernels use, for an mbarrier phase that nothing completes. After
+ * limit_cycles SM clock cycles (1 <= limit_cycles <= 2^40) the wait gives up, the kernel sets
+ * DSA_DEVERR_TIMEOUT | 0xEE in the device error word and returns; dsa_read_device_errors then
+ * reports it. Nothing faults, traps or hangs, and the CUDA context stays usable.
+ * Errors: DSA_ERR_INVALID for a limit outside the range, DSA_ERR_CUDA for a failed launch.
+ */
+int dsa_selftest_bounded_wait(int64_t limit_cycles, dsa_stream_t stream);
 
 /*
  * Host helper: number of tokens shard `rank` of `sp` holds, ceil((n_tokens - rank) / sp), or
@@ -160,6 +173,34 @@ int dsa_rr_rerange_paged(const void* gathered, void* pool, int64_t pool_rows, in
                          dsa_stream_t stream);
 
 /*
+ * Keep only this rank's own tokens in its paged KV cache.
+ * Source: "[DeepSeek v3.2] 上下文并行详解", section 4 part 3 step D: after attention the global
+ * KV is not kept; the rank's KV-cache manager stores only the tokens it is responsible for (CP=4,
+ * rank 1 keeps K1 and K5) in the cache pool, for the decode steps that follow.
+ *
+ * Shard token t (0 <= t < n_r = dsa_rr_shard_len(n_tokens, sp, rank)) is the flattened token
+ * g_t = rank + t*sp of request b (the largest b with cu[b] <= g_t); its slot in the rank's cache
+ * of request b is j = t - cu_shard[b], its index among request b's tokens on this rank
+ * (cu_shard[b] = the number of shard tokens with g < cu[b]). Then
+ *   pool[block_table[b * max_pages + j / page_size] * page_size + j % page_size, :] =
+ *       local_rows[t, :]
+ * local_rows [n_r, row_bytes] device: the rank's own rows in shard order (the rows its split
+ * gathered, or block `rank` of a packed all-gather). cu [n_req+1] int32 device (cu[0] = 0,
+ * non-decreasing, cu[n_req] = n_tokens); block_table [n_req, max_pages] int32 device, this
+ * rank's pages (request b needs cu_shard[b+1] - cu_shard[b] slots); pool [pool_rows, row_bytes]
+ * device; pool rows no token maps to are not written. A token whose page entry is negative,
+ * beyond max_pages or outside the pool is skipped and sets DSA_DEVERR_BAD_INDEX. 16-byte vectors
+ * when both buffers and row_bytes are multiples of 16, else byte copies.
+ * Errors: DSA_ERR_INVALID for sp < 1, rank outside [0, sp), n_tokens < 0 or >= 2^31,
+ * row_bytes <= 0, n_req < 1, page_size < 1, max_pages < 1 or null pointers (an empty shard is a
+ * no-op).
+ */
+int dsa_rr_cache_local_paged(const void* local_rows, void* pool, int64_t pool_rows,
+                             int64_t n_tokens, int sp, int rank, int64_t row_bytes,
+                             const int32_t* cu, int n_req, const int32_t* block_table,
+                             int max_pages, int page_size, dsa_stream_t stream);
+
+/*
  * Bytes of scratch dsa_indexer_topk needs: the fp32 score rows [n_q, stride(max_ctx)] plus a
  * small scheduling area. max_ctx = an upper bound of pos_t + 1 over the queries.
  */
@@ -217,23 +258,28 @@ int dsa_indexer_topk(const void* q_idx, const float* w, const void* k_idx, int64
                      size_t workspace_bytes, dsa_stream_t stream);
 
 /*
- * Sparse MLA (tcgen05 tensor cores, TMA row gather). "[RFC]: Parallel strategy for Deepseek
- * v3.2 like models": each query attends only its top-k keys, with all heads at once. For query
- * t and head h, over the valid entries idx_j >= 0 of topk[t, :]:
+ * Sparse MLA on tcgen05 tensor cores (the selected rows are gathered into shared memory by
+ * 16-byte cp.async copies for H = 128 and by TMA tile::gather4 for H = 8). "[RFC]: Parallel
+ * strategy for Deepseek v3.2 like models": each query attends only its top-k keys, with all
+ * heads at once. For query t and head h, over the valid entries of topk[t, :]:
  *
  *     S[h, j]   = scale * sum_{d < dqk} q[t, h, d] * c[row(b_t, idx_j), d]
  *     o[t, h,:] = sum_j softmax_j(S[h, :]) * c[row(b_t, idx_j), 0:dv]
  *     lse[t, h] = ln sum_j exp(S[h, j])
  *
- * (absorbed MLA: V is the first dv columns of the same latent row). A query without valid
- * entries gets o = 0 and lse = -inf.
+ * (absorbed MLA: V is the first dv columns of the same latent row). An entry is valid when
+ * 0 <= idx_j <= lim_t, lim_t = the last position of the query's request (contiguous mode:
+ * cu[b+1] - cu[b] - 1) or of its block-table row (paged: max_pages * page_size - 1); -1 entries
+ * are padding; an entry above lim_t is skipped (as if it were -1) and sets
+ * DSA_DEVERR_BAD_INDEX. A query without valid entries gets o = 0 and lse = -inf.
  *   q  bf16 [n_q, H, dqk]     c bf16 [n_kv_rows, dqk]     topk int32 [n_q, k]
  *   cu int32 [n_req+1] (contiguous mode) / block_table int32 [n_req, max_pages] (paged)
  *   n_req >= 1; bid entries outside [0, n_req) read zero rows and set DSA_DEVERR_BAD_INDEX
  *   bid int32 [n_q]           o bf16 [n_q, H, dv]         lse fp32 [n_q, H] or NULL
  * Supported: (H, dqk, dv) in {(128, 576, 512), (8, 80, 64)}, page_size 64 when paged.
  * Softmax in fp32 (exp2 with a running maximum), P rounded to bf16 for the P.V product.
- * Index entries that land outside the KV buffer read zero rows and set DSA_DEVERR_BAD_INDEX.
+ * Index entries that land outside the KV buffer (a missing page) read zero rows and set
+ * DSA_DEVERR_BAD_INDEX.
  */
 int dsa_sparse_mla(const void* q, const void* c, int64_t n_kv_rows, const int32_t* cu, int n_req,
                    const int32_t* bid, const int32_t* topk, int64_t n_q, int H, int dqk, int dv,
@@ -249,6 +295,9 @@ int dsa_sparse_mla(const void* q, const void* c, int64_t n_kv_rows, const int32_
  * min(p + 1, k) keys). Queries are sorted by that estimate, largest first, and dealt to the
  * pairs in rounds of alternating direction, so that the pairs finish together; o and lse are
  * bit-identical to dsa_sparse_mla's (each query's arithmetic does not depend on its pair).
+ * With the positions given, an entry is valid only when it also lies in the query's causal
+ * history: lim_t = min(pos_t, the request bound of dsa_sparse_mla); entries above it are
+ * skipped and set DSA_DEVERR_BAD_INDEX.
  * workspace: device, 16-byte aligned, >= dsa_sparse_mla_workspace_size(n_q) bytes (the
  * schedule, int32 [n_q]); owned by the caller, not read before it is written. Errors as
  * dsa_sparse_mla, plus DSA_ERR_WORKSPACE for a short workspace and DSA_ERR_INVALID for a null
@@ -272,10 +321,15 @@ int dsa_sparse_mla_balanced(const void* q, const void* c, int64_t n_kv_rows, con
  * device. The scratch space lives in one file-scope __device__ array of
  * DSA_NOALLOC_SCRATCH_BYTES bytes that every GPU loading the library keeps until exit.
  * Arguments and results are those of dsa_indexer_topk without workspace / workspace_bytes.
- * The first call on a device (that device current) looks up the array's address; make it before
- * any stream capture. All calls share the array: calls that may overlap on the GPU race and must
- * not be issued. Requests needing more scratch than the array (dsa_indexer_topk_workspace_size)
- * return DSA_ERR_WORKSPACE. No device memory is allocated or freed.
+ * The first call on a device (that device current) looks up the array's address with
+ * cudaGetSymbolAddress and caches it per device; with lazy module loading that first call also
+ * loads the library's device code on that device, which reserves the array and can synchronise
+ * the device, so make it before any stream capture and outside latency-critical regions. The
+ * cached address belongs to the device's current context: after cudaDeviceReset (or any
+ * teardown of the primary context) it is stale, and the entry point must not be called again in
+ * that process. All calls share the array: calls that may overlap on the GPU race and must not
+ * be issued. Requests needing more scratch than the array (dsa_indexer_topk_workspace_size)
+ * return DSA_ERR_WORKSPACE. No device memory is allocated or freed by the call itself.
  */
 #define DSA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 int dsa_indexer_topk_noalloc(const void* q_idx, const float* w, const void* k_idx,

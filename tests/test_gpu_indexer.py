@@ -81,3 +81,57 @@ def test_row_longer_than_max_ctx_is_flagged_not_written():
     flags = dsa.dsa_read_device_errors()
     assert flags & (dsa.DEVERR_BAD_INDEX | dsa.DEVERR_BAD_LENGTH)
     assert not torch.isnan(scores[:, :100][torch.as_tensor(sh.pos < 100)]).all()
+
+
+# ---- the fused path: dsa_indexer_topk with max_ctx > 8192 has the indexer histogram each
+# score's first radix digit, and the top-k reads each row once, keeping only candidates. It
+# must give exactly the index sets of the separate calls (same scores, same selection rule).
+def _fused_equals_separate(sh, max_ctx=None):
+    if max_ctx is not None:
+        sh.max_ctx = max_ctx
+    assert sh.max_ctx > 8192
+    _, sep = sh.run_indexer()
+    fused = sh.run_indexer_topk()
+    torch.cuda.synchronize()
+    assert torch.equal(fused, sep)
+    import deepseek_v3_sparse_round_gb300 as dsa
+    assert dsa.dsa_read_device_errors() == 0
+    return fused
+
+
+@pytest.mark.parametrize("wid,rank,integer", [(2, 5, True), (2, 1, False), (4, 0, True),
+                                              (4, 0, False)])
+def test_fused_indexer_topk_long_rows(wid, rank, integer):
+    sh = Shard(W.WORKLOADS[wid], rank, integer_indexer=integer)
+    fused = _fused_equals_separate(sh).cpu().numpy()
+    if integer:                                       # exact scores: the oracle's sets, bit for bit
+        sel = sh.samples(24)
+        ora = sh.oracle_topk(sh.oracle_scores(sel))
+        for i, t in enumerate(sel):
+            assert np.array_equal(fused[t], ora[i]), t
+
+
+@pytest.mark.parametrize("wid,rank", [(0, 1), (1, 3), (3, 2)])
+def test_fused_path_on_short_rows(wid, rank):
+    """The fused path forced on workloads whose rows are short (a larger max_ctx is a valid
+    upper bound): heavy integer ties (workload 0), rows around k, every request length."""
+    sh = Shard(W.WORKLOADS[wid], rank, integer_indexer=True)
+    fused = _fused_equals_separate(sh, max_ctx=9000).cpu().numpy()
+    sel = sh.samples(32)
+    ora = sh.oracle_topk(sh.oracle_scores(sel))
+    for i, t in enumerate(sel):
+        assert np.array_equal(fused[t], ora[i]), t
+
+
+def test_fused_crowded_boundary_bin_takes_the_global_path():
+    """All scores equal (q_idx = 0): the boundary bin holds the whole row, more entries than the
+    shared-memory list takes, so rows over 8,192 keys go through the global-memory passes; the
+    result is still the lowest k indices."""
+    sh = Shard(W.WORKLOADS[2], 7, integer_indexer=True)
+    sh.idx.q_idx = torch.zeros_like(sh.idx.q_idx)
+    fused = _fused_equals_separate(sh).cpu().numpy()
+    for t in (0, 2047, 2048, 4095):
+        L = int(sh.pos[t]) + 1
+        want = np.full(2048, -1)
+        want[:min(L, 2048)] = np.arange(min(L, 2048))
+        assert np.array_equal(fused[t], want), t

@@ -114,3 +114,52 @@ def test_unusual_k(k):
         n_pick = min(k, int(sh.pos[t]) + 1)
         topk[i, :n_pick] = np.sort(rng.choice(int(sh.pos[t]) + 1, n_pick, replace=False))
     _check(sh, sel, topk)
+
+
+@pytest.mark.parametrize("balanced", [False, True])
+def test_out_of_range_entries_are_skipped_and_flagged(balanced):
+    """Entries past the query's position (balanced call, which is given the positions) or past
+    its request's end (both calls, contiguous KV) are not attended: they are skipped like -1
+    padding and DEVERR_BAD_INDEX is set. The output equals the oracle over the remaining
+    entries."""
+    from dsa_cases import dsa
+    sh = Shard(W.WORKLOADS[1], 3)
+    rng = np.random.default_rng(11)
+    # queries of request 1 (800 tokens, rows 8000..8799) and request 3 (3000 tokens)
+    sel = np.concatenate([np.flatnonzero(sh.bid == 1)[20:23], np.flatnonzero(sh.bid == 3)[100:103]])
+    k = 256
+    topk = np.full((len(sel), k), -1, dtype=np.int64)
+    keep = np.full((len(sel), k), -1, dtype=np.int64)
+    for i, t in enumerate(sel):
+        p = int(sh.pos[t])
+        L = int(sh.cu[sh.bid[t] + 1] - sh.cu[sh.bid[t]])
+        good = rng.choice(p + 1, min(150, p + 1), replace=False)
+        past_req = L + rng.integers(0, 50, 3)                 # beyond the request: always invalid
+        past_pos = p + 1 + rng.integers(0, L - p - 1, 3) if L - p - 1 > 0 else np.zeros(0, int)
+        ent = np.concatenate([good, past_req, past_pos])
+        slots = rng.choice(k, len(ent), replace=False)
+        topk[i, slots] = ent
+        valid = (ent <= p) if balanced else (ent < L)
+        keep[i, slots[valid]] = ent[valid]
+    m = dsa()
+    q = sh.mla.q[torch.as_tensor(sel, device=sh.mla.q.device)].cuda()
+    o = torch.full((len(sel), 128, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((len(sel), 128), float("nan"), device="cuda")
+    m.dsa_read_device_errors()
+    bid, pos = i32(sh.bid[sel]), i32(sh.pos[sel])
+    if balanced:
+        ws = torch.empty(m.dsa_sparse_mla_workspace_size(len(sel)), dtype=torch.uint8, device="cuda")
+        m.dsa_sparse_mla_balanced(q, sh.mla.c.cuda(), sh.d_cu, sh.n_req, bid, pos, i32(topk),
+                                  sh.wl.scale, o, ws, lse=lse)
+    else:
+        m.dsa_sparse_mla(q, sh.mla.c.cuda(), sh.d_cu, sh.n_req, bid, i32(topk), sh.wl.scale, o, lse)
+    assert m.dsa_read_device_errors() & m.DEVERR_BAD_INDEX
+    # the oracle over the entries that stay (the plain call keeps entries past pos but inside
+    # the request; they are real keys of the request, so the oracle reads them too)
+    cu = sh.cu.astype(np.int64)
+    c64 = f64(sh.mla.c)
+    from oracle.kv import ContiguousKV
+    ref_o, ref_lse = omla.sparse_mla(f64(q), c64, ContiguousKV(cu), sh.bid[sel], keep,
+                                     sh.wl.scale, sh.wl.dv)
+    mla_close(f64(o), ref_o)
+    assert np.allclose(lse.cpu().numpy(), ref_lse, atol=1e-3, rtol=1e-4)

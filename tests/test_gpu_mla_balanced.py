@@ -38,12 +38,14 @@ def test_balanced_equals_plain_on_whole_shards(wid, rank):
     assert torch.equal(l1, l2)
 
 
-def test_balanced_with_positions_unrelated_to_the_rows():
-    # pos only steers the schedule: arbitrary values (negative, past k, shuffled) change nothing
+def test_balanced_with_positions_unrelated_to_the_work():
+    # Beyond bounding the valid entries (an entry must not exceed its query's position), pos
+    # only steers the schedule: positions at or above each query's own, raised by random
+    # amounts (past k, shuffled in size), keep every entry valid and change nothing.
     sh = Shard(W.WORKLOADS[1], 3, integer_indexer=False)
     topk = sh.run_indexer_topk()
     rng = np.random.default_rng(5)
-    pos = rng.integers(-5, 20000, sh.n_q).astype(np.int32)
+    pos = (sh.pos.astype(np.int64) + rng.integers(0, 20000, sh.n_q)).astype(np.int32)
     (o1, l1), (o2, l2) = _both(sh, topk, i32(pos))
     assert torch.equal(o1, o2)
     assert torch.equal(l1, l2)
@@ -70,7 +72,7 @@ def test_short_workspace_and_missing_pos_rejected():
     q, c = sh.mla.q.cuda(), sh.mla.c.cuda()
     o = torch.empty((sh.n_q, sh.wl.H, sh.wl.dv), dtype=torch.bfloat16, device="cuda")
     small = torch.empty(4, dtype=torch.uint8, device="cuda")
-    # the small-head path ignores pos and the workspace; the 128-head checks run on the host
+    # the small-head path runs unscheduled; the 128-head workspace checks run on the host
     m.dsa_sparse_mla_balanced(q, c, sh.d_cu, sh.n_req, sh.d_bid, sh.d_pos, topk, sh.wl.scale, o,
                               torch.empty(m.dsa_sparse_mla_workspace_size(sh.n_q),
                                           dtype=torch.uint8, device="cuda"))

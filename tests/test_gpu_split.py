@@ -147,3 +147,90 @@ def test_rerange_paged_missing_page_is_skipped_and_flagged():
     kv_rows = [int(keep[0, 0]) * 64 + s for s in range(64)] + [int(keep[1, 0]) * 64 + s for s in range(64)]
     src_rows = list(range(64)) + [130 + s for s in range(64)]
     assert torch.equal(got[kv_rows], x.cpu()[src_rows])
+
+
+def _local_table(cu, sp, r, ps, seed, spare=2):
+    """Rank r's own block table: request b needs ceil(cnt_b / ps) pages, cnt_b = its tokens on
+    the rank (counted from the oracle's token list); page ids a seeded permutation."""
+    rng = np.random.default_rng(seed)
+    tokens = osplit.shard_tokens(int(cu[-1]), sp, r)
+    counts = [int(np.sum((tokens >= cu[b]) & (tokens < cu[b + 1]))) for b in range(len(cu) - 1)]
+    need = [-(-c // ps) for c in counts]
+    perm = rng.permutation(sum(need) + spare)
+    table = np.full((len(counts), max(max(need), 1)), -1, dtype=np.int32)
+    at = 0
+    for b, p in enumerate(need):
+        table[b, :p] = perm[at:at + p]
+        at += p
+    return table, sum(need) + spare
+
+
+@pytest.mark.parametrize("wid", [1, 3])
+@pytest.mark.parametrize("width", [576, 128])
+def test_cache_local_paged_workloads(wid, width):
+    """Every rank keeps only its own tokens: bit-exact against the oracle for each shard, with
+    the rank's rows coming from the split's gather (as a rank holds them after step A)."""
+    from dsa_cases import dsa, i32
+    wl = W.WORKLOADS[wid]
+    cu = W.cu_seqlens(wl.lengths)
+    n = int(cu[-1])
+    x = W.normal_bf16((n, width), seed=70 + wid, device="cuda")
+    for r in range(wl.sp):
+        local = gpu_split(cu, wl.sp, r, src=x)["rows"]
+        table, n_pages = _local_table(cu, wl.sp, r, 64, 90 + r)
+        pool0 = torch.full((n_pages * 64, width), 3, dtype=torch.bfloat16, device="cuda")
+        pool = pool0.clone()
+        dsa().dsa_rr_cache_local_paged(local, pool, n, wl.sp, r, i32(cu), i32(table), 64)
+        want = orr.cache_local_into_pages(local.cpu().view(torch.uint8).numpy(), cu, wl.sp, r,
+                                          table, 64, pool0.cpu().view(torch.uint8).numpy())
+        assert np.array_equal(pool.cpu().view(torch.uint8).numpy(), want), r
+    assert dsa().dsa_read_device_errors() == 0
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_cache_local_paged_edge_cases(seed):
+    """Empty requests, requests with no token on the rank, odd page sizes, byte rows."""
+    from dsa_cases import dsa, i32
+    rng = np.random.default_rng(300 + seed)
+    lengths = [int(v) for v in rng.integers(0, 40, int(rng.integers(1, 9)))]
+    lengths[0] = 0
+    sp = int(rng.integers(1, 9))
+    ps = int(rng.choice([1, 3, 16, 64]))
+    width = int(rng.choice([7, 32]))
+    cu = W.cu_seqlens(lengths)
+    n = int(cu[-1])
+    x = W.int_uniform((max(n, 1), width), 0, 254, 60 + seed, dtype=torch.uint8, device="cuda")[:n]
+    for r in range(sp):
+        n_r = dsa().dsa_rr_shard_len(n, sp, r)
+        local = x[r::sp].contiguous() if n_r else torch.empty((0, width), dtype=torch.uint8, device="cuda")
+        table, n_pages = _local_table(cu, sp, r, ps, 400 + r)
+        pool0 = torch.full((n_pages * ps, width), 9, dtype=torch.uint8, device="cuda")
+        pool = pool0.clone()
+        dsa().dsa_rr_cache_local_paged(local, pool, n, sp, r, i32(cu), i32(table), ps)
+        want = orr.cache_local_into_pages(local.cpu().numpy(), cu, sp, r, table, ps,
+                                          pool0.cpu().numpy())
+        assert np.array_equal(pool.cpu().numpy(), want), (r, sp, ps)
+    assert dsa().dsa_read_device_errors() == 0
+
+
+def test_cache_local_paged_missing_page_is_skipped_and_flagged():
+    from dsa_cases import dsa, i32
+    cu = W.cu_seqlens([600, 90])
+    sp, r = 4, 1
+    x = W.normal_bf16((690, 128), seed=8, device="cuda")
+    local = gpu_split(cu, sp, r, src=x)["rows"]
+    table, n_pages = _local_table(cu, sp, r, 64, 5)
+    lost = int(table[0, 1])
+    bad = table.copy()
+    bad[0, 1] = -1                                   # request 0, rank-local slots 64..127
+    pool0 = torch.full((n_pages * 64, 128), 3, dtype=torch.bfloat16, device="cuda")
+    pool = pool0.clone()
+    dsa().dsa_rr_cache_local_paged(local, pool, 690, sp, r, i32(cu), i32(bad), 64)
+    assert dsa().dsa_read_device_errors() & dsa().DEVERR_BAD_INDEX
+    assert torch.equal(pool[lost * 64:(lost + 1) * 64], pool0[lost * 64:(lost + 1) * 64])
+    want = orr.cache_local_into_pages(local.cpu().view(torch.uint8).numpy(), cu, sp, r, table, 64,
+                                      pool0.cpu().view(torch.uint8).numpy())
+    got = pool.cpu().view(torch.uint8).numpy()
+    keep = np.ones(len(got), bool)
+    keep[lost * 64:(lost + 1) * 64] = False
+    assert np.array_equal(got[keep], want[keep])

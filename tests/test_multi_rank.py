@@ -1,6 +1,7 @@
-"""Host logic of the multi-GPU benchmark path on CPU with two gloo ranks: each rank takes a
-different shard of the same varlen batch (disjoint query sets that together with the other
-shards partition the batch), and the job time is the maximum over ranks."""
+"""Host logic of the multi-GPU benchmark path on CPU with two gloo ranks: every rank runs an
+independent replica of the whole many-request batch (all of its shards, which partition the
+batch's tokens), so the job processes world x the batch's queries, and the job time is the
+maximum over ranks."""
 import os
 import socket
 
@@ -24,32 +25,35 @@ def _worker(rank, world, port, out):
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
         wl = W.WORKLOADS[bench.WORKLOAD_ID]
-        shard = bench.shard_for_rank(rank, wl.sp)
+        shards = bench.shards_for_rank(rank, world, wl.sp)
         local = 1.0 + 0.25 * rank                       # pretend step time of this rank
-        out[rank] = (shard, bench.max_over_ranks(local, dist, "cpu"))
+        out[rank] = (tuple(shards), bench.max_over_ranks(local, dist, "cpu"))
         dist.barrier()
     finally:
         dist.destroy_process_group()
 
 
-def test_two_gloo_ranks_take_disjoint_shards_and_max_time():
+def test_two_gloo_ranks_run_whole_replicas_and_max_time():
     world = 2
     mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.start_processes(_worker, args=(world, _free_port(), out), nprocs=world, join=True,
                        start_method="spawn")
-    shards = [out[r][0] for r in range(world)]
-    assert len(set(shards)) == world
     assert all(out[r][1] == 1.25 for r in range(world))
-    wl = W.WORKLOADS[1]
-    cu = W.cu_seqlens(wl.lengths)
-    sets = [set(osplit.round_robin_split(cu, wl.sp, s)["gidx"].tolist()) for s in shards]
-    assert not (sets[0] & sets[1])
-    assert len(sets[0]) + len(sets[1]) == sum(len(osplit.round_robin_split(cu, wl.sp, s)["gidx"]) for s in shards)
-
-
-def test_shard_assignment_covers_all_shards_for_eight_ranks():
     import bench
-    wl = W.WORKLOADS[1]
-    assert sorted(bench.shard_for_rank(r, wl.sp) for r in range(wl.sp)) == list(range(wl.sp))
-    assert bench.shard_for_rank(0, wl.sp) == 3
+    wl = W.WORKLOADS[bench.WORKLOAD_ID]
+    cu = W.cu_seqlens(wl.lengths)
+    for r in range(world):
+        shards = out[r][0]
+        assert sorted(shards) == list(range(wl.sp))
+        # the shards of one replica partition the batch's tokens
+        sets = [set(osplit.round_robin_split(cu, wl.sp, s)["gidx"].tolist()) for s in shards]
+        assert sum(len(x) for x in sets) == int(cu[-1])
+        assert set().union(*sets) == set(range(int(cu[-1])))
+
+
+def test_default_workload_is_the_many_request_batch():
+    import bench
+    wl = W.WORKLOADS[bench.WORKLOAD_ID]
+    assert len(wl.lengths) == 32 and sum(wl.lengths) == 71014 and wl.sp == 4
+    assert list(wl.ranks) == [0, 1, 2, 3]
