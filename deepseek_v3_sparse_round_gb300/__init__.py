@@ -20,7 +20,8 @@ __all__ = [
     "dsa_indexer_topk_workspace_size", "dsa_score_row_stride", "dsa_indexer_scores",
     "dsa_topk_select", "dsa_indexer_topk", "dsa_indexer_topk_noalloc", "dsa_sparse_mla",
     "dsa_sparse_mla_workspace_size", "dsa_sparse_mla_balanced", "dsa_read_device_errors",
-    "dsa_rr_cache_local_paged", "dsa_selftest_bounded_wait",
+    "dsa_rr_cache_local_paged", "dsa_selftest_bounded_wait", "dsa_quantize_fp8_rows",
+    "dsa_indexer_scores_fp8", "dsa_indexer_topk_fp8",
     "DEVERR_TIMEOUT", "DEVERR_BAD_INDEX", "DEVERR_BAD_LENGTH",
 ]
 
@@ -276,6 +277,59 @@ def dsa_indexer_topk_noalloc(q_idx, w, k_idx, cu, n_req, pos, bid, k, max_ctx, t
     _check(_lib().dsa_indexer_topk_noalloc(
         _ptr(q_idx), _ptr(w), _ptr(k_idx), k_idx.shape[0], _ptr(cu), n_req, _ptr(pos), _ptr(bid),
         n_q, Hi, Di, k, max_ctx, _ptr(block_table), max_pages, page_size, _ptr(topk),
+        _stream(stream)))
+
+
+def dsa_quantize_fp8_rows(x, codes, scales, stream=None):
+    """x bf16 [rows, 128] -> codes uint8 [rows, 128] (E4M3), scales fp32 [rows]; x may be any
+    shape whose last dimension is 128 (q_idx [n_q, Hi, 128] gives scales [n_q, Hi])."""
+    _dev(x, torch.bfloat16, "x"); _dev(codes, torch.uint8, "codes"); _dev(scales, torch.float32, "scales")
+    cols = x.shape[-1]
+    rows = x.numel() // cols if cols else 0
+    if codes.shape != x.shape or scales.numel() != rows:
+        raise ValueError("codes must match x's shape and scales hold one value per row")
+    _check(_lib().dsa_quantize_fp8_rows(_ptr(x), rows, cols, _ptr(codes), _ptr(scales),
+                                        _stream(stream)))
+
+
+def _fp8_indexer_checks(q8, q_scale, w, k8, k_scale, pos, bid, block_table, n_req):
+    _dev(q8, torch.uint8, "q8"); _dev(k8, torch.uint8, "k8")
+    _dev(q_scale, torch.float32, "q_scale"); _dev(k_scale, torch.float32, "k_scale")
+    _dev(w, torch.float32, "w"); _dev(pos, torch.int32, "pos"); _dev(bid, torch.int32, "bid")
+    _dev(block_table, torch.int32, "block_table")
+    n_q, Hi, _ = q8.shape
+    _shape(q_scale, (n_q, Hi), "q_scale")
+    _shape(k_scale, (k8.shape[0],), "k_scale")
+    _indexer_shapes(q8, w, pos, bid, block_table, n_req)
+
+
+def dsa_indexer_scores_fp8(q8, q_scale, w, k8, k_scale, cu, n_req, pos, bid, max_ctx, scores,
+                           workspace, block_table=None, page_size=64, stream=None):
+    """Indexer scores on E4M3 rows: the indexer of (q_scale q8, k_scale k8)."""
+    _fp8_indexer_checks(q8, q_scale, w, k8, k_scale, pos, bid, block_table, n_req)
+    _dev(scores, torch.float32, "scores"); _dev(cu, torch.int32, "cu")
+    n_q, Hi, Di = q8.shape
+    _shape(scores, (n_q, None), "scores")
+    max_pages = block_table.shape[1] if block_table is not None else 0
+    _check(_lib().dsa_indexer_scores_fp8(
+        _ptr(q8), _ptr(q_scale), _ptr(w), _ptr(k8), _ptr(k_scale), k8.shape[0], _ptr(cu), n_req,
+        _ptr(pos), _ptr(bid), n_q, Hi, Di, max_ctx, _ptr(block_table), max_pages, page_size,
+        _ptr(scores), scores.shape[1], _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def dsa_indexer_topk_fp8(q8, q_scale, w, k8, k_scale, cu, n_req, pos, bid, k, max_ctx, topk,
+                         workspace, block_table=None, page_size=64, stream=None):
+    """dsa_indexer_topk on E4M3 rows (same workspace size, same selection rule)."""
+    _fp8_indexer_checks(q8, q_scale, w, k8, k_scale, pos, bid, block_table, n_req)
+    _dev(topk, torch.int32, "topk"); _dev(cu, torch.int32, "cu")
+    n_q, Hi, Di = q8.shape
+    _shape(topk, (n_q, k), "topk")
+    max_pages = block_table.shape[1] if block_table is not None else 0
+    _check(_lib().dsa_indexer_topk_fp8(
+        _ptr(q8), _ptr(q_scale), _ptr(w), _ptr(k8), _ptr(k_scale), k8.shape[0], _ptr(cu), n_req,
+        _ptr(pos), _ptr(bid), n_q, Hi, Di, k, max_ctx, _ptr(block_table), max_pages, page_size,
+        _ptr(topk), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
 
 

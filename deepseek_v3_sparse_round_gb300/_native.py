@@ -38,6 +38,13 @@ SIGNATURES = {
     "dsa_indexer_topk_noalloc": (c_int, [c_vp, c_vp, c_vp, c_i64, c_vp, c_int, c_vp, c_vp, c_i64,
                                          c_int, c_int, c_int, c_int, c_vp, c_int, c_int, c_vp,
                                          c_vp]),
+    "dsa_quantize_fp8_rows": (c_int, [c_vp, c_i64, c_int, c_vp, c_vp, c_vp]),
+    "dsa_indexer_scores_fp8": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp, c_int, c_vp,
+                                       c_vp, c_i64, c_int, c_int, c_int, c_vp, c_int, c_int, c_vp,
+                                       c_i64, c_vp, c_sz, c_vp]),
+    "dsa_indexer_topk_fp8": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp, c_int, c_vp, c_vp,
+                                     c_i64, c_int, c_int, c_int, c_int, c_vp, c_int, c_int, c_vp,
+                                     c_vp, c_sz, c_vp]),
     "dsa_sparse_mla": (c_int, [c_vp, c_vp, c_i64, c_vp, c_int, c_vp, c_vp, c_i64, c_int, c_int,
                                c_int, c_int, c_f, c_vp, c_int, c_int, c_vp, c_vp, c_vp]),
     "dsa_sparse_mla_workspace_size": (c_sz, [c_i64]),

@@ -22,7 +22,10 @@ int indexer_scores(const void* q_idx, const float* w, const void* k_idx, int64_t
                    const int32_t* cu, const int32_t* pos, const int32_t* bid, int64_t n_q, int n_req,
                    int Hi, int Di, int max_ctx, const int32_t* block_table, int max_pages,
                    int page_size, float* scores, int64_t stride, void* ws, size_t ws_bytes,
-                   uint32_t* hist, cudaStream_t stream);
+                   uint32_t* hist, const float* q_scale, const float* k_scale,
+                   cudaStream_t stream);
+int quantize_fp8_rows(const void* x, int64_t rows, int cols, void* codes, float* scales,
+                      cudaStream_t stream);
 int topk_select_hist(const float* scores, int64_t score_stride, const int32_t* pos, int64_t n_q,
                      int k, int max_ctx, const uint32_t* hist_rows, int32_t* topk,
                      cudaStream_t stream);
@@ -205,7 +208,7 @@ DSA_EXPORT int dsa_indexer_scores(const void* q_idx, const float* w, const void*
     return dsa::fail(DSA_ERR_INVALID, "indexer: score rows must be 16-byte aligned");
   return dsa::indexer_scores(q_idx, w, k_idx, n_kv_rows, cu, pos, bid, n_q, n_req, Hi, Di,
                              max_ctx, block_table, max_pages, page_size, scores, score_stride,
-                             workspace, workspace_bytes, nullptr,
+                             workspace, workspace_bytes, nullptr, nullptr, nullptr,
                              reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -215,38 +218,97 @@ DSA_EXPORT int dsa_topk_select(const float* scores, int64_t score_stride, const 
                           reinterpret_cast<cudaStream_t>(stream));
 }
 
+}  // extern "C"
+
+namespace dsa {
+
+// Indexer scores (bf16 rows, or FP8 rows with their scales) into the workspace's score rows,
+// then the per-query top-k; fused through the first-digit histograms for long rows.
+static int indexer_topk_impl(const void* q_idx, const float* q_scale, const float* w,
+                             const void* k_idx, const float* k_scale, int64_t n_kv_rows,
+                             const int32_t* cu, int n_req, const int32_t* pos, const int32_t* bid,
+                             int64_t n_q, int Hi, int Di, int k, int max_ctx,
+                             const int32_t* block_table, int max_pages, int page_size,
+                             int32_t* topk, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream) {
+  if (n_q < 0 || max_ctx < 1 || k < 1)
+    return fail(DSA_ERR_INVALID, "indexer_topk: need n_q >= 0, max_ctx >= 1, k >= 1");
+  if (n_q == 0) return DSA_OK;
+  const size_t need = dsa_indexer_topk_workspace_size(n_q, max_ctx, k);
+  if (!workspace || workspace_bytes < need)
+    return fail(DSA_ERR_WORKSPACE, "indexer_topk: workspace of %zu bytes < %zu",
+                workspace_bytes, need);
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return fail(DSA_ERR_INVALID, "indexer_topk: workspace must be 256-byte aligned");
+  if (n_req < 1) return fail(DSA_ERR_INVALID, "indexer: n_req must be >= 1");
+  if (!topk) return fail(DSA_ERR_INVALID, "topk: null pointer");
+  const size_t plan = round_up(indexer_plan_bytes(n_q), 256);
+  float* scores = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan);
+  const int64_t stride = dsa_score_row_stride(max_ctx);
+  const size_t score_bytes =
+      round_up(static_cast<size_t>(n_q) * static_cast<size_t>(stride) * sizeof(float), 256);
+  uint32_t* hist = hist_bytes(n_q, max_ctx) > 0
+                       ? reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + plan +
+                                                     score_bytes)
+                       : nullptr;
+  int rc = indexer_scores(q_idx, w, k_idx, n_kv_rows, cu, pos, bid, n_q, n_req, Hi, Di, max_ctx,
+                          block_table, max_pages, page_size, scores, stride, workspace, plan,
+                          hist, q_scale, k_scale, stream);
+  if (rc) return rc;
+  if (hist == nullptr) return topk_select(scores, stride, pos, n_q, k, max_ctx, topk, stream);
+  return topk_select_hist(scores, stride, pos, n_q, k, max_ctx, hist, topk, stream);
+}
+
+}  // namespace dsa
+
+extern "C" {
+
 DSA_EXPORT int dsa_indexer_topk(const void* q_idx, const float* w, const void* k_idx, int64_t n_kv_rows,
                      const int32_t* cu, int n_req, const int32_t* pos, const int32_t* bid,
                      int64_t n_q, int Hi, int Di, int k, int max_ctx, const int32_t* block_table,
                      int max_pages, int page_size, int32_t* topk, void* workspace,
                      size_t workspace_bytes, dsa_stream_t stream) {
-  if (n_q < 0 || max_ctx < 1 || k < 1)
-    return dsa::fail(DSA_ERR_INVALID, "indexer_topk: need n_q >= 0, max_ctx >= 1, k >= 1");
-  if (n_q == 0) return DSA_OK;
-  const size_t need = dsa_indexer_topk_workspace_size(n_q, max_ctx, k);
-  if (!workspace || workspace_bytes < need)
-    return dsa::fail(DSA_ERR_WORKSPACE, "indexer_topk: workspace of %zu bytes < %zu",
-                     workspace_bytes, need);
-  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
-    return dsa::fail(DSA_ERR_INVALID, "indexer_topk: workspace must be 256-byte aligned");
-  const size_t plan = dsa::round_up(dsa::indexer_plan_bytes(n_q), 256);
-  float* scores = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan);
-  const int64_t stride = dsa_score_row_stride(max_ctx);
-  const size_t score_bytes =
-      dsa::round_up(static_cast<size_t>(n_q) * static_cast<size_t>(stride) * sizeof(float), 256);
-  uint32_t* hist = dsa::hist_bytes(n_q, max_ctx) > 0
-                       ? reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + plan +
-                                                     score_bytes)
-                       : nullptr;
+  return dsa::indexer_topk_impl(q_idx, nullptr, w, k_idx, nullptr, n_kv_rows, cu, n_req, pos,
+                                bid, n_q, Hi, Di, k, max_ctx, block_table, max_pages, page_size,
+                                topk, workspace, workspace_bytes,
+                                reinterpret_cast<cudaStream_t>(stream));
+}
+
+DSA_EXPORT int dsa_quantize_fp8_rows(const void* x, int64_t rows, int cols, void* codes,
+                                     float* scales, dsa_stream_t stream) {
+  return dsa::quantize_fp8_rows(x, rows, cols, codes, scales,
+                                reinterpret_cast<cudaStream_t>(stream));
+}
+
+DSA_EXPORT int dsa_indexer_scores_fp8(const void* q8, const float* q_scale, const float* w,
+                                      const void* k8, const float* k_scale, int64_t n_kv_rows,
+                                      const int32_t* cu, int n_req, const int32_t* pos,
+                                      const int32_t* bid, int64_t n_q, int Hi, int Di,
+                                      int max_ctx, const int32_t* block_table, int max_pages,
+                                      int page_size, float* scores, int64_t score_stride,
+                                      void* workspace, size_t workspace_bytes,
+                                      dsa_stream_t stream) {
   if (n_req < 1) return dsa::fail(DSA_ERR_INVALID, "indexer: n_req must be >= 1");
-  int rc = dsa::indexer_scores(q_idx, w, k_idx, n_kv_rows, cu, pos, bid, n_q, n_req, Hi, Di,
-                               max_ctx, block_table, max_pages, page_size, scores, stride,
-                               workspace, plan, hist, reinterpret_cast<cudaStream_t>(stream));
-  if (rc) return rc;
-  if (hist == nullptr) return dsa_topk_select(scores, stride, pos, n_q, k, max_ctx, topk, stream);
-  if (!topk) return dsa::fail(DSA_ERR_INVALID, "topk: null pointer");
-  return dsa::topk_select_hist(scores, stride, pos, n_q, k, max_ctx, hist, topk,
-                               reinterpret_cast<cudaStream_t>(stream));
+  if (!q_scale || !k_scale) return dsa::fail(DSA_ERR_INVALID, "indexer: FP8 scales are required");
+  if (score_stride % 4 != 0 || reinterpret_cast<uintptr_t>(scores) % 16 != 0)
+    return dsa::fail(DSA_ERR_INVALID, "indexer: score rows must be 16-byte aligned");
+  return dsa::indexer_scores(q8, w, k8, n_kv_rows, cu, pos, bid, n_q, n_req, Hi, Di, max_ctx,
+                             block_table, max_pages, page_size, scores, score_stride, workspace,
+                             workspace_bytes, nullptr, q_scale, k_scale,
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+DSA_EXPORT int dsa_indexer_topk_fp8(const void* q8, const float* q_scale, const float* w,
+                                    const void* k8, const float* k_scale, int64_t n_kv_rows,
+                                    const int32_t* cu, int n_req, const int32_t* pos,
+                                    const int32_t* bid, int64_t n_q, int Hi, int Di, int k,
+                                    int max_ctx, const int32_t* block_table, int max_pages,
+                                    int page_size, int32_t* topk, void* workspace,
+                                    size_t workspace_bytes, dsa_stream_t stream) {
+  if (!q_scale || !k_scale) return dsa::fail(DSA_ERR_INVALID, "indexer: FP8 scales are required");
+  return dsa::indexer_topk_impl(q8, q_scale, w, k8, k_scale, n_kv_rows, cu, n_req, pos, bid,
+                                n_q, Hi, Di, k, max_ctx, block_table, max_pages, page_size, topk,
+                                workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 DSA_EXPORT int dsa_sparse_mla(const void* q, const void* c, int64_t n_kv_rows, const int32_t* cu, int n_req,

@@ -62,25 +62,32 @@ struct PlanLayout {
   }
 };
 
-template <int HI, int DI>
+// F8: q_idx / k_idx rows are E4M3 codes (1 byte each) with fp32 scales, the MMA kind::f8f6f4
+// (32 elements per instruction); otherwise bf16 rows and kind::f16 (16 per instruction). Either
+// way one instruction consumes 32 bytes of each operand row.
+template <int HI, int DI, bool F8 = false>
 struct Shape {
+  static constexpr int kEB = F8 ? 1 : 2;                 // bytes per element
   static constexpr int kQPA = 256 / HI;                  // queries per accumulator
   static constexpr int kGQ = 2 * kQPA;                   // queries per group
   static constexpr int kBRows = kGQ * HI;                // 512 rows of Q per group
-  static constexpr int kAtomElems = DI >= 64 ? 64 : DI;  // elements per swizzled row
-  static constexpr int kAtomBytes = kAtomElems * 2;      // 128 (SW128) or 64 (SW64)
+  static constexpr int kRowBytes = DI * kEB;
+  static constexpr int kAtomBytes = kRowBytes >= 128 ? 128 : kRowBytes;  // swizzled row bytes
+  static constexpr int kAtomElems = kAtomBytes / kEB;
   static constexpr int kAtoms = DI / kAtomElems;
-  static constexpr uint32_t kSwz = DI >= 64 ? kSwizzle128B : kSwizzle64B;
+  static constexpr uint32_t kSwz = kAtomBytes == 128 ? kSwizzle128B : kSwizzle64B;
   static constexpr CUtensorMapSwizzle kTmaSwz =
-      DI >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+      kAtomBytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  static constexpr CUtensorMapDataType kTmaType =
+      F8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   static constexpr int kSBO = 8 * kAtomBytes;            // 8-row core-matrix group stride
-  static constexpr int kAStage = kKeysPerTile * DI * 2;
+  static constexpr int kAStage = kKeysPerTile * kRowBytes;
   static constexpr int kAAtom = kKeysPerTile * kAtomBytes;
   static constexpr int kBAtom = kBRows * kAtomBytes;
-  static constexpr int kStages = DI >= 64 ? 3 : 4;
-  static constexpr int kBBytes = kBRows * DI * 2;
-  static constexpr int kKSteps = DI / 16;
-  static constexpr int kStepsPerAtom = kAtomElems / 16;
+  static constexpr int kStages = F8 ? 4 : (DI >= 64 ? 3 : 4);
+  static constexpr int kBBytes = kBRows * kRowBytes;
+  static constexpr int kKSteps = kRowBytes / 32;
+  static constexpr int kStepsPerAtom = kAtomBytes / 32;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kStages * kAStage;
   static constexpr int kOffW = kOffB + kBBytes;          // fp32 [kGQ][HI]
@@ -225,14 +232,24 @@ __device__ __forceinline__ int32_t subtile_row(const KeyRows& kr, int b, int s) 
   return page * kPageRows;
 }
 
-template <int HI, int DI>
-__global__ void __launch_bounds__(Shape<HI, DI>::kThreads, 1)
+// Row of key s of request b (contiguous: cu[b] + s; paged: through the block table), or -1.
+__device__ __forceinline__ int64_t key_row(const KeyRows& kr, int b, int s) {
+  if (kr.block_table == nullptr) return static_cast<int64_t>(__ldg(kr.cu + b)) + s;
+  const int pi = s / kPageRows;
+  const int page = pi < kr.max_pages ? __ldg(kr.block_table + static_cast<int64_t>(b) * kr.max_pages + pi) : -1;
+  if (page < 0 || page >= kr.n_pages) return -1;
+  return static_cast<int64_t>(page) * kPageRows + s % kPageRows;
+}
+
+template <int HI, int DI, bool F8>
+__global__ void __launch_bounds__(Shape<HI, DI, F8>::kThreads, 1)
 indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                const float* __restrict__ w, const int32_t* __restrict__ pos, KeyRows kr,
                const Plan* __restrict__ plan, const int4* __restrict__ groups,
                const int32_t* __restrict__ unit_start, float* __restrict__ scores,
-               int64_t stride, int max_ctx, int n_q, uint32_t* __restrict__ hist) {
-  using S = Shape<HI, DI>;
+               int64_t stride, int max_ctx, int n_q, uint32_t* __restrict__ hist,
+               const float* __restrict__ q_scale, const float* __restrict__ k_scale) {
+  using S = Shape<HI, DI, F8>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   const uint32_t warp = warp_id(), lane = lane_id();
@@ -320,7 +337,8 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           nq[h] = max(0, min(un.count - h * S::kQPA, S::kQPA));
           uint32_t n_cols = static_cast<uint32_t>(nq[h] * HI);
           n_cols = (n_cols + 15u) & ~15u;
-          idesc[h] = idesc_bf16(128, n_cols < 16u ? 16u : n_cols, 0, 0);
+          idesc[h] = F8 ? idesc_e4m3(128, n_cols < 16u ? 16u : n_cols)
+                        : idesc_bf16(128, n_cols < 16u ? 16u : n_cols, 0, 0);
         }
         bool ok = true;
         for (int tile = un.tile_begin; tile < un.tile_end && ok; ++tile) {
@@ -338,7 +356,10 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
               const int a = kk / S::kStepsPerAtom, off = (kk % S::kStepsPerAtom) * 32;
               const uint64_t da = smem_desc(a_base + a * S::kAAtom + off, 16, S::kSBO, S::kSwz);
               const uint64_t db = smem_desc(b_base + a * S::kBAtom + off, 16, S::kSBO, S::kSwz);
-              umma_ss(tmem + static_cast<uint32_t>(h * 256), da, db, idesc[h], kk > 0 ? 1u : 0u);
+              if constexpr (F8)
+                umma_ss_f8(tmem + static_cast<uint32_t>(h * 256), da, db, idesc[h], kk > 0 ? 1u : 0u);
+              else
+                umma_ss(tmem + static_cast<uint32_t>(h * 256), da, db, idesc[h], kk > 0 ? 1u : 0u);
             }
             umma_commit(bar(kAccFull + h));
           }
@@ -369,7 +390,10 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       if (!warp_wait(bar(kWEmpty + h), (w_uses & 1u) ^ 1u, 0x07, abort_flag)) break;
       for (int i = static_cast<int>(quad * 32u + lane); i < S::kQPA * HI; i += 128) {
         const int q = i / HI;
-        sw[i] = q < nq ? __ldg(w + static_cast<int64_t>(tq0 + q) * HI + (i % HI)) : 0.f;
+        const int64_t wi = static_cast<int64_t>(tq0 + q) * HI + (i % HI);
+        float wv = q < nq ? __ldg(w + wi) : 0.f;
+        if constexpr (F8) wv = q < nq ? wv * __ldg(q_scale + wi) : 0.f;   // w[t,h] * sq[t,h]
+        sw[i] = wv;
       }
       for (int q = static_cast<int>(quad * 32u + lane); q < S::kQPA; q += 128)
         spos[q] = q < nq ? __ldg(pos + tq0 + q) : -1;
@@ -418,21 +442,26 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kAccEmpty + h));
         const int s = tile * kKeysPerTile + row;
+        if constexpr (F8) {
+          // the key's scale: I = sk[s] * sum_h (w sq) ReLU(q8 . k8) (sk > 0 leaves the ReLU)
+          const int64_t r = key_row(kr, un.b, s);
+          const float ks = (r >= 0 && r < kr.n_rows) ? __ldg(k_scale + r) : 0.f;
+#pragma unroll
+          for (int q = 0; q < S::kQPA; ++q) acc[q] *= ks;
+        }
 #pragma unroll
         for (int q = 0; q < S::kQPA; ++q) {
           if (q < nq && s <= spos[q] && s < max_ctx)
             scores[static_cast<int64_t>(tq0 + q) * stride + s] = acc[q];
         }
-        if (hist != nullptr) {
-          // First-digit histogram of every written score (for the top-k that follows): the
-          // warp's lanes with the same (query, digit) add their count with one atomic.
+        if (hist != nullptr && (s % kHistSample) == 0) {
+          // First-digit histogram of a sample of the written scores (one position in
+          // kHistSample; the lanes whose key sits at such a position), for the top-k after.
 #pragma unroll
           for (int q = 0; q < S::kQPA; ++q) {
-            const bool v = q < nq && s <= spos[q] && s < max_ctx;
-            const uint32_t d = v ? first_digit(order_key(acc[q])) : 0xFFFFFFFFu;
-            const uint32_t peers = __match_any_sync(0xffffffffu, d);
-            if (v && static_cast<int>(lane) == __ffs(peers) - 1)
-              atomicAdd(hist + static_cast<int64_t>(tq0 + q) * kHistBins + d, __popc(peers));
+            if (q < nq && s <= spos[q] && s < max_ctx)
+              atomicAdd(hist + static_cast<int64_t>(tq0 + q) * kHistBins +
+                            first_digit(order_key(acc[q])), 1u);
           }
         }
       }
@@ -448,13 +477,13 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   }
 }
 
-template <int HI, int DI>
+template <int HI, int DI, bool F8>
 int launch_indexer(const void* q_idx, const float* w, const void* k_idx, int64_t n_kv_rows,
                    const int32_t* pos, const int32_t* bid, int64_t n_q, int n_req, int max_ctx,
                    const KeyRows& kr, float* scores, int64_t stride, Plan* plan, int4* groups,
                    int32_t* unit_start, int32_t* t0_list, int n_ctas, uint32_t* hist,
-                   cudaStream_t stream) {
-  using S = Shape<HI, DI>;
+                   const float* q_scale, const float* k_scale, cudaStream_t stream) {
+  using S = Shape<HI, DI, F8>;
   if (hist != nullptr)
     DSA_CHECK_CUDA(cudaMemsetAsync(hist, 0, static_cast<size_t>(n_q) * kHistBins * sizeof(uint32_t),
                                    stream));
@@ -464,17 +493,17 @@ int launch_indexer(const void* q_idx, const float* w, const void* k_idx, int64_t
                                                       unit_start, t0_list);
   DSA_CHECK_CUDA(cudaGetLastError());
   CUtensorMap tk, tq;
-  int rc = make_tmap_bf16_2d(&tk, k_idx, static_cast<uint64_t>(n_kv_rows), DI, DI * 2,
-                             S::kAtomElems, kPageRows, S::kTmaSwz);
+  int rc = make_tmap_2d(&tk, S::kTmaType, k_idx, static_cast<uint64_t>(n_kv_rows), DI,
+                        S::kRowBytes, S::kAtomElems, kPageRows, S::kTmaSwz);
   if (rc) return rc;
-  rc = make_tmap_bf16_2d(&tq, q_idx, static_cast<uint64_t>(n_q * HI), DI, DI * 2, S::kAtomElems,
-                         256, S::kTmaSwz);
+  rc = make_tmap_2d(&tq, S::kTmaType, q_idx, static_cast<uint64_t>(n_q * HI), DI, S::kRowBytes,
+                    S::kAtomElems, 256, S::kTmaSwz);
   if (rc) return rc;
-  DSA_CHECK_CUDA(cudaFuncSetAttribute(indexer_kernel<HI, DI>,
+  DSA_CHECK_CUDA(cudaFuncSetAttribute(indexer_kernel<HI, DI, F8>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmem));
-  indexer_kernel<HI, DI><<<n_ctas, S::kThreads, S::kSmem, stream>>>(
+  indexer_kernel<HI, DI, F8><<<n_ctas, S::kThreads, S::kSmem, stream>>>(
       tk, tq, w, pos, kr, plan, groups, unit_start, scores, stride, max_ctx,
-      static_cast<int>(n_q), hist);
+      static_cast<int>(n_q), hist, q_scale, k_scale);
   DSA_CHECK_CUDA(cudaGetLastError());
   return DSA_OK;
 }
@@ -487,7 +516,8 @@ int indexer_scores(const void* q_idx, const float* w, const void* k_idx, int64_t
                    const int32_t* cu, const int32_t* pos, const int32_t* bid, int64_t n_q, int n_req,
                    int Hi, int Di, int max_ctx, const int32_t* block_table, int max_pages,
                    int page_size, float* scores, int64_t stride, void* ws, size_t ws_bytes,
-                   uint32_t* hist, cudaStream_t stream) {
+                   uint32_t* hist, const float* q_scale, const float* k_scale,
+                   cudaStream_t stream) {
   if (n_q < 0 || max_ctx < 1 || n_kv_rows < 0)
     return fail(DSA_ERR_INVALID, "indexer: need n_q >= 0, max_ctx >= 1, n_kv_rows >= 0");
   if (n_q == 0) return DSA_OK;
@@ -511,14 +541,25 @@ int indexer_scores(const void* q_idx, const float* w, const void* k_idx, int64_t
   const int n_ctas = num_sms_cached();
   KeyRows kr{cu, block_table, max_pages, 0, n_kv_rows};
   if (block_table) kr.n_pages = static_cast<int>(n_kv_rows / kPageRows);
+  const bool f8 = q_scale != nullptr;
+  if (f8 != (k_scale != nullptr))
+    return fail(DSA_ERR_INVALID, "indexer: FP8 rows need both q_scale and k_scale");
+  if (f8) {
+    if (Hi == 64 && Di == 128)
+      return launch_indexer<64, 128, true>(q_idx, w, k_idx, n_kv_rows, pos, bid, n_q, n_req,
+                                           max_ctx, kr, scores, stride, plan, groups, unit_start,
+                                           t0_list, n_ctas, hist, q_scale, k_scale, stream);
+    return fail(DSA_ERR_UNSUPPORTED, "indexer: FP8 (Hi, Di) = (%d, %d) not built; supported "
+                                     "(64, 128)", Hi, Di);
+  }
   if (Hi == 64 && Di == 128)
-    return launch_indexer<64, 128>(q_idx, w, k_idx, n_kv_rows, pos, bid, n_q, n_req, max_ctx, kr,
-                                   scores, stride, plan, groups, unit_start, t0_list, n_ctas,
-                                   hist, stream);
+    return launch_indexer<64, 128, false>(q_idx, w, k_idx, n_kv_rows, pos, bid, n_q, n_req,
+                                          max_ctx, kr, scores, stride, plan, groups, unit_start,
+                                          t0_list, n_ctas, hist, nullptr, nullptr, stream);
   if (Hi == 4 && Di == 32)
-    return launch_indexer<4, 32>(q_idx, w, k_idx, n_kv_rows, pos, bid, n_q, n_req, max_ctx, kr,
-                                 scores, stride, plan, groups, unit_start, t0_list, n_ctas, hist,
-                                 stream);
+    return launch_indexer<4, 32, false>(q_idx, w, k_idx, n_kv_rows, pos, bid, n_q, n_req, max_ctx,
+                                        kr, scores, stride, plan, groups, unit_start, t0_list,
+                                        n_ctas, hist, nullptr, nullptr, stream);
   return fail(DSA_ERR_UNSUPPORTED, "indexer: (Hi, Di) = (%d, %d) not built; supported (64, 128), "
                                    "(4, 32)", Hi, Di);
 }

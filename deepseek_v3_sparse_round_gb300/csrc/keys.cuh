@@ -15,6 +15,9 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 
 constexpr int kHistBins = 2048;     // first radix digit: the top 11 bits of the key
 constexpr int kHistShift = 21;
+// The indexer histograms one key in kHistSample (positions s with s % kHistSample == 0): a
+// sample from which the top-k picks a threshold bin, then counts exactly.
+constexpr int kHistSample = 16;
 
 __device__ __forceinline__ uint32_t first_digit(uint32_t key) { return key >> kHistShift; }
 

@@ -281,6 +281,16 @@ __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D(tmem) (+)= A(smem desc) * B(smem desc)^T, kind::f8f6f4 (here both E4M3, fp32 accumulate);
+// one instruction covers K = 32 eight-bit elements (32 bytes of each operand row).
+__device__ __forceinline__ void umma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // D(tmem) (+)= A(tmem) * B(smem desc)^T, kind::f16. A: M lanes x K/2 columns (two bf16 per
 // 32-bit column, the lower K index in the low half).
 __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
@@ -368,6 +378,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N, uint32
          | (1u << 7)          // A format: bf16
          | (1u << 10)         // B format: bf16
          | (a_mn_major << 15) | (b_mn_major << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f8f6f4 with E4M3 A and B (format code 0 in both fields), fp32
+// D, dense, K-major operands, M x N.
+__host__ __device__ constexpr uint32_t idesc_e4m3(uint32_t M, uint32_t N) {
+  return (1u << 4)            // D format: f32
+         | (0u << 7)          // A format: E4M3
+         | (0u << 10)         // B format: E4M3
+         | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {

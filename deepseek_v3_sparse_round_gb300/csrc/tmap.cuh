@@ -22,11 +22,23 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// A row-major [rows, cols] bf16 tensor with the given row pitch. Box = box_cols x box_rows
-// elements; swizzle one of CU_TENSOR_MAP_SWIZZLE_{NONE,64B,128B}. Out-of-range elements read 0.
+// A row-major [rows, cols] tensor of 2-byte (bf16) or 1-byte (FP8 codes) elements with the
+// given row pitch. Box = box_cols x box_rows elements; swizzle one of
+// CU_TENSOR_MAP_SWIZZLE_{NONE,64B,128B}. Out-of-range elements read 0.
+inline int make_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base,
+                        uint64_t rows, uint64_t cols, uint64_t row_pitch_bytes, uint32_t box_cols,
+                        uint32_t box_rows, CUtensorMapSwizzle swizzle);
+
 inline int make_tmap_bf16_2d(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols,
                              uint64_t row_pitch_bytes, uint32_t box_cols, uint32_t box_rows,
                              CUtensorMapSwizzle swizzle) {
+  return make_tmap_2d(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rows, cols, row_pitch_bytes,
+                      box_cols, box_rows, swizzle);
+}
+
+inline int make_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base,
+                        uint64_t rows, uint64_t cols, uint64_t row_pitch_bytes, uint32_t box_cols,
+                        uint32_t box_rows, CUtensorMapSwizzle swizzle) {
   auto enc = tensor_map_encoder();
   if (!enc) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   if (reinterpret_cast<uintptr_t>(base) % 16 != 0 || row_pitch_bytes % 16 != 0)
@@ -35,7 +47,7 @@ inline int make_tmap_bf16_2d(CUtensorMap* tm, const void* base, uint64_t rows, u
   const cuuint64_t strides[1] = {row_pitch_bytes};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+  CUresult r = enc(tm, dtype, 2, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)

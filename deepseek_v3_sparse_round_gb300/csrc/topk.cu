@@ -305,19 +305,25 @@ topk_kernel(const float* __restrict__ scores, int64_t stride, const int32_t* __r
 }
 
 // ------------------------------------------------------------------------------------------
-// Top-k fed by the indexer's first-digit histograms (the fused indexer -> top-k path).
+// Top-k fed by the indexer's sampled first-digit histograms (the fused indexer -> top-k path).
 //
-// The indexer epilogue counted, for every query, how many of its scores fall in each of the
-// kBins first-digit bins (the top 11 bits of the order key). From that row of counts the bin T0
-// holding the k-th largest score and the number of scores above it are known before the row is
-// read. One pass over the row then keeps only the entries whose digit is >= T0, compacted in
-// index order into shared memory (key and index), typically k plus the boundary bin's few
-// hundred to few thousand entries; the two remaining radix passes and the ordered emission run
-// over that short list. A row whose kept entries exceed kCap (a histogram crowded at the
-// boundary) takes the global-memory passes instead, starting from the known first digit.
+// Rows of up to kCap entries are kept whole in shared memory (key and index). For longer rows
+// the indexer epilogue counted, per query, the first radix digit (top 11 bits of the order key)
+// of one score in kHistSample. From those counts the kernel takes the highest bin T0 above
+// which the sample holds comfortably more than k / kHistSample scores (a margin of four
+// standard deviations), so the entries with digit >= T0 very likely number at least k and only
+// a few thousand. One pass over the row (prefetched into L2 at the start) keeps exactly those
+// entries, compacted in index order; their exact count decides: between k and kCap, the three
+// radix passes and the ordered emission run over that short list; otherwise (a sample that
+// misled, or a crowded boundary) the row takes the global-memory passes. The result is exact
+// either way; the sample only decides how much work it takes.
 constexpr int kCap = 8192;                          // kept entries in shared memory (64 KB)
 constexpr int kCompactPerLane = 16;                 // entries per lane per compaction chunk
 constexpr int kCompactChunk = kThreads * kCompactPerLane;
+
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 __global__ void __launch_bounds__(kThreads, 2)
 topk_hist_kernel(const float* __restrict__ scores, int64_t stride, const int32_t* __restrict__ pos,
@@ -344,29 +350,28 @@ topk_hist_kernel(const float* __restrict__ scores, int64_t stride, const int32_t
     return;
   }
   const float* row = scores + t * stride;
-  {
+  if (threadIdx.x == 0) {                             // the row streams into L2 meanwhile
+    const uint32_t bytes = static_cast<uint32_t>((L + 3) / 4) * 16u;
+    for (uint32_t off = 0; off < bytes; off += 32768u)
+      prefetch_l2_bulk(reinterpret_cast<const char*>(row) + off, min(32768u, bytes - off));
+  }
+  uint32_t T0 = 0;                                    // keep every entry (rows of <= kCap)
+  if (L > kCap) {
     const uint4* h = reinterpret_cast<const uint4*>(hist_rows + t * kBins);
     for (int i = threadIdx.x; i < kBins / 4; i += kThreads)
       reinterpret_cast<uint4*>(hist)[i] = __ldcg(h + i);
-  }
-  __syncthreads();
-  pick_bin(hist, static_cast<uint32_t>(k), warp_tot, &s_digit, &s_above);
-  const uint32_t T0 = s_digit;
-  const uint32_t above = s_above;
-  const uint32_t n_keep = above + hist[T0];
-  __syncthreads();
-  const uint32_t prefix0 = T0 << kHistShift, mask0 = 0x7FFu << kHistShift;
-  uint32_t T, need_eq;
-  if (n_keep > static_cast<uint32_t>(kCap)) {
-    radix_threshold<false>(row, nullptr, L, k, 1, prefix0, mask0, static_cast<uint32_t>(k) - above,
-                           hist, warp_tot, &s_digit, &s_above, &T, &need_eq);
-    emit_ordered_global(row, L, T, need_eq, static_cast<uint32_t>(k) - need_eq, out, warp_tot);
-    return;
+    __syncthreads();
+    const float mean = static_cast<float>(k) / kHistSample;
+    const uint32_t need = static_cast<uint32_t>(ceilf(mean + 4.f * sqrtf(mean))) + 16u;
+    pick_bin(hist, need, warp_tot, &s_digit, &s_above);   // bin 0 if the sample falls short
+    T0 = s_digit;
+    __syncthreads();
   }
 
-  // ---- compaction: entries with digit >= T0, in index order. Warp w reads the 1,024 entries
-  // [base + 1024 w, base + 1024 (w + 1)) of a chunk as 8 coalesced rounds of 32 lanes x 4; the
-  // per-warp counts are scanned across the block, then each round is placed by a warp scan.
+  // ---- compaction: entries with digit >= T0, in index order. Warp w reads its
+  // kCompactPerLane * 32 entries of a chunk in coalesced rounds of 32 lanes x 4; the per-warp
+  // counts are scanned across the block, then each round is placed by a warp scan. Entries
+  // beyond kCap are counted, not stored.
   uint32_t kept_so_far = 0;
   for (int base = 0; base < L; base += kCompactChunk) {
     const int wb = base + warp * (kCompactPerLane * 32);
@@ -413,16 +418,16 @@ topk_hist_kernel(const float* __restrict__ scores, int64_t stride, const int32_t
         if ((keepm[j] & (1u << e)) && dst < static_cast<uint32_t>(kCap)) {
           ckey[dst] = key[j][e];
           cidx[dst] = static_cast<uint32_t>(i + e);
-          ++dst;
         }
+        dst += (keepm[j] >> e) & 1u;
       }
       at += __shfl_sync(0xffffffffu, incl, 31);
     }
     kept_so_far += tot;
   }
   __syncthreads();
-  if (kept_so_far != n_keep) {                        // the histogram does not match the row
-    if (threadIdx.x == 0) report_device_error(kErrBadIndex | 0xC1u);
+  uint32_t T, need_eq;
+  if (kept_so_far > static_cast<uint32_t>(kCap) || kept_so_far < static_cast<uint32_t>(k)) {
     radix_threshold<false>(row, nullptr, L, k, 0, 0u, 0u, static_cast<uint32_t>(k), hist,
                            warp_tot, &s_digit, &s_above, &T, &need_eq);
     emit_ordered_global(row, L, T, need_eq, static_cast<uint32_t>(k) - need_eq, out, warp_tot);
@@ -430,14 +435,14 @@ topk_hist_kernel(const float* __restrict__ scores, int64_t stride, const int32_t
   }
   const int n = static_cast<int>(kept_so_far);
 
-  // ---- radix passes 2 and 3 over the kept entries of the boundary bin ----
-  uint32_t prefix = prefix0, prefix_mask = mask0;
-  uint32_t remaining = static_cast<uint32_t>(k) - above;
+  // ---- three radix passes over the kept entries ----
+  uint32_t prefix = 0, prefix_mask = 0;
+  uint32_t remaining = static_cast<uint32_t>(k);
 #pragma unroll 1
-  for (int p = 1; p < 3; ++p) {
+  for (int p = 0; p < 3; ++p) {
     for (int b = threadIdx.x; b < kBins; b += kThreads) hist[b] = 0;
     __syncthreads();
-    const int sh = p == 1 ? 10 : 0;
+    const int sh = p == 0 ? 21 : (p == 1 ? 10 : 0);
     const uint32_t dm = p == 2 ? 0x3FFu : 0x7FFu;
     for (int i = threadIdx.x; i < n; i += kThreads) {
       const uint32_t key = ckey[i];
@@ -518,8 +523,8 @@ cudaError_t topk_read_errors(uint32_t* flags) { return read_and_clear_device_err
 
 namespace dsa {
 
-// Top-k of rows whose first-digit histograms (hist_rows [n_q, kHistBins] u32, complete counts
-// of every score s <= pos_t of the row) the indexer produced.
+// Top-k of rows whose sampled first-digit histograms (hist_rows [n_q, kHistBins] u32, counts of
+// the scores at positions s <= pos_t with s % kHistSample == 0) the indexer produced.
 int topk_select_hist(const float* scores, int64_t score_stride, const int32_t* pos, int64_t n_q,
                      int k, int max_ctx, const uint32_t* hist_rows, int32_t* topk,
                      cudaStream_t stream) {

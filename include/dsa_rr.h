@@ -250,12 +250,56 @@ int dsa_topk_select(const float* scores, int64_t score_stride, const int32_t* po
 /*
  * dsa_indexer_scores followed by dsa_topk_select, the score rows living in `workspace`.
  * topk: int32 [n_q, k], entries are positions s inside the query's request (0..pos_t) or -1.
+ * When max_ctx > 8192 the two steps are fused (same result): the indexer also counts, per
+ * query, the first radix digit (top 11 bits of the order-preserving key) of one score in 16, the
+ * top-k picks from those counts a threshold bin that very likely keeps at least k and only a few
+ * thousand entries, reads each row once keeping exactly the entries at or above it, and selects
+ * from that short list (rows where the sample misled are re-read in full). The workspace then
+ * also holds these counts (dsa_indexer_topk_workspace_size includes them).
  */
 int dsa_indexer_topk(const void* q_idx, const float* w, const void* k_idx, int64_t n_kv_rows,
                      const int32_t* cu, int n_req, const int32_t* pos, const int32_t* bid,
                      int64_t n_q, int Hi, int Di, int k, int max_ctx, const int32_t* block_table,
                      int max_pages, int page_size, int32_t* topk, void* workspace,
                      size_t workspace_bytes, dsa_stream_t stream);
+
+/*
+ * FP8 (E4M3) rows for the indexer ("[DeepSeek v3.2] 上下文并行详解", section 1: the round-robin
+ * split is what allows an FP8 KV cache). The page names no format; the library reads it as:
+ * E4M3 codes (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits; largest finite 448;
+ * S.1111.111 is NaN) with one fp32 scale per row of 128 values, the row standing for
+ * code * scale. Quantisation: scale = amax / 448 (1 for a row of zeros), code = E4M3(x / scale)
+ * rounded to nearest even and saturated at +-448, both divisions IEEE fp32.
+ *
+ * dsa_quantize_fp8_rows: x bf16 [rows, cols] -> codes uint8 [rows, cols], scales fp32 [rows];
+ * cols must be 128 (DSA_ERR_UNSUPPORTED otherwise); x 8-byte and codes 4-byte aligned. Used
+ * for k_idx (one row per token) and for q_idx (one row per (query, head): [n_q * Hi, 128]).
+ */
+int dsa_quantize_fp8_rows(const void* x, int64_t rows, int cols, void* codes, float* scales,
+                          dsa_stream_t stream);
+
+/*
+ * Lightning-indexer scores on FP8 rows (tcgen05 kind::f8f6f4, fp32 accumulation): the indexer
+ * of the dequantised rows,
+ *     I[t, s] = sum_h w[t, h] * ReLU( (q_scale[t, h] q8[t, h, :]) . (k_scale[r] k8[r, :]) ),
+ * r = row(b_t, s), computed as k_scale[r] * sum_h (w[t, h] q_scale[t, h]) ReLU(q8 . k8) (the
+ * scales are positive). q8 uint8 E4M3 [n_q, Hi, Di], q_scale fp32 [n_q, Hi], k8 uint8 E4M3
+ * [n_kv_rows, Di] (contiguous or a page pool), k_scale fp32 [n_kv_rows]. Every other argument,
+ * the layouts, the workspace and the errors are those of dsa_indexer_scores / dsa_indexer_topk.
+ * Supported: (Hi, Di) = (64, 128). Scales must be positive and finite.
+ */
+int dsa_indexer_scores_fp8(const void* q8, const float* q_scale, const float* w, const void* k8,
+                           const float* k_scale, int64_t n_kv_rows, const int32_t* cu, int n_req,
+                           const int32_t* pos, const int32_t* bid, int64_t n_q, int Hi, int Di,
+                           int max_ctx, const int32_t* block_table, int max_pages, int page_size,
+                           float* scores, int64_t score_stride, void* workspace,
+                           size_t workspace_bytes, dsa_stream_t stream);
+int dsa_indexer_topk_fp8(const void* q8, const float* q_scale, const float* w, const void* k8,
+                         const float* k_scale, int64_t n_kv_rows, const int32_t* cu, int n_req,
+                         const int32_t* pos, const int32_t* bid, int64_t n_q, int Hi, int Di,
+                         int k, int max_ctx, const int32_t* block_table, int max_pages,
+                         int page_size, int32_t* topk, void* workspace, size_t workspace_bytes,
+                         dsa_stream_t stream);
 
 /*
  * Sparse MLA on tcgen05 tensor cores (the selected rows are gathered into shared memory by

@@ -135,3 +135,19 @@ def test_fused_crowded_boundary_bin_takes_the_global_path():
         want = np.full(2048, -1)
         want[:min(L, 2048)] = np.arange(min(L, 2048))
         assert np.array_equal(fused[t], want), t
+
+
+def test_fused_misleading_sample_stays_exact():
+    """The indexer's histogram samples one key position in 16. Keys at sampled positions are
+    made to score higher than the rest (their k_idx rows tripled), so the sample points at a
+    threshold that keeps fewer than k entries of a long row: the kernel notices from the exact
+    count and takes the global-memory passes. The index sets are still the oracle's."""
+    sh = Shard(W.WORKLOADS[2], 3, integer_indexer=True)
+    k = sh.idx.k_idx.clone()
+    k[0::16] = (k[0::16].float() * 3).to(torch.bfloat16)         # one request: row = position
+    sh.idx.k_idx = k
+    fused = _fused_equals_separate(sh).cpu().numpy()
+    sel = np.array([4095, 4000, 2600, 1500, 1100])
+    ora = sh.oracle_topk(sh.oracle_scores(sel))
+    for i, t in enumerate(sel):
+        assert np.array_equal(fused[t], ora[i]), t

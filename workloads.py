@@ -206,3 +206,25 @@ def sample_queries(n_q: int, must: np.ndarray, n_sample: int, seed: int) -> np.n
     extra = max(0, n_sample - len(must))
     pick = rng.choice(rest, size=min(extra, len(rest)), replace=False) if len(rest) else rest
     return np.unique(np.concatenate([must, pick]))
+
+
+# E4M3 byte codes of the small integers -3..3 (sign bit 0x80; 1 = 0x38, 2 = 0x40, 3 = 0x44 under
+# the E4M3 layout: 4 exponent bits with bias 7, 3 mantissa bits). Input layout only: the tests
+# use them to build FP8 rows whose values are exact integers.
+_E4M3_SMALL_INT_CODES = {-3: 0xC4, -2: 0xC0, -1: 0xB8, 0: 0x00, 1: 0x38, 2: 0x40, 3: 0x44}
+
+
+def int_codes_e4m3(shape, lo: int, hi: int, seed: int, device="cpu") -> torch.Tensor:
+    """uint8 E4M3 codes of integers uniform in [lo, hi] (within -3..3)."""
+    assert -3 <= lo <= hi <= 3
+    table = torch.zeros(7, dtype=torch.uint8)
+    for v, c in _E4M3_SMALL_INT_CODES.items():
+        table[v + 3] = c
+    x = torch.randint(lo, hi + 1, tuple(shape), generator=_gen(seed, device), device=device)
+    return table.to(device)[x + 3]
+
+
+def pow2_scales(shape, lo_exp: int, hi_exp: int, seed: int, device="cpu") -> torch.Tensor:
+    """fp32 powers of two 2^e with e uniform in [lo_exp, hi_exp]."""
+    e = torch.randint(lo_exp, hi_exp + 1, tuple(shape), generator=_gen(seed, device), device=device)
+    return torch.pow(2.0, e.to(torch.float32))
