@@ -421,7 +421,7 @@ constexpr int kOffAlpha = kOffX + kXBytes;      // CTA 1: [2][kAFStride] alpha +
 constexpr int kOffL = kOffAlpha + 2 * kAFStride;  // CTA 1: fp32 [2][128]
 constexpr int kOffNT = kOffL + 2 * 128 * 4;     // both: int [2] tiles of the query
 constexpr int kOffBar = kOffNT + 8;
-constexpr int kNumBars = 4 * kStages + 22;
+constexpr int kNumBars = 4 * kStages + 21;
 constexpr int kOffTmem = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmem + 4;
 constexpr int kOffCorrJ = kOffAbort + 4;
@@ -437,13 +437,20 @@ constexpr int kMmaWarp = 4, kGatherWarp0 = 5, kCourierWarp = kGatherWarp0 + kSta
               kMetaWarp = kCourierWarp + 1, kGatherWarp1 = kMetaWarp + 1;
 static_assert(kGatherWarp1 + (kGatherPerSlot - 1) * kStages == kThreads / 32, "warp roles");
 constexpr float kLazyLog2 = 16.f;               // rescale O only when the max grows by > 2^16
+// CTA 0 brings each query's Q into TMEM through its ring: kQPieces ring entries ahead of the
+// query's key tiles, each 128 rows x kQAtomsPerPiece swizzle atoms of 64 dims (128 B per row),
+// gathered like key rows and copied into TMEM by the QK issuer (tcgen05.cp).
+constexpr int kQPieces = 3, kQAtomsPerPiece = 3;
+constexpr int kQAtomBytes = kH * 128;           // 128 rows x 128 B: 16 KB
+static_assert(kQPieces * kQAtomsPerPiece * 64 == kDQK, "Q pieces cover the 576 dims");
+static_assert(kQAtomsPerPiece * kQAtomBytes <= kStageS, "a Q piece fits a ring slot");
 // barrier indices
 constexpr int kKvFull = 0, kKvEmpty = kStages, kPStaged = 2 * kStages, kPSEmpty = kPStaged + 2,
               kSFull = kPStaged + 4, kSEmpty = kSFull + kStages, kPFull = kSEmpty + kStages,
               kPEmpty = kPFull + 2, kMetaFull = kPEmpty + 2, kMetaEmpty = kMetaFull + 2,
-              kLReady = kMetaEmpty + 2, kLEmpty = kLReady + 2, kQReady = kLEmpty + 2,
-              kQAck = kQReady + 1, kCorrGo = kQReady + 2, kCorrReady = kQReady + 3,
-              kCorrDone = kQReady + 4, kOFinal = kQReady + 5;
+              kLReady = kMetaEmpty + 2, kLEmpty = kLReady + 2, kQFree = kLEmpty + 2,
+              kCorrGo = kQFree + 1, kCorrReady = kQFree + 2, kCorrDone = kQFree + 3,
+              kOFinal = kQFree + 4;
 static_assert(kOFinal + 1 == kNumBars, "barrier count");
 static_assert(kSmem <= 232448, "smem budget");
 static_assert(kOffPS % 16 == 0 && kPSStride % 16 == 0, "bulk copy sources are 16-byte aligned");
@@ -462,6 +469,7 @@ static_assert(kStageS % 1024 == 0 && kStageO % 1024 == 0 && kAtomBytes % 1024 ==
 // Every role waits for every per-query phase in order, also for queries where it has no tile.
 __global__ void __launch_bounds__(pair::kThreads, 1)
 sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
+                       const __grid_constant__ CUtensorMap tm_q,
                        const __nv_bfloat16* __restrict__ c, const __nv_bfloat16* __restrict__ q,
                        const int32_t* __restrict__ bid, const int32_t* __restrict__ topk, int k,
                        int64_t n_q, KvMap kv, float scale_log2, float* __restrict__ lse,
@@ -507,8 +515,7 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
       mbar_init(bar(kLReady + i), 1);               // CTA 1: armed with 512 tx bytes per query
       mbar_init(bar(kLEmpty + i), 128);
     }
-    mbar_init(bar(kQReady), 128);
-    mbar_init(bar(kQAck), 1);
+    mbar_init(bar(kQFree), 1);                      // CTA 0: every QK of a query complete
     mbar_init(bar(kCorrGo), 1);
     mbar_init(bar(kCorrReady), 1);
     mbar_init(bar(kCorrDone), 128);
@@ -534,6 +541,7 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
   };
 
   if (warp == kMetaWarp) {
+    if (lane == 0 && crank == 0) tma_prefetch_desc(&tm_q);
     // ---------------------------------------------------------------- query metadata
     // Tile count (tiles up to the last valid entry) and, in CTA 0, the per-tile validity masks
     // of each query, two queries ahead; also pulls the query's Q rows into L2.
@@ -603,7 +611,11 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
     const uint32_t stage = sbase + s * (crank == 0 ? kStageS : kStageO);
     const int chunk = static_cast<int>(lane & 7);
     bool bad = false;
-    int64_t g0 = 0;                                  // global index of the query's first tile
+    int64_t q_tma_rp = -1;                           // ring position of this lane's last Q load
+    // Ring entries of a query: CTA 0 first its kQPieces Q pieces (not for a query without
+    // keys), then its key tiles; CTA 1 only the tiles (V). rpos0 = ring position of the query's
+    // first entry; slot s takes the positions = s (mod kStages).
+    int64_t rpos0 = 0;
     for (int n = 0; n < n_my && !*abort_flag; ++n) {
       const int nt = meta_wait(n, true);
       if (nt < 0) break;
@@ -616,33 +628,55 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
       bad |= !b_ok;
       const int bb = b_ok ? b : 0;
       const int lim = b_ok ? entry_limit(kv, b, t) : -1;
-      const int j_first = static_cast<int>(((s - g0) % kStages + kStages) % kStages);
+      const int n_pre = (crank == 0 && nt > 0) ? kQPieces : 0;
+      const int n_ent = n_pre + nt;
+      const int e_first = static_cast<int>(((s - rpos0) % kStages + kStages) % kStages);
       auto fetch = [&](int j, int& s0, int& s1) {
         const int e0 = j * kKeys + static_cast<int>(lane);
-        s0 = (j < nt && e0 < k && b_ok) ? __ldg(trow + e0) : -1;
-        s1 = (j < nt && lane < kKeys - 32 && e0 + 32 < k && b_ok) ? __ldg(trow + e0 + 32) : -1;
+        s0 = (j >= 0 && j < nt && e0 < k && b_ok) ? __ldg(trow + e0) : -1;
+        s1 = (j >= 0 && j < nt && lane < kKeys - 32 && e0 + 32 < k && b_ok) ? __ldg(trow + e0 + 32) : -1;
       };
       int s0, s1;
-      fetch(j_first, s0, s1);
+      {                                              // first key tile this warp gathers
+        int e = e_first;
+        while (e < n_pre) e += kStages;
+        fetch(e - n_pre, s0, s1);
+      }
       bool ok = true;
-      for (int j = j_first; j < nt; j += kStages) {
-        const int64_t g = g0 + j;
-        if (!warp_wait(bar(kKvEmpty + s), static_cast<uint32_t>(((g / kStages) & 1) ^ 1), 0x21,
+      for (int e = e_first; e < n_ent; e += kStages) {
+        const int64_t rp = rpos0 + e;
+        if (!warp_wait(bar(kKvEmpty + s), static_cast<uint32_t>(((rp / kStages) & 1) ^ 1), 0x21,
                        abort_flag)) { ok = false; break; }
-        const int32_t r0 = kv_row(kv, bb, s0, lim, &bad);
-        const int32_t r1 = kv_row(kv, bb, s1, lim, &bad);
-        fetch(j + kStages, s0, s1);
+        if (e < n_pre) {
+          // Q piece e: rows 0..127 (heads) of q[t], atoms kQAtomsPerPiece*e .. +2, each one TMA
+          // box of 128 rows x 64 dims in the 128B-swizzled layout; the bytes complete on the
+          // slot's full barrier next to the warps' usual arrivals (the byte count is added
+          // without an arrival of its own, before this lane's arrival below)
+          if (half == 0 && lane == 0) {
+            mbar_add_tx(bar(kKvFull + s), kQAtomsPerPiece * kQAtomBytes);
 #pragma unroll
-        for (int i = half; i < kKeys / 4; i += kGatherPerSlot) {
-          const int r = static_cast<int>(lane >> 3) + 4 * i;        // tile row of this lane
-          const int32_t ra = __shfl_sync(0xffffffffu, r0, r & 31);
-          const int32_t rb = __shfl_sync(0xffffffffu, r1, r & 31);
-          const int32_t row = r < 32 ? ra : rb;
-          const bool valid = row < kv.n_rows;
-          const __nv_bfloat16* src = c + (valid ? static_cast<int64_t>(row) * kDQK : 0) + chunk * 8;
-          const uint32_t dst = stage + r * 128 + ((chunk ^ (r & 7)) * 16);   // r & 7: atoms are 1 KB aligned
-          for (int a = 0; a < n_atoms; ++a)
-            cp_async16(dst + a * kAtomBytes, src + a * 64, valid ? 16u : 0u);
+            for (int a = 0; a < kQAtomsPerPiece; ++a)
+              tma_load_2d(stage + a * kQAtomBytes, &tm_q, (e * kQAtomsPerPiece + a) * 64,
+                          static_cast<int32_t>(t * kH), bar(kKvFull + s));
+            q_tma_rp = rp;
+          }
+        } else {
+          const int j = e - n_pre;
+          const int32_t r0 = kv_row(kv, bb, s0, lim, &bad);
+          const int32_t r1 = kv_row(kv, bb, s1, lim, &bad);
+          fetch(j + kStages, s0, s1);
+#pragma unroll
+          for (int i = half; i < kKeys / 4; i += kGatherPerSlot) {
+            const int r = static_cast<int>(lane >> 3) + 4 * i;        // tile row of this lane
+            const int32_t ra = __shfl_sync(0xffffffffu, r0, r & 31);
+            const int32_t rb = __shfl_sync(0xffffffffu, r1, r & 31);
+            const int32_t row = r < 32 ? ra : rb;
+            const bool valid = row < kv.n_rows;
+            const __nv_bfloat16* src = c + (valid ? static_cast<int64_t>(row) * kDQK : 0) + chunk * 8;
+            const uint32_t dst = stage + r * 128 + ((chunk ^ (r & 7)) * 16);   // r & 7: atoms are 1 KB aligned
+            for (int a = 0; a < n_atoms; ++a)
+              cp_async16(dst + a * kAtomBytes, src + a * 64, valid ? 16u : 0u);
+          }
         }
         cp_async_commit();
         cp_async_wait_all();
@@ -650,9 +684,16 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
         mbar_arrive(bar(kKvFull + s));
       }
       if (!ok) break;
-      g0 += nt;
+      rpos0 += n_ent;
     }
     cp_async_wait_all();
+    if (*abort_flag && q_tma_rp >= 0) {
+      // unwinding: let this lane's last Q load land before the CTA can exit (bounded)
+      const long long t0 = clock64();
+      while (!mbar_try_wait(bar(kKvFull + s), static_cast<uint32_t>((q_tma_rp / kStages) & 1)) &&
+             clock64() - t0 < kWaitLimitCycles) {
+      }
+    }
     if (__any_sync(0xffffffffu, bad) && lane == 0) report_device_error(kErrBadIndex);
   } else if (warp == kMmaWarp && crank == 0) {
     // ---------------------------------------------------------------- CTA 0: QK issuer
@@ -663,23 +704,49 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
     const bool leader = elect_one();
     const uint32_t idesc = idesc_bf16(128, kKeys, 0, 0);
     const uint64_t desc0 = smem_desc(sbase, 16, 1024, kSwizzle128B);
-    int64_t g0 = 0;
+    int64_t rpos0 = 0, g0 = 0;                       // ring position; S-buffer (tile) index
     bool ok = true;
     for (int n = 0; n < n_my && ok; ++n) {
       const int nt = meta_wait(n, true);
       if (nt < 0) break;
       __syncwarp();
       if (leader) mbar_arrive(bar(kMetaEmpty + (n & 1)));
-      if (!warp_wait(bar(kQReady), n & 1, 0x22, abort_flag)) break;
-      if (leader) mbar_arrive(bar(kQAck));         // lets the softmax load the next Q later
+      const int n_pre = nt > 0 ? kQPieces : 0;
+      // Q pieces -> TMEM columns kColQ.. (the A operand of QK), once every QK MMA and copy of
+      // the previous query is complete (kQFree; an MMA issued after a copy by this thread sees it).
+      for (int pce = 0; pce < n_pre; ++pce) {
+        const int64_t rp = rpos0 + pce;
+        const int s = static_cast<int>(rp % kStages);
+        if (!warp_wait(bar(kKvFull + s), static_cast<uint32_t>((rp / kStages) & 1), 0x22,
+                       abort_flag)) { ok = false; break; }
+        if (pce == 0 && n > 0 &&
+            !warp_wait(bar(kQFree), static_cast<uint32_t>((n - 1) & 1), 0x25, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (leader) {
+          const uint64_t dq = desc0 + static_cast<uint64_t>((s * kStageS) >> 4);
+#pragma unroll
+          for (int a = 0; a < kQAtomsPerPiece; ++a)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)           // 16 dims (8 columns) per copy
+              tmem_cp_128x256b(tmem + kColQ + (pce * kQAtomsPerPiece + a) * 32 + kk * 8,
+                               dq + static_cast<uint64_t>((a * kQAtomBytes + kk * 32) >> 4));
+          umma_commit(bar(kKvEmpty + s));            // the slot is free once the copies read it
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
       tc_fence_after();
       for (int j = 0; j < nt; ++j) {
-        const int64_t g = g0 + j;
-        const int s = static_cast<int>(g % kStages), sb = s;
+        const int64_t rp = rpos0 + n_pre + j, g = g0 + j;
+        const int s = static_cast<int>(rp % kStages), sb = static_cast<int>(g % kStages);
         const uint32_t d_s = tmem + kColS + sb * kSStride;
-        const uint32_t ph = static_cast<uint32_t>((g / kStages) & 1);
-        if (!warp_wait(bar(kKvFull + s), ph, 0x23, abort_flag)) { ok = false; break; }
-        if (!warp_wait(bar(kSEmpty + sb), ph ^ 1, 0x24, abort_flag)) { ok = false; break; }
+        if (!warp_wait(bar(kKvFull + s), static_cast<uint32_t>((rp / kStages) & 1), 0x23,
+                       abort_flag)) { ok = false; break; }
+        if (!warp_wait(bar(kSEmpty + sb), static_cast<uint32_t>(((g / kStages) & 1) ^ 1), 0x24,
+                       abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint64_t db0 = desc0 + static_cast<uint64_t>((s * kStageS) >> 4);
 #pragma unroll
@@ -694,6 +761,9 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
         }
         __syncwarp();
       }
+      if (leader) umma_commit(bar(kQFree));        // Q of this query no longer read
+      __syncwarp();
+      rpos0 += n_pre + nt;
       g0 += nt;
     }
   } else if (warp == kMmaWarp) {
@@ -779,7 +849,7 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
         if (!ok) break;
         g0 += nt;
       }
-      bulk_wait_read_all();
+      bulk_wait_all();                               // every copy to the peer has landed
     }
   } else if (crank == 0 && warp < 4) {
     // ---------------------------------------------------------------- CTA 0: softmax warps
@@ -790,64 +860,6 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
       const int nt = meta_wait(n, true);
       if (nt < 0) break;
       const int64_t t = query(n);
-      // Q row -> TMEM (A operand of QK) once every QK of the previous query is complete (its
-      // last softmax tile saw them) and both issuers acknowledged the previous Q.
-      if (n > 0 && !warp_wait(bar(kQAck), (n - 1) & 1, 0x42, abort_flag)) break;
-      {
-        // Coalesced: each warp-wide cp.async covers 4 rows x 128 B of the warp's 32 Q rows; the
-        // rows are transposed through swizzled 4 KB staging tiles so that lane i ends up holding
-        // row i (its TMEM lane), one 64-dim atom (32 TMEM columns) at a time, three atoms in
-        // flight. The tiles are the warp's slice of the Q staging region and of the two P
-        // staging buffers, which stay idle between the last P shipment of the previous query
-        // and this query's first softmax tile: wait until the courier has shipped them.
-        if (g0 >= 1 && !warp_wait(bar(kPSEmpty + static_cast<int>((g0 - 1) & 1)),
-                                  static_cast<uint32_t>(((g0 - 1) >> 1) & 1), 0x44, abort_flag)) break;
-        if (g0 >= 2 && !warp_wait(bar(kPSEmpty + static_cast<int>((g0 - 2) & 1)),
-                                  static_cast<uint32_t>(((g0 - 2) >> 1) & 1), 0x45, abort_flag)) break;
-        const char* qw = reinterpret_cast<const char*>(q + (t * kH + warp * 32) * kDQK);
-        const uint32_t xoff[3] = {static_cast<uint32_t>(kOffX + warp * (32 * 128)),
-                                  static_cast<uint32_t>(kOffPS + warp * (32 * 128)),
-                                  static_cast<uint32_t>(kOffPS + kPSStride + warp * (32 * 128))};
-        const int lrow = static_cast<int>(lane >> 3), lchunk = static_cast<int>(lane & 7);
-        constexpr int kQAtoms = kDQK / 64;           // 9
-        auto issue_atom = [&](int a) {
-          const uint32_t x = sbase + xoff[a % 3];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int row = 4 * i + lrow;
-            cp_async16(x + row * 128 + ((lchunk ^ (row & 7)) * 16),
-                       qw + row * (kDQK * 2) + a * 128 + lchunk * 16, 16u);
-          }
-          cp_async_commit();
-        };
-        issue_atom(0);
-        issue_atom(1);
-        issue_atom(2);
-#pragma unroll
-        for (int a = 0; a < kQAtoms; ++a) {
-          if (a + 2 < kQAtoms) cp_async_wait_group<2>();
-          else if (a + 1 < kQAtoms) cp_async_wait_group<1>();
-          else cp_async_wait_group<0>();
-          __syncwarp();                              // every lane's copies of atom a landed
-          const uint8_t* xr = smem + xoff[a % 3] + lane * 128;
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {     // 16 TMEM columns (32 dims) at a time
-            uint32_t r[16];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              const int cc = 4 * half + q4;
-              const uint4 u = *reinterpret_cast<const uint4*>(xr + ((cc ^ (lane & 7)) * 16));
-              r[4 * q4] = u.x; r[4 * q4 + 1] = u.y; r[4 * q4 + 2] = u.z; r[4 * q4 + 3] = u.w;
-            }
-            tmem_st16(tmem + lane_base + kColQ + a * 32 + half * 16, r);
-          }
-          __syncwarp();                              // the tile is refilled with atom a + 3
-          if (a + 3 < kQAtoms) issue_atom(a + 3);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(kQReady));
-      }
       const uint32_t* mwords = reinterpret_cast<const uint32_t*>(smem + kOffMask) + (n & 1) * kMaskWords;
       float m_ref = -INFINITY, l_run = 0.f;
       bool ok = true;
@@ -1090,10 +1102,13 @@ int launch_mla_pair(const void* q, const void* c, int64_t n_kv_rows, const KvMap
                     void* o, float* lse, const int32_t* pos, int32_t* order_ws,
                     cudaStream_t stream) {
   (void)n_kv_rows;
-  CUtensorMap tm_o;                                  // o as [n_q * 128 rows, 512 columns]
+  CUtensorMap tm_o, tm_q;                            // o as [n_q * 128 rows, 512 columns]
   int rc = make_tmap_bf16_2d(&tm_o, o, static_cast<uint64_t>(n_q) * pair::kH, pair::kDV,
                              pair::kDV * 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc) return rc;
+  rc = make_tmap_bf16_2d(&tm_q, q, static_cast<uint64_t>(n_q) * pair::kH, pair::kDQK,
+                         pair::kDQK * 2, 64, pair::kH, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc) return rc;                                 // q as [n_q * 128 rows, 576 columns]
   DSA_CHECK_CUDA(cudaFuncSetAttribute(sparse_mla_pair_kernel,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, pair::kSmem));
   const int64_t pairs = std::min<int64_t>(n_q, num_sms_cached() / 2);
@@ -1117,7 +1132,7 @@ int launch_mla_pair(const void* q, const void* c, int64_t n_kv_rows, const KvMap
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const float scale_log2 = scale * 1.4426950408889634f;
-  DSA_CHECK_CUDA(cudaLaunchKernelEx(&cfg, sparse_mla_pair_kernel, tm_o,
+  DSA_CHECK_CUDA(cudaLaunchKernelEx(&cfg, sparse_mla_pair_kernel, tm_o, tm_q,
                                     static_cast<const __nv_bfloat16*>(c),
                                     static_cast<const __nv_bfloat16*>(q), bid, topk, k, n_q, kv,
                                     scale_log2, lse, order));
@@ -1164,7 +1179,7 @@ int sparse_mla(const void* q, const void* c, int64_t n_kv_rows, const int32_t* c
   if (block_table && (page_size != kPageRows || max_pages < 1))
     return fail(DSA_ERR_UNSUPPORTED, "mla: paged KV needs page_size 64 (got %d)", page_size);
   if (k > kMaxK) return fail(DSA_ERR_UNSUPPORTED, "mla: k = %d > %d", k, kMaxK);
-  if (n_kv_rows >= (1ll << 31) || n_q > (1ll << 30))
+  if (n_kv_rows >= (1ll << 31) || n_q * static_cast<int64_t>(H) >= (1ll << 31))
     return fail(DSA_ERR_UNSUPPORTED, "mla: sizes beyond 32-bit TMA coordinates");
   if (reinterpret_cast<uintptr_t>(q) % 16 || reinterpret_cast<uintptr_t>(o) % 16)
     return fail(DSA_ERR_INVALID, "mla: q and o must be 16-byte aligned");

@@ -36,8 +36,15 @@ __device__ __forceinline__ void fence_mbar_init() {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// Arrive on `bar` and add `bytes` to its expected transaction count (one arrival).
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+// Add `bytes` to the expected transaction count of the current phase without arriving (for a
+// barrier whose arrivals come from other instructions).
+__device__ __forceinline__ void mbar_add_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
 // Arrive on the barrier at the same offset in another CTA of the cluster.
@@ -314,6 +321,14 @@ __device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t cta
       " [%0], %1;" ::"r"(bar),
       "h"(cta_mask)
       : "memory");
+}
+// Copy a 128-row x 256-bit block (32 bytes per row) from shared memory, described by a matrix
+// descriptor like an MMA operand, into TMEM lanes 0..127, 8 consecutive 32-bit columns from
+// `taddr`. Asynchronous: completion is tracked by tcgen05.commit; an MMA issued later by the same
+// thread sees the copied data.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t src_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(src_desc)
+               : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
