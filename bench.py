@@ -163,8 +163,9 @@ class ConfigStep:
     batch, back to back. Inputs are drawn on the device (seeded); `host()` makes pinned host
     copies for the end-to-end run."""
 
-    LAUNCHES_PER_SHARD = 8   # split (+gather), 2 reranges, indexer plan, indexer, top-k,
-    #                          MLA schedule, MLA -- as the ncu launch list of a step shows
+    LAUNCHES_PER_SHARD = 7   # split (+gather), rerange (k_idx and latent rows together),
+    #                          indexer plan, indexer, top-k, MLA schedule, MLA -- as the ncu
+    #                          launch list of a step shows
 
     def __init__(self, torch, dsa, W, wid, device):
         self.torch, self.dsa, self.W = torch, dsa, W
@@ -221,8 +222,8 @@ class ConfigStep:
         dsa.dsa_rr_split_metadata(sh["cu"], self.N, wl.sp, r, out["cu_shard"], out["pos"],
                                   out["bid"], out["gidx"], src_rows=sh["c_log"],
                                   dst_rows=out["c_local"])
-        dsa.dsa_rr_rerange(sh["k_gath"], self.k_idx, self.N, wl.sp, 0)
-        dsa.dsa_rr_rerange(sh["c_gath"], self.c, self.N, wl.sp, 0)
+        dsa.dsa_rr_rerange_multi([sh["k_gath"], sh["c_gath"]], [self.k_idx, self.c], self.N,
+                                 wl.sp, 0)
         if ev is not None:
             ev[1].record()
         topk = self.topk[:n]
@@ -505,7 +506,8 @@ def gpu_arm(args):
                    "queries_per_gpu": st.queries(), "kv_tokens": st.N, "topk": wl.topk,
                    "shard_queries": [st.n_r[r] for r in st.ranks],
                    "l2": "flushed between timed steps (256 MB write)",
-                   "step": "per shard: split+gather, 2x rerange, indexer scores, top-k, sparse MLA",
+                   "step": "per shard: split+gather, rerange (k_idx + latent rows, one launch), "
+                           "indexer scores, top-k, sparse MLA",
                    "multi_gpu": "independent replicas of the whole batch (no collective)"},
         "roofline": roofline_obj(
             "sparse_mla_pair_kernel", "tensor", mla_ach, pk["bf16"], "TFLOP/s", NOMINAL["bf16"],
@@ -525,7 +527,7 @@ def gpu_arm(args):
              "unit_of_work": "causal (query, key) pair: 2*64*128 = 16,384 flop",
              "timing": "CUDA events around each indexer+top-k call (plan, indexer, top-k)"}),
         "roofline_split_rerange": roofline_obj(
-            "split_kernel + copy_rows_v16_kernel", "hbm", cp_ach, pk["hbm"], "GB/s",
+            "split_kernel + rerange_multi_kernel", "hbm", cp_ach, pk["hbm"], "GB/s",
             NOMINAL["hbm"], None,
             {"algorithmic_bytes_per_step": work["copy_bytes"],
              "unit_of_work": "row moved: 2 x row bytes (read + write)"}),
@@ -812,7 +814,7 @@ def config_rows(args):
     for wid in (1, 2, 3, 4):
         wl = W.WORKLOADS[wid]
         ranks = (0,) if wl.decode_queries else wl.ranks
-        tot_q = tot_idx = tot_mla = 0.0
+        tot_q = tot_idx = tot_mla = tot_idx8 = 0.0
         idx_flop = mla_flop = idx_bytes = mla_bytes = 0.0
         for rank in ranks:
             si = shard_inputs(wl, rank)
@@ -834,6 +836,21 @@ def config_rows(args):
                                                         si["pos"], topk, wl.scale, o, mws,
                                                         lse=lse, block_table=si["bt"])
             t_idx, t_mla = timed([f_idx, f_mla])
+            # the FP8 (E4M3) indexer rows: quantised once, outside the timed region
+            q8 = torch.empty(idx.q_idx.shape, dtype=torch.uint8, device="cuda")
+            qs = torch.empty(idx.q_idx.shape[:2], dtype=torch.float32, device="cuda")
+            k8 = torch.empty(idx.k_idx.shape, dtype=torch.uint8, device="cuda")
+            ks = torch.empty(idx.k_idx.shape[0], dtype=torch.float32, device="cuda")
+            dsa.dsa_quantize_fp8_rows(idx.q_idx, q8, qs)
+            dsa.dsa_quantize_fp8_rows(idx.k_idx, k8, ks)
+            topk8 = torch.empty_like(topk)
+            f_idx8 = lambda: dsa.dsa_indexer_topk_fp8(q8, qs, idx.w, k8, ks, si["cu"], n_req,
+                                                      si["pos"], si["bid"], wl.topk,
+                                                      si["max_ctx"], topk8, ws,
+                                                      block_table=si["bt"])
+            (t_idx8,) = timed([f_idx8])
+            tot_idx8 += t_idx8
+            del q8, qs, k8, ks, topk8
             p = si["pos"].cpu().numpy().astype(np.int64)
             tot_q += n_q
             tot_idx += t_idx
@@ -854,9 +871,14 @@ def config_rows(args):
                 "indexer_topk_ms": round(tot_idx, 4), "mla_ms": round(tot_mla, 4),
                 "indexer_topk_tflops": round(idx_flop / (tot_idx * 1e-3) / 1e12, 1),
                 "indexer_topk_frac_bf16": round(idx_flop / (tot_idx * 1e-3) / 1e12 / pk["bf16"], 3),
+                "indexer_topk_fp8_ms": round(tot_idx8, 4),
+                "indexer_topk_fp8_tflops": round(idx_flop / (tot_idx8 * 1e-3) / 1e12, 1),
+                "indexer_topk_fp8_frac_fp8": round(idx_flop / (tot_idx8 * 1e-3) / 1e12 /
+                                                   (2.0 * pk["bf16"]), 3),
                 "mla_tflops": round(mla_flop / (tot_mla * 1e-3) / 1e12, 1),
                 "mla_frac_bf16": round(mla_flop / (tot_mla * 1e-3) / 1e12 / pk["bf16"], 3),
-                "runs": "median of 20 per shard, L2 flushed before each"}
+                "runs": "median of 20 per shard, L2 flushed before each",
+                "fp8_peak": "2 x the measured bf16 burst (the nominal fp8 / bf16 dense ratio)"}
         if args.with_oracle:
             line["oracle"] = {"tokens_per_s": round(or_q / or_s, 3), "kind": "oracle",
                               "cores": _blas_threads(),

@@ -16,7 +16,7 @@ from . import _native
 
 __all__ = [
     "DsaError", "dsa_version", "dsa_rr_shard_len", "dsa_rr_split_metadata", "dsa_rr_rerange",
-    "dsa_rr_rerange_paged", "dsa_rr_split_decode_metadata",
+    "dsa_rr_rerange_paged", "dsa_rr_split_decode_metadata", "dsa_rr_rerange_multi",
     "dsa_indexer_topk_workspace_size", "dsa_score_row_stride", "dsa_indexer_scores",
     "dsa_topk_select", "dsa_indexer_topk", "dsa_indexer_topk_noalloc", "dsa_sparse_mla",
     "dsa_sparse_mla_workspace_size", "dsa_sparse_mla_balanced", "dsa_read_device_errors",
@@ -173,6 +173,24 @@ def dsa_rr_rerange(gathered, out, n_tokens, sp, rank_stride_rows=0, stream=None)
     row_bytes = _row_bytes(out)
     _check(_lib().dsa_rr_rerange(_ptr(gathered), _ptr(out), n_tokens, sp, rank_stride_rows,
                                  row_bytes, _stream(stream)))
+
+
+def dsa_rr_rerange_multi(gathered, out, n_tokens, sp, rank_stride_rows=0, stream=None):
+    """dsa_rr_rerange of every (gathered[q], out[q]) pair in one launch (same row map)."""
+    if len(gathered) != len(out) or not gathered:
+        raise ValueError("gathered and out must be non-empty lists of the same length")
+    need = sp * rank_stride_rows if rank_stride_rows > 0 else n_tokens
+    for g, o in zip(gathered, out):
+        _dev(g, None, "gathered"); _dev(o, g.dtype, "out")
+        if o.shape[0] < n_tokens or g.shape[0] < need or tuple(o.shape[1:]) != tuple(g.shape[1:]):
+            raise ValueError(f"rerange needs gathered with >= {need} rows and out with >= "
+                             f"{n_tokens} rows of the same width")
+    n = len(gathered)
+    srcs = (ctypes.c_void_p * n)(*[g.data_ptr() for g in gathered])
+    dsts = (ctypes.c_void_p * n)(*[o.data_ptr() for o in out])
+    rb = (ctypes.c_int64 * n)(*[_row_bytes(o) for o in out])
+    _check(_lib().dsa_rr_rerange_multi(srcs, dsts, rb, n, n_tokens, sp, rank_stride_rows,
+                                       _stream(stream)))
 
 
 def dsa_rr_rerange_paged(gathered, pool, n_tokens, sp, cu, block_table, rank_stride_rows=0,

@@ -10,6 +10,7 @@ LIB_PATH = os.path.join(_HERE, "libdsa_rr.so")
 c_int, c_i64, c_sz, c_f, c_vp, c_u32p = (ctypes.c_int, ctypes.c_int64, ctypes.c_size_t,
                                          ctypes.c_float, ctypes.c_void_p,
                                          ctypes.POINTER(ctypes.c_uint32))
+c_vpp, c_i64p = ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_int64)
 
 # name -> (restype, argtypes), in header order
 SIGNATURES = {
@@ -23,6 +24,7 @@ SIGNATURES = {
     "dsa_rr_split_decode_metadata": (c_int, [c_vp, c_vp, c_int, c_i64, c_int, c_int, c_vp, c_vp,
                                              c_vp, c_vp, c_vp, c_vp, c_i64, c_vp]),
     "dsa_rr_rerange": (c_int, [c_vp, c_vp, c_i64, c_int, c_i64, c_i64, c_vp]),
+    "dsa_rr_rerange_multi": (c_int, [c_vpp, c_vpp, c_i64p, c_int, c_i64, c_int, c_i64, c_vp]),
     "dsa_rr_rerange_paged": (c_int, [c_vp, c_vp, c_i64, c_i64, c_int, c_i64, c_i64, c_vp, c_int,
                                      c_vp, c_int, c_int, c_vp]),
     "dsa_rr_cache_local_paged": (c_int, [c_vp, c_vp, c_i64, c_i64, c_int, c_int, c_i64, c_vp,

@@ -37,6 +37,9 @@ int sparse_mla(const void* q, const void* c, int64_t n_kv_rows, const int32_t* c
                float* lse, const int32_t* pos, void* ws, size_t ws_bytes, cudaStream_t stream);
 size_t sparse_mla_workspace_bytes(int64_t n_q);
 cudaError_t split_read_errors(uint32_t* flags);
+int rerange_multi(const void* const* gathered, void* const* out, const int64_t* row_bytes,
+                  int n_tensors, int64_t n_tokens, int sp, int64_t rank_stride_rows,
+                  cudaStream_t stream);
 int rerange_paged(const void* gathered, void* pool, int64_t pool_rows, int64_t n_tokens, int sp,
                   int64_t rank_stride_rows, int64_t row_bytes, const int32_t* cu, int n_req,
                   const int32_t* block_table, int max_pages, int page_size, cudaStream_t stream);
@@ -162,6 +165,13 @@ DSA_EXPORT int dsa_rr_rerange(const void* gathered, void* out, int64_t n_tokens,
                    int64_t rank_stride_rows, int64_t row_bytes, dsa_stream_t stream) {
   return dsa::rerange(gathered, out, n_tokens, sp, rank_stride_rows, row_bytes,
                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+DSA_EXPORT int dsa_rr_rerange_multi(const void* const* gathered, void* const* out,
+                                    const int64_t* row_bytes, int n_tensors, int64_t n_tokens,
+                                    int sp, int64_t rank_stride_rows, dsa_stream_t stream) {
+  return dsa::rerange_multi(gathered, out, row_bytes, n_tensors, n_tokens, sp, rank_stride_rows,
+                            reinterpret_cast<cudaStream_t>(stream));
 }
 
 DSA_EXPORT int dsa_rr_rerange_paged(const void* gathered, void* pool, int64_t pool_rows,

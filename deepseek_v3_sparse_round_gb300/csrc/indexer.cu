@@ -402,6 +402,13 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       ++w_uses;
       bool ok = true;
       for (int tile = un.tile_begin; tile < un.tile_end; ++tile) {
+        float ks = 1.f;
+        if constexpr (F8) {
+          // the key's scale, loaded before the accumulator wait so the load is off the epilogue's
+          // path: I = sk[s] * sum_h (w sq) ReLU(q8 . k8) (sk > 0 leaves the ReLU)
+          const int64_t r = key_row(kr, un.b, tile * kKeysPerTile + row);
+          ks = (r >= 0 && r < kr.n_rows) ? __ldg(k_scale + r) : 0.f;
+        }
         if (!warp_wait(bar(kAccFull + h), acc_uses & 1u, 0x06, abort_flag)) { ok = false; break; }
         ++acc_uses;
         tc_fence_after();
@@ -443,9 +450,6 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (lane == 0) mbar_arrive(bar(kAccEmpty + h));
         const int s = tile * kKeysPerTile + row;
         if constexpr (F8) {
-          // the key's scale: I = sk[s] * sum_h (w sq) ReLU(q8 . k8) (sk > 0 leaves the ReLU)
-          const int64_t r = key_row(kr, un.b, s);
-          const float ks = (r >= 0 && r < kr.n_rows) ? __ldg(k_scale + r) : 0.f;
 #pragma unroll
           for (int q = 0; q < S::kQPA; ++q) acc[q] *= ks;
         }

@@ -120,6 +120,45 @@ copy_rows_bytes_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ ds
   }
 }
 
+// Several tensors reranged by one launch: the flattened (tensor, row, 16-byte chunk) space of
+// up to kMaxMulti tensors that share the row map, so one grid streams all of them (one ramp and
+// one tail instead of one per tensor).
+constexpr int kMaxMulti = 4;
+struct MultiRows {
+  const int4* src[kMaxMulti];
+  int4* dst[kMaxMulti];
+  uint32_t cpr[kMaxMulti];         // 16-byte chunks per row
+  uint32_t begin[kMaxMulti + 1];   // first flattened chunk of each tensor
+  int n;
+};
+
+__global__ void __launch_bounds__(kThreads)
+rerange_multi_kernel(MultiRows mr, RerangeRows map) {
+  const uint32_t total = mr.begin[mr.n];
+  const uint32_t stride = gridDim.x * blockDim.x;
+  for (uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += kUnroll * stride) {
+    int4 v[kUnroll];
+    int4* d[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const uint32_t i = i0 + u * stride;
+      d[u] = nullptr;
+      if (i < total) {
+        int seg = 0;
+#pragma unroll
+        for (int q = 1; q < kMaxMulti; ++q) seg += (q < mr.n && i >= mr.begin[q]) ? 1 : 0;
+        const uint32_t li = i - mr.begin[seg], cpr = mr.cpr[seg];
+        const uint32_t r = li / cpr;
+        v[u] = ld_stream(mr.src[seg] + map(r) * cpr + (li - r * cpr));
+        d[u] = mr.dst[seg] + li;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (d[u] != nullptr) st_stream(d[u], v[u]);
+  }
+}
+
 // One launch for the whole split: shard cu_seqlens (closed form), per-token metadata (the
 // request found by binary search over cu staged in shared memory; positions offset by
 // pos_base[b] when given, for a decode step's new tokens) and, when asked, the 16-byte row
@@ -393,6 +432,43 @@ int rerange(const void* gathered, void* out, int64_t n_tokens, int sp, int64_t r
                 static_cast<long long>(rank_stride_rows), static_cast<long long>(need));
   RerangeRows map{sp, n_tokens / sp, n_tokens % sp, rank_stride_rows};
   return launch_copy_rows(gathered, out, n_tokens, row_bytes, map, stream);
+}
+
+int rerange_multi(const void* const* gathered, void* const* out, const int64_t* row_bytes,
+                  int n_tensors, int64_t n_tokens, int sp, int64_t rank_stride_rows,
+                  cudaStream_t stream) {
+  if (n_tensors < 1 || n_tensors > kMaxMulti)
+    return fail(DSA_ERR_INVALID, "rerange_multi: 1 to %d tensors (got %d)", kMaxMulti, n_tensors);
+  if (!gathered || !out || !row_bytes) return fail(DSA_ERR_INVALID, "rerange_multi: null array");
+  if (sp < 1 || n_tokens < 0 || rank_stride_rows < 0)
+    return fail(DSA_ERR_INVALID, "rerange_multi: need sp >= 1, n_tokens >= 0");
+  const int64_t need = (n_tokens + sp - 1) / sp;
+  if (rank_stride_rows > 0 && rank_stride_rows < need)
+    return fail(DSA_ERR_INVALID, "rerange_multi: rank_stride_rows %lld < ceil(N/sp) = %lld",
+                static_cast<long long>(rank_stride_rows), static_cast<long long>(need));
+  MultiRows mr{};
+  mr.n = n_tensors;
+  int64_t total = 0;
+  for (int q = 0; q < n_tensors; ++q) {
+    if (!gathered[q] || !out[q] || row_bytes[q] <= 0)
+      return fail(DSA_ERR_INVALID, "rerange_multi: tensor %d has a null buffer or no bytes", q);
+    if (row_bytes[q] % 16 || reinterpret_cast<uintptr_t>(gathered[q]) % 16 ||
+        reinterpret_cast<uintptr_t>(out[q]) % 16)
+      return fail(DSA_ERR_INVALID, "rerange_multi: tensor %d is not in 16-byte rows", q);
+    mr.src[q] = static_cast<const int4*>(gathered[q]);
+    mr.dst[q] = static_cast<int4*>(out[q]);
+    mr.cpr[q] = static_cast<uint32_t>(row_bytes[q] / 16);
+    mr.begin[q] = static_cast<uint32_t>(total);
+    total += n_tokens * (row_bytes[q] / 16);
+    if (total >= (int64_t(1) << 31))
+      return fail(DSA_ERR_UNSUPPORTED, "rerange_multi: more than 2^31 chunks in one launch");
+  }
+  mr.begin[n_tensors] = static_cast<uint32_t>(total);
+  if (total == 0) return DSA_OK;
+  RerangeRows map{sp, n_tokens / sp, n_tokens % sp, rank_stride_rows};
+  rerange_multi_kernel<<<grid_for(total, kUnroll), kThreads, 0, stream>>>(mr, map);
+  DSA_CHECK_CUDA(cudaGetLastError());
+  return DSA_OK;
 }
 
 int rerange_paged(const void* gathered, void* pool, int64_t pool_rows, int64_t n_tokens, int sp,

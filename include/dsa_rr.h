@@ -148,6 +148,20 @@ int dsa_rr_rerange(const void* gathered, void* out, int64_t n_tokens, int sp,
                    int64_t rank_stride_rows, int64_t row_bytes, dsa_stream_t stream);
 
 /*
+ * dsa_rr_rerange of several tensors that share the all-gather layout (the k_idx rows and the
+ * latent rows of the same tokens), in one launch: for q < n_tensors,
+ *   out[q][g, :] = gathered[q][off[g % sp] + g / sp, :]   (rows of row_bytes[q] bytes),
+ * off[] as in dsa_rr_rerange. gathered / out / row_bytes are HOST arrays of n_tensors device
+ * pointers and sizes (1 <= n_tensors <= 4); every buffer 16-byte aligned and every row_bytes a
+ * multiple of 16. Same source passage as dsa_rr_rerange.
+ * Errors: DSA_ERR_INVALID for a bad count, null or unaligned buffers, sp < 1, n_tokens < 0 or a
+ * short stride; DSA_ERR_UNSUPPORTED above 2^31 16-byte chunks in total.
+ */
+int dsa_rr_rerange_multi(const void* const* gathered, void* const* out, const int64_t* row_bytes,
+                         int n_tensors, int64_t n_tokens, int sp, int64_t rank_stride_rows,
+                         dsa_stream_t stream);
+
+/*
  * Rerange fused with the write of a paged KV cache.
  * Source: "[RFC]: Parallel strategy for Deepseek v3.2 like models", "New proposal" (the KV is
  * all-gathered before the KV-cache update step) and "[DeepSeek v3.2] 上下文并行详解", section 4

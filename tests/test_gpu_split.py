@@ -234,3 +234,34 @@ def test_cache_local_paged_missing_page_is_skipped_and_flagged():
     keep = np.ones(len(got), bool)
     keep[lost * 64:(lost + 1) * 64] = False
     assert np.array_equal(got[keep], want[keep])
+
+
+@pytest.mark.parametrize("wid", [0, 1, 2, 3])
+@pytest.mark.parametrize("padded", [False, True])
+def test_rerange_multi_matches_oracle(wid, padded):
+    """k_idx rows (256 B) and latent rows (1152 B) of the same tokens reranged by one launch:
+    each bit-exact against the oracle's rerange of the oracle's all-gather layout."""
+    from dsa_cases import dsa
+    wl = W.WORKLOADS[wid]
+    cu = W.cu_seqlens(wl.lengths)
+    n = int(cu[-1])
+    stride = (-(-n // wl.sp)) if padded else 0
+    xs = [W.int_uniform((n, width), -32768, 32767, 40 + width, dtype=torch.int32,
+                        device="cuda").to(torch.int16) for width in (128, 576, 8)]
+    gathered = []
+    for x in xs:
+        g = orr.all_gather([osplit.split_rows(x.cpu().numpy(), wl.sp, r) for r in range(wl.sp)],
+                           stride)
+        gathered.append(torch.as_tensor(g).cuda())
+    outs = [torch.full_like(x, 7) for x in xs]
+    dsa().dsa_rr_rerange_multi(gathered, outs, n, wl.sp, stride)
+    for x, g, o in zip(xs, gathered, outs):
+        assert np.array_equal(o.cpu().numpy(), orr.rerange(g.cpu().numpy(), n, wl.sp, stride))
+        assert torch.equal(o, x)
+
+
+def test_rerange_multi_rejects_unaligned_rows():
+    from dsa_cases import dsa
+    a = torch.zeros((10, 3), dtype=torch.uint8, device="cuda")     # 3-byte rows
+    with pytest.raises(dsa().DsaError):
+        dsa().dsa_rr_rerange_multi([a], [torch.empty_like(a)], 10, 2)
