@@ -403,11 +403,15 @@ constexpr int kAtomsS = 9;                      // CTA 0: dims 0..575
 constexpr int kAtomsO = 8;                      // CTA 1: dims 0..511
 constexpr int kStageS = kAtomsS * kAtomBytes;   // 54 KB
 constexpr int kStageO = kAtomsO * kAtomBytes;   // 48 KB
-constexpr int kPBytes = 128 * 128;              // 128 rows x 64 keys bf16 (48 used), SW128 K-major
+// P (128 rows x 48 keys bf16) in the 32B-swizzled K-major layout: three 16-key atoms of
+// 128 rows x 32 B (4 KB each); row h at (h / 8) * 256 + (h % 8) * 32, its 16-byte chunk c at
+// (c ^ ((h / 4) % 2)) * 16. 12 KB, all of it used (a 128B-swizzled tile would need 16 KB).
+constexpr int kPAtomBytes = 128 * 32;
+constexpr int kPBytes = (kKeys / 16) * kPAtomBytes;
 constexpr int kAFBytes = 128 * 4 + 16;          // alpha[128] fp32 + flags[4] u32 (528 bytes)
 constexpr int kAFStride = 544;
 constexpr int kOffP = kStages * kStageO;        // CTA 1: two P buffers
-constexpr int kPSStride = kPBytes + kAFBytes;   // CTA 0: staged P + alpha + flags
+constexpr int kPSStride = (kPBytes + kAFBytes + 1023) / 1024 * 1024;  // CTA 0: P + alpha + flags
 constexpr int kOffPS = kStages * kStageS;       // CTA 0: two P staging buffers
 constexpr int kOffMask = kOffPS + 2 * kPSStride;  // CTA 0: u32 [2][kMaskWords]
 constexpr int kEndS = kOffMask + 2 * kMaskWords * 4, kEndO = kOffP + 2 * kPBytes;
@@ -453,7 +457,8 @@ constexpr int kKvFull = 0, kKvEmpty = kStages, kPStaged = 2 * kStages, kPSEmpty 
               kOFinal = kQFree + 4;
 static_assert(kOFinal + 1 == kNumBars, "barrier count");
 static_assert(kSmem <= 232448, "smem budget");
-static_assert(kOffPS % 16 == 0 && kPSStride % 16 == 0, "bulk copy sources are 16-byte aligned");
+static_assert(kOffPS % 1024 == 0 && kPSStride % 1024 == 0 && kOffP % 1024 == 0 &&
+              kPBytes % 1024 == 0, "P tiles: bulk copies 16-byte, swizzle atoms 256-byte aligned");
 static_assert(kColS >= kColQ + kQCols && kColS + (kStages - 1) * kSStride + kKeys <= 512,
               "TMEM budget");
 static_assert(kAFBytes % 16 == 0, "P staging");
@@ -771,7 +776,7 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
       // -------------------------------------------------------------- CTA 1: PV issuer
       const uint32_t idesc = idesc_bf16(128, 256, 0, 1);
       volatile int* corr_j = reinterpret_cast<volatile int*>(smem + kOffCorrJ);
-      const uint64_t p_desc0 = smem_desc(sbase + kOffP, 16, 1024, kSwizzle128B);
+      const uint64_t p_desc0 = smem_desc(sbase + kOffP, 16, 256, kSwizzle32B);
       const uint64_t v_desc0 = smem_desc(sbase, kAtomBytes, 1024, kSwizzle128B);
       uint32_t n_ev = 0;
       bool ok = true;
@@ -808,7 +813,7 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
           for (int kk = 0; kk < kKeys / 16; ++kk) {
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf)
-              umma_ss(tmem + hf * 256, da0 + static_cast<uint64_t>((kk * 32) >> 4),
+              umma_ss(tmem + hf * 256, da0 + static_cast<uint64_t>((kk * kPAtomBytes) >> 4),
                       dv0 + static_cast<uint64_t>((hf * 4 * kAtomBytes + kk * 2048) >> 4), idesc,
                       (j > 0 || kk > 0) ? 1u : 0u);
           }
@@ -935,10 +940,11 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
         // once the courier has shipped its previous contents.
         if (!warp_wait(bar(kPSEmpty + psb), static_cast<uint32_t>(((g >> 1) & 1) ^ 1), 0x29, abort_flag)) { ok = false; break; }
         uint8_t* slot = smem + kOffPS + psb * kPSStride;
-        uint8_t* prow = slot + (h >> 3) * 1024 + (h & 7) * 128;
+        uint8_t* prow = slot + (h >> 3) * 256 + (h & 7) * 32;
+        const int swz = (h >> 2) & 1;
 #pragma unroll
-        for (int cc = 0; cc < kKeys / 8; ++cc)
-          *reinterpret_cast<uint4*>(prow + ((cc ^ (h & 7)) * 16)) =
+        for (int cc = 0; cc < kKeys / 8; ++cc)       // chunk cc: keys 8cc..8cc+7, atom cc / 2
+          *reinterpret_cast<uint4*>(prow + (cc >> 1) * kPAtomBytes + (((cc & 1) ^ swz) * 16)) =
               make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
         reinterpret_cast<float*>(slot + kPBytes)[h] = alpha;
         if (lane == 0) reinterpret_cast<uint32_t*>(slot + kPBytes + 512)[warp] = any;
