@@ -934,7 +934,8 @@ def profile_run(args):
       launches per step: the launch list);
     --profile-case: one shard of the many-request batch (rank 1) cut to an evenly spaced
       subset of 2,048 of its queries (every request, short and long histories; about 0.7 GB on
-      the device), indexer + top-k and balanced sparse MLA run twice (one kernel capture)."""
+      the device): indexer + top-k, balanced sparse MLA, the FP8 row quantisation and the FP8
+      indexer + top-k, each twice (kernel captures)."""
     import torch
     import __graft_entry__ as ge
     ge.build()
@@ -974,11 +975,20 @@ def profile_run(args):
     o = e(n, wl.H, wl.dv, dt=torch.bfloat16)
     lse = e(n, wl.H, dt=torch.float32)
     mws = e(dsa.dsa_sparse_mla_workspace_size(n), dt=torch.uint8)
+    q8 = e(*q_idx.shape, dt=torch.uint8)
+    qs = e(*q_idx.shape[:2], dt=torch.float32)
+    k8 = e(*k_idx.shape, dt=torch.uint8)
+    ks = e(k_idx.shape[0], dt=torch.float32)
+    topk8 = e(n, wl.topk)
     for _ in range(2):
         dsa.dsa_indexer_topk(q_idx, w, k_idx, cu, len(wl.lengths), pos, bid, wl.topk, max_ctx,
                              topk, ws)
         dsa.dsa_sparse_mla_balanced(q, c, cu, len(wl.lengths), bid, pos, topk, wl.scale, o, mws,
                                     lse=lse)
+        dsa.dsa_quantize_fp8_rows(q_idx, q8, qs)
+        dsa.dsa_quantize_fp8_rows(k_idx, k8, ks)
+        dsa.dsa_indexer_topk_fp8(q8, qs, w, k8, ks, cu, len(wl.lengths), pos, bid, wl.topk,
+                                 max_ctx, topk8, ws)
     torch.cuda.synchronize()
     p = pos.cpu().numpy().astype(np.int64)
     print(json.dumps({"profile_case": "many_req rank 1, 2048 evenly spaced queries",
