@@ -912,11 +912,27 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
           }
         } else {
           const float nm = -m_ref;
-          float xm = -INFINITY;
+          float xm;
+          if (full) {
+            // every entry valid (the common case, the same for the whole warp): two-wide FMAs
+            // and four independent running maxima, without a per-entry mask test
+            const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(nm, nm);
+            float xa = -INFINITY, xb = -INFINITY, xc = -INFINITY, xd = -INFINITY;
 #pragma unroll
-          for (int i = 0; i < kKeys; ++i) {
-            sv[i] = valid_at(i) ? fmaf(sv[i], scale_log2, nm) : -INFINITY;
-            xm = fmaxf(xm, sv[i]);
+            for (int i = 0; i < kKeys; i += 4) {
+              const float2 a = __ffma2_rn(make_float2(sv[i], sv[i + 1]), sc2, nm2);
+              const float2 b = __ffma2_rn(make_float2(sv[i + 2], sv[i + 3]), sc2, nm2);
+              sv[i] = a.x; sv[i + 1] = a.y; sv[i + 2] = b.x; sv[i + 3] = b.y;
+              xa = fmaxf(xa, a.x); xb = fmaxf(xb, a.y); xc = fmaxf(xc, b.x); xd = fmaxf(xd, b.y);
+            }
+            xm = fmaxf(fmaxf(xa, xb), fmaxf(xc, xd));
+          } else {
+            xm = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < kKeys; ++i) {
+              sv[i] = valid_at(i) ? fmaf(sv[i], scale_log2, nm) : -INFINITY;
+              xm = fmaxf(xm, sv[i]);
+            }
           }
           if (xm > kLazyLog2) {                      // rare: move the reference maximum
             alpha = ex2_approx(-xm);
