@@ -410,22 +410,23 @@ constexpr int kPAtomBytes = 128 * 32;
 constexpr int kPBytes = (kKeys / 16) * kPAtomBytes;
 constexpr int kAFBytes = 128 * 4 + 16;          // alpha[128] fp32 + flags[4] u32 (528 bytes)
 constexpr int kAFStride = 544;
-constexpr int kOffP = kStages * kStageO;        // CTA 1: two P buffers
+constexpr int kPBuf = 3;                        // P tiles in flight between the CTAs
+constexpr int kOffP = kStages * kStageO;        // CTA 1: kPBuf P buffers
 constexpr int kPSStride = (kPBytes + kAFBytes + 1023) / 1024 * 1024;  // CTA 0: P + alpha + flags
-constexpr int kOffPS = kStages * kStageS;       // CTA 0: two P staging buffers
-constexpr int kOffMask = kOffPS + 2 * kPSStride;  // CTA 0: u32 [2][kMaskWords]
-constexpr int kEndS = kOffMask + 2 * kMaskWords * 4, kEndO = kOffP + 2 * kPBytes;
+constexpr int kOffPS = kStages * kStageS;       // CTA 0: kPBuf P staging buffers
+constexpr int kOffMask = kOffPS + kPBuf * kPSStride;  // CTA 0: u32 [2][kMaskWords]
+constexpr int kEndS = kOffMask + 2 * kMaskWords * 4, kEndO = kOffP + kPBuf * kPBytes;
 constexpr int kRegion = ((kEndS > kEndO ? kEndS : kEndO) + 15) / 16 * 16;
 // 32 rows x 128 B per row warp, 1 KB aligned (128B swizzle): CTA 0 transposes Q rows through
 // it on their way to TMEM, CTA 1 stages bf16 o for TMA stores.
 constexpr int kOffX = (kRegion + 1023) / 1024 * 1024;
 constexpr int kXBytes = 4 * 32 * 128;
 constexpr int kOffXO1 = kEndO;                  // CTA 1: second o staging tile per row warp
-constexpr int kOffAlpha = kOffX + kXBytes;      // CTA 1: [2][kAFStride] alpha + flags
-constexpr int kOffL = kOffAlpha + 2 * kAFStride;  // CTA 1: fp32 [2][128]
+constexpr int kOffAlpha = kOffX + kXBytes;      // CTA 1: [kPBuf][kAFStride] alpha + flags
+constexpr int kOffL = kOffAlpha + kPBuf * kAFStride;  // CTA 1: fp32 [2][128]
 constexpr int kOffNT = kOffL + 2 * 128 * 4;     // both: int [2] tiles of the query
 constexpr int kOffBar = kOffNT + 8;
-constexpr int kNumBars = 4 * kStages + 21;
+constexpr int kNumBars = 4 * kStages + 4 * kPBuf + 13;
 constexpr int kOffTmem = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmem + 4;
 constexpr int kOffCorrJ = kOffAbort + 4;
@@ -449,9 +450,9 @@ constexpr int kQAtomBytes = kH * 128;           // 128 rows x 128 B: 16 KB
 static_assert(kQPieces * kQAtomsPerPiece * 64 == kDQK, "Q pieces cover the 576 dims");
 static_assert(kQAtomsPerPiece * kQAtomBytes <= kStageS, "a Q piece fits a ring slot");
 // barrier indices
-constexpr int kKvFull = 0, kKvEmpty = kStages, kPStaged = 2 * kStages, kPSEmpty = kPStaged + 2,
-              kSFull = kPStaged + 4, kSEmpty = kSFull + kStages, kPFull = kSEmpty + kStages,
-              kPEmpty = kPFull + 2, kMetaFull = kPEmpty + 2, kMetaEmpty = kMetaFull + 2,
+constexpr int kKvFull = 0, kKvEmpty = kStages, kPStaged = 2 * kStages, kPSEmpty = kPStaged + kPBuf,
+              kSFull = kPSEmpty + kPBuf, kSEmpty = kSFull + kStages, kPFull = kSEmpty + kStages,
+              kPEmpty = kPFull + kPBuf, kMetaFull = kPEmpty + kPBuf, kMetaEmpty = kMetaFull + 2,
               kLReady = kMetaEmpty + 2, kLEmpty = kLReady + 2, kQFree = kLEmpty + 2,
               kCorrGo = kQFree + 1, kCorrReady = kQFree + 2, kCorrDone = kQFree + 3,
               kOFinal = kQFree + 4;
@@ -509,11 +510,13 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
       mbar_init(bar(kSFull + i), (crank == 0 || i > 0) ? 1 : 4);  // CTA 1: first = o_drained
       mbar_init(bar(kSEmpty + i), 4);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kPBuf; ++i) {
       mbar_init(bar(kPStaged + i), 128);
       mbar_init(bar(kPSEmpty + i), 1);
       mbar_init(bar(kPFull + i), 1);
       mbar_init(bar(kPEmpty + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kMetaFull + i), 1);
       mbar_init(bar(kMetaEmpty + i),
                 crank == 0 ? kGatherPerSlot * kStages + 6 : kGatherPerSlot * kStages + 5);
@@ -781,7 +784,7 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
       uint32_t n_ev = 0;
       bool ok = true;
       // each P buffer always has one armed delivery (one bulk copy of P + alpha + flags)
-      for (int i = 0; i < 2; ++i) mbar_expect_tx(bar(kPFull + i), kPBytes + kAFBytes);
+      for (int i = 0; i < kPBuf; ++i) mbar_expect_tx(bar(kPFull + i), kPBytes + kAFBytes);
       int64_t g0 = 0;
       for (int n = 0; n < n_my && ok; ++n) {
         const int nt = meta_wait(n, false);
@@ -792,9 +795,9 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
         tc_fence_after();
         for (int j = 0; j < nt && ok; ++j) {
           const int64_t g = g0 + j;
-          const int s = static_cast<int>(g % kStages), pb = static_cast<int>(g & 1);
+          const int s = static_cast<int>(g % kStages), pb = static_cast<int>(g % kPBuf);
           if (!mbar_wait(bar(kKvFull + s), static_cast<uint32_t>((g / kStages) & 1), 0x25, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(bar(kPFull + pb), static_cast<uint32_t>((g >> 1) & 1), 0x26, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(bar(kPFull + pb), static_cast<uint32_t>((g / kPBuf) & 1), 0x26, abort_flag)) { ok = false; break; }
           mbar_expect_tx(bar(kPFull + pb), kPBytes + kAFBytes);
           const volatile uint32_t* flags =
               reinterpret_cast<const volatile uint32_t*>(smem + kOffAlpha + pb * kAFStride + 512);
@@ -840,9 +843,10 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
         bool ok = true;
         for (int j = 0; j < nt; ++j) {
           const int64_t g = g0 + j;
-          const int pb = static_cast<int>(g & 1);
-          if (!mbar_wait(bar(kPStaged + pb), static_cast<uint32_t>((g >> 1) & 1), 0x2E, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(bar(kPEmpty + pb), static_cast<uint32_t>(((g >> 1) & 1) ^ 1), 0x2F, abort_flag)) { ok = false; break; }
+          const int pb = static_cast<int>(g % kPBuf);
+          const uint32_t pph = static_cast<uint32_t>((g / kPBuf) & 1);
+          if (!mbar_wait(bar(kPStaged + pb), pph, 0x2E, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(bar(kPEmpty + pb), pph ^ 1u, 0x2F, abort_flag)) { ok = false; break; }
           const uint32_t src = sbase + kOffPS + pb * kPSStride;
           bulk_copy_to_peer(sbase + kOffP + pb * kPBytes, src, kPBytes, bar(kPFull + pb), peer);
           bulk_copy_to_peer(sbase + kOffAlpha + pb * kAFStride, src + kPBytes, kAFBytes,
@@ -870,7 +874,7 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
       bool ok = true;
       for (int j = 0; j < nt; ++j) {
         const int64_t g = g0 + j;
-        const int sb = static_cast<int>(g % kStages), psb = static_cast<int>(g & 1);
+        const int sb = static_cast<int>(g % kStages), psb = static_cast<int>(g % kPBuf);
         if (!warp_wait(bar(kSFull + sb), static_cast<uint32_t>((g / kStages) & 1), 0x28, abort_flag)) { ok = false; break; }
         tc_fence_after();
         float sv[kKeys];
@@ -952,9 +956,9 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
         }
         l_run += psum;
         const uint32_t any = __any_sync(0xffffffffu, alpha != 1.f) ? 1u : 0u;
-        // Stage P (swizzled K-major rows), alpha and the warp flags in staging buffer g % 2
+        // Stage P (swizzled K-major rows), alpha and the warp flags in staging buffer g % kPBuf
         // once the courier has shipped its previous contents.
-        if (!warp_wait(bar(kPSEmpty + psb), static_cast<uint32_t>(((g >> 1) & 1) ^ 1), 0x29, abort_flag)) { ok = false; break; }
+        if (!warp_wait(bar(kPSEmpty + psb), static_cast<uint32_t>(((g / kPBuf) & 1) ^ 1), 0x29, abort_flag)) { ok = false; break; }
         uint8_t* slot = smem + kOffPS + psb * kPSStride;
         uint8_t* prow = slot + (h >> 3) * 256 + (h & 7) * 32;
         const int swz = (h >> 2) & 1;
