@@ -210,8 +210,8 @@ class ConfigStep:
         self.launches_per_step = self.LAUNCHES_PER_SHARD * len(self.ranks)
 
     def run_shard(self, r, inp=None, shared=None, o=None, ev=None):
-        """One shard's path. ev: optional 4 events recorded after split+reranges, after
-        indexer+top-k and after the MLA (and before the split)."""
+        """One shard's path. ev: optional 5 events recorded before the split, after it, after
+        the rerange, after indexer+top-k and after the MLA."""
         dsa, wl = self.dsa, self.wl
         inp = self.inp[r] if inp is None else inp
         sh = self.shared if shared is None else shared
@@ -222,20 +222,22 @@ class ConfigStep:
         dsa.dsa_rr_split_metadata(sh["cu"], self.N, wl.sp, r, out["cu_shard"], out["pos"],
                                   out["bid"], out["gidx"], src_rows=sh["c_log"],
                                   dst_rows=out["c_local"])
+        if ev is not None:
+            ev[1].record()
         dsa.dsa_rr_rerange_multi([sh["k_gath"], sh["c_gath"]], [self.k_idx, self.c], self.N,
                                  wl.sp, 0)
         if ev is not None:
-            ev[1].record()
+            ev[2].record()
         topk = self.topk[:n]
         dsa.dsa_indexer_topk(inp["q_idx"], inp["w"], self.k_idx, sh["cu"], self.n_req, out["pos"],
                              out["bid"], wl.topk, self.max_ctx, topk, self.ws)
         if ev is not None:
-            ev[2].record()
+            ev[3].record()
         dsa.dsa_sparse_mla_balanced(inp["q"], self.c, sh["cu"], self.n_req, out["bid"],
                                     out["pos"], topk, wl.scale, out["o"] if o is None else o,
                                     self.mla_ws, lse=out["lse"])
         if ev is not None:
-            ev[3].record()
+            ev[4].record()
 
     def run(self):
         for r in self.ranks:
@@ -253,10 +255,10 @@ class ConfigStep:
             pairs_s += int(np.sum(np.minimum(pos + 1, wl.topk)))
         idx = 2.0 * wl.Hi * wl.Di * pairs_c
         mla = 2.0 * wl.H * (wl.dqk + wl.dv) * pairs_s
-        nbytes = sum(2 * self.n_r[r] * wl.dqk * 2 + 2 * self.N * (wl.Di + wl.dqk) * 2
-                     for r in self.ranks)
+        rerange_bytes = 2 * self.N * (wl.Di + wl.dqk) * 2 * len(self.ranks)
+        nbytes = sum(2 * self.n_r[r] * wl.dqk * 2 for r in self.ranks) + rerange_bytes
         return {"indexer_flop": idx, "mla_flop": mla, "causal_pairs": pairs_c,
-                "selected_pairs": pairs_s, "copy_bytes": nbytes}
+                "selected_pairs": pairs_s, "copy_bytes": nbytes, "rerange_bytes": rerange_bytes}
 
     def queries(self):
         return sum(self.n_r.values())
@@ -300,7 +302,7 @@ def time_steps(torch, st, steps, flush, stream):
         e0.record(stream)
         per = []
         for r in st.ranks:
-            ev = (mk(), mk(), mk(), mk())
+            ev = (mk(), mk(), mk(), mk(), mk())
             st.run_shard(r, ev=ev)
             per.append(ev)
         e1 = mk()
@@ -308,12 +310,13 @@ def time_steps(torch, st, steps, flush, stream):
         evs.append((e0, e1, per))
     torch.cuda.synchronize()
     total = sum(a.elapsed_time(b) for a, b, _ in evs) / 1e3
-    parts = {"split_rerange": 0.0, "indexer_topk": 0.0, "mla": 0.0}
+    parts = {"split_rerange": 0.0, "rerange": 0.0, "indexer_topk": 0.0, "mla": 0.0}
     for _, _, per in evs:
         for ev in per:
-            parts["split_rerange"] += ev[0].elapsed_time(ev[1]) / 1e3
-            parts["indexer_topk"] += ev[1].elapsed_time(ev[2]) / 1e3
-            parts["mla"] += ev[2].elapsed_time(ev[3]) / 1e3
+            parts["split_rerange"] += ev[0].elapsed_time(ev[2]) / 1e3
+            parts["rerange"] += ev[1].elapsed_time(ev[2]) / 1e3
+            parts["indexer_topk"] += ev[2].elapsed_time(ev[3]) / 1e3
+            parts["mla"] += ev[3].elapsed_time(ev[4]) / 1e3
     return total, parts
 
 
@@ -486,6 +489,8 @@ def gpu_arm(args):
     mla_ach = work["mla_flop"] / mla_s / 1e12
     idx_ach = work["indexer_flop"] / idx_s / 1e12
     cp_ach = work["copy_bytes"] / cp_s / 1e9
+    rr_s = parts["rerange"] / args.steps
+    rr_ach = work["rerange_bytes"] / rr_s / 1e9
     mla_tr = profiled_traffic("sparse_mla_pair_kernel")
     traffic = None
     if mla_tr is not None:    # DRAM bytes per selected pair from a capture, scaled to a launch
@@ -530,7 +535,13 @@ def gpu_arm(args):
             "split_kernel + rerange_multi_kernel", "hbm", cp_ach, pk["hbm"], "GB/s",
             NOMINAL["hbm"], None,
             {"algorithmic_bytes_per_step": work["copy_bytes"],
-             "unit_of_work": "row moved: 2 x row bytes (read + write)"}),
+             "unit_of_work": "row moved: 2 x row bytes (read + write)",
+             "timing": "CUDA events before the split and after the rerange (two launches)"}),
+        "roofline_rerange": roofline_obj(
+            "rerange_multi_kernel", "hbm", rr_ach, pk["hbm"], "GB/s", NOMINAL["hbm"], None,
+            {"algorithmic_bytes_per_launch": work["rerange_bytes"] / len(st.ranks),
+             "unit_of_work": "token: 2 x (256 + 1152) B (k_idx and latent rows, read + write)",
+             "timing": "CUDA events around each rerange launch, mean over the timed steps"}),
         "ms_split_rerange": round(cp_s * 1e3, 4), "ms_indexer_topk": round(idx_s * 1e3, 4),
         "ms_mla": round(mla_s * 1e3, 4),
         "e2e": {"value": round(queries * e2e_steps / e2e_s, 2), "unit": "tokens/s",
