@@ -305,6 +305,148 @@ topk_kernel(const float* __restrict__ scores, int64_t stride, const int32_t* __r
 }
 
 // ------------------------------------------------------------------------------------------
+// Rows of at most kShortMax entries (batches whose longest row is that short): the same
+// selection as topk_kernel<true, ...> with a 256-thread CTA per row, so that more rows are in
+// flight per SM and every block-wide barrier spans 8 warps instead of 16; each thread owns 8
+// histogram bins.
+constexpr int kShortMax = 4096;
+constexpr int kShortThreads = 256;
+constexpr int kShortWarps = kShortThreads / 32;
+constexpr int kShortBinsPerThread = kBins / kShortThreads;
+
+__device__ __forceinline__ uint32_t short_block_scan(uint32_t v, uint32_t* warp_tot,
+                                                     uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = lane < kShortWarps ? warp_tot[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < kShortWarps) warp_tot[lane] = w;
+  }
+  __syncthreads();
+  const uint32_t before = (warp > 0 ? warp_tot[warp - 1] : 0u) + x - v;
+  *total = warp_tot[kShortWarps - 1];
+  __syncthreads();
+  return before;
+}
+
+__global__ void __launch_bounds__(kShortThreads, 6)
+topk_short_kernel(const float* __restrict__ scores, int64_t stride,
+                  const int32_t* __restrict__ pos, int k, int max_ctx,
+                  int32_t* __restrict__ topk) {
+  __shared__ __align__(16) uint32_t stash[kShortMax];
+  __shared__ uint32_t hist[kBins];
+  __shared__ uint32_t warp_tot[kShortWarps];
+  __shared__ uint32_t s_digit, s_above;
+  const int64_t t = static_cast<int64_t>(gridDim.x) - 1 - blockIdx.x;   // longest rows first
+  int32_t* out = topk + t * k;
+  const int L = __ldg(pos + t) + 1;
+  if (L < 1 || L > max_ctx || L > kShortMax) {
+    if (threadIdx.x == 0) report_device_error(kErrBadLength);
+    for (int j = threadIdx.x; j < k; j += kShortThreads) out[j] = -1;
+    return;
+  }
+  if (L <= k) {
+    for (int j = threadIdx.x; j < k; j += kShortThreads) out[j] = j < L ? j : -1;
+    return;
+  }
+  const float* row = scores + t * stride;
+  // the row's keys into shared memory: every thread's 16-byte loads issued before their stores
+  {
+    constexpr int kLoads = kShortMax / (kShortThreads * 4);   // 4
+    float4 v[kLoads];
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) {
+      const int i = (u * kShortThreads + static_cast<int>(threadIdx.x)) * 4;
+      if (i + 4 <= L) v[u] = __ldcg(reinterpret_cast<const float4*>(row + i));
+    }
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) {
+      const int i = (u * kShortThreads + static_cast<int>(threadIdx.x)) * 4;
+      if (i + 4 <= L) {
+        *reinterpret_cast<uint4*>(stash + i) =
+            make_uint4(order_key(v[u].x), order_key(v[u].y), order_key(v[u].z), order_key(v[u].w));
+      } else {
+        for (int j = i; j < L && j < i + 4; ++j) stash[j] = order_key(__ldcg(row + j));
+      }
+    }
+  }
+  // three radix passes over the stash (11, 11, 10 bits)
+  uint32_t prefix = 0, prefix_mask = 0, remaining = static_cast<uint32_t>(k);
+#pragma unroll 1
+  for (int p = 0; p < 3; ++p) {
+    for (int b = threadIdx.x; b < kBins; b += kShortThreads) hist[b] = 0;
+    if (threadIdx.x == 0) { s_digit = 0u; s_above = 0u; }
+    __syncthreads();
+    const int sh = p == 0 ? 21 : (p == 1 ? 10 : 0);
+    const uint32_t dm = p == 2 ? 0x3FFu : 0x7FFu;
+    for (int i = threadIdx.x; i < L; i += kShortThreads) {
+      const uint32_t key = stash[i];
+      if ((key & prefix_mask) == prefix) atomicAdd(&hist[(key >> sh) & dm], 1u);
+    }
+    __syncthreads();
+    // thread j owns the bins of mirror index m = kShortThreads-1-j, so the exclusive scan in
+    // thread order counts every bin above them
+    const int m = kShortThreads - 1 - static_cast<int>(threadIdx.x);
+    uint32_t hs[kShortBinsPerThread], sum = 0;
+#pragma unroll
+    for (int q = 0; q < kShortBinsPerThread; ++q) {
+      hs[q] = hist[kShortBinsPerThread * m + q];
+      sum += hs[q];
+    }
+    uint32_t tot;
+    uint32_t above = short_block_scan(sum, warp_tot, &tot);
+#pragma unroll
+    for (int q = kShortBinsPerThread - 1; q >= 0; --q) {
+      if (above < remaining && above + hs[q] >= remaining) {
+        s_digit = static_cast<uint32_t>(kShortBinsPerThread * m + q);
+        s_above = above;
+      }
+      above += hs[q];
+    }
+    __syncthreads();
+    remaining -= s_above;
+    prefix |= s_digit << sh;
+    prefix_mask |= dm << sh;
+    __syncthreads();
+  }
+  const uint32_t T = prefix, need_eq = remaining;
+  // ordered emission: one contiguous odd-length segment per thread, one block-wide scan
+  const int seg = ((L + kShortThreads - 1) / kShortThreads) | 1;
+  const int lo = min(static_cast<int>(threadIdx.x) * seg, L), hi = min(lo + seg, L);
+  uint32_t n_g = 0, n_e = 0;
+  for (int i = lo; i < hi; ++i) {
+    const uint32_t key = stash[i];
+    n_g += key > T;
+    n_e += key == T;
+  }
+  uint32_t tot;
+  const uint32_t before = short_block_scan((n_g << 16) | n_e, warp_tot, &tot);
+  uint32_t g_before = before >> 16, e_before = before & 0xFFFFu;
+  for (int i = lo; i < hi; ++i) {
+    const uint32_t key = stash[i];
+    if (key > T) {
+      out[g_before + (e_before < need_eq ? e_before : need_eq)] = i;
+      ++g_before;
+    } else if (key == T) {
+      if (e_before < need_eq) out[g_before + e_before] = i;
+      ++e_before;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------
 // Top-k fed by the indexer's sampled first-digit histograms (the fused indexer -> top-k path).
 //
 // Rows of up to kCap entries are kept whole in shared memory (key and index). For longer rows
@@ -495,7 +637,10 @@ int topk_select(const float* scores, int64_t score_stride, const int32_t* pos, i
     return fail(DSA_ERR_INVALID, "topk: score_stride must be >= max_ctx, a multiple of 4, and "
                                  "scores 16-byte aligned");
   if (n_q > INT32_MAX) return fail(DSA_ERR_UNSUPPORTED, "topk: n_q too large");
-  if (max_ctx <= kStashKeys) {
+  if (max_ctx <= kShortMax) {
+    topk_short_kernel<<<static_cast<unsigned>(n_q), kShortThreads, 0, stream>>>(
+        scores, score_stride, pos, k, max_ctx, topk);
+  } else if (max_ctx <= kStashKeys) {
     const size_t smem = static_cast<size_t>(((max_ctx + 3) / 4) * 4) * sizeof(uint32_t);
     const int max_smem = kStashKeys * static_cast<int>(sizeof(uint32_t));
     if (max_ctx <= kShortRow) {

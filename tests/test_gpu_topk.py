@@ -71,3 +71,17 @@ def test_real_valued_rows_match_exactly():
     got = _run(rows, 2048)
     for i, r in enumerate(rows):
         assert np.array_equal(got[i], topk_indices(r, 2048))
+
+
+@pytest.mark.parametrize("k", [1, 7, 2048])
+def test_batches_of_rows_of_at_most_4096(k):
+    """Every row at most 4,096 long: the 256-thread kernel. Ragged lengths (not multiples of 4
+    or of the thread count), heavy ties, constant and signed-zero rows, and a full 4,096 row."""
+    rng = np.random.default_rng(100 + k)
+    lengths = [1, 2, k, k + 1, 1000, 2049, 4093, 4095, 4096]
+    rows = [rng.integers(-5, 6, L).astype(np.float32) for L in lengths]
+    rows += [rng.normal(size=4096).astype(np.float32), np.full(3001, 3.5, np.float32),
+             np.array([-0.0, 0.0] * 1500, dtype=np.float32)]
+    got = _run(rows, k)
+    for i, r in enumerate(rows):
+        assert np.array_equal(got[i], topk_indices(r, k)), (k, len(r))
