@@ -442,6 +442,7 @@ constexpr int kMmaWarp = 4, kGatherWarp0 = 5, kCourierWarp = kGatherWarp0 + kSta
               kMetaWarp = kCourierWarp + 1, kGatherWarp1 = kMetaWarp + 1;
 static_assert(kGatherWarp1 + (kGatherPerSlot - 1) * kStages == kThreads / 32, "warp roles");
 constexpr float kLazyLog2 = 16.f;               // rescale O only when the max grows by > 2^16
+constexpr float kLazySum = 32768.f;             // 2^(kLazyLog2 - 1): a row sum that checks the max
 // CTA 0 brings each query's Q into TMEM through its ring: kQPieces ring entries ahead of the
 // query's key tiles, each 128 rows x kQAtomsPerPiece swizzle atoms of 64 dims (128 B per row),
 // gathered like key rows and copied into TMEM by the QK issuer (tcgen05.cp).
@@ -712,7 +713,8 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
     const bool leader = elect_one();
     const uint32_t idesc = idesc_bf16(128, kKeys, 0, 0);
     const uint64_t desc0 = smem_desc(sbase, 16, 1024, kSwizzle128B);
-    int64_t rpos0 = 0, g0 = 0;                       // ring position; S-buffer (tile) index
+    int rs = 0, sb = 0;                              // ring slot of the next entry; S buffer
+    uint32_t r_ph = 0, s_ph = 0;                     // ... and the parity of their current use
     bool ok = true;
     for (int n = 0; n < n_my && ok; ++n) {
       const int nt = meta_wait(n, true);
@@ -723,10 +725,8 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
       // Q pieces -> TMEM columns kColQ.. (the A operand of QK), once every QK MMA and copy of
       // the previous query is complete (kQFree; an MMA issued after a copy by this thread sees it).
       for (int pce = 0; pce < n_pre; ++pce) {
-        const int64_t rp = rpos0 + pce;
-        const int s = static_cast<int>(rp % kStages);
-        if (!warp_wait(bar(kKvFull + s), static_cast<uint32_t>((rp / kStages) & 1), 0x22,
-                       abort_flag)) { ok = false; break; }
+        const int s = rs;
+        if (!warp_wait(bar(kKvFull + s), r_ph, 0x22, abort_flag)) { ok = false; break; }
         if (pce == 0 && n > 0 &&
             !warp_wait(bar(kQFree), static_cast<uint32_t>((n - 1) & 1), 0x25, abort_flag)) {
           ok = false;
@@ -744,17 +744,15 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
           umma_commit(bar(kKvEmpty + s));            // the slot is free once the copies read it
         }
         __syncwarp();
+        if (++rs == kStages) { rs = 0; r_ph ^= 1u; }
       }
       if (!ok) break;
       tc_fence_after();
       for (int j = 0; j < nt; ++j) {
-        const int64_t rp = rpos0 + n_pre + j, g = g0 + j;
-        const int s = static_cast<int>(rp % kStages), sb = static_cast<int>(g % kStages);
+        const int s = rs;
         const uint32_t d_s = tmem + kColS + sb * kSStride;
-        if (!warp_wait(bar(kKvFull + s), static_cast<uint32_t>((rp / kStages) & 1), 0x23,
-                       abort_flag)) { ok = false; break; }
-        if (!warp_wait(bar(kSEmpty + sb), static_cast<uint32_t>(((g / kStages) & 1) ^ 1), 0x24,
-                       abort_flag)) { ok = false; break; }
+        if (!warp_wait(bar(kKvFull + s), r_ph, 0x23, abort_flag)) { ok = false; break; }
+        if (!warp_wait(bar(kSEmpty + sb), s_ph ^ 1u, 0x24, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint64_t db0 = desc0 + static_cast<uint64_t>((s * kStageS) >> 4);
 #pragma unroll
@@ -768,11 +766,11 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
           umma_commit(bar(kKvEmpty + s));          // the slot is free once these MMAs finish
         }
         __syncwarp();
+        if (++rs == kStages) { rs = 0; r_ph ^= 1u; }
+        if (++sb == kStages) { sb = 0; s_ph ^= 1u; }
       }
       if (leader) umma_commit(bar(kQFree));        // Q of this query no longer read
       __syncwarp();
-      rpos0 += n_pre + nt;
-      g0 += nt;
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
@@ -785,7 +783,8 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
       bool ok = true;
       // each P buffer always has one armed delivery (one bulk copy of P + alpha + flags)
       for (int i = 0; i < kPBuf; ++i) mbar_expect_tx(bar(kPFull + i), kPBytes + kAFBytes);
-      int64_t g0 = 0;
+      int s = 0, pb = 0;                             // ring slot and P buffer of the tile
+      uint32_t r_ph = 0, p_ph = 0;                   // ... and the parity of their current use
       for (int n = 0; n < n_my && ok; ++n) {
         const int nt = meta_wait(n, false);
         if (nt < 0) break;
@@ -794,10 +793,8 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
         if (n > 0 && !mbar_wait(bar(kOD), (n - 1) & 1, 0x32, abort_flag)) break;
         tc_fence_after();
         for (int j = 0; j < nt && ok; ++j) {
-          const int64_t g = g0 + j;
-          const int s = static_cast<int>(g % kStages), pb = static_cast<int>(g % kPBuf);
-          if (!mbar_wait(bar(kKvFull + s), static_cast<uint32_t>((g / kStages) & 1), 0x25, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(bar(kPFull + pb), static_cast<uint32_t>((g / kPBuf) & 1), 0x26, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(bar(kKvFull + s), r_ph, 0x25, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(bar(kPFull + pb), p_ph, 0x26, abort_flag)) { ok = false; break; }
           mbar_expect_tx(bar(kPFull + pb), kPBytes + kAFBytes);
           const volatile uint32_t* flags =
               reinterpret_cast<const volatile uint32_t*>(smem + kOffAlpha + pb * kAFStride + 512);
@@ -822,12 +819,13 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
           }
           umma_commit_multicast(bar(kPEmpty + pb), static_cast<uint16_t>(1u << peer));
           umma_commit(bar(kKvEmpty + s));
+          if (++s == kStages) { s = 0; r_ph ^= 1u; }
+          if (++pb == kPBuf) { pb = 0; p_ph ^= 1u; }
         }
         if (!ok) break;
         umma_commit(bar(kOFinal));                   // O of this query complete
         *corr_j = -1;                                // end of this query's rescale requests
         mbar_arrive(bar(kCorrGo));
-        g0 += nt;
       }
     }
   } else if (warp == kCourierWarp) {
@@ -835,16 +833,14 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
       // -------------------------------------------------------------- CTA 0: P courier
       // Ships each staged P tile (+ alpha, flags) to CTA 1 with two bulk copies that complete
       // on CTA 1's p_full barrier, then hands the staging buffer back to the softmax warps.
-      int64_t g0 = 0;
+      int pb = 0;                                    // P buffer of the tile
+      uint32_t pph = 0;                              // ... and the parity of its current use
       for (int n = 0; n < n_my; ++n) {
         const int nt = meta_wait(n, false);
         if (nt < 0) break;
         mbar_arrive(bar(kMetaEmpty + (n & 1)));
         bool ok = true;
         for (int j = 0; j < nt; ++j) {
-          const int64_t g = g0 + j;
-          const int pb = static_cast<int>(g % kPBuf);
-          const uint32_t pph = static_cast<uint32_t>((g / kPBuf) & 1);
           if (!mbar_wait(bar(kPStaged + pb), pph, 0x2E, abort_flag)) { ok = false; break; }
           if (!mbar_wait(bar(kPEmpty + pb), pph ^ 1u, 0x2F, abort_flag)) { ok = false; break; }
           const uint32_t src = sbase + kOffPS + pb * kPSStride;
@@ -854,9 +850,9 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
           bulk_commit();
           bulk_wait_read_all();
           mbar_arrive(bar(kPSEmpty + pb));
+          if (++pb == kPBuf) { pb = 0; pph ^= 1u; }
         }
         if (!ok) break;
-        g0 += nt;
       }
       bulk_wait_all();                               // every copy to the peer has landed
     }
@@ -864,7 +860,8 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
     // ---------------------------------------------------------------- CTA 0: softmax warps
     const int h = static_cast<int>(threadIdx.x);
     const uint32_t lane_base = (warp * 32u) << 16;
-    int64_t g0 = 0;
+    int sb = 0, psb = 0;                             // S buffer and P staging buffer of the tile
+    uint32_t s_ph = 0, ps_ph = 0;                    // ... and the parity of their current use
     for (int n = 0; n < n_my; ++n) {
       const int nt = meta_wait(n, true);
       if (nt < 0) break;
@@ -873,9 +870,7 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
       float m_ref = -INFINITY, l_run = 0.f;
       bool ok = true;
       for (int j = 0; j < nt; ++j) {
-        const int64_t g = g0 + j;
-        const int sb = static_cast<int>(g % kStages), psb = static_cast<int>(g % kPBuf);
-        if (!warp_wait(bar(kSFull + sb), static_cast<uint32_t>((g / kStages) & 1), 0x28, abort_flag)) { ok = false; break; }
+        if (!warp_wait(bar(kSFull + sb), s_ph, 0x28, abort_flag)) { ok = false; break; }
         tc_fence_after();
         float sv[kKeys];
         {
@@ -900,7 +895,10 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
           return full || (i < 32 ? ((mlo >> i) & 1u) != 0u : ((mhi >> (i - 32)) & 1u) != 0u);
         };
         // x_i = scale * s_i - m_ref in the log2 domain (one FMA); masked entries -inf, whose
-        // ex2 is 0. m_ref moves only when a row's maximum grows by more than 2^kLazyLog2.
+        // ex2 is 0. m_ref moves only when a row's maximum x grows above kLazyLog2. The common
+        // case takes no maximum: p = 2^x against the current m_ref, and since the row's sum of p
+        // bounds its largest p, only a sum of at least 2^(kLazyLog2 - 1) (an x above
+        // kLazyLog2 - 1) looks at the maximum and, if it moved, redoes p.
         float alpha = 1.f;
         if (m_ref == -INFINITY) {                    // no valid entry in this row so far
           float mt = -INFINITY;
@@ -914,51 +912,51 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
 #pragma unroll
             for (int i = 0; i < kKeys; ++i) sv[i] -= mt;
           }
+        } else if (full) {
+          // every entry valid (the common case, the same for the whole warp): two-wide FMAs
+          // without a per-entry mask test
+          const float nm = -m_ref;
+          const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(nm, nm);
+#pragma unroll
+          for (int i = 0; i < kKeys; i += 2) {
+            const float2 a = __ffma2_rn(make_float2(sv[i], sv[i + 1]), sc2, nm2);
+            sv[i] = a.x; sv[i + 1] = a.y;
+          }
         } else {
           const float nm = -m_ref;
-          float xm;
-          if (full) {
-            // every entry valid (the common case, the same for the whole warp): two-wide FMAs
-            // and four independent running maxima, without a per-entry mask test
-            const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(nm, nm);
-            float xa = -INFINITY, xb = -INFINITY, xc = -INFINITY, xd = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < kKeys; i += 4) {
-              const float2 a = __ffma2_rn(make_float2(sv[i], sv[i + 1]), sc2, nm2);
-              const float2 b = __ffma2_rn(make_float2(sv[i + 2], sv[i + 3]), sc2, nm2);
-              sv[i] = a.x; sv[i + 1] = a.y; sv[i + 2] = b.x; sv[i + 3] = b.y;
-              xa = fmaxf(xa, a.x); xb = fmaxf(xb, a.y); xc = fmaxf(xc, b.x); xd = fmaxf(xd, b.y);
-            }
-            xm = fmaxf(fmaxf(xa, xb), fmaxf(xc, xd));
-          } else {
-            xm = -INFINITY;
+          for (int i = 0; i < kKeys; ++i) sv[i] = valid_at(i) ? fmaf(sv[i], scale_log2, nm) : -INFINITY;
+        }
+        uint32_t pk[kKeys / 2];
+        auto exp_pack = [&]() {                      // p = 2^x as bf16 pairs; returns sum p
+          float sa = 0.f, sc = 0.f;
 #pragma unroll
-            for (int i = 0; i < kKeys; ++i) {
-              sv[i] = valid_at(i) ? fmaf(sv[i], scale_log2, nm) : -INFINITY;
-              xm = fmaxf(xm, sv[i]);
-            }
+          for (int i = 0; i < kKeys; i += 2) {
+            const float p0 = ex2_approx(sv[i]), p1 = ex2_approx(sv[i + 1]);
+            sa += p0;
+            sc += p1;
+            pk[i / 2] = bf16x2_bits(p0, p1);
           }
-          if (xm > kLazyLog2) {                      // rare: move the reference maximum
+          return sa + sc;
+        };
+        float psum = exp_pack();
+        if (!(psum < kLazySum)) {                    // rare (also taken by a NaN sum)
+          float xm = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < kKeys; ++i) xm = fmaxf(xm, sv[i]);
+          if (xm > kLazyLog2) {                      // move the reference maximum
             alpha = ex2_approx(-xm);
             m_ref += xm;
 #pragma unroll
             for (int i = 0; i < kKeys; ++i) sv[i] -= xm;
+            psum = exp_pack();
           }
         }
-        l_run *= alpha;
-        float psum = 0.f;
-        uint32_t pk[kKeys / 2];
-#pragma unroll
-        for (int i = 0; i < kKeys; i += 2) {
-          const float p0 = ex2_approx(sv[i]), p1 = ex2_approx(sv[i + 1]);
-          psum += p0 + p1;
-          pk[i / 2] = bf16x2_bits(p0, p1);
-        }
-        l_run += psum;
+        l_run = l_run * alpha + psum;
         const uint32_t any = __any_sync(0xffffffffu, alpha != 1.f) ? 1u : 0u;
-        // Stage P (swizzled K-major rows), alpha and the warp flags in staging buffer g % kPBuf
+        // Stage P (swizzled K-major rows), alpha and the warp flags in staging buffer psb
         // once the courier has shipped its previous contents.
-        if (!warp_wait(bar(kPSEmpty + psb), static_cast<uint32_t>(((g / kPBuf) & 1) ^ 1), 0x29, abort_flag)) { ok = false; break; }
+        if (!warp_wait(bar(kPSEmpty + psb), ps_ph ^ 1u, 0x29, abort_flag)) { ok = false; break; }
         uint8_t* slot = smem + kOffPS + psb * kPSStride;
         uint8_t* prow = slot + (h >> 3) * 256 + (h & 7) * 32;
         const int swz = (h >> 2) & 1;
@@ -970,6 +968,8 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
         if (lane == 0) reinterpret_cast<uint32_t*>(slot + kPBytes + 512)[warp] = any;
         fence_proxy_async_smem();
         mbar_arrive(bar(kPStaged + psb));
+        if (++sb == kStages) { sb = 0; s_ph ^= 1u; }
+        if (++psb == kPBuf) { psb = 0; ps_ph ^= 1u; }
       }
       if (!ok) break;
       // l of this query -> CTA 1 (buffer n % 2, free once CTA 1 read query n - 2's) as an
@@ -982,7 +982,6 @@ sparse_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_o,
         lse[t * kH + h] = l_run > 0.f ? (m_ref + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kMetaEmpty + (n & 1)));
-      g0 += nt;
     }
   } else if (crank == 1 && warp < 4) {
     // ---------------------------------------------------------------- CTA 1: O rows
