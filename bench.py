@@ -1008,6 +1008,46 @@ def profile_run(args):
                       "device_errors": dsa.dsa_read_device_errors()}))
 
 
+def gather_probe(args):
+    """Rate of the sparse MLA's row gather on its own: 152 CTAs (one per SM) each fill a 3-slot
+    ring of 48-row x 576-column bf16 tiles from uniform random rows of the many-request batch's
+    latent cache (71,014 rows x 1,152 B, inside L2), by 16-byte cp.async (the kernel's path) and
+    by TMA tile::gather4 with 1, 4, 12 or 32 issuing lanes. One JSON line per variant."""
+    import torch
+    import __graft_entry__ as ge
+    ge.build()
+    import deepseek_v3_sparse_round_gb300 as dsa
+    import workloads as W
+    wl = W.WORKLOADS[WORKLOAD_ID]
+    n_rows = int(sum(wl.lengths))
+    n_ctas = torch.cuda.get_device_properties(0).multi_processor_count
+    n_tiles = args.gather_probe
+    g = torch.Generator(device="cpu").manual_seed(7)
+    c = torch.randn(n_rows, 576, generator=g).to(torch.bfloat16).cuda()
+    rows = torch.randint(0, n_rows, (n_ctas * n_tiles * 48,), generator=g, dtype=torch.int32).cuda()
+    cycles = torch.zeros(n_ctas, dtype=torch.int64, device="cuda")
+    tile_bytes = 48 * 1152
+    for mode, issuers in ((0, 0), (1, 1), (1, 4), (1, 12), (1, 32)):
+        ms = []
+        for rep in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            dsa.dsa_probe_row_gather(c, rows, n_ctas, n_tiles, mode, max(issuers, 1), cycles)
+            e1.record()
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        cyc = float(cycles.double().mean())
+        t = sorted(ms[1:])[0]
+        print(json.dumps({
+            "gather_probe": "cp.async 16 B, 3 warps per slot" if mode == 0
+            else f"TMA tile::gather4, {issuers} issuing lane(s)",
+            "ctas": n_ctas, "tiles_per_cta": n_tiles, "tile": "48 rows x 1,152 B (9 SW128 atoms)",
+            "bytes_per_clk_per_sm": round(n_tiles * tile_bytes / cyc, 2),
+            "cycles_per_tile": round(cyc / n_tiles, 1),
+            "gb_per_s": round(n_ctas * n_tiles * tile_bytes / t / 1e6, 1), "ms": round(t, 4),
+            "device_errors": dsa.dsa_read_device_errors()}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1029,7 +1069,12 @@ def main():
                     help="ncu launch list: 1 + K default-workload steps, nothing else, then exit")
     ap.add_argument("--profile-case", action="store_true",
                     help="ncu capture: one 2,048-query cut of a many-request shard, then exit")
+    ap.add_argument("--gather-probe", type=int, nargs="?", const=400, default=0,
+                    help="row-gather rate probe, cp.async vs TMA gather4 (tiles per CTA), then exit")
     args = ap.parse_args()
+    if args.gather_probe:
+        gather_probe(args)
+        return
     if args.profile_steps or args.profile_case:
         profile_run(args)
         return

@@ -20,7 +20,8 @@ __all__ = [
     "dsa_indexer_topk_workspace_size", "dsa_score_row_stride", "dsa_indexer_scores",
     "dsa_topk_select", "dsa_indexer_topk", "dsa_indexer_topk_noalloc", "dsa_sparse_mla",
     "dsa_sparse_mla_workspace_size", "dsa_sparse_mla_balanced", "dsa_read_device_errors",
-    "dsa_rr_cache_local_paged", "dsa_selftest_bounded_wait", "dsa_quantize_fp8_rows",
+    "dsa_rr_cache_local_paged", "dsa_selftest_bounded_wait", "dsa_probe_row_gather",
+    "dsa_quantize_fp8_rows",
     "dsa_indexer_scores_fp8", "dsa_indexer_topk_fp8",
     "DEVERR_TIMEOUT", "DEVERR_BAD_INDEX", "DEVERR_BAD_LENGTH",
 ]
@@ -111,6 +112,21 @@ def dsa_selftest_bounded_wait(limit_cycles: int, stream=None):
     limit_cycles the wait gives up and sets DEVERR_TIMEOUT | 0xEE (read it with
     dsa_read_device_errors)."""
     _check(_lib().dsa_selftest_bounded_wait(int(limit_cycles), _stream(stream)))
+
+
+def dsa_probe_row_gather(c, rows, n_ctas, n_tiles, mode, issuers, cycles, stream=None):
+    """Row-gather rate probe: c bf16 [n_rows, 576]; rows int32 [n_ctas * n_tiles * 48];
+    mode 0 = cp.async (three warps per ring slot), 1 = TMA tile::gather4 by `issuers` lanes;
+    cycles int64 [n_ctas] receives each CTA's loop time in SM clock cycles."""
+    _dev(c, torch.bfloat16, "c")
+    _dev(rows, torch.int32, "rows")
+    _dev(cycles, torch.int64, "cycles")
+    if c.dim() != 2 or c.shape[1] != 576:
+        raise ValueError(f"c must be [n_rows, 576], got {tuple(c.shape)}")
+    _shape(rows, (int(n_ctas) * int(n_tiles) * 48,), "rows")
+    _shape(cycles, (int(n_ctas),), "cycles")
+    _check(_lib().dsa_probe_row_gather(_ptr(c), c.shape[0], _ptr(rows), int(n_ctas), int(n_tiles),
+                                       int(mode), int(issuers), _ptr(cycles), _stream(stream)))
 
 
 def dsa_rr_split_metadata(cu, n_tokens, sp, rank, cu_shard, pos, bid, gidx=None,

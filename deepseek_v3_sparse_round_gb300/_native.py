@@ -18,6 +18,7 @@ SIGNATURES = {
     "dsa_version": (c_int, []),
     "dsa_read_device_errors": (c_int, [c_u32p]),
     "dsa_selftest_bounded_wait": (c_int, [c_i64, c_vp]),
+    "dsa_probe_row_gather": (c_int, [c_vp, c_i64, c_vp, c_int, c_int, c_int, c_int, c_vp, c_vp]),
     "dsa_rr_shard_len": (c_i64, [c_i64, c_int, c_int]),
     "dsa_rr_split_metadata": (c_int, [c_vp, c_int, c_i64, c_int, c_int, c_vp, c_vp, c_vp, c_vp,
                                       c_vp, c_vp, c_i64, c_vp]),

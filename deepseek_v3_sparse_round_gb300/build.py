@@ -16,7 +16,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdsa_rr.so")
-SOURCES = ["api.cu", "split.cu", "topk.cu", "indexer.cu", "mla.cu", "noalloc.cu", "selftest.cu", "quant.cu"]
+SOURCES = ["api.cu", "split.cu", "topk.cu", "indexer.cu", "mla.cu", "noalloc.cu", "selftest.cu", "quant.cu",
+           "probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "-diag-suppress", "177"]

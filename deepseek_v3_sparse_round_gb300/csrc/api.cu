@@ -49,6 +49,9 @@ int cache_local_paged(const void* local_rows, void* pool, int64_t pool_rows, int
                       cudaStream_t stream);
 int selftest_bounded_wait(long long limit_cycles, cudaStream_t stream);
 cudaError_t selftest_read_errors(uint32_t* flags);
+int probe_row_gather(const void* c, int64_t n_rows, const int32_t* rows, int n_ctas, int n_tiles,
+                     int mode, int issuers, unsigned long long* cycles, cudaStream_t stream);
+cudaError_t probe_read_errors(uint32_t* flags);
 cudaError_t topk_read_errors(uint32_t* flags);
 cudaError_t indexer_read_errors(uint32_t* flags);
 cudaError_t mla_read_errors(uint32_t* flags);
@@ -128,6 +131,7 @@ DSA_EXPORT int dsa_read_device_errors(uint32_t* flags) {
   DSA_CHECK_CUDA(dsa::indexer_read_errors(flags));
   DSA_CHECK_CUDA(dsa::mla_read_errors(flags));
   DSA_CHECK_CUDA(dsa::selftest_read_errors(flags));
+  DSA_CHECK_CUDA(dsa::probe_read_errors(flags));
   return DSA_OK;
 }
 
@@ -136,6 +140,25 @@ DSA_EXPORT int dsa_selftest_bounded_wait(int64_t limit_cycles, dsa_stream_t stre
     return dsa::fail(DSA_ERR_INVALID, "selftest: limit_cycles must be in [1, 2^40]");
   return dsa::selftest_bounded_wait(static_cast<long long>(limit_cycles),
                                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+DSA_EXPORT int dsa_probe_row_gather(const void* c, int64_t n_rows, const int32_t* rows, int n_ctas,
+                                    int n_tiles, int mode, int issuers, uint64_t* cycles,
+                                    dsa_stream_t stream) {
+  if (c == nullptr || rows == nullptr || cycles == nullptr)
+    return dsa::fail(DSA_ERR_INVALID, "probe: null pointer");
+  if (n_rows < 1 || n_rows > (1ll << 31) - 1 || n_ctas < 1 || n_ctas > 65535 || n_tiles < 1 ||
+      static_cast<int64_t>(n_ctas) * n_tiles * 48 > (1ll << 31) - 1)
+    return dsa::fail(DSA_ERR_INVALID, "probe: need 1 <= n_rows < 2^31, 1 <= n_ctas <= 65535, "
+                                      "n_tiles >= 1 and n_ctas * n_tiles * 48 < 2^31");
+  if (mode != 0 && mode != 1) return dsa::fail(DSA_ERR_INVALID, "probe: mode is 0 or 1");
+  if (mode == 1 && (issuers < 1 || issuers > 32))
+    return dsa::fail(DSA_ERR_INVALID, "probe: 1 <= issuers <= 32 for mode 1");
+  if ((reinterpret_cast<uintptr_t>(c) & 15u) != 0)
+    return dsa::fail(DSA_ERR_INVALID, "probe: c must be 16-byte aligned");
+  return dsa::probe_row_gather(c, n_rows, rows, n_ctas, n_tiles, mode, issuers,
+                               reinterpret_cast<unsigned long long*>(cycles),
+                               reinterpret_cast<cudaStream_t>(stream));
 }
 
 DSA_EXPORT int64_t dsa_rr_shard_len(int64_t n_tokens, int sp, int rank) {

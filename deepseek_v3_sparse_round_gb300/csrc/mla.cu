@@ -380,17 +380,17 @@ sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_c, const __nv_bfloat16*
 //     warp-uniform QK issuer takes every tile in order, so it sees every phase of the barriers
 //     it waits on (an issuer skipping another issuer's tiles on a 3-slot ring could take a
 //     parity two phases ahead). Its softmax warps stage P (bf16), the per-row rescale factors
-//     and flags in one of two staging buffers; a courier warp ships each to CTA 1 with bulk
+//     and flags in one of kPBuf staging buffers; a courier warp ships each to CTA 1 with bulk
 //     DSMEM copies (one bulk copy moves a tile far faster than per-thread DSMEM stores). A ring
 //     slot is free as soon as its QK MMAs finish.
 //   CTA 1 ("O side"): O (128 x 512 fp32) fills its TMEM; it accumulates O += P . V with two
 //     N = 256 MMAs per 16 keys and writes o = O / l at the end (TMA stores).
 // Each CTA gathers the selected rows it needs into its own 3-slot ring of 48-key tiles (CTA 0:
-// all 576 columns, CTA 1: the 512 latent columns), three gather warps per slot. At a query
-// boundary CTA 0 brings the next Q into TMEM through shared-memory staging tiles (the Q region
-// and the then idle P staging buffers). The running maximum is lazy: O is rescaled only when a
-// row's maximum grows by more than 2^16 (rare; then CTA 1's four row warps rescale O between
-// two PV steps).
+// all 576 columns, CTA 1: the 512 latent columns), three gather warps per slot. Ahead of a
+// query's tiles, CTA 0's ring carries its Q in three TMA-loaded pieces that the QK issuer copies
+// into TMEM (tcgen05.cp) once the previous query's QK MMAs are done. The running maximum is
+// lazy: O is rescaled only when a row's maximum grows by more than 2^16 (rare; then CTA 1's
+// four row warps rescale O between two PV steps).
 namespace pair {
 constexpr int kH = 128, kDQK = 576, kDV = 512;
 constexpr int kKeys = 48;                       // keys per tile
@@ -417,8 +417,8 @@ constexpr int kOffPS = kStages * kStageS;       // CTA 0: kPBuf P staging buffer
 constexpr int kOffMask = kOffPS + kPBuf * kPSStride;  // CTA 0: u32 [2][kMaskWords]
 constexpr int kEndS = kOffMask + 2 * kMaskWords * 4, kEndO = kOffP + kPBuf * kPBytes;
 constexpr int kRegion = ((kEndS > kEndO ? kEndS : kEndO) + 15) / 16 * 16;
-// 32 rows x 128 B per row warp, 1 KB aligned (128B swizzle): CTA 0 transposes Q rows through
-// it on their way to TMEM, CTA 1 stages bf16 o for TMA stores.
+// 32 rows x 128 B per row warp, 1 KB aligned (128B swizzle): CTA 1 stages bf16 o in it for
+// TMA stores.
 constexpr int kOffX = (kRegion + 1023) / 1024 * 1024;
 constexpr int kXBytes = 4 * 32 * 128;
 constexpr int kOffXO1 = kEndO;                  // CTA 1: second o staging tile per row warp

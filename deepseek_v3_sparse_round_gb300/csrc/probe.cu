@@ -1,0 +1,138 @@
+// Row-gather throughput probe: the two ways the sparse MLA could bring its selected latent rows
+// (576 bf16 = 1,152 B each) into shared memory, timed on their own with nothing consuming the
+// tiles. Each CTA fills a 3-slot ring of 48-row tiles in the MLA's layout (nine 128B-swizzled
+// 64-column atoms per tile) from a list of row indices, and a consumer lane hands every slot
+// back as soon as it is full, so only the gather's own rate and latency bound the loop.
+//
+//   mode 0 (the MLA's path): three warps per slot, 16-byte cp.async copies, one lane per 16-byte
+//     chunk of a row; each warp waits for its copies, fences them for the async proxy and
+//     arrives on the slot's full barrier.
+//   mode 1: TMA tile::gather4 (four rows of one 64-column box per instruction, 108 per tile),
+//     issued by `issuers` lanes of one warp, completing on the slot's full barrier by bytes.
+//
+// Every wait is bounded; row indices outside [0, n_rows) are replaced by row 0 and reported as
+// DSA_DEVERR_BAD_INDEX. Each CTA writes the clock cycles its loop took.
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+#include "status.cuh"
+#include "tmap.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kRows = 48, kAtoms = 9, kAtomBytes = kRows * 128, kTile = kAtoms * kAtomBytes;
+constexpr int kSlots = 3, kWarpsPerSlot = 3, kGatherWarps = kSlots * kWarpsPerSlot;
+constexpr int kThreads = 32 * (kGatherWarps + 1);           // + the consumer warp
+constexpr int kSmem = kSlots * kTile;                       // 162 KB, 1 KB aligned tiles
+constexpr uint32_t kSite = 0xF0u;
+constexpr long long kLimit = 2000000000ll;                  // about a second per wait
+
+__global__ void __launch_bounds__(kThreads, 1)
+row_gather_probe_kernel(const __grid_constant__ CUtensorMap tm, const __nv_bfloat16* __restrict__ c,
+                        int64_t n_rows, const int32_t* __restrict__ rows, int n_tiles, int mode,
+                        int issuers, unsigned long long* __restrict__ cycles) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[2 * kSlots];
+  __shared__ uint32_t abort_flag;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t warp = warp_id(), lane = lane_id();
+  auto full = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty = [&](int s) { return smem_u32(&bars[kSlots + s]); };
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(full(s), mode == 0 ? 32 * kWarpsPerSlot : 1);
+      mbar_init(empty(s), 1);
+    }
+    abort_flag = (sbase & 1023u) == 0 ? 0u : 1u;
+    if (abort_flag) report_device_error(kErrBadIndex | kSite | 0xFu);   // ring not 1 KB aligned
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int32_t* my_rows = rows + static_cast<int64_t>(blockIdx.x) * n_tiles * kRows;
+  bool bad = false;
+  auto row_at = [&](int j, int r) {
+    const int32_t v = __ldg(my_rows + static_cast<int64_t>(j) * kRows + r);
+    if (v < 0 || v >= n_rows) { bad = true; return 0; }
+    return static_cast<int>(v);
+  };
+  const long long t0 = clock64();
+  if (warp == kGatherWarps) {
+    // consumer: every full slot goes straight back
+    for (int j = 0; j < n_tiles; ++j) {
+      const int s = j % kSlots;
+      if (!warp_wait(full(s), static_cast<uint32_t>((j / kSlots) & 1), kSite, &abort_flag, kLimit)) break;
+      if (lane == 0) mbar_arrive(empty(s));
+    }
+  } else if (mode == 0) {
+    const int s = static_cast<int>(warp) % kSlots, part = static_cast<int>(warp) / kSlots;
+    const int chunk = static_cast<int>(lane & 7);
+    const uint32_t stage = sbase + s * kTile;
+    for (int j = s; j < n_tiles; j += kSlots) {
+      if (!warp_wait(empty(s), static_cast<uint32_t>(((j / kSlots) & 1) ^ 1), kSite | 1u, &abort_flag, kLimit)) break;
+      for (int i = part; i < kRows / 4; i += kWarpsPerSlot) {
+        const int r = static_cast<int>(lane >> 3) + 4 * i;
+        const __nv_bfloat16* src = c + static_cast<int64_t>(row_at(j, r)) * (kAtoms * 64) + chunk * 8;
+        const uint32_t dst = stage + r * 128 + ((chunk ^ (r & 7)) * 16);
+        for (int a = 0; a < kAtoms; ++a) cp_async16(dst + a * kAtomBytes, src + a * 64, 16u);
+      }
+      cp_async_commit();
+      cp_async_wait_all();
+      fence_proxy_async_smem();
+      mbar_arrive(full(s));
+    }
+    cp_async_wait_all();
+  } else if (warp == 0) {
+    int last = -1;                                   // the last tile this warp started
+    for (int j = 0; j < n_tiles; ++j) {
+      const int s = j % kSlots;
+      if (!warp_wait(empty(s), static_cast<uint32_t>(((j / kSlots) & 1) ^ 1), kSite | 2u, &abort_flag, kLimit)) break;
+      if (lane == 0) mbar_expect_tx(full(s), kTile);
+      __syncwarp();
+      if (static_cast<int>(lane) < issuers) {
+        for (int g = static_cast<int>(lane); g < kAtoms * (kRows / 4); g += issuers) {
+          const int a = g / (kRows / 4), q4 = g % (kRows / 4);
+          tma_gather4(sbase + s * kTile + a * kAtomBytes + q4 * 4 * 128, &tm, a * 64,
+                      row_at(j, 4 * q4), row_at(j, 4 * q4 + 1), row_at(j, 4 * q4 + 2),
+                      row_at(j, 4 * q4 + 3), full(s));
+        }
+      }
+      __syncwarp();
+      last = j;
+    }
+    // unwinding: let the loads already issued land before the CTA can exit (bounded)
+    for (int j = last - kSlots + 1; j <= last; ++j) {
+      if (j < 0) continue;
+      const long long w0 = clock64();
+      while (!mbar_try_wait(full(j % kSlots), static_cast<uint32_t>((j / kSlots) & 1)) &&
+             clock64() - w0 < kLimit) {
+      }
+    }
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) report_device_error(kErrBadIndex | kSite);
+  __syncthreads();
+  if (threadIdx.x == 0) cycles[blockIdx.x] = static_cast<unsigned long long>(clock64() - t0);
+}
+
+}  // namespace
+
+int probe_row_gather(const void* c, int64_t n_rows, const int32_t* rows, int n_ctas, int n_tiles,
+                     int mode, int issuers, unsigned long long* cycles, cudaStream_t stream) {
+  CUtensorMap tm;
+  int rc = make_tmap_bf16_2d(&tm, c, static_cast<uint64_t>(n_rows), kAtoms * 64, kAtoms * 128,
+                             64, 1, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc) return rc;
+  DSA_CHECK_CUDA(cudaFuncSetAttribute(row_gather_probe_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem));
+  row_gather_probe_kernel<<<n_ctas, kThreads, kSmem, stream>>>(
+      tm, static_cast<const __nv_bfloat16*>(c), n_rows, rows, n_tiles, mode, issuers, cycles);
+  DSA_CHECK_CUDA(cudaGetLastError());
+  return DSA_OK;
+}
+
+cudaError_t probe_read_errors(uint32_t* flags) { return read_and_clear_device_error(flags); }
+
+}  // namespace dsa

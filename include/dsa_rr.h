@@ -77,6 +77,27 @@ int dsa_read_device_errors(uint32_t* flags);
 int dsa_selftest_bounded_wait(int64_t limit_cycles, dsa_stream_t stream);
 
 /*
+ * Measurement probe (no counterpart on the pages): the rate at which one SM brings selected
+ * latent rows into shared memory, by either of the two mechanisms the sparse MLA could use for
+ * its row gather ("[RFC]: Parallel strategy for Deepseek v3.2 like models", Pros: the MLA runs
+ * all heads on the gathered rows). Enqueues n_ctas CTAs (one per SM at most); CTA i fills a
+ * 3-slot ring of 48-row tiles in the MLA's 128B-swizzled layout from rows[i * n_tiles * 48 ..],
+ * n_tiles tiles, with nothing consuming them, and writes the SM clock cycles its loop took to
+ * cycles[i].
+ *   c:     device, bf16 [n_rows, 576] (1,152-byte rows), 16-byte aligned; read only.
+ *   rows:  device, int32 [n_ctas * n_tiles * 48], each in [0, n_rows) (others read row 0 and
+ *          set DSA_DEVERR_BAD_INDEX).
+ *   mode:  0 = 16-byte cp.async copies by three warps per slot (the MLA's path);
+ *          1 = TMA tile::gather4 issued by `issuers` (1..32) lanes of one warp.
+ *   cycles: device, uint64 [n_ctas], written.
+ * Every in-kernel wait is bounded. Errors: DSA_ERR_INVALID for a null pointer, a size out of
+ * range or a bad mode; DSA_ERR_CUDA for a failed launch.
+ */
+int dsa_probe_row_gather(const void* c, int64_t n_rows, const int32_t* rows, int n_ctas,
+                         int n_tiles, int mode, int issuers, uint64_t* cycles,
+                         dsa_stream_t stream);
+
+/*
  * Host helper: number of tokens shard `rank` of `sp` holds, ceil((n_tokens - rank) / sp), or
  * 0 when rank >= n_tokens. Source: "[DeepSeek v3.2] 上下文并行详解", section 2.B
  * (arange(cp_rank, tokens, cp_size)). Returns -1 for sp < 1, rank < 0, rank >= sp or
