@@ -1027,24 +1027,38 @@ def gather_probe(args):
     rows = torch.randint(0, n_rows, (n_ctas * n_tiles * 48,), generator=g, dtype=torch.int32).cuda()
     cycles = torch.zeros(n_ctas, dtype=torch.int64, device="cuda")
     tile_bytes = 48 * 1152
-    for mode, issuers in ((0, 0), (1, 1), (1, 4), (1, 12), (1, 32)):
+    variants = [(n_ctas, 0, 0), (n_ctas, 1, 1), (n_ctas, 1, 4), (n_ctas, 1, 12), (n_ctas, 1, 32),
+                (n_ctas, 2, 0), (n_ctas // 2, 0, 0), (n_ctas // 4, 0, 0), (n_ctas, 3, 0)]
+    for ctas, mode, issuers in variants:
         ms = []
         for rep in range(3):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
-            dsa.dsa_probe_row_gather(c, rows, n_ctas, n_tiles, mode, max(issuers, 1), cycles)
+            dsa.dsa_probe_row_gather(c, rows[:ctas * n_tiles * 48], ctas, n_tiles, mode,
+                                     max(issuers, 1), cycles[:ctas])
             e1.record()
             torch.cuda.synchronize()
             ms.append(e0.elapsed_time(e1))
-        cyc = float(cycles.double().mean())
+        cyc = float(cycles[:ctas].double().mean())
+        if mode == 3:                                # 192 KB into (and out of) each SM a round
+            rounds_bytes = n_tiles * 192 * 1024
+            print(json.dumps({
+                "dsmem_probe": "bulk copies between the CTAs of each pair, 6 x 32 KB per round",
+                "ctas": ctas, "rounds": n_tiles,
+                "bytes_per_clk_per_sm_in": round(rounds_bytes / cyc, 2),
+                "gb_per_s": round(ctas * rounds_bytes / sorted(ms[1:])[0] / 1e6, 1),
+                "device_errors": dsa.dsa_read_device_errors()}), flush=True)
+            continue
         t = sorted(ms[1:])[0]
+        how = {0: "cp.async 16 B, 3 warps per slot",
+               1: f"TMA tile::gather4, {issuers} issuing lane(s)",
+               2: "cp.async for columns 0-511 + TMA tile::gather4 for 512-575"}[mode]
         print(json.dumps({
-            "gather_probe": "cp.async 16 B, 3 warps per slot" if mode == 0
-            else f"TMA tile::gather4, {issuers} issuing lane(s)",
-            "ctas": n_ctas, "tiles_per_cta": n_tiles, "tile": "48 rows x 1,152 B (9 SW128 atoms)",
+            "gather_probe": how,
+            "ctas": ctas, "tiles_per_cta": n_tiles, "tile": "48 rows x 1,152 B (9 SW128 atoms)",
             "bytes_per_clk_per_sm": round(n_tiles * tile_bytes / cyc, 2),
             "cycles_per_tile": round(cyc / n_tiles, 1),
-            "gb_per_s": round(n_ctas * n_tiles * tile_bytes / t / 1e6, 1), "ms": round(t, 4),
+            "gb_per_s": round(ctas * n_tiles * tile_bytes / t / 1e6, 1), "ms": round(t, 4),
             "device_errors": dsa.dsa_read_device_errors()}), flush=True)
 
 

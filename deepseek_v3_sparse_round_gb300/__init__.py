@@ -116,7 +116,9 @@ def dsa_selftest_bounded_wait(limit_cycles: int, stream=None):
 
 def dsa_probe_row_gather(c, rows, n_ctas, n_tiles, mode, issuers, cycles, stream=None):
     """Row-gather rate probe: c bf16 [n_rows, 576]; rows int32 [n_ctas * n_tiles * 48];
-    mode 0 = cp.async (three warps per ring slot), 1 = TMA tile::gather4 by `issuers` lanes;
+    mode 0 = cp.async (three warps per ring slot), 1 = TMA tile::gather4 by `issuers` lanes,
+    2 = columns 0..511 by cp.async and 512..575 by tile::gather4, 3 = DSMEM push between the
+    CTAs of pairs (192 KB per round, n_tiles rounds);
     cycles int64 [n_ctas] receives each CTA's loop time in SM clock cycles."""
     _dev(c, torch.bfloat16, "c")
     _dev(rows, torch.int32, "rows")

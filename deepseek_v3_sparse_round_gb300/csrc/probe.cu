@@ -9,6 +9,12 @@
 //     arrives on the slot's full barrier.
 //   mode 1: TMA tile::gather4 (four rows of one 64-column box per instruction, 108 per tile),
 //     issued by `issuers` lanes of one warp, completing on the slot's full barrier by bytes.
+//   mode 2: both at once: atoms 0-7 by mode 0's cp.async warps, atom 8 (the rope columns) by
+//     12 tile::gather4 issued by lane 0 of the slot's first gather warp.
+//   mode 3: not a gather: the rate of the DSMEM path between the two CTAs of a cluster (what
+//     the MLA's courier uses). Each CTA pushes 192 KB per round into its peer's shared memory
+//     with six 32 KB bulk copies that complete on the peer's barrier; a cluster barrier keeps
+//     the two CTAs in step; n_tiles rounds.
 //
 // Every wait is bounded; row indices outside [0, n_rows) are replaced by row 0 and reported as
 // DSA_DEVERR_BAD_INDEX. Each CTA writes the clock cycles its loop took.
@@ -44,7 +50,7 @@ row_gather_probe_kernel(const __grid_constant__ CUtensorMap tm, const __nv_bfloa
   auto empty = [&](int s) { return smem_u32(&bars[kSlots + s]); };
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSlots; ++s) {
-      mbar_init(full(s), mode == 0 ? 32 * kWarpsPerSlot : 1);
+      mbar_init(full(s), mode == 1 ? 1 : 32 * kWarpsPerSlot);
       mbar_init(empty(s), 1);
     }
     abort_flag = (sbase & 1023u) == 0 ? 0u : 1u;
@@ -67,17 +73,29 @@ row_gather_probe_kernel(const __grid_constant__ CUtensorMap tm, const __nv_bfloa
       if (!warp_wait(full(s), static_cast<uint32_t>((j / kSlots) & 1), kSite, &abort_flag, kLimit)) break;
       if (lane == 0) mbar_arrive(empty(s));
     }
-  } else if (mode == 0) {
+  } else if (mode == 0 || mode == 2) {
     const int s = static_cast<int>(warp) % kSlots, part = static_cast<int>(warp) / kSlots;
     const int chunk = static_cast<int>(lane & 7);
     const uint32_t stage = sbase + s * kTile;
+    const int n_cp = mode == 0 ? kAtoms : kAtoms - 1;       // atoms copied by cp.async
+    int last = -1;                                   // mode 2: the last tile this lane's TMA filled
     for (int j = s; j < n_tiles; j += kSlots) {
       if (!warp_wait(empty(s), static_cast<uint32_t>(((j / kSlots) & 1) ^ 1), kSite | 1u, &abort_flag, kLimit)) break;
+      if (mode == 2 && part == 0 && lane == 0) {
+        // atom 8 by TMA: its bytes complete on the slot's full barrier (the count is added
+        // without an arrival of its own, before this lane's arrival below)
+        mbar_add_tx(full(s), kAtomBytes);
+        for (int q4 = 0; q4 < kRows / 4; ++q4)
+          tma_gather4(stage + (kAtoms - 1) * kAtomBytes + q4 * 4 * 128, &tm, (kAtoms - 1) * 64,
+                      row_at(j, 4 * q4), row_at(j, 4 * q4 + 1), row_at(j, 4 * q4 + 2),
+                      row_at(j, 4 * q4 + 3), full(s));
+        last = j;
+      }
       for (int i = part; i < kRows / 4; i += kWarpsPerSlot) {
         const int r = static_cast<int>(lane >> 3) + 4 * i;
         const __nv_bfloat16* src = c + static_cast<int64_t>(row_at(j, r)) * (kAtoms * 64) + chunk * 8;
         const uint32_t dst = stage + r * 128 + ((chunk ^ (r & 7)) * 16);
-        for (int a = 0; a < kAtoms; ++a) cp_async16(dst + a * kAtomBytes, src + a * 64, 16u);
+        for (int a = 0; a < n_cp; ++a) cp_async16(dst + a * kAtomBytes, src + a * 64, 16u);
       }
       cp_async_commit();
       cp_async_wait_all();
@@ -85,6 +103,13 @@ row_gather_probe_kernel(const __grid_constant__ CUtensorMap tm, const __nv_bfloa
       mbar_arrive(full(s));
     }
     cp_async_wait_all();
+    if (last >= 0) {
+      // unwinding: let this lane's last TMA fill land before the CTA can exit (bounded)
+      const long long w0 = clock64();
+      while (!mbar_try_wait(full(s), static_cast<uint32_t>((last / kSlots) & 1)) &&
+             clock64() - w0 < kLimit) {
+      }
+    }
   } else if (warp == 0) {
     int last = -1;                                   // the last tile this warp started
     for (int j = 0; j < n_tiles; ++j) {
@@ -117,10 +142,68 @@ row_gather_probe_kernel(const __grid_constant__ CUtensorMap tm, const __nv_bfloa
   if (threadIdx.x == 0) cycles[blockIdx.x] = static_cast<unsigned long long>(clock64() - t0);
 }
 
+constexpr int kXChunk = 32768, kXChunks = 6, kXRound = kXChunk * kXChunks;   // 192 KB a round
+
+__global__ void __launch_bounds__(128, 1)
+dsmem_probe_kernel(int rounds, unsigned long long* __restrict__ cycles) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  const uint32_t sbase = smem_u32(smem), b = smem_u32(&bar);
+  const uint32_t peer = cluster_ctarank() ^ 1u;
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    abort_flag = 0u;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  cluster_sync();                                    // the peer's barrier exists from here on
+  const long long t0 = clock64();
+  // Every CTA runs every round (no early exit), so both reach every cluster barrier; a wait
+  // that gives up only sets the error word and the abort flag (later waits return at once).
+  for (int r = 0; r < rounds; ++r) {
+    if (threadIdx.x == 0) mbar_expect_tx(b, kXRound);   // this round's incoming bytes
+    cluster_sync();                                  // both CTAs armed before any copy lands
+    if (threadIdx.x == 0) {
+      // the source is the CTA's own buffer while the peer's copies land in it: the bytes are
+      // not used, only their rate
+      for (int i = 0; i < kXChunks; ++i)
+        bulk_copy_to_peer(sbase + i * kXChunk, sbase + i * kXChunk, kXChunk, b, peer);
+      bulk_commit();
+      mbar_wait(b, static_cast<uint32_t>(r & 1), kSite | 3u, &abort_flag, kLimit);
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    bulk_wait_all();                                 // this CTA's outgoing copies are done
+    cycles[blockIdx.x] = static_cast<unsigned long long>(clock64() - t0);
+  }
+  __syncthreads();
+  cluster_sync();                                    // no CTA leaves while its peer may write
+}
+
 }  // namespace
 
 int probe_row_gather(const void* c, int64_t n_rows, const int32_t* rows, int n_ctas, int n_tiles,
                      int mode, int issuers, unsigned long long* cycles, cudaStream_t stream) {
+  if (mode == 3) {
+    DSA_CHECK_CUDA(cudaFuncSetAttribute(dsmem_probe_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kXRound));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(n_ctas));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = kXRound;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    DSA_CHECK_CUDA(cudaLaunchKernelEx(&cfg, dsmem_probe_kernel, n_tiles, cycles));
+    return DSA_OK;
+  }
   CUtensorMap tm;
   int rc = make_tmap_bf16_2d(&tm, c, static_cast<uint64_t>(n_rows), kAtoms * 64, kAtoms * 128,
                              64, 1, CU_TENSOR_MAP_SWIZZLE_128B);

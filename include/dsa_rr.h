@@ -88,7 +88,11 @@ int dsa_selftest_bounded_wait(int64_t limit_cycles, dsa_stream_t stream);
  *   rows:  device, int32 [n_ctas * n_tiles * 48], each in [0, n_rows) (others read row 0 and
  *          set DSA_DEVERR_BAD_INDEX).
  *   mode:  0 = 16-byte cp.async copies by three warps per slot (the MLA's path);
- *          1 = TMA tile::gather4 issued by `issuers` (1..32) lanes of one warp.
+ *          1 = TMA tile::gather4 issued by `issuers` (1..32) lanes of one warp;
+ *          2 = both at once: columns 0..511 by cp.async, 512..575 by tile::gather4;
+ *          3 = no gather: CTA pairs (clusters of 2, n_ctas even) push 192 KB per round into
+ *              each other's shared memory by bulk DSMEM copies, n_tiles rounds (the rate of
+ *              the path the MLA's courier uses); rows and c are not read.
  *   cycles: device, uint64 [n_ctas], written.
  * Every in-kernel wait is bounded. Errors: DSA_ERR_INVALID for a null pointer, a size out of
  * range or a bad mode; DSA_ERR_CUDA for a failed launch.
