@@ -258,7 +258,8 @@ class ConfigStep:
         rerange_bytes = 2 * self.N * (wl.Di + wl.dqk) * 2 * len(self.ranks)
         nbytes = sum(2 * self.n_r[r] * wl.dqk * 2 for r in self.ranks) + rerange_bytes
         return {"indexer_flop": idx, "mla_flop": mla, "causal_pairs": pairs_c,
-                "selected_pairs": pairs_s, "copy_bytes": nbytes, "rerange_bytes": rerange_bytes}
+                "selected_pairs": pairs_s, "copy_bytes": nbytes, "rerange_bytes": rerange_bytes,
+                "shard_queries": [self.n_r[r] for r in self.ranks]}
 
     def queries(self):
         return sum(self.n_r.values())
@@ -359,6 +360,43 @@ def shard_balance(torch, dsa, W, device, wid=3):
     return {"workload": "many_req: 32 requests U[128,4096] (N=71,014), sp=4",
             "round_robin": {"queries": rr_q, "causal_pairs": rr_p, "pair_spread": spread(rr_p)},
             "in_seq": {"queries": is_q, "causal_pairs": is_p, "pair_spread": spread(is_p)}}
+
+
+def mla_gather_roofline(torch, dsa, W, device, work, mla_s, clocks):
+    """The sparse MLA against the resource that binds it: the rate at which an SM brings
+    selected latent rows into shared memory. CTA 0 of each pair gathers 1,152 B per selected
+    pair; the ceiling is measured in this run by the library's row-gather probe (16-byte
+    cp.async, every SM, a 3-slot ring of 48-row tiles, nothing consuming them), as bytes per SM
+    clock. Achieved = CTA 0's bytes per launch / (MLA time x the SM clock sampled during the
+    timed steps)."""
+    n_ctas = torch.cuda.get_device_properties(device).multi_processor_count
+    n_tiles = 400
+    n_rows = int(sum(W.WORKLOADS[WORKLOAD_ID].lengths))
+    g = torch.Generator(device="cpu").manual_seed(7)
+    c = torch.randn(n_rows, 576, generator=g).to(torch.bfloat16).to(device)
+    rows = torch.randint(0, n_rows, (n_ctas * n_tiles * 48,), generator=g,
+                         dtype=torch.int32).to(device)
+    cycles = torch.zeros(n_ctas, dtype=torch.int64, device=device)
+    per_tile = []
+    for _ in range(3):
+        dsa.dsa_probe_row_gather(c, rows, n_ctas, n_tiles, 0, 1, cycles)
+        torch.cuda.synchronize()
+        per_tile.append(float(cycles.double().mean()) / n_tiles)
+    ceiling = 48 * 1152 / sorted(per_tile)[1]        # B per SM clock (median of 3)
+    sm_mhz = clocks.get("sm_mhz") if isinstance(clocks, dict) else None
+    pairs_per_launch = min(n_ctas // 2, min(work["shard_queries"]))
+    launches = len(work["shard_queries"])
+    if not sm_mhz:
+        return {"bound": "l2_row_gather", "peak": round(ceiling, 2), "achieved": None,
+                "note": "no SM clock sample"}
+    b_sm = work["selected_pairs"] * 1152 / launches / pairs_per_launch   # CTA 0, one launch
+    achieved = b_sm / ((mla_s / launches) * sm_mhz * 1e6)
+    return {"bound": "l2_row_gather", "achieved": round(achieved, 2), "peak": round(ceiling, 2),
+            "unit": "B per SM clock (CTA 0 of each pair)", "frac": round(achieved / ceiling, 4),
+            "peak_source": "dsa_probe_row_gather mode 0 in this run (median of 3)",
+            "clock_mhz": sm_mhz,
+            "unit_of_work": "selected (query, key) pair: CTA 0 gathers its 576-column row "
+                            "(1,152 B); CTA 1 gathers 1,024 B of the same row"}
 
 
 def gpu_arm(args):
@@ -495,6 +533,7 @@ def gpu_arm(args):
     traffic = None
     if mla_tr is not None:    # DRAM bytes per selected pair from a capture, scaled to a launch
         traffic = int(mla_tr["dram_bytes_per_unit"] * work["selected_pairs"] / len(st.ranks))
+    gather = mla_gather_roofline(torch, dsa, W, device, work, mla_s, clk.summary())
     cpu = None
     if not args.no_cpu_baseline:
         cpu = cpu_baseline(args.cpu_baseline_queries)
@@ -542,6 +581,7 @@ def gpu_arm(args):
             {"algorithmic_bytes_per_launch": work["rerange_bytes"] / len(st.ranks),
              "unit_of_work": "token: 2 x (256 + 1152) B (k_idx and latent rows, read + write)",
              "timing": "CUDA events around each rerange launch, mean over the timed steps"}),
+        "roofline_mla_gather": gather,
         "ms_split_rerange": round(cp_s * 1e3, 4), "ms_indexer_topk": round(idx_s * 1e3, 4),
         "ms_mla": round(mla_s * 1e3, 4),
         "e2e": {"value": round(queries * e2e_steps / e2e_s, 2), "unit": "tokens/s",
