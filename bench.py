@@ -362,6 +362,43 @@ def shard_balance(torch, dsa, W, device, wid=3):
             "in_seq": {"queries": is_q, "causal_pairs": is_p, "pair_spread": spread(is_p)}}
 
 
+def host_link(torch, device, h2d_bytes, d2h_bytes):
+    """The host link the e2e line runs over: 1 GiB pinned copies, each direction alone and both
+    at once on two streams (CUDA events, best of 3), and the per-step time those rates allow
+    for the step's bytes with both directions busy."""
+    n = 1 << 30
+    h = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    h2 = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(n, dtype=torch.uint8, device=device)
+    d2 = torch.empty(n, dtype=torch.uint8, device=device)
+    s1, s2 = torch.cuda.Stream(device), torch.cuda.Stream(device)
+
+    def best(fn):
+        ts = []
+        for _ in range(3):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            ts.append(time.perf_counter() - t0)
+        return min(ts)
+
+    def both():
+        with torch.cuda.stream(s1):
+            d.copy_(h, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h2.copy_(d2, non_blocking=True)
+
+    h2d = n / best(lambda: d.copy_(h, non_blocking=True)) / 1e9
+    d2h = n / best(lambda: h2.copy_(d2, non_blocking=True)) / 1e9
+    each = n / best(both) / 1e9
+    del h, h2, d, d2
+    return {"h2d_gbps": round(h2d, 1), "d2h_gbps": round(d2h, 1),
+            "both_directions_gbps_each": round(each, 1),
+            "ms_per_step_at_link_rate": round(max(h2d_bytes, d2h_bytes) / each / 1e6, 2),
+            "how": "1 GiB pinned copies, best of 3"}
+
+
 def mla_gather_roofline(torch, dsa, W, device, work, mla_s, clocks):
     """The sparse MLA against the resource that binds it: the rate at which an SM brings
     selected latent rows into shared memory. CTA 0 of each pair gathers 1,152 B per selected
@@ -514,6 +551,7 @@ def gpu_arm(args):
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, dist, device)
 
+    link = host_link(torch, device, st.h2d_bytes(), st.d2h_bytes())
     errors = dsa.dsa_read_device_errors()
     if rank != 0:
         if dist:
@@ -587,8 +625,10 @@ def gpu_arm(args):
         "e2e": {"value": round(queries * e2e_steps / e2e_s, 2), "unit": "tokens/s",
                 "steps": e2e_steps, "h2d_bytes_per_step": st.h2d_bytes(),
                 "d2h_bytes_per_step": st.d2h_bytes(),
+                "ms_per_step": round(e2e_s * 1e3 / e2e_steps, 2),
                 "how": "pinned host inputs uploaded and o read back every step, pipelined per "
-                       "shard over 2 buffer sets and 3 streams"},
+                       "shard over 2 buffer sets and 3 streams",
+                "host_link": link},
         "gpu_launches": st.launches_per_step * args.steps,
         "clocks": clk.summary(),
         "device_errors": errors,
@@ -1068,7 +1108,8 @@ def gather_probe(args):
     cycles = torch.zeros(n_ctas, dtype=torch.int64, device="cuda")
     tile_bytes = 48 * 1152
     variants = [(n_ctas, 0, 0), (n_ctas, 1, 1), (n_ctas, 1, 4), (n_ctas, 1, 12), (n_ctas, 1, 32),
-                (n_ctas, 2, 0), (n_ctas // 2, 0, 0), (n_ctas // 4, 0, 0), (n_ctas, 3, 0)]
+                (n_ctas, 2, 0), (n_ctas // 2, 0, 0), (n_ctas // 4, 0, 0), (n_ctas, 4, 0),
+                (n_ctas // 2, 4, 0), (n_ctas, 6, 0), (n_ctas, 5, 0), (n_ctas, 3, 0)]
     for ctas, mode, issuers in variants:
         ms = []
         for rep in range(3):
@@ -1091,6 +1132,9 @@ def gather_probe(args):
             continue
         t = sorted(ms[1:])[0]
         how = {0: "cp.async 16 B, 3 warps per slot",
+               4: "ld.global 16 B + st.shared, 3 warps per slot",
+               5: "ld.global + st.shared for columns 0-319, cp.async for 320-575",
+               6: "ld.global 16 B + st.shared, every row of a warp in flight",
                1: f"TMA tile::gather4, {issuers} issuing lane(s)",
                2: "cp.async for columns 0-511 + TMA tile::gather4 for 512-575"}[mode]
         print(json.dumps({

@@ -11,6 +11,11 @@
 //     issued by `issuers` lanes of one warp, completing on the slot's full barrier by bytes.
 //   mode 2: both at once: atoms 0-7 by mode 0's cp.async warps, atom 8 (the rope columns) by
 //     12 tile::gather4 issued by lane 0 of the slot's first gather warp.
+//   mode 4: as mode 0 through registers: 16-byte ld.global (L1 no-allocate) and st.shared,
+//     each warp keeping two rows' nine chunks in flight per lane.
+//   mode 5: both paths at once: atoms 0-4 of every row through registers as in mode 4,
+//     atoms 5-8 by cp.async as in mode 0.
+//   mode 6: as mode 4 with all four of a warp's row groups in flight at once.
 //   mode 3: not a gather: the rate of the DSMEM path between the two CTAs of a cluster (what
 //     the MLA's courier uses). Each CTA pushes 192 KB per round into its peer's shared memory
 //     with six 32 KB bulk copies that complete on the peer's barrier; a cluster barrier keeps
@@ -37,6 +42,56 @@ constexpr int kSmem = kSlots * kTile;                       // 162 KB, 1 KB alig
 constexpr uint32_t kSite = 0xF0u;
 constexpr long long kLimit = 2000000000ll;                  // about a second per wait
 
+
+// Register path of the gather (modes 4-6): this warp's row groups (part, part + 3, ...),
+// kInFlight at a time, atoms 0..kReg-1 by 16-byte ld.global + st.shared, the rest (if any) by
+// cp.async issued first.
+template <int kInFlight, int kReg, typename RowAt, typename FullBar, typename EmptyBar>
+__device__ __forceinline__ void reg_gather(const __nv_bfloat16* __restrict__ c, uint32_t sbase,
+                                           uint8_t* smem, uint32_t warp, uint32_t lane,
+                                           int n_tiles, RowAt& row_at, FullBar& full,
+                                           EmptyBar& empty, uint32_t* abort_flag) {
+  const int s = static_cast<int>(warp) % kSlots, part = static_cast<int>(warp) / kSlots;
+  const int chunk = static_cast<int>(lane & 7);
+  constexpr int kGroups = kRows / 4 / kWarpsPerSlot;        // 4 row groups of 4 rows per warp
+  static_assert(kGroups % kInFlight == 0, "row groups in flight");
+  for (int j = s; j < n_tiles; j += kSlots) {
+    if (!warp_wait(empty(s), static_cast<uint32_t>(((j / kSlots) & 1) ^ 1), kSite | 4u, abort_flag, kLimit)) break;
+    if (kReg < kAtoms) {
+      for (int i = part; i < kRows / 4; i += kWarpsPerSlot) {
+        const int r = static_cast<int>(lane >> 3) + 4 * i;
+        const __nv_bfloat16* src = c + static_cast<int64_t>(row_at(j, r)) * (kAtoms * 64) + chunk * 8;
+        const uint32_t dst = sbase + s * kTile + r * 128 + ((chunk ^ (r & 7)) * 16);
+        for (int a = kReg; a < kAtoms; ++a) cp_async16(dst + a * kAtomBytes, src + a * 64, 16u);
+      }
+      cp_async_commit();
+    }
+#pragma unroll
+    for (int i0 = 0; i0 < kGroups; i0 += kInFlight) {
+      uint4 v[kInFlight][kReg];
+#pragma unroll
+      for (int u = 0; u < kInFlight; ++u) {
+        const int r = static_cast<int>(lane >> 3) + 4 * (part + kWarpsPerSlot * (i0 + u));
+        const uint4* src = reinterpret_cast<const uint4*>(
+            c + static_cast<int64_t>(row_at(j, r)) * (kAtoms * 64) + chunk * 8);
+#pragma unroll
+        for (int a = 0; a < kReg; ++a) v[u][a] = ld_nc_v4(src + a * 8);
+      }
+#pragma unroll
+      for (int u = 0; u < kInFlight; ++u) {
+        const int r = static_cast<int>(lane >> 3) + 4 * (part + kWarpsPerSlot * (i0 + u));
+        uint4* dst = reinterpret_cast<uint4*>(smem + s * kTile + r * 128 + ((chunk ^ (r & 7)) * 16));
+#pragma unroll
+        for (int a = 0; a < kReg; ++a) dst[a * (kAtomBytes / 16)] = v[u][a];
+      }
+    }
+    if (kReg < kAtoms) cp_async_wait_all();
+    fence_proxy_async_smem();
+    mbar_arrive(full(s));
+  }
+  cp_async_wait_all();
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 row_gather_probe_kernel(const __grid_constant__ CUtensorMap tm, const __nv_bfloat16* __restrict__ c,
                         int64_t n_rows, const int32_t* __restrict__ rows, int n_tiles, int mode,
@@ -50,7 +105,7 @@ row_gather_probe_kernel(const __grid_constant__ CUtensorMap tm, const __nv_bfloa
   auto empty = [&](int s) { return smem_u32(&bars[kSlots + s]); };
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSlots; ++s) {
-      mbar_init(full(s), mode == 1 ? 1 : 32 * kWarpsPerSlot);
+      mbar_init(full(s), mode == 1 ? 1 : 32 * kWarpsPerSlot);   // modes 0, 2, 4: every lane
       mbar_init(empty(s), 1);
     }
     abort_flag = (sbase & 1023u) == 0 ? 0u : 1u;
@@ -110,6 +165,12 @@ row_gather_probe_kernel(const __grid_constant__ CUtensorMap tm, const __nv_bfloa
              clock64() - w0 < kLimit) {
       }
     }
+  } else if (mode == 4) {
+    reg_gather<2, kAtoms>(c, sbase, smem, warp, lane, n_tiles, row_at, full, empty, &abort_flag);
+  } else if (mode == 5) {
+    reg_gather<2, 5>(c, sbase, smem, warp, lane, n_tiles, row_at, full, empty, &abort_flag);
+  } else if (mode == 6) {
+    reg_gather<4, kAtoms>(c, sbase, smem, warp, lane, n_tiles, row_at, full, empty, &abort_flag);
   } else if (warp == 0) {
     int last = -1;                                   // the last tile this warp started
     for (int j = 0; j < n_tiles; ++j) {

@@ -92,7 +92,10 @@ int dsa_selftest_bounded_wait(int64_t limit_cycles, dsa_stream_t stream);
  *          2 = both at once: columns 0..511 by cp.async, 512..575 by tile::gather4;
  *          3 = no gather: CTA pairs (clusters of 2, n_ctas even) push 192 KB per round into
  *              each other's shared memory by bulk DSMEM copies, n_tiles rounds (the rate of
- *              the path the MLA's courier uses); rows and c are not read.
+ *              the path the MLA's courier uses); rows and c are not read;
+ *          4 = as 0 through registers (16-byte ld.global + st.shared);
+ *          5 = columns 0..319 through registers, 320..575 by cp.async;
+ *          6 = as 4 with every row of a warp in flight at once.
  *   cycles: device, uint64 [n_ctas], written.
  * Every in-kernel wait is bounded. Errors: DSA_ERR_INVALID for a null pointer, a size out of
  * range or a bad mode; DSA_ERR_CUDA for a failed launch.
