@@ -817,6 +817,32 @@ def next_rows(args):
                                   "l2": "flushed between launches"}), flush=True)
             torch.cuda.empty_cache()
     if not large:
+        # the step's rerange (k_idx + latent rows through one row map, one launch) over a range
+        # of sizes around the many-request batch, L2 flushed: time = ramp + bytes / rate
+        wl3 = W.WORKLOADS[3]
+        sizes, times = [], []
+        for scale in (0.125, 0.25, 0.5, 1, 2, 4, 8):
+            n = int(sum(wl3.lengths) * scale)
+            kg = torch.randn(n, wl3.Di, device="cuda").to(torch.bfloat16)
+            cg = torch.randn(n, wl3.dqk, device="cuda").to(torch.bfloat16)
+            ko, co = torch.empty_like(kg), torch.empty_like(cg)
+            nbytes = 2 * n * (wl3.Di + wl3.dqk) * 2
+            ms = timeit(lambda: dsa.dsa_rr_rerange_multi([kg, cg], [ko, co], n, wl3.sp, 0), 20, True)
+            sizes.append(nbytes)
+            times.append(ms * 1e3)
+            print(json.dumps({"kernel": "rerange_multi (k_idx 256 B + latent 1,152 B rows)",
+                              "tokens": n, "bytes": nbytes, "us": round(ms * 1e3, 1),
+                              "GB/s": round(nbytes / ms / 1e6),
+                              "frac_of_measured_hbm": round(nbytes / ms / 1e6 / hbm, 3),
+                              "l2": "flushed between launches"}), flush=True)
+            del kg, cg, ko, co
+            torch.cuda.empty_cache()
+        slope, ramp = np.polyfit(np.asarray(sizes, dtype=np.float64), np.asarray(times), 1)
+        print(json.dumps({"kernel": "rerange_multi", "fit": "us = ramp + bytes / rate",
+                          "ramp_us": round(float(ramp), 2),
+                          "rate_GB/s": round(1e-3 / float(slope)),
+                          "rate_frac_of_measured_hbm": round(1e-3 / float(slope) / hbm, 3)}),
+              flush=True)
         wl = W.WORKLOADS[4]
         q = wl.decode_queries
         ctx = np.asarray(wl.lengths, dtype=np.int64)

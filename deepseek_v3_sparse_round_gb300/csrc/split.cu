@@ -124,16 +124,35 @@ copy_rows_bytes_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ ds
 // up to kMaxMulti tensors that share the row map, so one grid streams all of them (one ramp and
 // one tail instead of one per tensor).
 constexpr int kMaxMulti = 4;
+// Unsigned division of n < 2^31 by a divisor fixed at launch: q = (n * m) >> shift with
+// l = ceil(log2 d), shift = 31 + l, m = floor(2^shift / d) + 1 (< 2^32). The error term
+// n * (m * d - 2^shift) / (d * 2^shift) stays below 1/d, so the floor is exact.
+struct FastDiv {
+  uint32_t d, m, shift;
+  __device__ __forceinline__ uint32_t div(uint32_t n) const {
+    return static_cast<uint32_t>((static_cast<uint64_t>(n) * m) >> shift);
+  }
+};
+FastDiv make_fastdiv(uint32_t d) {
+  uint32_t l = 0;
+  while ((uint64_t(1) << l) < d) ++l;
+  const uint32_t shift = 31 + l;
+  return FastDiv{d, static_cast<uint32_t>((uint64_t(1) << shift) / d + 1), shift};
+}
+
 struct MultiRows {
   const int4* src[kMaxMulti];
   int4* dst[kMaxMulti];
-  uint32_t cpr[kMaxMulti];         // 16-byte chunks per row
+  FastDiv cpr[kMaxMulti];          // 16-byte chunks per row
   uint32_t begin[kMaxMulti + 1];   // first flattened chunk of each tensor
   int n;
 };
 
+// Flattened (tensor, row, chunk) index space; each index's source row from the rerange map with
+// the divisions by the chunk count and by sp done by multiply-shift (this loop issues about as
+// many integer operations as it moves 16-byte chunks, so the divisions decide its rate).
 __global__ void __launch_bounds__(kThreads)
-rerange_multi_kernel(MultiRows mr, RerangeRows map) {
+rerange_multi_kernel(MultiRows mr, RerangeRows map, FastDiv fsp) {
   const uint32_t total = mr.begin[mr.n];
   const uint32_t stride = gridDim.x * blockDim.x;
   for (uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += kUnroll * stride) {
@@ -147,9 +166,13 @@ rerange_multi_kernel(MultiRows mr, RerangeRows map) {
         int seg = 0;
 #pragma unroll
         for (int q = 1; q < kMaxMulti; ++q) seg += (q < mr.n && i >= mr.begin[q]) ? 1 : 0;
-        const uint32_t li = i - mr.begin[seg], cpr = mr.cpr[seg];
-        const uint32_t r = li / cpr;
-        v[u] = ld_stream(mr.src[seg] + map(r) * cpr + (li - r * cpr));
+        const uint32_t li = i - mr.begin[seg], cpr = mr.cpr[seg].d;
+        const uint32_t r = mr.cpr[seg].div(li);
+        const uint32_t j = fsp.div(r), rank = r - j * fsp.d;   // r = j * sp + rank
+        const int64_t off = map.stride > 0
+            ? static_cast<int64_t>(rank) * map.stride
+            : static_cast<int64_t>(rank) * map.per_rank + (rank < map.rem ? rank : map.rem);
+        v[u] = ld_stream(mr.src[seg] + (off + j) * cpr + (li - r * cpr));
         d[u] = mr.dst[seg] + li;
       }
     }
@@ -457,7 +480,7 @@ int rerange_multi(const void* const* gathered, void* const* out, const int64_t* 
       return fail(DSA_ERR_INVALID, "rerange_multi: tensor %d is not in 16-byte rows", q);
     mr.src[q] = static_cast<const int4*>(gathered[q]);
     mr.dst[q] = static_cast<int4*>(out[q]);
-    mr.cpr[q] = static_cast<uint32_t>(row_bytes[q] / 16);
+    mr.cpr[q] = make_fastdiv(static_cast<uint32_t>(row_bytes[q] / 16));
     mr.begin[q] = static_cast<uint32_t>(total);
     total += n_tokens * (row_bytes[q] / 16);
     if (total >= (int64_t(1) << 31))
@@ -466,7 +489,8 @@ int rerange_multi(const void* const* gathered, void* const* out, const int64_t* 
   mr.begin[n_tensors] = static_cast<uint32_t>(total);
   if (total == 0) return DSA_OK;
   RerangeRows map{sp, n_tokens / sp, n_tokens % sp, rank_stride_rows};
-  rerange_multi_kernel<<<grid_for(total, kUnroll), kThreads, 0, stream>>>(mr, map);
+  rerange_multi_kernel<<<grid_for(total, kUnroll), kThreads, 0, stream>>>(
+      mr, map, make_fastdiv(static_cast<uint32_t>(sp)));
   DSA_CHECK_CUDA(cudaGetLastError());
   return DSA_OK;
 }
