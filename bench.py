@@ -1049,6 +1049,7 @@ def profile_run(args):
     """Small, fixed launch sequences for ncu (no timing, no flush, nothing else on the GPU):
     --profile-steps K: the default workload's whole step, 1 untimed step then K more (32
       launches per step: the launch list);
+    --profile-decode: the paged decode batch, indexer + top-k and MLA twice;
     --profile-case: one shard of the many-request batch (rank 1) cut to an evenly spaced
       subset of 2,048 of its queries (every request, short and long histories; about 0.7 GB on
       the device): indexer + top-k, balanced sparse MLA, the FP8 row quantisation and the FP8
@@ -1059,6 +1060,37 @@ def profile_run(args):
     import deepseek_v3_sparse_round_gb300 as dsa
     import workloads as W
     dev = torch.device("cuda", 0)
+    if args.profile_decode:
+        # the paged decode batch (64 requests x 2 queries over 2.65 M cached tokens, about
+        # 4 GB on the device): indexer + top-k and balanced sparse MLA, each twice
+        wl = W.WORKLOADS[4]
+        table, n_pages = W.random_block_table(wl.lengths, wl.page_size,
+                                              W.seed_of(wl, "block_table"))
+        bid_np, pos_np = W.decode_queries(wl.lengths, wl.decode_queries)
+        n_rows = n_pages * wl.page_size
+        cu = torch.zeros(len(wl.lengths) + 1, dtype=torch.int32, device=dev)
+        bt = torch.as_tensor(table, device=dev)
+        bid = torch.as_tensor(np.asarray(bid_np, np.int32), device=dev)
+        pos = torch.as_tensor(np.asarray(pos_np, np.int32), device=dev)
+        n_q, max_ctx, n_req = pos.numel(), int(max(wl.lengths)), len(wl.lengths)
+        idx = W.indexer_inputs(wl, n_q, n_rows, 0, device=dev)
+        mi = W.mla_inputs(wl, n_q, n_rows, 0, device=dev)
+        ws = torch.empty(dsa.dsa_indexer_topk_workspace_size(n_q, max_ctx, wl.topk),
+                         dtype=torch.uint8, device=dev)
+        mws = torch.empty(dsa.dsa_sparse_mla_workspace_size(n_q), dtype=torch.uint8, device=dev)
+        topk = torch.empty((n_q, wl.topk), dtype=torch.int32, device=dev)
+        o = torch.empty((n_q, wl.H, wl.dv), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((n_q, wl.H), device=dev)
+        for _ in range(2):
+            dsa.dsa_indexer_topk(idx.q_idx, idx.w, idx.k_idx, cu, n_req, pos, bid, wl.topk,
+                                 max_ctx, topk, ws, block_table=bt)
+            dsa.dsa_sparse_mla_balanced(mi.q, mi.c, cu, n_req, bid, pos, topk, wl.scale, o, mws,
+                                        lse=lse, block_table=bt)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_decode": "64 requests x 2 queries, paged", "queries": n_q,
+                          "cached_tokens": int(sum(wl.lengths)),
+                          "device_errors": dsa.dsa_read_device_errors()}))
+        return
     if args.profile_steps:
         st = ConfigStep(torch, dsa, W, WORKLOAD_ID, dev)
         torch.cuda.synchronize()
@@ -1193,13 +1225,15 @@ def main():
                     help="ncu launch list: 1 + K default-workload steps, nothing else, then exit")
     ap.add_argument("--profile-case", action="store_true",
                     help="ncu capture: one 2,048-query cut of a many-request shard, then exit")
+    ap.add_argument("--profile-decode", action="store_true",
+                    help="ncu capture: the paged decode batch's indexer + top-k and MLA, twice")
     ap.add_argument("--gather-probe", type=int, nargs="?", const=400, default=0,
                     help="row-gather rate probe, cp.async vs TMA gather4 (tiles per CTA), then exit")
     args = ap.parse_args()
     if args.gather_probe:
         gather_probe(args)
         return
-    if args.profile_steps or args.profile_case:
+    if args.profile_steps or args.profile_case or args.profile_decode:
         profile_run(args)
         return
     if args.configs:
