@@ -515,22 +515,38 @@ topk_hist_kernel(const float* __restrict__ scores, int64_t stride, const int32_t
   // counts are scanned across the block, then each round is placed by a warp scan. Entries
   // beyond kCap are counted, not stored.
   uint32_t kept_so_far = 0;
+  // this lane's 16 entries of chunk `base` (coalesced rounds of 32 lanes x 4), loaded one
+  // chunk ahead of their use
+  auto load_chunk = [&](int base, float4 (&v)[kCompactPerLane / 4]) {
+    const int wb = base + warp * (kCompactPerLane * 32);
+#pragma unroll
+    for (int j = 0; j < kCompactPerLane / 4; ++j) {
+      const int i = wb + 128 * j + 4 * lane;
+      if (i + 4 <= L) {
+        v[j] = __ldcg(reinterpret_cast<const float4*>(row + i));
+      } else {
+        v[j].x = i < L ? __ldcg(row + i) : 0.f;
+        v[j].y = i + 1 < L ? __ldcg(row + i + 1) : 0.f;
+        v[j].z = i + 2 < L ? __ldcg(row + i + 2) : 0.f;
+        v[j].w = i + 3 < L ? __ldcg(row + i + 3) : 0.f;
+      }
+    }
+  };
+  float4 vnext[kCompactPerLane / 4];
+  load_chunk(0, vnext);
   for (int base = 0; base < L; base += kCompactChunk) {
     const int wb = base + warp * (kCompactPerLane * 32);
+    float4 vcur[kCompactPerLane / 4];
+#pragma unroll
+    for (int j = 0; j < kCompactPerLane / 4; ++j) vcur[j] = vnext[j];
+    if (base + kCompactChunk < L) load_chunk(base + kCompactChunk, vnext);
     uint32_t key[kCompactPerLane / 4][4];
     uint32_t keepm[kCompactPerLane / 4];
     uint32_t cnt = 0;
 #pragma unroll
     for (int j = 0; j < kCompactPerLane / 4; ++j) {
       const int i = wb + 128 * j + 4 * lane;
-      float f[4] = {0.f, 0.f, 0.f, 0.f};
-      if (i + 4 <= L) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(row + i));
-        f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
-      } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) f[e] = i + e < L ? __ldcg(row + i + e) : 0.f;
-      }
+      const float f[4] = {vcur[j].x, vcur[j].y, vcur[j].z, vcur[j].w};
       uint32_t m = 0;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
