@@ -15,17 +15,17 @@ pytestmark = pytest.mark.gpu
 
 
 def _rerange_kv(sh):
-    """Split (row gather per shard) -> rank-major gathered buffer -> rerange, for k_idx and c."""
+    """Split (row gather per shard) -> rank-major gathered buffer -> one rerange launch for
+    k_idx and c together (the benchmark's dsa_rr_rerange_multi)."""
     m = dsa()
     wl, cu = sh.wl, sh.cu
     n = int(cu[-1])
-    out = []
+    gathered, out = [], []
     for src in (sh.idx.k_idx.cuda(), sh.mla.c.cuda()):
         shards = [gpu_split(cu, wl.sp, r, src=src)["rows"] for r in range(wl.sp)]
-        gathered = torch.cat(shards)
-        logical = torch.empty_like(src)
-        m.dsa_rr_rerange(gathered, logical, n, wl.sp, 0)
-        out.append(logical)
+        gathered.append(torch.cat(shards))
+        out.append(torch.empty_like(src))
+    m.dsa_rr_rerange_multi(gathered, out, n, wl.sp, 0)
     return out
 
 
@@ -46,8 +46,9 @@ def _run(sh, sel):
                        sh.d_bid, wl.topk, sh.max_ctx, topk, ws, block_table=sh.block_table)
     o = torch.full((sh.n_q, wl.H, wl.dv), float("nan"), dtype=torch.bfloat16, device="cuda")
     lse = torch.full((sh.n_q, wl.H), float("nan"), device="cuda")
-    m.dsa_sparse_mla(sh.mla.q.cuda(), c, sh.d_cu, sh.n_req, sh.d_bid, topk, wl.scale, o, lse,
-                     block_table=sh.block_table)
+    mws = torch.empty(m.dsa_sparse_mla_workspace_size(sh.n_q), dtype=torch.uint8, device="cuda")
+    m.dsa_sparse_mla_balanced(sh.mla.q.cuda(), c, sh.d_cu, sh.n_req, sh.d_bid, sh.d_pos, topk,
+                              wl.scale, o, mws, lse=lse, block_table=sh.block_table)
     torch.cuda.synchronize()
     assert m.dsa_read_device_errors() == 0
     view = sh.oracle_view(sel)
