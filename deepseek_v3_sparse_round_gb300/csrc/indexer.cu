@@ -131,31 +131,16 @@ __device__ __forceinline__ uint32_t plan_scan(uint32_t v, uint32_t* wt, uint32_t
   return before;
 }
 
-// Up to this many queries, pos and bid are first copied into shared memory with coalesced
-// loads (each thread then reads a contiguous range many times); beyond it, from global memory.
-constexpr int kPlanStage = 24576;                   // 2 x 96 KB
-
 __global__ void __launch_bounds__(kPlanThreads)
-indexer_plan_kernel(const int32_t* __restrict__ pos_g, const int32_t* __restrict__ bid_g, int n_q,
+indexer_plan_kernel(const int32_t* __restrict__ pos, const int32_t* __restrict__ bid, int n_q,
                     int n_req, int max_ctx, int gq, int n_ctas, Plan* plan, int4* groups,
                     int32_t* unit_start, int32_t* t0_list) {
   (void)n_ctas;
   __shared__ uint32_t wt[32];
-  extern __shared__ int32_t s_stage[];                // [2][n_q] when staged
-  const bool staged = n_q <= kPlanStage;
-  if (staged) {
-    for (int i = static_cast<int>(threadIdx.x); i < n_q; i += kPlanThreads) {
-      s_stage[i] = __ldg(pos_g + i);
-      s_stage[n_q + i] = __ldg(bid_g + i);
-    }
-    __syncthreads();
-  }
-  auto pos_at = [&](int t) { return staged ? s_stage[t] : __ldg(pos_g + t); };
-  auto bid_at = [&](int t) { return staged ? s_stage[n_q + t] : __ldg(bid_g + t); };
   const int per = (n_q + kPlanThreads - 1) / kPlanThreads;
   const int lo = min(static_cast<int>(threadIdx.x) * per, n_q), hi = min(lo + per, n_q);
   auto starts = [&](int t) {
-    return t == 0 || (t % gq) == 0 || bid_at(t) != bid_at(t - 1);
+    return t == 0 || (t % gq) == 0 || __ldg(bid + t) != __ldg(bid + t - 1);
   };
   uint32_t cnt = 0;
   for (int t = lo; t < hi; ++t) cnt += starts(t);
@@ -172,10 +157,10 @@ indexer_plan_kernel(const int32_t* __restrict__ pos_g, const int32_t* __restrict
   bool bad = false;
   for (int gi = glo; gi < ghi; ++gi) {
     const int t0 = t0_list[gi], t1 = gi + 1 < G ? t0_list[gi + 1] : n_q;
-    int b = bid_at(t0);
+    int b = __ldg(bid + t0);
     if (b < 0 || b >= n_req) { bad = true; b = b < 0 ? 0 : n_req - 1; }
     int pmax = -1;
-    for (int t = t0; t < t1; ++t) pmax = max(pmax, pos_at(t));
+    for (int t = t0; t < t1; ++t) pmax = max(pmax, __ldg(pos + t));
     if (pmax >= max_ctx) { bad = true; pmax = max_ctx - 1; }
     const int tiles = pmax >= 0 ? pmax / kKeysPerTile + 1 : 0;
     groups[gi] = make_int4(t0, t1 - t0, b, pmax);
@@ -507,14 +492,9 @@ int launch_indexer(const void* q_idx, const float* w, const void* k_idx, int64_t
     DSA_CHECK_CUDA(cudaMemsetAsync(hist, 0, static_cast<size_t>(n_q) * kHistBins * sizeof(uint32_t),
                                    stream));
   const int n_req_eff = kr.block_table ? n_req : n_req;
-  const size_t plan_smem = n_q <= kPlanStage ? static_cast<size_t>(n_q) * 2 * sizeof(int32_t) : 0;
-  if (plan_smem > 48 * 1024)                         // above the default dynamic limit
-    DSA_CHECK_CUDA(cudaFuncSetAttribute(indexer_plan_kernel,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kPlanStage * 2 * static_cast<int>(sizeof(int32_t))));
-  indexer_plan_kernel<<<1, kPlanThreads, plan_smem, stream>>>(
-      pos, bid, static_cast<int>(n_q), n_req_eff, max_ctx, S::kGQ, n_ctas, plan, groups,
-      unit_start, t0_list);
+  indexer_plan_kernel<<<1, kPlanThreads, 0, stream>>>(pos, bid, static_cast<int>(n_q), n_req_eff,
+                                                      max_ctx, S::kGQ, n_ctas, plan, groups,
+                                                      unit_start, t0_list);
   DSA_CHECK_CUDA(cudaGetLastError());
   CUtensorMap tk, tq;
   int rc = make_tmap_2d(&tk, S::kTmaType, k_idx, static_cast<uint64_t>(n_kv_rows), DI,

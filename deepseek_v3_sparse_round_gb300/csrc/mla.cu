@@ -1103,15 +1103,7 @@ mla_order_kernel(const int32_t* __restrict__ pos, int k, int n_q, int n_pairs,
     const int sel = p < 0 ? 0 : (p >= k ? k : p + 1);
     return (sel + pair::kKeys - 1) / pair::kKeys;
   };
-  // Counting with one shared-memory atomic per distinct bucket of a warp (most queries of a
-  // long batch share the top bucket, so per-query atomics would serialise on it).
-  const int lane = static_cast<int>(threadIdx.x & 31u);
-  for (int base = 0; base < n_q; base += blockDim.x) {
-    const int t = base + static_cast<int>(threadIdx.x);
-    const int bkt = t < n_q ? tiles_of(t) : -1;
-    const unsigned same = __match_any_sync(0xffffffffu, bkt);
-    if (bkt >= 0 && lane == __ffs(same) - 1) atomicAdd(&hist[bkt], static_cast<uint32_t>(__popc(same)));
-  }
+  for (int t = threadIdx.x; t < n_q; t += blockDim.x) atomicAdd(&hist[tiles_of(t)], 1u);
   __syncthreads();
   if (threadIdx.x == 0) {                            // bucket b starts after every larger bucket
     uint32_t run = 0;
@@ -1121,17 +1113,8 @@ mla_order_kernel(const int32_t* __restrict__ pos, int k, int n_q, int n_pairs,
     }
   }
   __syncthreads();
-  for (int base = 0; base < n_q; base += blockDim.x) {
-    const int t = base + static_cast<int>(threadIdx.x);
-    const int bkt = t < n_q ? tiles_of(t) : -1;
-    const unsigned same = __match_any_sync(0xffffffffu, bkt);
-    const int leader = __ffs(same) - 1;
-    uint32_t first = 0;
-    if (bkt >= 0 && lane == leader) first = atomicAdd(&next[bkt], static_cast<uint32_t>(__popc(same)));
-    first = __shfl_sync(0xffffffffu, first, leader);
-    if (bkt < 0) continue;
-    // rank, largest first: the warp's queries of one bucket take consecutive ranks in lane order
-    const int p = static_cast<int>(first) + __popc(same & ((1u << lane) - 1u));
+  for (int t = threadIdx.x; t < n_q; t += blockDim.x) {
+    const int p = static_cast<int>(atomicAdd(&next[tiles_of(t)], 1u));   // rank, largest first
     const int r = p / n_pairs;
     int j = p - r * n_pairs;
     if ((r & 1) && (r + 1) * n_pairs <= n_q) j = n_pairs - 1 - j;          // full rounds snake
