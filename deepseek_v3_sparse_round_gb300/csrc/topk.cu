@@ -382,8 +382,9 @@ topk_short_kernel(const float* __restrict__ scores, int64_t stride,
       }
     }
   }
-  // three radix passes over the stash (11, 11, 10 bits)
+  // up to three radix passes over the stash (11, 11, 10 bits)
   uint32_t prefix = 0, prefix_mask = 0, remaining = static_cast<uint32_t>(k);
+  bool whole_bin = false;                            // every entry of the final bin is taken
 #pragma unroll 1
   for (int p = 0; p < 3; ++p) {
     for (int b = threadIdx.x; b < kBins; b += kShortThreads) hist[b] = 0;
@@ -419,9 +420,13 @@ topk_short_kernel(const float* __restrict__ scores, int64_t stride,
     remaining -= s_above;
     prefix |= s_digit << sh;
     prefix_mask |= dm << sh;
+    // the bin holds exactly the entries still to take: all of them, no further pass
+    const bool done = p < 2 && hist[s_digit] == remaining && prefix != 0u;
     __syncthreads();
+    if (done) { whole_bin = true; break; }
   }
-  const uint32_t T = prefix, need_eq = remaining;
+  // whole_bin: taken = every key at or above the bin's lowest key (its lower bits all zero)
+  const uint32_t T = whole_bin ? prefix - 1u : prefix, need_eq = whole_bin ? 0u : remaining;
   // ordered emission: one contiguous odd-length segment per thread, one block-wide scan
   const int seg = ((L + kShortThreads - 1) / kShortThreads) | 1;
   const int lo = min(static_cast<int>(threadIdx.x) * seg, L), hi = min(lo + seg, L);
