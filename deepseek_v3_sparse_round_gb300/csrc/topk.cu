@@ -174,7 +174,14 @@ __device__ __forceinline__ void radix_threshold(const float* __restrict__ row,
     remaining -= *s_above;
     prefix |= *s_digit << sh;
     prefix_mask |= dm << sh;
+    // the bin holds exactly the entries still to take: every key at or above its lowest key
+    const bool done = p < 2 && hist[*s_digit] == remaining && prefix != 0u;
     __syncthreads();
+    if (done) {
+      *T_out = prefix - 1u;
+      *need_eq_out = 0u;
+      return;
+    }
   }
   *T_out = prefix;
   *need_eq_out = remaining;
@@ -616,7 +623,14 @@ topk_hist_kernel(const float* __restrict__ scores, int64_t stride, const int32_t
     remaining -= s_above;
     prefix |= s_digit << sh;
     prefix_mask |= dm << sh;
+    // the bin holds exactly the entries still to take: every key at or above its lowest key
+    const bool done = p < 2 && hist[s_digit] == remaining && prefix != 0u;
     __syncthreads();
+    if (done) {
+      prefix -= 1u;
+      remaining = 0u;
+      break;
+    }
   }
   T = prefix;
   need_eq = remaining;
