@@ -85,3 +85,24 @@ def test_batches_of_rows_of_at_most_4096(k):
     got = _run(rows, k)
     for i, r in enumerate(rows):
         assert np.array_equal(got[i], topk_indices(r, k)), (k, len(r))
+
+
+@pytest.mark.parametrize("L", [3000, 9000, 50000])
+def test_bin_holding_exactly_the_remaining_entries(L):
+    """Rows whose first radix bin (or first two) already holds exactly the entries still to
+    take, so the passes stop early and every key at or above that bin is selected: k entries of
+    one value above the rest, a second set where 2048 - 7 keys sit above one bin of 7, and the
+    same values with one extra entry in the boundary bin (no early stop)."""
+    rng = np.random.default_rng(L)
+    k = 2048
+    a = np.full(L, 1.0, np.float32)
+    a[rng.choice(L, k, replace=False)] = 3.0                     # bin of 3.0 holds exactly k
+    b = np.full(L, 0.5, np.float32)
+    idx = rng.choice(L, k, replace=False)
+    b[idx[:k - 7]] = 6.0
+    b[idx[k - 7:]] = 2.0                                         # 7 entries in the bin of 2.0
+    c = b.copy()
+    c[np.flatnonzero(c == 0.5)[0]] = 2.0                         # 8 there: a tie to break
+    got = _run([a, b, c], k)
+    for i, r in enumerate((a, b, c)):
+        assert np.array_equal(got[i], topk_indices(r, k)), (L, i)
