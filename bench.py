@@ -1167,7 +1167,8 @@ def gather_probe(args):
     tile_bytes = 48 * 1152
     variants = [(n_ctas, 0, 0), (n_ctas, 1, 1), (n_ctas, 1, 4), (n_ctas, 1, 12), (n_ctas, 1, 32),
                 (n_ctas, 2, 0), (n_ctas // 2, 0, 0), (n_ctas // 4, 0, 0), (n_ctas, 4, 0),
-                (n_ctas // 2, 4, 0), (n_ctas, 6, 0), (n_ctas, 5, 0), (n_ctas, 3, 0)]
+                (n_ctas // 2, 4, 0), (n_ctas, 6, 0), (n_ctas, 5, 0), (n_ctas, 3, 0),
+                (n_ctas, 7, 0), (n_ctas // 2, 7, 0)]
     for ctas, mode, issuers in variants:
         ms = []
         for rep in range(3):
@@ -1194,7 +1195,8 @@ def gather_probe(args):
                5: "ld.global + st.shared for columns 0-319, cp.async for 320-575",
                6: "ld.global 16 B + st.shared, every row of a warp in flight",
                1: f"TMA tile::gather4, {issuers} issuing lane(s)",
-               2: "cp.async for columns 0-511 + TMA tile::gather4 for 512-575"}[mode]
+               2: "cp.async for columns 0-511 + TMA tile::gather4 for 512-575",
+               7: "TMA tiled boxes of 48 consecutive rows (not a gather)"}[mode]
         print(json.dumps({
             "gather_probe": how,
             "ctas": ctas, "tiles_per_cta": n_tiles, "tile": "48 rows x 1,152 B (9 SW128 atoms)",

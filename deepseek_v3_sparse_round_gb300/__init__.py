@@ -119,8 +119,8 @@ def dsa_probe_row_gather(c, rows, n_ctas, n_tiles, mode, issuers, cycles, stream
     mode 0 = cp.async (three warps per ring slot), 1 = TMA tile::gather4 by `issuers` lanes,
     2 = columns 0..511 by cp.async and 512..575 by tile::gather4, 3 = DSMEM push between the
     CTAs of pairs (192 KB per round, n_tiles rounds), 4 = as 0 through registers, 5 = columns
-    0..319 through registers and 320..575 by cp.async, 6 = as 4 with all rows in flight;
-    cycles int64 [n_ctas] receives each CTA's loop time in SM clock cycles."""
+    0..319 through registers and 320..575 by cp.async, 6 = as 4 with all rows in flight,
+    7 = TMA tiled boxes of the 48 consecutive rows from each tile's first listed row; cycles int64 [n_ctas] receives each CTA's loop time in SM clock cycles."""
     _dev(c, torch.bfloat16, "c")
     _dev(rows, torch.int32, "rows")
     _dev(cycles, torch.int64, "cycles")

@@ -151,7 +151,7 @@ DSA_EXPORT int dsa_probe_row_gather(const void* c, int64_t n_rows, const int32_t
       static_cast<int64_t>(n_ctas) * n_tiles * 48 > (1ll << 31) - 1)
     return dsa::fail(DSA_ERR_INVALID, "probe: need 1 <= n_rows < 2^31, 1 <= n_ctas <= 65535, "
                                       "n_tiles >= 1 and n_ctas * n_tiles * 48 < 2^31");
-  if (mode < 0 || mode > 6) return dsa::fail(DSA_ERR_INVALID, "probe: mode is 0 to 6");
+  if (mode < 0 || mode > 7) return dsa::fail(DSA_ERR_INVALID, "probe: mode is 0 to 7");
   if (mode == 3 && (n_ctas % 2) != 0)
     return dsa::fail(DSA_ERR_INVALID, "probe: mode 3 runs CTA pairs: n_ctas must be even");
   if (mode == 1 && (issuers < 1 || issuers > 32))

@@ -16,6 +16,9 @@
 //   mode 5: both paths at once: atoms 0-4 of every row through registers as in mode 4,
 //     atoms 5-8 by cp.async as in mode 0.
 //   mode 6: as mode 4 with all four of a warp's row groups in flight at once.
+//   mode 7: not a gather: each tile is the 48 consecutive rows starting at its first listed row,
+//     loaded as nine 64-column x 48-row TMA boxes (128B swizzle) by one lane (the rate for a
+//     run of consecutive keys, e.g. every key of a short history).
 //   mode 3: not a gather: the rate of the DSMEM path between the two CTAs of a cluster (what
 //     the MLA's courier uses). Each CTA pushes 192 KB per round into its peer's shared memory
 //     with six 32 KB bulk copies that complete on the peer's barrier; a cluster barrier keeps
@@ -105,7 +108,8 @@ row_gather_probe_kernel(const __grid_constant__ CUtensorMap tm, const __nv_bfloa
   auto empty = [&](int s) { return smem_u32(&bars[kSlots + s]); };
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSlots; ++s) {
-      mbar_init(full(s), mode == 1 ? 1 : 32 * kWarpsPerSlot);   // modes 0, 2, 4: every lane
+      // modes 1 and 7: one arrival with the byte count; the others: every gather lane
+      mbar_init(full(s), mode == 1 || mode == 7 ? 1 : 32 * kWarpsPerSlot);
       mbar_init(empty(s), 1);
     }
     abort_flag = (sbase & 1023u) == 0 ? 0u : 1u;
@@ -178,7 +182,14 @@ row_gather_probe_kernel(const __grid_constant__ CUtensorMap tm, const __nv_bfloa
       if (!warp_wait(empty(s), static_cast<uint32_t>(((j / kSlots) & 1) ^ 1), kSite | 2u, &abort_flag, kLimit)) break;
       if (lane == 0) mbar_expect_tx(full(s), kTile);
       __syncwarp();
-      if (static_cast<int>(lane) < issuers) {
+      if (mode == 7) {
+        if (lane == 0) {
+          // rows past the end of the cache read the fill value (zero); the start is in range
+          const int r0 = row_at(j, 0);
+          for (int a = 0; a < kAtoms; ++a)
+            tma_load_2d(sbase + s * kTile + a * kAtomBytes, &tm, a * 64, r0, full(s));
+        }
+      } else if (static_cast<int>(lane) < issuers) {
         for (int g = static_cast<int>(lane); g < kAtoms * (kRows / 4); g += issuers) {
           const int a = g / (kRows / 4), q4 = g % (kRows / 4);
           tma_gather4(sbase + s * kTile + a * kAtomBytes + q4 * 4 * 128, &tm, a * 64,
@@ -266,8 +277,9 @@ int probe_row_gather(const void* c, int64_t n_rows, const int32_t* rows, int n_c
     return DSA_OK;
   }
   CUtensorMap tm;
+  // one-row boxes for tile::gather4, 48-row boxes for the runs of mode 7
   int rc = make_tmap_bf16_2d(&tm, c, static_cast<uint64_t>(n_rows), kAtoms * 64, kAtoms * 128,
-                             64, 1, CU_TENSOR_MAP_SWIZZLE_128B);
+                             64, mode == 7 ? kRows : 1, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc) return rc;
   DSA_CHECK_CUDA(cudaFuncSetAttribute(row_gather_probe_kernel,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem));

@@ -95,7 +95,9 @@ int dsa_selftest_bounded_wait(int64_t limit_cycles, dsa_stream_t stream);
  *              the path the MLA's courier uses); rows and c are not read;
  *          4 = as 0 through registers (16-byte ld.global + st.shared);
  *          5 = columns 0..319 through registers, 320..575 by cp.async;
- *          6 = as 4 with every row of a warp in flight at once.
+ *          6 = as 4 with every row of a warp in flight at once;
+ *          7 = no gather: each tile is the 48 consecutive rows from its first listed row on,
+ *              nine 64-column x 48-row TMA tiled boxes (rows past n_rows read zeros).
  *   cycles: device, uint64 [n_ctas], written.
  * Every in-kernel wait is bounded. Errors: DSA_ERR_INVALID for a null pointer, a size out of
  * range or a bad mode; DSA_ERR_CUDA for a failed launch.

@@ -1,5 +1,5 @@
-"""GPU: the row-gather rate probe runs both mechanisms (cp.async and TMA tile::gather4) to
-completion on a small case, with every CTA reporting its cycle count and no device error; rows
+"""GPU: the row-gather rate probe runs every mechanism (cp.async, TMA tile::gather4, registers,
+DSMEM, TMA boxes of consecutive rows) to completion on a small case, with every CTA reporting its cycle count and no device error; rows
 outside the cache are reported, not read."""
 import pytest
 import torch
@@ -14,7 +14,7 @@ def _case(n_rows=1000, n_ctas=4, n_tiles=7, seed=0):
     return c, rows, torch.zeros(n_ctas, dtype=torch.int64, device="cuda")
 
 
-@pytest.mark.parametrize("mode,issuers", [(0, 1), (1, 1), (1, 5), (1, 32), (2, 1), (3, 1), (4, 1), (5, 1), (6, 1)])
+@pytest.mark.parametrize("mode,issuers", [(0, 1), (1, 1), (1, 5), (1, 32), (2, 1), (3, 1), (4, 1), (5, 1), (6, 1), (7, 1)])
 def test_probe_runs_clean(mode, issuers):
     import deepseek_v3_sparse_round_gb300 as dsa
     dsa.dsa_read_device_errors()
@@ -41,6 +41,6 @@ def test_probe_rejects_bad_arguments():
     with pytest.raises(ValueError):
         dsa.dsa_probe_row_gather(c, rows[:-1], 4, 7, 0, 1, cycles)
     with pytest.raises(RuntimeError):
-        dsa.dsa_probe_row_gather(c, rows, 4, 7, 7, 1, cycles)
+        dsa.dsa_probe_row_gather(c, rows, 4, 7, 8, 1, cycles)
     with pytest.raises(RuntimeError):
         dsa.dsa_probe_row_gather(c, rows, 4, 7, 1, 33, cycles)
