@@ -244,20 +244,23 @@ class ConfigStep:
             self.run_shard(r)
 
     def work(self):
-        """Algorithmic work of one step: indexer flop (causal pairs), MLA flop (selected
+        """Algorithmic work of one step: indexer flop (the causal pairs of the queries whose
+        history exceeds k: the others select every key and need no score), MLA flop (selected
         pairs), bytes moved by the split gather and the two reranges."""
         wl = self.wl
         idx = mla = 0.0
-        pairs_c = pairs_s = 0
+        pairs_c = pairs_i = pairs_s = 0
         for r in self.ranks:
             pos = self.out[r]["pos"].cpu().numpy().astype(np.int64)
             pairs_c += int(np.sum(pos + 1))
+            pairs_i += int(np.sum((pos + 1)[pos + 1 > wl.topk]))
             pairs_s += int(np.sum(np.minimum(pos + 1, wl.topk)))
-        idx = 2.0 * wl.Hi * wl.Di * pairs_c
+        idx = 2.0 * wl.Hi * wl.Di * pairs_i
         mla = 2.0 * wl.H * (wl.dqk + wl.dv) * pairs_s
         rerange_bytes = 2 * self.N * (wl.Di + wl.dqk) * 2 * len(self.ranks)
         nbytes = sum(2 * self.n_r[r] * wl.dqk * 2 for r in self.ranks) + rerange_bytes
         return {"indexer_flop": idx, "mla_flop": mla, "causal_pairs": pairs_c,
+                "indexer_pairs": pairs_i,
                 "selected_pairs": pairs_s, "copy_bytes": nbytes, "rerange_bytes": rerange_bytes,
                 "shard_queries": [self.n_r[r] for r in self.ranks]}
 
@@ -606,7 +609,10 @@ def gpu_arm(args):
             "indexer_kernel<64,128> + topk_kernel", "tensor", idx_ach, pk["bf16"], "TFLOP/s",
             NOMINAL["bf16"], None,
             {"algorithmic_flop_per_step": work["indexer_flop"],
-             "unit_of_work": "causal (query, key) pair: 2*64*128 = 16,384 flop",
+             "unit_of_work": "causal (query, key) pair of a query whose history exceeds k "
+                             "(the others take every key and need no score): 2*64*128 = "
+                             "16,384 flop",
+             "causal_pairs_all_queries": work["causal_pairs"],
              "timing": "CUDA events around each indexer+top-k call (plan, indexer, top-k)"}),
         "roofline_split_rerange": roofline_obj(
             "split_kernel + rerange_multi_kernel", "hbm", cp_ach, pk["hbm"], "GB/s",
@@ -972,7 +978,7 @@ def config_rows(args):
             tot_q += n_q
             tot_idx += t_idx
             tot_mla += t_mla
-            idx_flop += 2.0 * wl.Hi * wl.Di * float(np.sum(p + 1))
+            idx_flop += 2.0 * wl.Hi * wl.Di * float(np.sum((p + 1)[p + 1 > wl.topk]))
             sel = float(np.sum(np.minimum(p + 1, wl.topk)))
             mla_flop += 2.0 * wl.H * (wl.dqk + wl.dv) * sel
             if wl.decode_queries:
@@ -1142,6 +1148,7 @@ def profile_run(args):
     p = pos.cpu().numpy().astype(np.int64)
     print(json.dumps({"profile_case": "many_req rank 1, 2048 evenly spaced queries",
                       "queries": n, "causal_pairs": int(np.sum(p + 1)),
+                      "indexer_pairs": int(np.sum((p + 1)[p + 1 > wl.topk])),
                       "selected_pairs": int(np.sum(np.minimum(p + 1, wl.topk))),
                       "device_errors": dsa.dsa_read_device_errors()}))
 

@@ -22,7 +22,7 @@ int indexer_scores(const void* q_idx, const float* w, const void* k_idx, int64_t
                    const int32_t* cu, const int32_t* pos, const int32_t* bid, int64_t n_q, int n_req,
                    int Hi, int Di, int max_ctx, const int32_t* block_table, int max_pages,
                    int page_size, float* scores, int64_t stride, void* ws, size_t ws_bytes,
-                   uint32_t* hist, const float* q_scale, const float* k_scale,
+                   uint32_t* hist, const float* q_scale, const float* k_scale, int skip_le,
                    cudaStream_t stream);
 int quantize_fp8_rows(const void* x, int64_t rows, int cols, void* codes, float* scales,
                       cudaStream_t stream);
@@ -243,7 +243,7 @@ DSA_EXPORT int dsa_indexer_scores(const void* q_idx, const float* w, const void*
     return dsa::fail(DSA_ERR_INVALID, "indexer: score rows must be 16-byte aligned");
   return dsa::indexer_scores(q_idx, w, k_idx, n_kv_rows, cu, pos, bid, n_q, n_req, Hi, Di,
                              max_ctx, block_table, max_pages, page_size, scores, score_stride,
-                             workspace, workspace_bytes, nullptr, nullptr, nullptr,
+                             workspace, workspace_bytes, nullptr, nullptr, nullptr, 0,
                              reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -286,9 +286,11 @@ static int indexer_topk_impl(const void* q_idx, const float* q_scale, const floa
                        ? reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + plan +
                                                      score_bytes)
                        : nullptr;
+  // A query whose history holds at most k keys selects all of them, so the top-k reads no score
+  // of it: its group of queries is left out of the indexer when every query in it is such.
   int rc = indexer_scores(q_idx, w, k_idx, n_kv_rows, cu, pos, bid, n_q, n_req, Hi, Di, max_ctx,
                           block_table, max_pages, page_size, scores, stride, workspace, plan,
-                          hist, q_scale, k_scale, stream);
+                          hist, q_scale, k_scale, k, stream);
   if (rc) return rc;
   if (hist == nullptr) return topk_select(scores, stride, pos, n_q, k, max_ctx, topk, stream);
   return topk_select_hist(scores, stride, pos, n_q, k, max_ctx, hist, topk, stream);
@@ -329,7 +331,7 @@ DSA_EXPORT int dsa_indexer_scores_fp8(const void* q8, const float* q_scale, cons
     return dsa::fail(DSA_ERR_INVALID, "indexer: score rows must be 16-byte aligned");
   return dsa::indexer_scores(q8, w, k8, n_kv_rows, cu, pos, bid, n_q, n_req, Hi, Di, max_ctx,
                              block_table, max_pages, page_size, scores, score_stride, workspace,
-                             workspace_bytes, nullptr, q_scale, k_scale,
+                             workspace_bytes, nullptr, q_scale, k_scale, 0,
                              reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -18,7 +18,9 @@
 //  * Warp roles: warps 0-3 and 4-7 are the epilogues of accumulators 0 and 1 (TMEM lane
 //    quadrant = warp % 4), warp 8 issues TMA, warp 9 issues tcgen05.mma.
 //  * Persistent grid (one CTA per SM). A one-CTA planning kernel cuts the queries into groups
-//    (never across a request, at most 8 queries) and counts each group's causal 128-key tiles;
+//    (never across a request, at most 8 queries) and counts each group's causal 128-key tiles
+//    (none when the caller only needs the scores of histories longer than some k, and no query
+//    of the group has one: a top-k then takes every key of such a query whatever its scores);
 //    the groups' tiles, concatenated in order, are split into equal contiguous ranges, one per
 //    CTA (a range covers one or a few groups, so each CTA loads few Q blocks). Only tiles that
 //    hold some causal key are computed; keys past a query's position are masked in the
@@ -133,9 +135,13 @@ __device__ __forceinline__ uint32_t plan_scan(uint32_t v, uint32_t* wt, uint32_t
 
 __global__ void __launch_bounds__(kPlanThreads)
 indexer_plan_kernel(const int32_t* __restrict__ pos, const int32_t* __restrict__ bid, int n_q,
-                    int n_req, int max_ctx, int gq, int n_ctas, Plan* plan, int4* groups,
+                    int n_req, int max_ctx, int gq, int skip_le, Plan* plan, int4* groups,
                     int32_t* unit_start, int32_t* t0_list) {
-  (void)n_ctas;
+  // key tiles of a group whose last position is pmax (none for an empty group, or when every
+  // query's history pos + 1 is at most skip_le)
+  auto group_tiles = [&](int pmax) {
+    return pmax >= 0 && pmax + 1 > skip_le ? static_cast<uint32_t>(pmax / kKeysPerTile + 1) : 0u;
+  };
   __shared__ uint32_t wt[32];
   const int per = (n_q + kPlanThreads - 1) / kPlanThreads;
   const int lo = min(static_cast<int>(threadIdx.x) * per, n_q), hi = min(lo + per, n_q);
@@ -162,9 +168,8 @@ indexer_plan_kernel(const int32_t* __restrict__ pos, const int32_t* __restrict__
     int pmax = -1;
     for (int t = t0; t < t1; ++t) pmax = max(pmax, __ldg(pos + t));
     if (pmax >= max_ctx) { bad = true; pmax = max_ctx - 1; }
-    const int tiles = pmax >= 0 ? pmax / kKeysPerTile + 1 : 0;
     groups[gi] = make_int4(t0, t1 - t0, b, pmax);
-    tiles_sum += tiles;
+    tiles_sum += group_tiles(pmax);
   }
   if (bad) report_device_error(kErrBadIndex);
   // Tile prefix per group: the indexer hands each CTA an equal, contiguous range of the
@@ -173,8 +178,7 @@ indexer_plan_kernel(const int32_t* __restrict__ pos, const int32_t* __restrict__
   uint32_t ts = plan_scan(tiles_sum, wt, &total_tiles);
   for (int gi = glo; gi < ghi; ++gi) {
     unit_start[gi] = static_cast<int32_t>(ts);
-    const int pmax = groups[gi].w;
-    ts += pmax >= 0 ? static_cast<uint32_t>(pmax / kKeysPerTile + 1) : 0u;
+    ts += group_tiles(groups[gi].w);
   }
   if (threadIdx.x == 0) {
     unit_start[G] = static_cast<int32_t>(total_tiles);
@@ -486,14 +490,14 @@ int launch_indexer(const void* q_idx, const float* w, const void* k_idx, int64_t
                    const int32_t* pos, const int32_t* bid, int64_t n_q, int n_req, int max_ctx,
                    const KeyRows& kr, float* scores, int64_t stride, Plan* plan, int4* groups,
                    int32_t* unit_start, int32_t* t0_list, int n_ctas, uint32_t* hist,
-                   const float* q_scale, const float* k_scale, cudaStream_t stream) {
+                   const float* q_scale, const float* k_scale, int skip_le, cudaStream_t stream) {
   using S = Shape<HI, DI, F8>;
   if (hist != nullptr)
     DSA_CHECK_CUDA(cudaMemsetAsync(hist, 0, static_cast<size_t>(n_q) * kHistBins * sizeof(uint32_t),
                                    stream));
   const int n_req_eff = kr.block_table ? n_req : n_req;
   indexer_plan_kernel<<<1, kPlanThreads, 0, stream>>>(pos, bid, static_cast<int>(n_q), n_req_eff,
-                                                      max_ctx, S::kGQ, n_ctas, plan, groups,
+                                                      max_ctx, S::kGQ, skip_le, plan, groups,
                                                       unit_start, t0_list);
   DSA_CHECK_CUDA(cudaGetLastError());
   CUtensorMap tk, tq;
@@ -520,7 +524,7 @@ int indexer_scores(const void* q_idx, const float* w, const void* k_idx, int64_t
                    const int32_t* cu, const int32_t* pos, const int32_t* bid, int64_t n_q, int n_req,
                    int Hi, int Di, int max_ctx, const int32_t* block_table, int max_pages,
                    int page_size, float* scores, int64_t stride, void* ws, size_t ws_bytes,
-                   uint32_t* hist, const float* q_scale, const float* k_scale,
+                   uint32_t* hist, const float* q_scale, const float* k_scale, int skip_le,
                    cudaStream_t stream) {
   if (n_q < 0 || max_ctx < 1 || n_kv_rows < 0)
     return fail(DSA_ERR_INVALID, "indexer: need n_q >= 0, max_ctx >= 1, n_kv_rows >= 0");
@@ -552,18 +556,19 @@ int indexer_scores(const void* q_idx, const float* w, const void* k_idx, int64_t
     if (Hi == 64 && Di == 128)
       return launch_indexer<64, 128, true>(q_idx, w, k_idx, n_kv_rows, pos, bid, n_q, n_req,
                                            max_ctx, kr, scores, stride, plan, groups, unit_start,
-                                           t0_list, n_ctas, hist, q_scale, k_scale, stream);
+                                           t0_list, n_ctas, hist, q_scale, k_scale, skip_le, stream);
     return fail(DSA_ERR_UNSUPPORTED, "indexer: FP8 (Hi, Di) = (%d, %d) not built; supported "
                                      "(64, 128)", Hi, Di);
   }
   if (Hi == 64 && Di == 128)
     return launch_indexer<64, 128, false>(q_idx, w, k_idx, n_kv_rows, pos, bid, n_q, n_req,
                                           max_ctx, kr, scores, stride, plan, groups, unit_start,
-                                          t0_list, n_ctas, hist, nullptr, nullptr, stream);
+                                          t0_list, n_ctas, hist, nullptr, nullptr, skip_le,
+                                          stream);
   if (Hi == 4 && Di == 32)
     return launch_indexer<4, 32, false>(q_idx, w, k_idx, n_kv_rows, pos, bid, n_q, n_req, max_ctx,
                                         kr, scores, stride, plan, groups, unit_start, t0_list,
-                                        n_ctas, hist, nullptr, nullptr, stream);
+                                        n_ctas, hist, nullptr, nullptr, skip_le, stream);
   return fail(DSA_ERR_UNSUPPORTED, "indexer: (Hi, Di) = (%d, %d) not built; supported (64, 128), "
                                    "(4, 32)", Hi, Di);
 }

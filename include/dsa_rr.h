@@ -294,6 +294,9 @@ int dsa_topk_select(const float* scores, int64_t score_stride, const int32_t* po
 /*
  * dsa_indexer_scores followed by dsa_topk_select, the score rows living in `workspace`.
  * topk: int32 [n_q, k], entries are positions s inside the query's request (0..pos_t) or -1.
+ * A query whose history holds at most k keys (pos_t + 1 <= k) takes every key whatever its
+ * scores, so the indexer leaves out every group of consecutive queries (one request, at most 8)
+ * in which all queries are such; their score rows in the workspace are not written.
  * When max_ctx > 8192 the two steps are fused (same result): the indexer also counts, per
  * query, the first radix digit (top 11 bits of the order-preserving key) of one score in 16, the
  * top-k picks from those counts a threshold bin that very likely keeps at least k and only a few

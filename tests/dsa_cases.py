@@ -108,13 +108,14 @@ class Shard:
         m.dsa_topk_select(self.scores, self.d_pos, self.wl.topk, self.max_ctx, self.topk)
         return self.scores, self.topk
 
-    def run_indexer_topk(self):
+    def run_indexer_topk(self, k=None):
         m = dsa()
-        ws = torch.empty(m.dsa_indexer_topk_workspace_size(self.n_q, self.max_ctx, self.wl.topk),
+        k = self.wl.topk if k is None else k
+        ws = torch.empty(m.dsa_indexer_topk_workspace_size(self.n_q, self.max_ctx, k),
                          dtype=torch.uint8, device="cuda")
-        topk = torch.full((self.n_q, self.wl.topk), -9, dtype=torch.int32, device="cuda")
+        topk = torch.full((self.n_q, k), -9, dtype=torch.int32, device="cuda")
         m.dsa_indexer_topk(self.idx.q_idx.cuda(), self.idx.w.cuda(), self.idx.k_idx.cuda(), self.d_cu,
-                           self.n_req, self.d_pos, self.d_bid, self.wl.topk, self.max_ctx, topk, ws,
+                           self.n_req, self.d_pos, self.d_bid, k, self.max_ctx, topk, ws,
                            block_table=self.block_table)
         return topk
 

@@ -72,6 +72,25 @@ def test_composite_call_equals_separate_calls():
     assert torch.equal(sh.run_indexer_topk(), topk)
 
 
+@pytest.mark.parametrize("k", [700, 3000, 8000])
+def test_groups_whose_histories_fit_in_k_are_left_out(k):
+    """dsa_indexer_topk computes no score for a group of queries whose histories all hold at most
+    k keys (the top-k of such a query is every key, whatever the scores): with k = 700, 3,000 or
+    8,000 on the varlen shard (histories of up to 8,000 keys) a few, most or all groups are left
+    out, and the index sets still equal the oracle's (integer inputs)."""
+    from oracle.topk import topk_rows
+    sh = Shard(W.WORKLOADS[1], 3, integer_indexer=True)
+    t_np = sh.run_indexer_topk(k=k).cpu().numpy()
+    for t in np.flatnonzero(sh.pos + 1 <= k):
+        L = int(sh.pos[t]) + 1
+        assert np.array_equal(t_np[t, :L], np.arange(L)) and np.all(t_np[t, L:] == -1), t
+    near = np.argsort(np.abs(sh.pos.astype(np.int64) + 1 - k), kind="stable")[:6]
+    sel = np.union1d(sh.samples(40), near)            # the queries on either side of k as well
+    ref = topk_rows(sh.oracle_scores(sel), k)
+    for i, t in enumerate(sel):
+        assert np.array_equal(t_np[t], ref[i]), (t, int(sh.pos[t]))
+
+
 def test_row_longer_than_max_ctx_is_flagged_not_written():
     import deepseek_v3_sparse_round_gb300 as dsa
     sh = Shard(W.WORKLOADS[0], 1)

@@ -84,3 +84,30 @@ def test_short_workspace_and_missing_pos_rejected():
                                   o, None)
     assert m.dsa_sparse_mla_workspace_size(0) == 0
     assert m.dsa_sparse_mla_workspace_size(1476) == 1476 * 4
+
+
+@pytest.mark.parametrize("n", [1, 2, 75, 77, 153])
+def test_query_counts_around_the_number_of_pairs(n):
+    """Fewer queries than CTA pairs (1, 2), one below and one above a pair per query on a 152-SM
+    GPU (75, 77: 76 pairs), and two queries per pair plus one (153): plain and balanced calls on
+    the same subset agree bit for bit and match the oracle."""
+    m = dsa()
+    sh = Shard(W.WORKLOADS[1], 3, integer_indexer=False)
+    sel = np.linspace(0, sh.n_q - 1, n).round().astype(np.int64)
+    view = sh.oracle_view(sel)
+    topk_np = sh.oracle_topk(sh.oracle_scores(sel, view))
+    sel_t = torch.as_tensor(sel, device="cuda")
+    q, c, topk = sh.mla.q[sel_t].cuda(), sh.mla.c.cuda(), i32(topk_np)
+    bid, pos = i32(sh.bid[sel]), i32(sh.pos[sel])
+    o1 = torch.full((n, sh.wl.H, sh.wl.dv), float("nan"), dtype=torch.bfloat16, device="cuda")
+    l1 = torch.full((n, sh.wl.H), float("nan"), device="cuda")
+    o2, l2 = o1.clone(), l1.clone()
+    m.dsa_sparse_mla(q, c, sh.d_cu, sh.n_req, bid, topk, sh.wl.scale, o1, l1)
+    ws = torch.empty(m.dsa_sparse_mla_workspace_size(n), dtype=torch.uint8, device="cuda")
+    m.dsa_sparse_mla_balanced(q, c, sh.d_cu, sh.n_req, bid, pos, topk, sh.wl.scale, o2, ws, lse=l2)
+    torch.cuda.synchronize()
+    assert m.dsa_read_device_errors() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    ref_o, ref_lse = sh.oracle_mla(sel, topk_np, view)
+    mla_close(f64(o1), ref_o)
+    assert np.allclose(l1.cpu().numpy(), ref_lse, atol=1e-3, rtol=1e-4)
