@@ -187,12 +187,44 @@ __device__ __forceinline__ void radix_threshold(const float* __restrict__ row,
   *need_eq_out = remaining;
 }
 
+// Output of a row: k int32 indices. Writing them with 16-byte stores needs k % 4 == 0 and a
+// 16-byte aligned row (the caller's topk pointer is only known to be 4-byte aligned).
+__device__ __forceinline__ bool wide_out(const int32_t* out, int k) {
+  return (k & 3) == 0 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+}
+
+// out[j] = j < n ? j : -1 for j < k (every index of a row of n <= k entries; n = 0: none).
+__device__ __forceinline__ void fill_taken(int32_t* out, int k, int n, int n_threads) {
+  if (wide_out(out, k)) {
+    for (int j = static_cast<int>(threadIdx.x) * 4; j < k; j += n_threads * 4)
+      *reinterpret_cast<int4*>(out + j) = make_int4(j < n ? j : -1, j + 1 < n ? j + 1 : -1,
+                                                    j + 2 < n ? j + 2 : -1, j + 3 < n ? j + 3 : -1);
+  } else {
+    for (int j = static_cast<int>(threadIdx.x); j < k; j += n_threads) out[j] = j < n ? j : -1;
+  }
+}
+
+// The ordered emission writes each selected index at its rank, a scattered 4-byte store. When
+// the k indices fit the (then unused) 16-byte aligned histogram array and the row allows wide
+// stores, they are ranked into that array instead and copied out with 16-byte stores.
+__device__ __forceinline__ uint32_t* out_stage(uint32_t* hist, const int32_t* out, int k) {
+  return k <= kBins && wide_out(out, k) ? hist : nullptr;
+}
+__device__ __forceinline__ void copy_stage(const uint32_t* stage, int32_t* out, int k,
+                                           int n_threads) {
+  __syncthreads();                                  // every rank written
+  for (int j = static_cast<int>(threadIdx.x) * 4; j < k; j += n_threads * 4)
+    *reinterpret_cast<int4*>(out + j) = *reinterpret_cast<const int4*>(stage + j);
+}
+
 // Ordered emission reading the row from global memory in chunks: every index with key > T and
-// the lowest-index need_eq entries with key == T, in ascending index order.
+// the lowest-index need_eq entries with key == T, in ascending index order (into `stage` when
+// it is given, then copied to out).
 __device__ __forceinline__ void emit_ordered_global(const float* __restrict__ row, int L,
                                                     uint32_t T, uint32_t need_eq, uint32_t n_gt,
-                                                    int32_t* __restrict__ out,
-                                                    uint32_t* warp_tot) {
+                                                    int k, int32_t* __restrict__ out,
+                                                    uint32_t* warp_tot, uint32_t* stage) {
+  int32_t* dst = stage != nullptr ? reinterpret_cast<int32_t*>(stage) : out;
   uint32_t gt_done = 0, eq_done = 0;
   for (int base = 0; base < L && (gt_done < n_gt || eq_done < need_eq); base += kChunk) {
     uint32_t key[kPerThread];
@@ -212,16 +244,17 @@ __device__ __forceinline__ void emit_ordered_global(const float* __restrict__ ro
     for (int j = 0; j < kPerThread; ++j) {
       if (!valid[j]) continue;
       if (key[j] > T) {
-        out[g_before + (e_before < need_eq ? e_before : need_eq)] = i0 + j;
+        dst[g_before + (e_before < need_eq ? e_before : need_eq)] = i0 + j;
         ++g_before;
       } else if (key[j] == T) {
-        if (e_before < need_eq) out[g_before + e_before] = i0 + j;
+        if (e_before < need_eq) dst[g_before + e_before] = i0 + j;
         ++e_before;
       }
     }
     gt_done += tot >> 16;
     eq_done += tot & 0xFFFFu;
   }
+  if (stage != nullptr) copy_stage(stage, out, k, kThreads);
 }
 
 // kIn: 16-byte loads in flight per thread while the stash fills. Short rows (several CTAs per SM)
@@ -232,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, kIn <= 2 ? 3 : 1)
 topk_kernel(const float* __restrict__ scores, int64_t stride, const int32_t* __restrict__ pos,
             int k, int max_ctx, int32_t* __restrict__ topk) {
   extern __shared__ __align__(16) uint32_t stash[];
-  __shared__ uint32_t hist[kBins];
+  __shared__ __align__(16) uint32_t hist[kBins];
   __shared__ uint32_t warp_tot[kWarps];
   __shared__ uint32_t s_digit, s_above;
 
@@ -243,11 +276,11 @@ topk_kernel(const float* __restrict__ scores, int64_t stride, const int32_t* __r
   const int L = __ldg(pos + t) + 1;
   if (L < 1 || L > max_ctx) {
     if (threadIdx.x == 0) report_device_error(kErrBadLength);
-    for (int j = threadIdx.x; j < k; j += kThreads) out[j] = -1;
+    fill_taken(out, k, 0, kThreads);
     return;
   }
   if (L <= k) {                                     // every index is taken
-    for (int j = threadIdx.x; j < k; j += kThreads) out[j] = j < L ? j : -1;
+    fill_taken(out, k, L, kThreads);
     return;
   }
   const float* row = scores + t * stride;
@@ -296,19 +329,22 @@ topk_kernel(const float* __restrict__ scores, int64_t stride, const int32_t* __r
     uint32_t tot;                                   // counts < 2^16: L <= kStashKeys
     const uint32_t before = block_exclusive_scan((n_g << 16) | n_e, warp_tot, &tot);
     uint32_t g_before = before >> 16, e_before = before & 0xFFFFu;
+    uint32_t* stage = out_stage(hist, out, k);
+    int32_t* dst = stage != nullptr ? reinterpret_cast<int32_t*>(stage) : out;
     for (int i = lo; i < hi; ++i) {
       const uint32_t key = stash[i];
       if (key > T) {
-        out[g_before + (e_before < need_eq ? e_before : need_eq)] = i;
+        dst[g_before + (e_before < need_eq ? e_before : need_eq)] = i;
         ++g_before;
       } else if (key == T) {
-        if (e_before < need_eq) out[g_before + e_before] = i;
+        if (e_before < need_eq) dst[g_before + e_before] = i;
         ++e_before;
       }
     }
+    if (stage != nullptr) copy_stage(stage, out, k, kThreads);
     return;
   }
-  emit_ordered_global(row, L, T, need_eq, n_gt, out, warp_tot);
+  emit_ordered_global(row, L, T, need_eq, n_gt, k, out, warp_tot, out_stage(hist, out, k));
 }
 
 // ------------------------------------------------------------------------------------------
@@ -353,7 +389,7 @@ topk_short_kernel(const float* __restrict__ scores, int64_t stride,
                   const int32_t* __restrict__ pos, int k, int max_ctx,
                   int32_t* __restrict__ topk) {
   __shared__ __align__(16) uint32_t stash[kShortMax];
-  __shared__ uint32_t hist[kBins];
+  __shared__ __align__(16) uint32_t hist[kBins];
   __shared__ uint32_t warp_tot[kShortWarps];
   __shared__ uint32_t s_digit, s_above;
   const int64_t t = static_cast<int64_t>(gridDim.x) - 1 - blockIdx.x;   // longest rows first
@@ -361,11 +397,11 @@ topk_short_kernel(const float* __restrict__ scores, int64_t stride,
   const int L = __ldg(pos + t) + 1;
   if (L < 1 || L > max_ctx || L > kShortMax) {
     if (threadIdx.x == 0) report_device_error(kErrBadLength);
-    for (int j = threadIdx.x; j < k; j += kShortThreads) out[j] = -1;
+    fill_taken(out, k, 0, kShortThreads);
     return;
   }
   if (L <= k) {
-    for (int j = threadIdx.x; j < k; j += kShortThreads) out[j] = j < L ? j : -1;
+    fill_taken(out, k, L, kShortThreads);
     return;
   }
   const float* row = scores + t * stride;
@@ -446,16 +482,19 @@ topk_short_kernel(const float* __restrict__ scores, int64_t stride,
   uint32_t tot;
   const uint32_t before = short_block_scan((n_g << 16) | n_e, warp_tot, &tot);
   uint32_t g_before = before >> 16, e_before = before & 0xFFFFu;
+  uint32_t* stage = out_stage(hist, out, k);
+  int32_t* dst = stage != nullptr ? reinterpret_cast<int32_t*>(stage) : out;
   for (int i = lo; i < hi; ++i) {
     const uint32_t key = stash[i];
     if (key > T) {
-      out[g_before + (e_before < need_eq ? e_before : need_eq)] = i;
+      dst[g_before + (e_before < need_eq ? e_before : need_eq)] = i;
       ++g_before;
     } else if (key == T) {
-      if (e_before < need_eq) out[g_before + e_before] = i;
+      if (e_before < need_eq) dst[g_before + e_before] = i;
       ++e_before;
     }
   }
+  if (stage != nullptr) copy_stage(stage, out, k, kShortThreads);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -484,7 +523,7 @@ topk_hist_kernel(const float* __restrict__ scores, int64_t stride, const int32_t
                  int k, int max_ctx, const uint32_t* __restrict__ hist_rows,
                  int32_t* __restrict__ topk) {
   extern __shared__ __align__(16) uint32_t kept[];   // keys [kCap], then indices [kCap]
-  __shared__ uint32_t hist[kBins];
+  __shared__ __align__(16) uint32_t hist[kBins];
   __shared__ uint32_t warp_tot[kWarps];
   __shared__ uint32_t s_digit, s_above;
   uint32_t* ckey = kept;
@@ -496,11 +535,11 @@ topk_hist_kernel(const float* __restrict__ scores, int64_t stride, const int32_t
   const int L = __ldg(pos + t) + 1;
   if (L < 1 || L > max_ctx) {
     if (threadIdx.x == 0) report_device_error(kErrBadLength);
-    for (int j = threadIdx.x; j < k; j += kThreads) out[j] = -1;
+    fill_taken(out, k, 0, kThreads);
     return;
   }
   if (L <= k) {
-    for (int j = threadIdx.x; j < k; j += kThreads) out[j] = j < L ? j : -1;
+    fill_taken(out, k, L, kThreads);
     return;
   }
   const float* row = scores + t * stride;
@@ -600,7 +639,8 @@ topk_hist_kernel(const float* __restrict__ scores, int64_t stride, const int32_t
   if (kept_so_far > static_cast<uint32_t>(kCap) || kept_so_far < static_cast<uint32_t>(k)) {
     radix_threshold<false>(row, nullptr, L, k, 0, 0u, 0u, static_cast<uint32_t>(k), hist,
                            warp_tot, &s_digit, &s_above, &T, &need_eq);
-    emit_ordered_global(row, L, T, need_eq, static_cast<uint32_t>(k) - need_eq, out, warp_tot);
+    emit_ordered_global(row, L, T, need_eq, static_cast<uint32_t>(k) - need_eq, k, out, warp_tot,
+                        out_stage(hist, out, k));
     return;
   }
   const int n = static_cast<int>(kept_so_far);
@@ -647,16 +687,19 @@ topk_hist_kernel(const float* __restrict__ scores, int64_t stride, const int32_t
   uint32_t tot;                                       // counts < 2^16: n <= kCap
   const uint32_t before = block_exclusive_scan((n_g << 16) | n_e, warp_tot, &tot);
   uint32_t g_before = before >> 16, e_before = before & 0xFFFFu;
+  uint32_t* stage = out_stage(hist, out, k);
+  int32_t* dst = stage != nullptr ? reinterpret_cast<int32_t*>(stage) : out;
   for (int i = lo; i < hi; ++i) {
     const uint32_t key = ckey[i];
     if (key > T) {
-      out[g_before + (e_before < need_eq ? e_before : need_eq)] = static_cast<int32_t>(cidx[i]);
+      dst[g_before + (e_before < need_eq ? e_before : need_eq)] = static_cast<int32_t>(cidx[i]);
       ++g_before;
     } else if (key == T) {
-      if (e_before < need_eq) out[g_before + e_before] = static_cast<int32_t>(cidx[i]);
+      if (e_before < need_eq) dst[g_before + e_before] = static_cast<int32_t>(cidx[i]);
       ++e_before;
     }
   }
+  if (stage != nullptr) copy_stage(stage, out, k, kThreads);
 }
 
 }  // namespace

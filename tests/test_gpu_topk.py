@@ -106,3 +106,31 @@ def test_bin_holding_exactly_the_remaining_entries(L):
     got = _run([a, b, c], k)
     for i, r in enumerate((a, b, c)):
         assert np.array_equal(got[i], topk_indices(r, k)), (L, i)
+
+
+@pytest.mark.parametrize("k", [100, 2048, 4096])
+@pytest.mark.parametrize("L", [3000, 9000, 50000])
+def test_output_rows_that_allow_no_wide_stores(k, L):
+    """The selected indices are ranked in shared memory and stored 16 bytes at a time only when
+    k <= 2048, k % 4 == 0 and the row is 16-byte aligned; an output buffer at a 4-byte offset
+    (every row misaligned) and k = 4096 (too many to stage) take the direct stores: same result
+    on the short-row, shared-memory and global paths, short rows' fills included."""
+    import deepseek_v3_sparse_round_gb300 as dsa
+    rng = np.random.default_rng(k + L)
+    rows = [rng.integers(-50, 51, L).astype(np.float32), rng.normal(size=L).astype(np.float32),
+            rng.normal(size=max(k - 3, 1)).astype(np.float32)]
+    max_ctx = max(len(r) for r in rows)
+    stride = dsa.dsa_score_row_stride(max_ctx)
+    s = np.full((len(rows), stride), np.nan, dtype=np.float32)
+    for i, r in enumerate(rows):
+        s[i, :len(r)] = r
+    pos = torch.tensor([len(r) - 1 for r in rows], dtype=torch.int32, device="cuda")
+    flat = torch.full((len(rows) * k + 1,), -9, dtype=torch.int32, device="cuda")
+    out = flat[1:].view(len(rows), k)                # data pointer 4 bytes past an aligned one
+    assert out.data_ptr() % 16 == 4
+    dsa.dsa_topk_select(torch.as_tensor(s).cuda(), pos, k, max_ctx, out)
+    got = out.cpu().numpy()
+    assert int(flat[0]) == -9                        # nothing written before the rows
+    for i, r in enumerate(rows):
+        assert np.array_equal(got[i], topk_indices(r, k)), (k, L, i)
+    assert np.array_equal(_run(rows, k), got)        # the aligned buffer gives the same rows
