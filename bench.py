@@ -5,7 +5,8 @@ N = 71,014 tokens), sp = 4, all four shards processed back to back on one GPU (1
 queries each, 71,014 in total); indexer 64 heads x 128, top-k 2048; MLA 128 heads, qk 576 /
 v 512, bf16. A step is the whole shard path of every shard through the C ABI:
   split metadata + the shard's row gather -> rerange of the all-gathered k_idx and latent rows
-  -> indexer scores + top-k -> sparse MLA.
+  -> indexer scores (for the groups of queries whose history exceeds k; the others take every
+  key) + top-k -> sparse MLA.
 The other shards' rows are inputs (one GPU, no collective). The long single prompt (32,768
 tokens, sp = 8, all eight shards) is timed the same way and reported under "config_long".
 With --gpus N (torchrun) every GPU runs an independent replica of the same batch: weak scaling,
