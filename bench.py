@@ -577,7 +577,7 @@ def gpu_arm(args):
         traffic = int(mla_tr["dram_bytes_per_unit"] * work["selected_pairs"] / len(st.ranks))
     gather = mla_gather_roofline(torch, dsa, W, device, work, mla_s, clk.summary())
     cpu = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and ws == 1:       # the oracle baseline is a one-GPU figure
         cpu = cpu_baseline(args.cpu_baseline_queries)
     wl = st.wl
     line = {
