@@ -607,14 +607,17 @@ def gpu_arm(args):
              "traffic_note": None if traffic is None else
              f"ncu DRAM bytes per selected pair x pairs per launch ({mla_tr['workload']})"}),
         "roofline_indexer": roofline_obj(
-            "indexer_kernel<64,128> + topk_kernel", "tensor", idx_ach, pk["bf16"], "TFLOP/s",
+            "indexer_plan_kernel + indexer_kernel<64,128> + topk_short_kernel (one call)",
+            "tensor", idx_ach, pk["bf16"], "TFLOP/s",
             NOMINAL["bf16"], None,
             {"algorithmic_flop_per_step": work["indexer_flop"],
              "unit_of_work": "causal (query, key) pair of a query whose history exceeds k "
                              "(the others take every key and need no score): 2*64*128 = "
                              "16,384 flop",
              "causal_pairs_all_queries": work["causal_pairs"],
-             "timing": "CUDA events around each indexer+top-k call (plan, indexer, top-k)"}),
+             "timing": "CUDA events around each indexer+top-k call (plan, indexer, top-k)",
+             # k int32 indices for every query, those whose history fits in k included
+             "topk_output_bytes_per_step": int(st.queries() * st.wl.topk * 4)}),
         "roofline_split_rerange": roofline_obj(
             "split_kernel + rerange_multi_kernel", "hbm", cp_ach, pk["hbm"], "GB/s",
             NOMINAL["hbm"], None,
