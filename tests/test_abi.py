@@ -106,3 +106,23 @@ def test_sparse_mla_balanced_arguments_rejected(lib):
     assert f(*args(fake, ctypes.c_void_p(4100), 16)) == -1             # not 16-byte aligned
     assert lib.dsa_sparse_mla_workspace_size(1476) == 1476 * 4
     assert lib.dsa_sparse_mla_workspace_size(0) == 0
+
+
+def test_sparse_mla_shapes_rejected_before_any_launch(lib):
+    """Widths and shapes the MLA kernels are not built for, and misaligned q / o, come back as
+    return codes from host checks (no device memory is touched)."""
+    null, fake = ctypes.c_void_p(0), ctypes.c_void_p(4096)
+    f = lib.dsa_sparse_mla
+
+    def call(k=2048, H=128, dqk=576, dv=512, q=fake, o=fake, page_size=64, table=null):
+        return f(q, fake, 1000, fake, 1, fake, fake, 4, H, dqk, dv, k, 0.05, table, 1, page_size,
+                 o, null, null)
+
+    assert call(k=4097) == -2                                          # beyond the 4096-wide mask
+    assert call(H=64) == -2 and call(dqk=512) == -2 and call(dv=256) == -2
+    assert call(k=0) == -1
+    assert call(q=ctypes.c_void_p(4100)) == -1                         # q not 16-byte aligned
+    assert call(o=ctypes.c_void_p(4104)) == -1                         # o not 16-byte aligned
+    assert call(table=fake, page_size=32) == -2                        # pages of 64 tokens only
+    assert f(null, fake, 1000, fake, 1, fake, fake, 4, 128, 576, 512, 2048, 0.05, null, 1, 64,
+             fake, null, null) == -1                                   # null q
