@@ -17,6 +17,13 @@ in the design notes):
   * The indexer on quantised rows is the indexer of the dequantised values:
         I[t, s] = sum_h w[t, h] * ReLU( (sq[t, h] q8[t, h]) . (sk[s] k8[s]) )
     which, the scales being positive, equals sk[s] * sum_h (w[t, h] sq[t, h]) ReLU(q8 . k8).
+  * The latent (MLA) cache in FP8, the same rule per block of 128 values: a token's 576-value
+    latent row is its 512 latent values, quantised as four blocks of 128 (one fp32 scale each),
+    followed by its 64 rope values kept in bf16 (the positional part the page says nothing
+    about). Packed row of 656 bytes: the 512 codes, the 4 scales, the 64 bf16 rope values. The
+    attention consumes bf16 rows: each latent value is bf16(fl32(code * scale)) -- the product
+    rounded to fp32, then to bf16 (round to nearest, ties to even, both times); the rope values
+    are the stored bf16 values.
 """
 from __future__ import annotations
 
@@ -91,3 +98,42 @@ def indexer_scores_fp8(q8, q_scale, w, k8, k_scale, kv, pos, bid) -> list:
     q = np.asarray(q8, np.float64) * np.asarray(q_scale, np.float64)[..., None]
     k = np.asarray(k8, np.float64) * np.asarray(k_scale, np.float64)[:, None]
     return indexer_scores(q, w, k, kv, pos, bid)
+
+
+# ---------------------------------------------------------------- FP8 latent (MLA) cache rows
+LATENT_NOPE, LATENT_ROPE, LATENT_BLOCK = 512, 64, 128
+
+
+def quantize_latent_rows(c) -> tuple:
+    """Latent rows [n, 576] (bf16 values widened) -> (code values fp64 [n, 512], scales fp32
+    [n, 4], rope fp64 [n, 64]): each block of 128 latent values quantised like an indexer row."""
+    c = np.asarray(c, dtype=np.float64)
+    n = c.shape[0]
+    blocks = c[:, :LATENT_NOPE].reshape(n * (LATENT_NOPE // LATENT_BLOCK), LATENT_BLOCK)
+    vals, scales = quantize_rows(blocks)
+    return (vals.reshape(n, LATENT_NOPE), scales.reshape(n, LATENT_NOPE // LATENT_BLOCK),
+            c[:, LATENT_NOPE:].copy())
+
+
+def round_fp32_to_bf16(x) -> np.ndarray:
+    """Nearest bf16 value of each fp32 value (ties to the even 8-bit significand), as fp64;
+    finite inputs."""
+    x32 = np.asarray(x, dtype=np.float32)
+    a = np.abs(x32).astype(np.float64)
+    out = np.zeros(x32.shape, dtype=np.float64)
+    nz = a > 0
+    e = np.floor(np.log2(np.where(nz, a, 1.0)))
+    e = np.maximum(e, -126)                                 # below 2^-126: the subnormal spacing
+    quantum = np.exp2(e - 7)                                # bf16 keeps 8 significant bits
+    out = np.where(nz, np.rint(a / quantum) * quantum, 0.0)  # np.rint: ties to even
+    return np.copysign(out, x32.astype(np.float64))
+
+
+def dequantize_latent_rows(vals, scales, rope) -> np.ndarray:
+    """The bf16 rows the attention reads: [n, 576] fp64 values (exactly bf16)."""
+    vals = np.asarray(vals, dtype=np.float64)
+    n = vals.shape[0]
+    per = np.repeat(np.asarray(scales, dtype=np.float32), LATENT_BLOCK, axis=1)
+    prod32 = (vals.astype(np.float32) * per).astype(np.float32)   # IEEE fp32 product
+    nope = round_fp32_to_bf16(prod32)
+    return np.concatenate([nope, np.asarray(rope, np.float64).reshape(n, LATENT_ROPE)], axis=1)

@@ -106,3 +106,61 @@ def test_indexer_on_quantised_rows_brute_force():
             row = cu[bid[t]] + s_
             alt = ks[row] * sum(w[t, h] * qs[t, h] * max(q8[t, h] @ k8[row], 0.0) for h in range(Hi))
             assert np.isclose(got[t][s_], alt, rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------ FP8 latent (MLA) cache rows
+def test_bf16_rounding_against_the_library_conversion():
+    import torch
+    rng = np.random.default_rng(7)
+    x = (rng.normal(size=20000) * 10.0 ** rng.integers(-30, 30, 20000)).astype(np.float32)
+    ties = np.float32(1.0) + np.float32(2.0 ** -8) * np.arange(1, 8, 2, dtype=np.float32)  # halfway
+    tiny = (np.arange(1, 200, dtype=np.float32) * np.float32(2.0 ** -140))                   # subnormal
+    x = np.concatenate([x[np.isfinite(x)], ties, -ties, tiny, [0.0, -0.0]]).astype(np.float32)
+    ref = torch.tensor(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(fp8.round_fp32_to_bf16(x), ref)
+
+
+def test_latent_blocks_scale_rope_and_zero_block():
+    rng = np.random.default_rng(3)
+    c = rng.normal(size=(3, 576))
+    c[1, 128:256] = 0.0                                   # a zero block: scale 1, codes 0
+    c[2, 300] = -50.0                                     # block 2's largest magnitude
+    vals, scales, rope = fp8.quantize_latent_rows(c)
+    assert vals.shape == (3, 512) and scales.shape == (3, 4) and rope.shape == (3, 64)
+    assert np.array_equal(rope, c[:, 512:])               # the rope part is not quantised
+    assert scales[1, 1] == 1.0 and np.all(vals[1, 128:256] == 0.0)
+    assert scales[2, 2] == np.float32(50.0 / 448.0) and vals[2, 300] == -448.0
+    for r in range(3):
+        for b in range(4):
+            blk = c[r, 128 * b:128 * (b + 1)]
+            if np.any(blk):
+                assert np.max(np.abs(vals[r, 128 * b:128 * (b + 1)])) == 448.0
+                assert scales[r, b] == np.float32(np.float32(np.max(np.abs(blk))) / np.float32(448))
+
+
+def test_latent_dequantised_values():
+    vals = np.zeros((1, 512)); scales = np.ones((1, 4), np.float32)
+    vals[0, 0], scales[0, 0] = 448.0, np.float32(2.0)     # 896: exact in bf16
+    vals[0, 128], scales[0, 1] = 1.0, np.float32(0.1)     # fp32 0.1, then bf16: 0.10009765625
+    vals[0, 256], scales[0, 2] = 1.125, np.float32(3.0)   # 3.375 (8 significant bits suffice)
+    vals[0, 384], scales[0, 3] = 1.875, np.float32(1.0 + 2.0 ** -7)   # 1.889648..., rounded
+    rope = np.arange(64, dtype=np.float64).reshape(1, 64)
+    out = fp8.dequantize_latent_rows(vals, scales, rope)
+    assert out[0, 0] == 896.0 and out[0, 128] == 0.10009765625 and out[0, 256] == 3.375
+    exact = 1.875 * (1.0 + 2.0 ** -7)                     # 1.8896484375 = 1.1110001111... in binary
+    assert out[0, 384] == 1.890625 and abs(out[0, 384] - exact) <= 2.0 ** -8
+    assert np.array_equal(out[0, 512:], rope[0])
+
+
+def test_latent_round_trip_within_the_format_bound():
+    rng = np.random.default_rng(11)
+    c = rng.normal(size=(64, 576)) * 10.0 ** rng.integers(-3, 3, (64, 1))
+    vals, scales, rope = fp8.quantize_latent_rows(c)
+    back = fp8.dequantize_latent_rows(vals, scales, rope)
+    per = np.repeat(scales.astype(np.float64), 128, axis=1)
+    x = c[:, :512].astype(np.float32).astype(np.float64)
+    # E4M3: half a spacing, 2^-4 relative for normal codes, 2^-10 scale in the subnormal range;
+    # then the fp32 and bf16 roundings of the product
+    bound = 2.0 ** -4 * np.abs(x) + 2.0 ** -10 * per + 2.0 ** -8 * np.abs(back[:, :512])
+    assert np.all(np.abs(back[:, :512] - x) <= bound)
+    assert np.array_equal(back[:, 512:], c[:, 512:])
