@@ -21,7 +21,8 @@ __all__ = [
     "dsa_topk_select", "dsa_indexer_topk", "dsa_indexer_topk_noalloc", "dsa_sparse_mla",
     "dsa_sparse_mla_workspace_size", "dsa_sparse_mla_balanced", "dsa_read_device_errors",
     "dsa_rr_cache_local_paged", "dsa_selftest_bounded_wait", "dsa_probe_row_gather",
-    "dsa_quantize_fp8_rows",
+    "dsa_quantize_fp8_rows", "dsa_quantize_fp8_latent", "dsa_dequantize_fp8_latent",
+    "FP8_LATENT_ROW_BYTES",
     "dsa_indexer_scores_fp8", "dsa_indexer_topk_fp8",
     "DEVERR_TIMEOUT", "DEVERR_BAD_INDEX", "DEVERR_BAD_LENGTH",
 ]
@@ -327,6 +328,30 @@ def dsa_quantize_fp8_rows(x, codes, scales, stream=None):
         raise ValueError("codes must match x's shape and scales hold one value per row")
     _check(_lib().dsa_quantize_fp8_rows(_ptr(x), rows, cols, _ptr(codes), _ptr(scales),
                                         _stream(stream)))
+
+
+FP8_LATENT_ROW_BYTES = 656
+
+
+def _latent_pair(c, packed):
+    _dev(c, torch.bfloat16, "c"); _dev(packed, torch.uint8, "packed")
+    if c.dim() != 2 or c.shape[1] != 576:
+        raise ValueError(f"c must be [rows, 576], got {tuple(c.shape)}")
+    _shape(packed, (c.shape[0], FP8_LATENT_ROW_BYTES), "packed")
+    return c.shape[0]
+
+
+def dsa_quantize_fp8_latent(c, packed, stream=None):
+    """c bf16 [rows, 576] -> packed uint8 [rows, 656]: 512 E4M3 codes, 4 fp32 block scales,
+    64 bf16 rope values."""
+    rows = _latent_pair(c, packed)
+    _check(_lib().dsa_quantize_fp8_latent(_ptr(c), rows, _ptr(packed), _stream(stream)))
+
+
+def dsa_dequantize_fp8_latent(packed, c, stream=None):
+    """packed uint8 [rows, 656] -> c bf16 [rows, 576], the rows the sparse MLA reads."""
+    rows = _latent_pair(c, packed)
+    _check(_lib().dsa_dequantize_fp8_latent(_ptr(packed), rows, _ptr(c), _stream(stream)))
 
 
 def _fp8_indexer_checks(q8, q_scale, w, k8, k_scale, pos, bid, block_table, n_req):

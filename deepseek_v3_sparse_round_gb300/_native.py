@@ -42,6 +42,8 @@ SIGNATURES = {
                                          c_int, c_int, c_int, c_int, c_vp, c_int, c_int, c_vp,
                                          c_vp]),
     "dsa_quantize_fp8_rows": (c_int, [c_vp, c_i64, c_int, c_vp, c_vp, c_vp]),
+    "dsa_quantize_fp8_latent": (c_int, [c_vp, c_i64, c_vp, c_vp]),
+    "dsa_dequantize_fp8_latent": (c_int, [c_vp, c_i64, c_vp, c_vp]),
     "dsa_indexer_scores_fp8": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp, c_int, c_vp,
                                        c_vp, c_i64, c_int, c_int, c_int, c_vp, c_int, c_int, c_vp,
                                        c_i64, c_vp, c_sz, c_vp]),

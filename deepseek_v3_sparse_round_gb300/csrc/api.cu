@@ -26,6 +26,8 @@ int indexer_scores(const void* q_idx, const float* w, const void* k_idx, int64_t
                    cudaStream_t stream);
 int quantize_fp8_rows(const void* x, int64_t rows, int cols, void* codes, float* scales,
                       cudaStream_t stream);
+int quantize_fp8_latent(const void* c, int64_t rows, void* packed, cudaStream_t stream);
+int dequantize_fp8_latent(const void* packed, int64_t rows, void* c, cudaStream_t stream);
 int topk_select_hist(const float* scores, int64_t score_stride, const int32_t* pos, int64_t n_q,
                      int k, int max_ctx, const uint32_t* hist_rows, int32_t* topk,
                      cudaStream_t stream);
@@ -315,6 +317,16 @@ DSA_EXPORT int dsa_quantize_fp8_rows(const void* x, int64_t rows, int cols, void
                                      float* scales, dsa_stream_t stream) {
   return dsa::quantize_fp8_rows(x, rows, cols, codes, scales,
                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+DSA_EXPORT int dsa_quantize_fp8_latent(const void* c, int64_t rows, void* packed,
+                                       dsa_stream_t stream) {
+  return dsa::quantize_fp8_latent(c, rows, packed, reinterpret_cast<cudaStream_t>(stream));
+}
+
+DSA_EXPORT int dsa_dequantize_fp8_latent(const void* packed, int64_t rows, void* c,
+                                         dsa_stream_t stream) {
+  return dsa::dequantize_fp8_latent(packed, rows, c, reinterpret_cast<cudaStream_t>(stream));
 }
 
 DSA_EXPORT int dsa_indexer_scores_fp8(const void* q8, const float* q_scale, const float* w,

@@ -326,6 +326,26 @@ int dsa_quantize_fp8_rows(const void* x, int64_t rows, int cols, void* codes, fl
                           dsa_stream_t stream);
 
 /*
+ * FP8 latent (MLA) cache rows, the same reading per block of 128 latent values: a token's
+ * 576-value latent row (512 latent + 64 rope values, bf16) is stored as a packed row of
+ * DSA_FP8_LATENT_ROW_BYTES = 656 bytes: bytes [0, 512) the E4M3 codes of the 512 latent values,
+ * [512, 528) four fp32 scales (value j uses scale j / 128), [528, 656) the 64 rope values,
+ * bf16, unchanged. The attention consumes bf16 rows; a latent value expands to
+ * bf16(fl32(code * scale)) (fp32 product, then bf16, both rounded to nearest even).
+ * Packed rows are plain 656-byte rows for the split's row gather, the reranges and the paged
+ * writes (the all-gathered cache moves in FP8).
+ *
+ * dsa_quantize_fp8_latent: c bf16 [rows, 576] -> packed uint8 [rows, 656].
+ * dsa_dequantize_fp8_latent: packed uint8 [rows, 656] -> c bf16 [rows, 576].
+ * Both device pointers 16-byte aligned, caller-owned; rows >= 0 (0: nothing to do).
+ * Errors: DSA_ERR_INVALID for a null or misaligned pointer or rows < 0, DSA_ERR_CUDA for a
+ * failed launch.
+ */
+#define DSA_FP8_LATENT_ROW_BYTES 656
+int dsa_quantize_fp8_latent(const void* c, int64_t rows, void* packed, dsa_stream_t stream);
+int dsa_dequantize_fp8_latent(const void* packed, int64_t rows, void* c, dsa_stream_t stream);
+
+/*
  * Lightning-indexer scores on FP8 rows (tcgen05 kind::f8f6f4, fp32 accumulation): the indexer
  * of the dequantised rows,
  *     I[t, s] = sum_h w[t, h] * ReLU( (q_scale[t, h] q8[t, h, :]) . (k_scale[r] k8[r, :]) ),

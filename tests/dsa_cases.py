@@ -150,6 +150,7 @@ class Shard:
             "kv": ContiguousKV(cu2),
             "pos": self.pos[sel],
             "bid": np.asarray([remap[int(b)] for b in self.bid[sel]], dtype=np.int64),
+            "row_ids": rows,                             # the view's rows in the full tensors
         }
         return view
 
