@@ -988,6 +988,7 @@ def config_rows(args):
             if wl.decode_queries:
                 idx_bytes = float(sum(wl.lengths)) * wl.Di * 2
                 mla_bytes += sel * wl.dqk * 2
+            si_rows = si["n_rows"]
             if args.with_oracle and rank == ranks[-1]:
                 or_q, or_s = _oracle_sample_time(W, wl, si, idx, mi, 16 if wl.decode_queries else 64)
             del idx, mi, ws, mws, topk, o, lse, si
@@ -1011,6 +1012,21 @@ def config_rows(args):
                               "cores": _blas_threads(),
                               "sample": f"{or_q} evenly spaced queries of one shard (the longest "
                                         f"included), {or_s:.2f} s, extrapolated per query"}
+        # the FP8 latent cache: packing the batch's latent rows (or the decode pool) and
+        # expanding them back to the bf16 rows the MLA reads; 1,152 + 656 bytes per row each way
+        n_lat = int(sum(wl.lengths)) if not wl.decode_queries else int(si_rows)
+        c_lat = torch.randn(n_lat, 576, device="cuda").to(torch.bfloat16)
+        p_lat = torch.empty((n_lat, 656), dtype=torch.uint8, device="cuda")
+        t_q, t_d = timed([lambda: dsa.dsa_quantize_fp8_latent(c_lat, p_lat),
+                          lambda: dsa.dsa_dequantize_fp8_latent(p_lat, c_lat)])
+        lat_bytes = n_lat * (1152 + 656)
+        line["fp8_latent"] = {"rows": n_lat, "quantize_ms": round(t_q, 4),
+                              "dequantize_ms": round(t_d, 4),
+                              "dequantize_gbs": round(lat_bytes / (t_d * 1e-3) / 1e9, 1),
+                              "dequantize_frac_hbm": round(lat_bytes / (t_d * 1e-3) / 1e9 / pk["hbm"], 3),
+                              "bytes_per_row": {"bf16": 1152, "fp8": 656}}
+        del c_lat, p_lat
+        torch.cuda.empty_cache()
         if wl.decode_queries:
             line["indexer_topk_gbs"] = round(idx_bytes / (tot_idx * 1e-3) / 1e9, 1)
             line["indexer_topk_frac_hbm"] = round(idx_bytes / (tot_idx * 1e-3) / 1e9 / pk["hbm"], 3)
