@@ -335,10 +335,14 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (!mbar_wait(bar(kBFull), b_uses & 1u, 0x03, abort_flag)) break;
         ++b_uses;
         tc_fence_after();
+        // A group of at most one accumulator's queries (the decode batch's, the ends of
+        // requests) uses the two accumulators on alternate tiles, so that its next MMA overlaps
+        // this tile's epilogue; a larger group has one half of its queries in each.
+        const bool alt = un.count <= S::kQPA;
         int nq[2];
         uint32_t idesc[2];
         for (int h = 0; h < 2; ++h) {
-          nq[h] = max(0, min(un.count - h * S::kQPA, S::kQPA));
+          nq[h] = alt ? un.count : max(0, min(un.count - h * S::kQPA, S::kQPA));
           uint32_t n_cols = static_cast<uint32_t>(nq[h] * HI);
           n_cols = (n_cols + 15u) & ~15u;
           idesc[h] = F8 ? idesc_e4m3(128, n_cols < 16u ? 16u : n_cols)
@@ -350,11 +354,12 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           tc_fence_after();
           const uint32_t a_base = sbase + S::kOffA + stage * S::kAStage;
           for (int h = 0; h < 2; ++h) {
-            if (nq[h] == 0) continue;
+            if (nq[h] == 0 || (alt && h != (tile & 1))) continue;
             if (!mbar_wait(bar(kAccEmpty + h), (acc_uses[h] & 1u) ^ 1u, 0x05, abort_flag)) { ok = false; break; }
             ++acc_uses[h];
             tc_fence_after();
-            const uint32_t b_base = sbase + S::kOffB + h * S::kQPA * HI * S::kAtomBytes;
+            const uint32_t b_base =
+                sbase + S::kOffB + (alt ? 0 : h) * S::kQPA * HI * S::kAtomBytes;
 #pragma unroll
             for (int kk = 0; kk < S::kKSteps; ++kk) {
               const int a = kk / S::kStepsPerAtom, off = (kk % S::kStepsPerAtom) * 32;
@@ -386,9 +391,12 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     int ug = g_lo, ucur = t_lo;
     Unit un;
     while (!*abort_flag && next_unit(groups, unit_start, n_groups, ug, ucur, t_hi, un)) {
-      const int nq = max(0, min(un.count - h * S::kQPA, S::kQPA));
+      const bool alt = un.count <= S::kQPA;          // the MMA issuer's choice, as above
+      const int nq = alt ? un.count : max(0, min(un.count - h * S::kQPA, S::kQPA));
       if (nq == 0) continue;
-      const int tq0 = un.t0 + h * S::kQPA;
+      const int tq0 = un.t0 + (alt ? 0 : h * S::kQPA);
+      // alternating: this half's tiles are those of its parity
+      const int t_first = un.tile_begin + ((un.tile_begin & 1) != h);
       // The half's four warps share w / pos in smem: wait until all 128 threads finished with
       // the previous unit's copy, write this unit's, wait until every thread has written.
       if (!warp_wait(bar(kWEmpty + h), (w_uses & 1u) ^ 1u, 0x07, abort_flag)) break;
@@ -405,7 +413,9 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       if (!warp_wait(bar(kWFull + h), w_uses & 1u, 0x08, abort_flag)) break;
       ++w_uses;
       bool ok = true;
-      for (int tile = un.tile_begin; tile < un.tile_end; ++tile) {
+      // one tile of this unit; two loops below, so that the loop over every tile of a full
+      // group stays as it was
+      auto one_tile = [&](int tile) -> bool {
         float ks = 1.f;
         if constexpr (F8) {
           // the key's scale, loaded before the accumulator wait so the load is off the epilogue's
@@ -413,7 +423,7 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           const int64_t r = key_row(kr, un.b, tile * kKeysPerTile + row);
           ks = (r >= 0 && r < kr.n_rows) ? __ldg(k_scale + r) : 0.f;
         }
-        if (!warp_wait(bar(kAccFull + h), acc_uses & 1u, 0x06, abort_flag)) { ok = false; break; }
+        if (!warp_wait(bar(kAccFull + h), acc_uses & 1u, 0x06, abort_flag)) return false;
         ++acc_uses;
         tc_fence_after();
         // Four partial sums per query (heads h with h % 4 == 0, 1, 2, 3), held as two packed
@@ -472,6 +482,14 @@ indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                             first_digit(order_key(acc[q])), 1u);
           }
         }
+        return true;
+      };
+      if (alt) {
+        for (int tile = t_first; tile < un.tile_end; tile += 2)
+          if (!one_tile(tile)) { ok = false; break; }
+      } else {
+        for (int tile = un.tile_begin; tile < un.tile_end; ++tile)
+          if (!one_tile(tile)) { ok = false; break; }
       }
       mbar_arrive(bar(kWEmpty + h));                  // done reading this unit's w / pos
       if (!ok) break;
