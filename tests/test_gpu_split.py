@@ -36,7 +36,7 @@ def test_split_metadata_matches_oracle(case):
 
 @pytest.mark.parametrize("wid", [0, 1, 2, 3])
 @pytest.mark.parametrize("padded", [False, True])
-@pytest.mark.parametrize("width", [576, 128])          # latent rows (1152 B), k_idx rows (256 B)
+@pytest.mark.parametrize("width", [576, 128, 328])     # latent rows (1152 B), k_idx rows (256 B), FP8 latent rows (656 B)
 def test_gather_and_rerange_workloads(wid, padded, width):
     wl = W.WORKLOADS[wid]
     cu = W.cu_seqlens(wl.lengths)
@@ -94,7 +94,7 @@ def _oracle_pool(gathered, cu, sp, stride, table, ps, pool0):
 
 @pytest.mark.parametrize("wid", [1, 3])
 @pytest.mark.parametrize("padded", [False, True])
-@pytest.mark.parametrize("width", [576, 128])
+@pytest.mark.parametrize("width", [576, 128, 328])   # 328 bf16 = 656 B, a packed FP8 latent row
 def test_rerange_paged_workloads(wid, padded, width):
     from dsa_cases import dsa, i32
     wl = W.WORKLOADS[wid]
@@ -166,7 +166,7 @@ def _local_table(cu, sp, r, ps, seed, spare=2):
 
 
 @pytest.mark.parametrize("wid", [1, 3])
-@pytest.mark.parametrize("width", [576, 128])
+@pytest.mark.parametrize("width", [576, 128, 328])   # 328 bf16 = 656 B, a packed FP8 latent row
 def test_cache_local_paged_workloads(wid, width):
     """Every rank keeps only its own tokens: bit-exact against the oracle for each shard, with
     the rank's rows coming from the split's gather (as a rank holds them after step A)."""
