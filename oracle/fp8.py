@@ -3,8 +3,8 @@
 Test infrastructure only (see the package docstring).
 
 "[DeepSeek v3.2] 上下文并行详解", section 1: the round-robin split is what allows an FP8 KV
-cache. The page names no format, so this build takes the following reading (stated once here and
-in the design notes):
+cache. The page names no format, so the following reading is taken (stated once here and in the
+design notes):
 
   * E4M3 as defined by the OCP 8-bit floating point format: 1 sign bit, 4 exponent bits with
     bias 7, 3 mantissa bits; subnormals at exponent field 0 (value m/8 * 2^-6); the code
